@@ -1,0 +1,533 @@
+#!/usr/bin/env python3
+"""GVA decode benchmark: cache-read HBM GB/s and microseconds per layer step.
+
+One step = one decode token through a stack of `--layers` layers of the chosen
+workload (default: the 350M-class layer, B=8, H=16, G=4, d_h=64, d_n=64, d_r=16,
+T=4096, bf16).  Every layer has its own cache (more bytes in total than the 126 MB
+L2), and a layer step is: gva_append_cache (the current token at t = L_b - 1) then
+gva_decode_attention (absorb, split-K partial, log-sum-exp combine).  The whole step
+is captured in one CUDA graph and replayed; time is taken with CUDA events on the
+launching stream, max over ranks.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle on the
+host cores on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GVA decode cache-read HBM GB/s (% of B300 peak) and μs/step, B=8 T=4096"
+SPEC_HBM_GBS = 8000.0          # the "~8 TB/s" B300 HBM figure the target is stated against
+FALLBACK_HBM_GBS = 6400.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+def algorithmic_bytes(w, lengths) -> int:
+    """Cache bytes one decode of one layer must read: sum_b L_b (G d_h + d_r) x elem."""
+    elem = 2 if w.cache_dtype == "bf16" else 4
+    return int(sum(int(L) for L in lengths)) * (w.G * w.d_h + w.d_r) * elem
+
+
+def gqa_bytes(w, lengths) -> int:
+    elem = 2 if w.cache_dtype == "bf16" else 4
+    return int(sum(int(L) for L in lengths)) * 2 * w.G * w.d_h * elem
+
+
+# --------------------------------------------------------------------------- #
+# distributed plumbing (one process per GPU; weak scaling, no data-path collective)
+# --------------------------------------------------------------------------- #
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float, device=None) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def aggregate(units_per_rank, max_seconds):
+    """Whole-job throughput: units processed by all ranks over the slowest rank's time."""
+    return units_per_rank / max_seconds
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_marks = {}
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t0 = time.time()
+
+        def rd():
+            for line in self.proc.stdout:
+                self.lines.append((time.time(), line.strip()))
+        self.th = threading.Thread(target=rd, daemon=True)
+        self.th.start()
+
+    def mark(self, name):
+        self.t_marks[name] = time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.th.join(timeout=2)
+
+    def summary(self, t_from, t_to):
+        mhz, mx, reasons = [], None, set()
+        names = ("active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        for t, line in self.lines:
+            if not (t_from - 0.15 <= t <= t_to + 0.15):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    import gva_inputs
+    import value_only_kv_gva_b300 as gva
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    w = gva_inputs.workload(args.workload)
+    c = gva_inputs.make_case(w)
+    lengths = c.seq_len.tolist()
+    nl = args.layers
+    dims = gva.Dims(w.B, w.H, w.G, w.d_h, w.d_n, w.d_r,
+                    gva.GVA_F32 if w.cache_dtype == "f32" else gva.GVA_BF16,
+                    gva.GVA_F32 if w.q_dtype == "f32" else gva.GVA_BF16)
+    log(f"[bench] workload {w.name}: B={w.B} H={w.H} G={w.G} d_h={w.d_h} d_r={w.d_r} "
+        f"tokens={sum(lengths)} layers={nl}")
+
+    # per-layer device state: every layer owns its cache and its new-token inputs
+    def dev_rows(V):
+        offs = c.offsets.to(dev) if c.offsets is not None else None
+        bt = c.block_table.to(dev) if c.block_table is not None else None
+        return gva.Rows(w.layout, c.num_rows, T_cap=c.T_cap, offsets=offs, block_table=bt,
+                        page_size=w.page_size)
+
+    V0, K0 = c.V.to(dev), c.Kr.to(dev)
+    layers = []
+    for li in range(nl):
+        V = V0.clone() if li else V0
+        K = K0.clone() if li else K0
+        layers.append(dict(
+            cache=gva.Cache(dev_rows(V), V, K),
+            q_nope=c.q_nope.to(dev).clone(), q_rope=c.q_rope.to(dev).clone(),
+            M=c.M.to(dev).clone(), v_new=c.v_new.to(dev).clone(), k_new=c.k_new.to(dev).clone(),
+            out=torch.empty((w.B, w.H, w.d_h), device=dev),
+            lse=torch.empty((w.B, w.H), device=dev)))
+    seq = c.seq_len.to(dev)
+    pos = (c.seq_len - 1).to(torch.int32).to(dev)
+    tab = gva.gva_rope_table_fill(int(max(lengths)) + 1, w.d_r, w.base).to(dev)
+    ws = gva.workspace(dims, dev)
+    path = args.path
+
+    def layer_step(L):
+        gva.gva_append_cache(dims, L["v_new"], L["k_new"], pos, None, L["cache"], tab)
+        gva.gva_decode_attention(dims, L["q_nope"], L["q_rope"], L["M"], seq, L["cache"], tab,
+                                 w.scale, L["out"], L["lse"], ws, path=path)
+
+    def decode_only(L):
+        gva.gva_decode_attention(dims, L["q_nope"], L["q_rope"], L["M"], seq, L["cache"], tab,
+                                 w.scale, L["out"], L["lse"], ws, path=path)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for L in layers:        # eager once (sets kernel attributes), then capture
+                fn(L)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for L in layers:
+                    fn(L)
+        torch.cuda.synchronize()
+        return g
+
+    g_step = capture(layer_step)
+    g_dec = capture(decode_only)
+    assert gva.gva_get_device_status() == 0
+
+    def timed(graph, K, W, sampler=None):
+        for _ in range(W):
+            graph.replay()
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if sampler:
+            sampler.mark("t0")
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark("t1")
+        dist.barrier()
+        return e0.elapsed_time(e1) / 1e3
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    # soak so the clocks under load are what the samples see (not timed)
+    soak_t = time.time()
+    while time.time() - soak_t < args.soak:
+        for _ in range(20):
+            g_step.replay()
+        torch.cuda.synchronize()
+    secs = timed(g_step, args.steps, args.warmup, sampler)
+    clocks = sampler.summary(sampler.t_marks.get("t0", soak_t) - args.soak,
+                             sampler.t_marks.get("t1", time.time()))
+    sampler.stop()
+    max_secs = dist.max(secs, dev)
+    bytes_layer = algorithmic_bytes(w, lengths)
+    step_bytes = bytes_layer * nl
+    value = aggregate(step_bytes * args.steps * dist.world, max_secs) / 1e9   # GB/s, all ranks
+    ms_per_step = max_secs / args.steps * 1e3
+    us_layer = ms_per_step * 1e3 / nl
+
+    # the decode op alone (absorb + split-K partial + combine), same stream, live
+    dsecs = dist.max(timed(g_dec, args.steps, max(3, args.warmup)), dev)
+    us_decode = dsecs / (args.steps * nl) * 1e6
+    achieved = bytes_layer / (us_decode * 1e-6) / 1e9
+
+    peaks = measured_peaks()
+    hbm_peak = peaks["hbm_gbs"] if peaks else FALLBACK_HBM_GBS
+
+    # GQA comparator of matched H, G, d_h reading explicit K and V
+    gqa = None
+    if not args.no_gqa:
+        Kq0 = gva_inputs.make_gqa_keys(c).to(dev)
+        qq = gva_inputs.make_gqa_query(c).to(dev)
+        glayers = []
+        for li in range(nl):
+            glayers.append(dict(kv=gva.KVCache(dev_rows(V0), Kq0.clone() if li else Kq0,
+                                               layers[li]["cache"].V), q=qq.clone(),
+                                out=torch.empty((w.B, w.H, w.d_h), device=dev),
+                                lse=torch.empty((w.B, w.H), device=dev)))
+
+        def gqa_call(L):
+            gva.gva_gqa_decode_attention(dims, L["q"], seq, L["kv"], 1.0 / math.sqrt(w.d_h),
+                                         L["out"], L["lse"], ws, path=path)
+        gg = capture_list(torch, stream, glayers, gqa_call)
+        gsecs = dist.max(timed(gg, args.steps, max(3, args.warmup)), dev)
+        us_gqa = gsecs / (args.steps * nl) * 1e6
+        gb = gqa_bytes(w, lengths)
+        gqa = {"us_per_layer": round(us_gqa, 3), "bytes_per_layer": gb,
+               "gbs": round(gb / (us_gqa * 1e-6) / 1e9, 1),
+               "gva_bytes_saved_pct": round(100 * (1 - bytes_layer / gb), 3),
+               "gva_time_saved_pct": round(100 * (1 - us_decode / us_gqa), 1)}
+        del glayers, gg, Kq0
+
+    # end to end through the public API with host buffers (eager calls, pinned copies)
+    e2e = run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path,
+                  bytes_layer, dist)
+
+    # the CPU oracle on a bounded sample (rank 0 only)
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(w, c, budget_s=args.cpu_seconds)
+
+    launches_per_step = nl * 4
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if w.cache_dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: GVA decode layer B={w.B} H={w.H} G={w.G} d_h={w.d_h} "
+                        f"d_n={w.d_n} d_r={w.d_r} "
+                        + (f"T={w.T}" if w.layout == "contiguous" else f"{w.layout} lengths")
+                        + f" {w.cache_dtype} cache; step = append + decode through {nl} layers",
+            "layers": nl, "tokens_per_layer": int(sum(lengths)),
+            "bytes_per_layer": bytes_layer, "us_per_layer_step": round(us_layer, 3),
+            "us_per_decode": round(us_decode, 3),
+            "pct_of_8tbs_spec": round(100 * value / dist.world / SPEC_HBM_GBS, 2),
+            "pct_of_measured_copy": round(100 * value / dist.world / hbm_peak, 2),
+            "seqs_steps_per_s": round(w.B * dist.world / (ms_per_step * 1e-3), 1),
+            "l2": f"inputs larger than L2: {nl} distinct layer caches, "
+                  f"{bytes_layer * nl / 1e6:.0f} MB",
+            "path": path, "accumulate": "fp32", "parallelism": f"replicas x{dist.world}",
+            "gqa_comparator": gqa,
+        },
+        "roofline": {"bound": "hbm", "kernel": "gva_decode_attention (absorb + split-K "
+                     "partial + combine), per call", "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4),
+                     "peak_source": "measured" if peaks else "fallback",
+                     "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def capture_list(torch, stream, items, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for it in items:
+            fn(it)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for it in items:
+                fn(it)
+    torch.cuda.synchronize()
+    return g
+
+
+def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, bytes_layer,
+            dist):
+    """Same metric through the public API, eager, with this step's inputs copied from
+    pinned host memory and every layer's output read back, inside the timed region."""
+    nl = len(layers)
+    hq_n = c.q_nope.pin_memory()
+    hq_r = c.q_rope.pin_memory()
+    hv = c.v_new.pin_memory()
+    hk = c.k_new.pin_memory()
+    hout = torch.empty((nl, w.B, w.H, w.d_h), dtype=torch.float32).pin_memory()
+    steps = max(3, min(args.steps, args.e2e_steps))
+    h2d = d2h = 0
+
+    def one_step():
+        nonlocal h2d, d2h
+        h2d = d2h = 0
+        for li, L in enumerate(layers):
+            L["q_nope"].copy_(hq_n, non_blocking=True)
+            L["q_rope"].copy_(hq_r, non_blocking=True)
+            L["v_new"].copy_(hv, non_blocking=True)
+            L["k_new"].copy_(hk, non_blocking=True)
+            h2d += sum(t.numel() * t.element_size() for t in (hq_n, hq_r, hv, hk))
+            gva.gva_append_cache(dims, L["v_new"], L["k_new"], pos, None, L["cache"], tab)
+            gva.gva_decode_attention(dims, L["q_nope"], L["q_rope"], L["M"], seq, L["cache"],
+                                     tab, w.scale, L["out"], L["lse"], ws, path=path)
+            hout[li].copy_(L["out"], non_blocking=True)
+            d2h += L["out"].numel() * 4
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one_step()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    t = dist.max(time.perf_counter() - t0, dev)
+    val = bytes_layer * nl * steps * dist.world / t / 1e9
+    return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 4),
+            "how": "eager C-ABI calls per layer; pinned host->device inputs and "
+                   "device->host outputs inside the timed region"}
+
+
+# --------------------------------------------------------------------------- #
+# the oracle on the host cores
+# --------------------------------------------------------------------------- #
+def oracle_sample(w, c, budget_s):
+    """Run the fp64 oracle over whole sequences of one layer until ~budget_s elapses;
+    returns (seconds, cache bytes read, description, threads)."""
+    import numpy as np
+
+    import oracle
+    rows_all = {"contiguous": None}
+    nthr = os.cpu_count() or 1
+    oracle.set_threads(nthr)
+    V = oracle._np(c.V)
+    K = oracle._np(c.Kr)
+    done_bytes = 0
+    t0 = time.perf_counter()
+    nseq = 0
+    b = 0
+    while time.perf_counter() - t0 < budget_s or nseq == 0:
+        sample = [b % w.B]
+        if w.layout == "contiguous":
+            R = oracle.Rows("ragged", offsets=np.array([sample[0] * c.T_cap, 0]))
+        elif w.layout == "ragged":
+            R = oracle.Rows("ragged", offsets=np.array([int(c.offsets[sample[0]]), 0]))
+        else:
+            R = oracle.Rows("paged", block_table=c.block_table.numpy()[sample],
+                            page_size=w.page_size)
+        sl = c.seq_len.numpy()[sample].astype(np.int64)
+        oracle.gva_decode(c.q_nope[sample], c.q_rope[sample], c.M, sl, R, V, K, w.scale, w.base,
+                          w.G)
+        done_bytes += algorithmic_bytes(w, sl)
+        nseq += 1
+        b += 1
+    secs = time.perf_counter() - t0
+    del rows_all
+    return secs, done_bytes, nseq, oracle.get_threads()
+
+
+def oracle_baseline(w, c, budget_s=10.0):
+    secs, nbytes, nseq, thr = oracle_sample(w, c, budget_s)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": thr,
+            "kind": "oracle",
+            "sample": f"{nseq} whole sequences of one {w.name} layer (all {w.H} heads each), "
+                      f"fp64 C oracle with OpenMP over (b, h), {secs:.1f} s"}
+
+
+def run_reference(args, dist: Dist):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    if dist.world > 1 and dist.rank != 0:
+        return
+    import gva_inputs
+    w = gva_inputs.workload(args.workload)
+    c = gva_inputs.make_case(w)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(w, c, 0.0)
+    tot_s = tot_b = 0.0
+    nseq = 0
+    thr = 1
+    for _ in range(args.steps):
+        s, b, n, thr = oracle_sample(w, c, per_step)
+        tot_s += s
+        tot_b += b
+        nseq += n
+    val = tot_b / tot_s / 1e9
+    desc = (f"{nseq} whole sequences of one {w.name} layer over {args.steps} steps "
+            f"(~{per_step:.1f} s each), fp64 C oracle, OpenMP over (b, h)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: GVA decode layer B={w.B} H={w.H} G={w.G} "
+                                   f"d_h={w.d_h} d_r={w.d_r}, oracle on host cores"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": thr,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="350m",
+                    choices=["tiny", "350m", "ragged", "long", "paged"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers per step (0 = enough distinct caches to exceed L2)")
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing (s)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-gqa", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.layers == 0:
+        import gva_inputs
+        w = gva_inputs.workload(args.workload)
+        c_bytes = (w.B * (w.T or sum(w.len_range) // 2)) * (w.G * w.d_h + w.d_r) * 2
+        args.layers = max(1, min(64, math.ceil(4 * 126e6 / c_bytes)))
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    main()

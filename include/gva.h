@@ -1,0 +1,228 @@
+/*
+ * gva.h -- C ABI of libgva.so: Grouped Value Attention (GVA) decode on one B300 GPU.
+ *
+ * GVA caches only the grouped values V[.., G, d_h] and one shared, already-rotated
+ * positional key K_rope[.., d_r] per token.  Each query head h owns a map
+ * M_h in R^{d_h x d_n}; its content key K_h = V_{g(h)} M_h is never materialised.
+ * Instead the query is absorbed once per step, q~_h = q_h^nope M_h^T, and every
+ * cached position j is scored as q~_h . v_{j,g(h)} + q_h^rope . k_rope_j, followed
+ * by a softmax and the weighted sum of the same V.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [A] "GVA：KV 缓存里的 Key 其实可以不存——从 Value 里"现算"出来就行": 第二次尝试
+ *       (K_h = V_{g(h)} M_h), 关键技巧一 (absorption), 关键技巧二 (decoupled shared
+ *       RoPE), 缓存账本 (N_GVA = T G d_h + T d_r).
+ *   [S] "Grouped Value Attention: Efficient KV Caching via On-Demand Key
+ *       Reconstruction": the positional key is cached already rotated; the
+ *       absorption is exact.
+ *   [K] "KV Cache 优化（一）：从 MHA 到 MQA 与 GQA": §1 (append the current token,
+ *       then attend over all history), §4 (GQA), §6.2 (decode shapes), §7 (paging
+ *       moves bytes, not maths).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument named "device" is CUDA device memory owned by the
+ *     caller.  The library never allocates or frees memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and return after enqueueing.  The return value covers host-side
+ *     argument validation and launch errors (cudaGetLastError after the launches).
+ *   - Device pointers must be 16-byte aligned; otherwise GVA_ERR_ARG.
+ *   - No call throws.  Device-side checks (a length beyond the cache capacity, a
+ *     block-table entry out of range, a position beyond the RoPE table) never trap:
+ *     the offending token or sequence is skipped, and the first such code is kept
+ *     in a per-device status word that gva_get_device_status() reads and clears.
+ *   - Head grouping: head h reads value group g(h) = h / (H/G) (contiguous blocks).
+ *   - Positions are 0-based.  A decode over L_b cached tokens puts the query at
+ *     position t = L_b - 1 (the current token is appended before attending, [K] §1).
+ *   - RoPE: interleaved pairs (x[2i], x[2i+1]), theta_i = base^(-2i/d_r),
+ *     Rot(p): y0 = x0 cos(p theta_i) - x1 sin(p theta_i), y1 = x0 sin + x1 cos.
+ *   - Thread safety: calls on different streams may run concurrently; calls that
+ *     share a workspace must be ordered by the caller.
+ */
+#ifndef GVA_H
+#define GVA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GVA_ABI_VERSION 1
+
+typedef enum {
+    GVA_OK = 0,
+    GVA_ERR_ARG = -1,          /* invalid argument (null, misaligned, inconsistent) */
+    GVA_ERR_UNSUPPORTED = -2,  /* valid, but a shape / dtype this build does not run */
+    GVA_ERR_CUDA = -3,         /* a CUDA runtime call or a launch failed */
+    GVA_ERR_WORKSPACE = -4,    /* workspace NULL, too small or not 256-byte aligned */
+    GVA_ERR_DEVICE_CHECK = -5  /* returned by gva_get_device_status(): a device check tripped */
+} gva_status;
+
+/* Device-side check codes kept in the status word (see gva_get_device_status). */
+typedef enum {
+    GVA_DEV_OK = 0,
+    GVA_DEV_BAD_LENGTH = 1,    /* seq_len[b] < 0 or beyond the sequence's capacity */
+    GVA_DEV_BAD_PAGE = 2,      /* block-table entry outside [0, num_rows/page_size) */
+    GVA_DEV_BAD_POSITION = 3,  /* append position out of range, or beyond the RoPE table */
+    GVA_DEV_TIMEOUT = 4        /* a bounded wait inside a kernel gave up */
+} gva_device_check;
+
+typedef enum { GVA_F32 = 0, GVA_BF16 = 1 } gva_dtype;
+
+typedef enum {
+    GVA_LAYOUT_CONTIGUOUS = 0, /* row = b * T_cap + j */
+    GVA_LAYOUT_RAGGED = 1,     /* row = offsets[b] + j */
+    GVA_LAYOUT_PAGED = 2       /* row = block_table[b][j / page_size] * page_size + j % page_size */
+} gva_layout;
+
+/* Problem shape.  Supported: H % G == 0 with r = H/G in 1..8; d_h in {32, 64, 128};
+ * d_n in 8..256, a multiple of 8; d_r in {0, 8, 16, 24, 32}; 1 <= B <= 4096. */
+typedef struct {
+    int B;            /* sequences in the batch */
+    int H;            /* query heads */
+    int G;            /* value groups (GVA) or KV heads (GQA) */
+    int d_h;          /* value width (and GQA key width) */
+    int d_n;          /* content-query width (GVA) */
+    int d_r;          /* positional width (GVA); 0 = no positional slice */
+    int cache_dtype;  /* gva_dtype of the cache rows */
+    int q_dtype;      /* gva_dtype of the queries */
+} gva_dims;
+
+/* Where logical token j of sequence b is stored. */
+typedef struct {
+    int layout;              /* gva_layout */
+    long long num_rows;      /* rows allocated behind every row pointer of the cache */
+    long long T_cap;         /* contiguous: rows per sequence (capacity) */
+    const int *offsets;      /* ragged: device [B+1], row starts; capacity offsets[b+1]-offsets[b] */
+    const int *block_table;  /* paged: device [B][max_pages] physical page ids; capacity
+                                max_pages * page_size; pages hold page_size rows */
+    int max_pages;           /* paged: columns of block_table */
+    int page_size;           /* paged: tokens per page, a positive multiple of 16 */
+} gva_rows;
+
+/* GVA cache ([A] 缓存账本; [S]): V rows [G][d_h], K_rope rows [d_r] (already rotated to
+ * the row's own position), both cache_dtype, both laid out by `rows`. */
+typedef struct {
+    gva_rows rows;
+    void *V;                 /* device */
+    void *K_rope;            /* device; may be NULL when d_r == 0 */
+} gva_cache;
+
+/* Matched GQA cache for the comparator ([K] §4): explicit K and V rows [G][d_h]. */
+typedef struct {
+    gva_rows rows;
+    void *K;                 /* device */
+    void *V;                 /* device */
+} gva_kv_cache;
+
+typedef enum {
+    GVA_PATH_AUTO = 0,       /* tensor-core kernel where it applies, else CUDA cores */
+    GVA_PATH_SIMT = 1,       /* CUDA-core kernel (fp32 FMA); every supported shape */
+    GVA_PATH_MMA = 2         /* bf16 tensor-core kernel (bf16 cache only) */
+} gva_path;
+
+typedef struct {
+    int path;                /* gva_path */
+    int num_ctas;            /* decode grid size; 0 = the library's choice for this GPU */
+    int flags;               /* reserved, must be 0 */
+} gva_decode_opts;
+
+/* ------------------------------------------------------------------------- */
+
+/* Human-readable name of a gva_status or gva_device_check value (static string). */
+const char *gva_status_string(int status);
+
+/* GVA_ABI_VERSION of the loaded library. */
+int gva_abi_version(void);
+
+/* Fill a HOST table [max_pos][d_r/2][2] of fp32 (cos, sin)(p * theta_i),
+ * theta_i = base^(-2i/d_r), each computed in double and rounded once.  The caller
+ * copies it to the device and passes it as `rope_tab` below.  Reading of [A]
+ * 关键技巧二 (the pages name only the relative rotation R_{j-t}).  With d_r = 0 there
+ * is nothing to fill and host_tab may be NULL.
+ * Errors: GVA_ERR_ARG for a NULL table (d_r > 0), max_pos < 1, odd or negative d_r,
+ * base <= 0. */
+int gva_rope_table_fill(float *host_tab, int max_pos, int d_r, double base);
+
+/* Query absorption ([A] 关键技巧一, [S]):
+ *   q_tilde[b,h,:]    = scale * q_nope[b,h,:] M_h^T         M: device fp32 [H][d_h][d_n]
+ *   q_rope_rot[b,h,:] = scale * Rot(L_b - 1) q_rope[b,h,:]  (position 0 when L_b = 0)
+ * q_nope [B][H][d_n], q_rope [B][H][d_r] (q_dtype), seq_len device int [B],
+ * rope_tab device [rope_max_pos][d_r/2][2]; outputs device fp32 [B][H][d_h] and
+ * [B][H][d_r] (q_rope_rot may be NULL when d_r == 0).  gva_decode_attention runs
+ * the same step internally; this entry point exposes it for reuse and testing. */
+int gva_absorb_query(void *stream, const gva_dims *dims, const void *q_nope,
+                     const void *q_rope, const float *M, const int *seq_len,
+                     const float *rope_tab, int rope_max_pos, float scale,
+                     float *q_tilde, float *q_rope_rot);
+
+/* Cache append ([S]: cached already rotated; [K] §1: append, then attend):
+ *   V[row(b, pos[b])]      = v_new[b]                   (rounded once to cache_dtype)
+ *   K_rope[row(b, pos[b])] = Rot(pos[b]) k_rope_new[b]
+ * The rotated key is computed in fp32 in a fixed order with no fused multiply-add,
+ * y0 = (x0*c) - (x1*s), y1 = (x0*s) + (x1*c), c/s from rope_tab, then rounded once
+ * (RNE) to the cache dtype, so the stored bytes are reproducible bit for bit.
+ * v_new device fp32 [B][G][d_h]; k_rope_new device fp32 [B][d_r] (unrotated);
+ * pos device int [B]; seq_len_out (optional, device int [B]) receives pos[b] + 1
+ * and may alias pos.  A position outside the sequence's capacity or the RoPE
+ * table skips that sequence and sets GVA_DEV_BAD_POSITION. */
+int gva_append_cache(void *stream, const gva_dims *dims, const float *v_new,
+                     const float *k_rope_new, const int *pos, int *seq_len_out,
+                     const gva_cache *cache, const float *rope_tab, int rope_max_pos);
+
+/* Bytes of device workspace gva_decode_attention / gva_gqa_decode_attention need for
+ * `dims` on the current device (split-K partials and the absorbed queries).
+ * 0 on invalid dims. */
+size_t gva_decode_workspace_size(const gva_dims *dims);
+
+/* GVA decode attention over a contiguous, ragged or paged cache ([A] 关键技巧一/二;
+ * [K] §1, §6.2).  For every sequence b and head h, with t = L_b - 1 = seq_len[b] - 1:
+ *   z_j = scale * (q~_h . v_{j,g(h)} + Rot(t) q_rope_h . k_rope_j),  j < L_b
+ *   out[b,h,:] = sum_j softmax(z)_j v_{j,g(h)}     (device fp32 [B][H][d_h])
+ *   lse[b,h]   = ln sum_j exp(z_j)                 (device fp32 [B][H], or NULL)
+ * L_b = 0 gives out = 0 and lse = -inf.  Runs absorb, a split-K partial kernel
+ * (flash-decoding over 16-token slabs spread evenly over the GPU) and a
+ * log-sum-exp combine.  The workspace (device, >= gva_decode_workspace_size(dims),
+ * 256-byte aligned) is scratch, overwritten by each call.  q_nope/q_rope/M/seq_len/
+ * rope_tab as in gva_absorb_query. */
+int gva_decode_attention(void *stream, const gva_dims *dims, const void *q_nope,
+                         const void *q_rope, const float *M, const int *seq_len,
+                         const gva_cache *cache, const float *rope_tab, int rope_max_pos,
+                         float scale, float *out, float *lse, void *workspace,
+                         size_t ws_bytes);
+
+/* gva_decode_attention with kernel options (path selection, grid size); opts may be
+ * NULL.  GVA_ERR_UNSUPPORTED when the requested path cannot run `dims`. */
+int gva_decode_attention_ex(void *stream, const gva_dims *dims, const void *q_nope,
+                            const void *q_rope, const float *M, const int *seq_len,
+                            const gva_cache *cache, const float *rope_tab,
+                            int rope_max_pos, float scale, float *out, float *lse,
+                            void *workspace, size_t ws_bytes, const gva_decode_opts *opts);
+
+/* Matched GQA decode, the comparator ([K] §4): out[b,h] = softmax(scale q_h K_g^T) V_g
+ * with explicit K and V rows [G][d_h] (cache_dtype).  q device [B][H][d_h] (q_dtype);
+ * dims.d_n and dims.d_r are ignored.  Same split-K design, workspace and outputs as
+ * gva_decode_attention; opts may be NULL. */
+int gva_gqa_decode_attention(void *stream, const gva_dims *dims, const void *q,
+                             const int *seq_len, const gva_kv_cache *cache, float scale,
+                             float *out, float *lse, void *workspace, size_t ws_bytes,
+                             const gva_decode_opts *opts);
+
+/* Read and clear the current device's status word (synchronous: it waits for all
+ * work on the device).  *code_out receives a gva_device_check value.  Returns
+ * GVA_OK when no check tripped, GVA_ERR_DEVICE_CHECK when one did, GVA_ERR_CUDA on
+ * a CUDA failure. */
+int gva_get_device_status(int *code_out);
+
+/* Streaming multiprocessors of the current device (the decode grid is sized from it). */
+int gva_num_sms(void);
+
+/* cudaError_t code of the most recent CUDA failure seen by a gva_* call on the calling
+ * host thread (0 if none); it explains a GVA_ERR_CUDA return. */
+int gva_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GVA_H */

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: libgva.so loads, exports every entry point that
+include/gva.h declares, and its host-only paths behave (RoPE table, status strings,
+argument validation that returns before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gva.h")
+
+
+@pytest.fixture(scope="module")
+def gva():
+    from value_only_kv_gva_b300 import _build
+    _build.build()
+    import value_only_kv_gva_b300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gva_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gva_absorb_query", "gva_append_cache", "gva_decode_attention",
+              "gva_gqa_decode_attention", "gva_decode_workspace_size", "gva_rope_table_fill",
+              "gva_status_string", "gva_get_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(gva):
+    out = subprocess.run(["nm", "-D", "--defined-only", gva.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gva_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in declared_functions():
+        assert hasattr(gva._lib, n)
+    assert set(gva.EXPORTS) <= exported
+
+
+def test_abi_version_and_status_strings(gva):
+    assert gva.gva_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, 1, 2, 3, 4):
+        s = gva.gva_status_string(code)
+        assert s and "unknown" not in s
+    assert "unknown" in gva.gva_status_string(12345)
+
+
+@pytest.mark.parametrize("max_pos,d_r", [(1, 2), (4096, 16), (300, 24), (8192, 8), (17, 32)])
+def test_rope_table_matches_oracle_bitwise(gva, max_pos, d_r):
+    """Two independent fills of the same definition (libm cos/sin in double, one fp32
+    rounding) agree bit for bit."""
+    tab = gva.gva_rope_table_fill(max_pos, d_r, 10000.0).numpy()
+    ref = oracle.rope_table_f32(max_pos, d_r, 10000.0)
+    assert tab.shape == ref.shape and np.array_equal(tab.view(np.uint32), ref.view(np.uint32))
+
+
+def test_rope_table_rejects_bad_args(gva):
+    lib = gva._lib
+    buf = (ctypes.c_float * 64)()
+    assert lib.gva_rope_table_fill(None, 4, 8, 10000.0) == gva.GVA_ERR_ARG
+    assert lib.gva_rope_table_fill(buf, 0, 8, 10000.0) == gva.GVA_ERR_ARG
+    assert lib.gva_rope_table_fill(buf, 4, 7, 10000.0) == gva.GVA_ERR_ARG
+    assert lib.gva_rope_table_fill(buf, 4, 8, -1.0) == gva.GVA_ERR_ARG
+
+
+def _dims(gva, **kw):
+    base = dict(B=2, H=16, G=4, d_h=64, d_n=64, d_r=16, cache_dtype=1, q_dtype=1)
+    base.update(kw)
+    return gva.gva_dims(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(G=5), dict(H=64, G=4), dict(d_h=48), dict(d_r=12),
+                                 dict(d_n=4), dict(B=0), dict(cache_dtype=7), dict(B=5000)])
+def test_invalid_dims_rejected_before_cuda(gva, bad):
+    lib = gva._lib
+    d = _dims(gva, **bad)
+    fake = ctypes.c_void_p(0x10000)
+    cache = gva.gva_cache(gva.gva_rows(0, 1 << 20, 1024, None, None, 0, 0), fake, fake)
+    assert lib.gva_decode_workspace_size(ctypes.byref(d)) == 0
+    st = lib.gva_decode_attention(None, ctypes.byref(d), fake, fake, fake, fake,
+                                  ctypes.byref(cache), fake, 100, ctypes.c_float(0.1), fake,
+                                  None, fake, ctypes.c_size_t(1 << 30))
+    assert st == gva.GVA_ERR_ARG
+    st = lib.gva_append_cache(None, ctypes.byref(d), fake, fake, fake, None,
+                              ctypes.byref(cache), fake, 100)
+    assert st == gva.GVA_ERR_ARG
+
+
+def test_null_and_misaligned_pointers_rejected(gva):
+    lib = gva._lib
+    d = _dims(gva)
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    rows = gva.gva_rows(0, 2 * 1024, 1024, None, None, 0, 0)
+    good = gva.gva_cache(rows, fake, fake)
+    # NULL output
+    assert lib.gva_decode_attention(None, ctypes.byref(d), fake, fake, fake, fake,
+                                    ctypes.byref(good), fake, 100, ctypes.c_float(0.1), None,
+                                    None, fake, ctypes.c_size_t(1 << 30)) == gva.GVA_ERR_ARG
+    # misaligned output
+    assert lib.gva_decode_attention(None, ctypes.byref(d), fake, fake, fake, fake,
+                                    ctypes.byref(good), fake, 100, ctypes.c_float(0.1), odd,
+                                    None, fake, ctypes.c_size_t(1 << 30)) == gva.GVA_ERR_ARG
+    # contiguous rows smaller than B * T_cap
+    short = gva.gva_cache(gva.gva_rows(0, 100, 1024, None, None, 0, 0), fake, fake)
+    assert lib.gva_append_cache(None, ctypes.byref(d), fake, fake, fake, None,
+                                ctypes.byref(short), fake, 100) == gva.GVA_ERR_ARG
+    # paged with a page size that is not a multiple of 16
+    paged = gva.gva_cache(gva.gva_rows(2, 640, 0, None, fake, 4, 40), fake, fake)
+    assert lib.gva_append_cache(None, ctypes.byref(d), fake, fake, fake, None,
+                                ctypes.byref(paged), fake, 100) == gva.GVA_ERR_ARG
+    # ragged without offsets
+    rag = gva.gva_cache(gva.gva_rows(1, 640, 0, None, None, 0, 0), fake, fake)
+    assert lib.gva_append_cache(None, ctypes.byref(d), fake, fake, fake, None,
+                                ctypes.byref(rag), fake, 100) == gva.GVA_ERR_ARG
+    # positional key missing while d_r > 0
+    nokr = gva.gva_cache(rows, fake, None)
+    assert lib.gva_append_cache(None, ctypes.byref(d), fake, fake, fake, None,
+                                ctypes.byref(nokr), fake, 100) == gva.GVA_ERR_ARG

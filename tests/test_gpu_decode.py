@@ -1,0 +1,302 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs.  Decode within the workloads' tolerances (bf16 cache: max-abs 2e-2 and
+relative L2 1e-3; fp32 cache: 1e-5 for both); append and paged gather bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gva_inputs import make_case, make_gqa_keys, make_gqa_query, workload
+from helpers import Dev, assert_close, gva, oracle_append, oracle_decode, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _mma_ok(c):
+    """The tensor-core path's support matrix (include/gva.h: bf16 cache, d_h 64 or 128,
+    at most 8 value groups)."""
+    w = c.w
+    return w.cache_dtype == "bf16" and w.d_h in (64, 128) and w.G <= 8
+
+
+def paths_for(c):
+    return ["simt", "mma"] if _mma_ok(c) else ["simt"]
+
+
+# small variants of the five workloads: several slabs and CTAs, ragged tails
+SMALL = {
+    "tiny": {},
+    "350m": dict(T=300, B=3),
+    "ragged": dict(B=7, len_range=(1, 700)),
+    "long": dict(B=2, T=3001),
+    "paged": dict(B=5, len_range=(64, 900)),
+}
+
+
+def _step(c, path, num_ctas=0):
+    """append at t = L - 1 then decode over 0..t, on both sides"""
+    D = Dev(c)
+    pos = (c.seq_len - 1).to(torch.int32)
+    D.append(pos)
+    out, lse = D.decode(path=path, num_ctas=num_ctas)
+    assert gva().gva_get_device_status() == 0
+    V, K = oracle_append(c, pos, D.tab_h)
+    ref, ref_lse = oracle_decode(c, V, K)
+    return out, lse, ref, ref_lse, D
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("path", ["simt", "mma", "auto"])
+def test_step_small_workloads(name, path):
+    c = make_case(workload(name, **SMALL[name]))
+    if path == "mma" and not _mma_ok(c):
+        pytest.skip("tensor-core path needs a bf16 cache")
+    out, lse, ref, ref_lse, _ = _step(c, path)
+    assert_close(out, ref, c.w.cache_dtype, f"{name}/{path} out")
+    assert_close(lse, ref_lse, c.w.cache_dtype, f"{name}/{path} lse")
+
+
+@pytest.mark.parametrize("num_ctas", [1, 2, 7, 148, 1000])
+def test_split_counts(num_ctas):
+    c = make_case(workload("350m", T=257, B=3))
+    for path in paths_for(c):
+        D = Dev(c)
+        out, lse = D.decode(path=path, num_ctas=num_ctas)
+        ref, ref_lse = oracle_decode(c)
+        assert_close(out, ref, "bf16", f"{path} n={num_ctas}")
+        assert_close(lse, ref_lse, "bf16", f"{path} n={num_ctas} lse")
+
+
+@pytest.mark.parametrize("lengths", [[1, 1, 1], [15, 16, 17], [0, 33, 0], [0, 0, 0],
+                                     [100, 1, 31]])
+def test_edge_lengths(lengths):
+    c = make_case(workload("350m", T=100, B=3), lengths=lengths)
+    for path in paths_for(c):
+        D = Dev(c)
+        out, lse = D.decode(path=path)
+        ref, ref_lse = oracle_decode(c)
+        assert_close(out, ref, "bf16", f"{path} {lengths}")
+        assert_close(lse, ref_lse, "bf16", f"{path} {lengths} lse")
+        for b, L in enumerate(lengths):
+            if L == 0:
+                assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b]))
+            if L == 1:   # a single cached token returns its value (rounding only)
+                v = oracle.f64(c.V)[b * c.T_cap, :, :]
+                r = c.w.H // c.w.G
+                for h in range(c.w.H):
+                    assert np.max(np.abs(out[b, h] - v[h // r])) <= 1e-6
+
+
+@pytest.mark.parametrize("H,G,d_h,d_n,d_r", [
+    (8, 8, 64, 64, 16), (8, 4, 64, 32, 8), (8, 2, 128, 128, 24), (8, 1, 64, 64, 32),
+    (16, 2, 32, 32, 0), (4, 4, 128, 64, 16), (32, 4, 64, 128, 16), (3, 3, 64, 64, 16),
+])
+@pytest.mark.parametrize("cache", ["bf16", "f32"])
+def test_shapes(H, G, d_h, d_n, d_r, cache):
+    w = workload("350m", B=2, T=133, H=H, G=G, d_h=d_h, d_n=d_n, d_r=d_r, cache_dtype=cache,
+                 q_dtype="f32" if cache == "f32" else "bf16")
+    c = make_case(w)
+    for path in paths_for(c):
+        out, lse, ref, ref_lse, _ = _step(c, path)
+        assert_close(out, ref, cache, f"{path} out")
+        assert_close(lse, ref_lse, cache, f"{path} lse")
+
+
+def test_garbage_beyond_length_is_ignored():
+    """Slots past a sequence's end may hold anything, NaN included."""
+    c = make_case(workload("350m", T=160, B=3), lengths=[150, 37, 1])
+    ref, ref_lse = oracle_decode(c)
+    V = c.V.clone()
+    K = c.Kr.clone()
+    for b, L in enumerate(c.seq_len.tolist()):
+        V[b * c.T_cap + L:(b + 1) * c.T_cap] = float("nan")
+        K[b * c.T_cap + L:(b + 1) * c.T_cap] = float("inf")
+    c.V, c.Kr = V, K
+    for path in paths_for(c):
+        out, lse = Dev(c).decode(path=path)
+        assert_close(out, ref, "bf16", path)
+        assert_close(lse, ref_lse, "bf16", path)
+
+
+def test_paged_nan_slack():
+    c = make_case(workload("paged", B=4, len_range=(70, 300), extra_slots=40))
+    ref, ref_lse = oracle_decode(c)
+    V = c.V.clone()
+    bt = c.block_table
+    for b, L in enumerate(c.seq_len.tolist()):
+        for j in range(L, (L + 40 + 63) // 64 * 64):
+            if j // 64 < bt.shape[1] and bt[b, j // 64] >= 0:
+                V[int(bt[b, j // 64]) * 64 + j % 64] = float("nan")
+    c.V = V
+    for path in paths_for(c):
+        out, lse = Dev(c).decode(path=path)
+        assert_close(out, ref, "bf16", path)
+
+
+# --------------------------------------------------------------------------- #
+# append: bit-exact against the oracle's fp32-decided rounding
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("layout", ["contiguous", "ragged", "paged"])
+@pytest.mark.parametrize("cache", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", ["overwrite", "extend"])
+def test_append_bit_exact(layout, cache, mode):
+    name = {"contiguous": "350m", "ragged": "ragged", "paged": "paged"}[layout]
+    over = dict(B=6, cache_dtype=cache, extra_slots=3 if mode == "extend" else 0)
+    if layout == "contiguous":
+        over["T"] = 200
+    else:
+        over["len_range"] = (1, 500)
+    c = make_case(workload(name, **over))
+    D = Dev(c)
+    if mode == "overwrite":
+        pos = (c.seq_len - 1).to(torch.int32)
+        D.append(pos)
+        new_len = c.seq_len
+    else:
+        pos = c.seq_len.clone()
+        lens = D.seq_len.clone()
+        D.append(lens, seq_len_out=lens)   # pos and seq_len_out alias
+        new_len = lens.cpu()
+        assert torch.equal(new_len, c.seq_len + 1)
+    torch.cuda.synchronize()
+    assert gva().gva_get_device_status() == 0
+    V, K = oracle_append(c, pos, D.tab_h)
+    gv = oracle._np(D.V.cpu())
+    gk = oracle._np(D.Kr.cpu())
+    assert np.array_equal(gv.view(np.uint8), V.view(np.uint8))
+    assert np.array_equal(gk.view(np.uint8), K.view(np.uint8))
+    # and the decode over the extended cache matches
+    if mode == "extend":
+        out, lse = D.decode(seq_len=lens)
+        ref, ref_lse = oracle_decode(c, V, K, seq_len=new_len)
+        assert_close(out, ref, cache, "decode after extend")
+
+
+def test_absorb_matches_oracle():
+    c = make_case(workload("350m", T=50, B=5))
+    D = Dev(c)
+    w = c.w
+    qt = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    qh = torch.empty((w.B, w.H, w.d_r), device="cuda")
+    gva().gva_absorb_query(D.dims, D.q_nope, D.q_rope, D.M, D.seq_len, D.tab, w.scale, qt, qh)
+    torch.cuda.synchronize()
+    rt, rh = oracle.absorb(c.q_nope, c.q_rope, c.M, c.seq_len, w.scale, w.base)
+    for got, ref in ((qt, rt), (qh, rh)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g - ref)) <= 2e-6 * max(1.0, np.max(np.abs(ref)))
+
+
+# --------------------------------------------------------------------------- #
+# device-side checks: no trap, a status code, the other sequences still right
+# --------------------------------------------------------------------------- #
+def test_length_beyond_capacity_is_reported():
+    c = make_case(workload("350m", T=64, B=3), lengths=[64, 20, 10])
+    D = Dev(c)
+    bad = torch.tensor([64, 9999, 10], dtype=torch.int32, device="cuda")
+    out, lse = D.decode(seq_len=bad)
+    assert gva().gva_get_device_status() == gva().GVA_DEV_BAD_LENGTH
+    ref, ref_lse = oracle_decode(c)
+    for b in (0, 2):
+        assert_close(out[b], ref[b], "bf16", f"b={b}")
+    assert np.all(out[1] == 0) and np.isneginf(lse[1]).all()
+    assert gva().gva_get_device_status() == 0
+
+
+def test_bad_page_is_reported():
+    c = make_case(workload("paged", B=3, len_range=(100, 200)))
+    D = Dev(c)
+    D.block_table[1, 0] = 10 ** 6
+    D.decode()
+    assert gva().gva_get_device_status() == gva().GVA_DEV_BAD_PAGE
+
+
+def test_append_bad_position_is_reported():
+    c = make_case(workload("350m", T=32, B=2))
+    D = Dev(c)
+    D.append(torch.tensor([5, 32], dtype=torch.int32))
+    torch.cuda.synchronize()
+    assert gva().gva_get_device_status() == gva().GVA_DEV_BAD_POSITION
+
+
+def test_host_argument_errors():
+    c = make_case(workload("350m", T=32, B=2))
+    D = Dev(c)
+    g = gva()
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    out = torch.empty((2, 16, 64), device="cuda")
+    with pytest.raises(g.GvaError) as e:
+        g.gva_decode_attention(D.dims, D.q_nope, D.q_rope, D.M, D.seq_len, D.cache, D.tab,
+                               0.1, out, None, small)
+    assert e.value.status == g.GVA_ERR_WORKSPACE
+    bad = g.Dims(2, 16, 5, 64, 64, 16)
+    with pytest.raises(g.GvaError) as e:
+        g.gva_decode_attention(bad, D.q_nope, D.q_rope, D.M, D.seq_len, D.cache, D.tab, 0.1,
+                               out, None, D.ws)
+    assert e.value.status == g.GVA_ERR_ARG
+    f32 = workload("tiny")
+    cf = make_case(f32)
+    Df = Dev(cf)
+    with pytest.raises(g.GvaError) as e:
+        Df.decode(path="mma")
+    assert e.value.status == g.GVA_ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------------------- #
+# GQA comparator
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("name", ["350m", "ragged", "paged"])
+def test_gqa_comparator(name):
+    c = make_case(workload(name, **SMALL[name]))
+    K = make_gqa_keys(c)
+    q = make_gqa_query(c)
+    D = Dev(c)
+    g = gva()
+    kv = g.KVCache(D.rows, K.cuda(), D.V)
+    w = c.w
+    scale = 1.0 / np.sqrt(w.d_h)
+    ref, ref_lse = oracle.gqa_decode(q, c.seq_len, oracle_rows(c), K, c.V, scale, w.G)
+    for path in paths_for(c):
+        out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+        lse = torch.empty((w.B, w.H), device="cuda")
+        g.gva_gqa_decode_attention(D.dims, q.cuda(), D.seq_len, kv, scale, out, lse, D.ws,
+                                   path=path)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), ref, "bf16", f"gqa {path}")
+        assert_close(lse.cpu().numpy(), ref_lse, "bf16", f"gqa {path} lse")
+
+
+# --------------------------------------------------------------------------- #
+# CUDA graphs: the calls can be captured (torch's default global capture mode)
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("path", ["simt", "mma"])
+def test_graph_capture_and_replay(path):
+    c = make_case(workload("350m", T=200, B=3))
+    D = Dev(c)
+    w = c.w
+    g = gva()
+    pos = (c.seq_len - 1).to(torch.int32).cuda()
+    out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    lse = torch.empty((w.B, w.H), device="cuda")
+
+    def step():
+        g.gva_append_cache(D.dims, D.v_new, D.k_new, pos, None, D.cache, D.tab)
+        g.gva_decode_attention(D.dims, D.q_nope, D.q_rope, D.M, D.seq_len, D.cache, D.tab,
+                               w.scale, out, lse, D.ws, path=path)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step()                      # first call eagerly (per-device set-up)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+            step()                  # second call follows a kernel node (programmatic edge)
+    out.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert gva().gva_get_device_status() == 0
+    V, K = oracle_append(c, pos.cpu(), D.tab_h)
+    ref, ref_lse = oracle_decode(c, V, K)
+    assert_close(out.cpu().numpy(), ref, "bf16", f"graph {path}")
+    assert_close(lse.cpu().numpy(), ref_lse, "bf16", f"graph {path} lse")

@@ -1,0 +1,302 @@
+"""Python binding of libgva.so -- Grouped Value Attention decode on a B300 (sm_103a).
+
+Argument marshalling only: every function here has the name of a C entry point in
+``include/gva.h``, checks that the torch tensors it is handed have the device,
+dtype and layout the C ABI documents, and passes their data pointers and the
+current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback.  Importing fails when ``libgva.so`` is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgva.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+        "or `python -m value_only_kv_gva_b300._build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# --------------------------------------------------------------------------- #
+# C structs
+# --------------------------------------------------------------------------- #
+GVA_OK, GVA_ERR_ARG, GVA_ERR_UNSUPPORTED, GVA_ERR_CUDA, GVA_ERR_WORKSPACE, \
+    GVA_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
+GVA_DEV_OK, GVA_DEV_BAD_LENGTH, GVA_DEV_BAD_PAGE, GVA_DEV_BAD_POSITION, \
+    GVA_DEV_TIMEOUT = 0, 1, 2, 3, 4
+GVA_F32, GVA_BF16 = 0, 1
+LAYOUTS = {"contiguous": 0, "ragged": 1, "paged": 2}
+PATHS = {"auto": 0, "simt": 1, "mma": 2}
+
+
+class gva_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("G", ctypes.c_int),
+                ("d_h", ctypes.c_int), ("d_n", ctypes.c_int), ("d_r", ctypes.c_int),
+                ("cache_dtype", ctypes.c_int), ("q_dtype", ctypes.c_int)]
+
+
+class gva_rows(ctypes.Structure):
+    _fields_ = [("layout", ctypes.c_int), ("num_rows", ctypes.c_longlong),
+                ("T_cap", ctypes.c_longlong), ("offsets", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("max_pages", ctypes.c_int),
+                ("page_size", ctypes.c_int)]
+
+
+class gva_cache(ctypes.Structure):
+    _fields_ = [("rows", gva_rows), ("V", ctypes.c_void_p), ("K_rope", ctypes.c_void_p)]
+
+
+class gva_kv_cache(ctypes.Structure):
+    _fields_ = [("rows", gva_rows), ("K", ctypes.c_void_p), ("V", ctypes.c_void_p)]
+
+
+class gva_decode_opts(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("flags", ctypes.c_int)]
+
+
+_P, _I, _F, _D, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
+_PD, _PC = ctypes.POINTER(gva_dims), ctypes.POINTER(gva_cache)
+_PKV, _PO = ctypes.POINTER(gva_kv_cache), ctypes.POINTER(gva_decode_opts)
+
+_lib.gva_status_string.restype = ctypes.c_char_p
+_lib.gva_status_string.argtypes = [_I]
+_lib.gva_abi_version.restype = _I
+_lib.gva_num_sms.restype = _I
+_lib.gva_rope_table_fill.argtypes = [_P, _I, _I, _D]
+_lib.gva_absorb_query.argtypes = [_P, _PD, _P, _P, _P, _P, _P, _I, _F, _P, _P]
+_lib.gva_append_cache.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I]
+_lib.gva_decode_workspace_size.restype = _Z
+_lib.gva_decode_workspace_size.argtypes = [_PD]
+_lib.gva_decode_attention.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I, _F, _P, _P, _P, _Z]
+_lib.gva_decode_attention_ex.argtypes = _lib.gva_decode_attention.argtypes + [_PO]
+_lib.gva_gqa_decode_attention.argtypes = [_P, _PD, _P, _P, _PKV, _F, _P, _P, _P, _Z, _PO]
+_lib.gva_get_device_status.argtypes = [ctypes.POINTER(_I)]
+_lib.gva_last_cuda_error.restype = _I
+
+EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_table_fill",
+           "gva_absorb_query", "gva_append_cache", "gva_decode_workspace_size",
+           "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
+           "gva_get_device_status", "gva_last_cuda_error"]
+
+
+class GvaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        extra = ""
+        if status == GVA_ERR_CUDA:
+            extra = f", cudaError {int(_lib.gva_last_cuda_error())}"
+        super().__init__(f"{what}: {gva_status_string(status)} ({status}{extra})")
+        self.status = status
+
+
+def _check(status: int, what: str) -> None:
+    if status != GVA_OK:
+        raise GvaError(status, what)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GVA_F32
+    if t.dtype == torch.bfloat16:
+        return GVA_BF16
+    raise TypeError(f"dtype {t.dtype} is not fp32 or bf16")
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# --------------------------------------------------------------------------- #
+# argument holders
+# --------------------------------------------------------------------------- #
+@dataclass
+class Dims:
+    B: int
+    H: int
+    G: int
+    d_h: int
+    d_n: int = 0
+    d_r: int = 0
+    cache_dtype: int = GVA_BF16
+    q_dtype: int = GVA_BF16
+
+    def c(self) -> gva_dims:
+        return gva_dims(self.B, self.H, self.G, self.d_h, self.d_n, self.d_r,
+                        self.cache_dtype, self.q_dtype)
+
+
+@dataclass
+class Rows:
+    """Where token j of sequence b is stored (gva_rows)."""
+    layout: str
+    num_rows: int
+    T_cap: int = 0
+    offsets: torch.Tensor | None = None       # int32 [B+1] on the device (ragged)
+    block_table: torch.Tensor | None = None   # int32 [B, max_pages] on the device (paged)
+    page_size: int = 0
+
+    def c(self) -> gva_rows:
+        r = gva_rows()
+        r.layout = LAYOUTS[self.layout]
+        r.num_rows = int(self.num_rows)
+        r.T_cap = int(self.T_cap)
+        r.offsets = _ptr(self.offsets, torch.int32, "offsets")
+        r.block_table = _ptr(self.block_table, torch.int32, "block_table")
+        r.max_pages = int(self.block_table.shape[1]) if self.block_table is not None else 0
+        r.page_size = int(self.page_size)
+        return r
+
+
+@dataclass
+class Cache:
+    """GVA cache: V rows [G, d_h] and K_rope rows [d_r] on the device (gva_cache)."""
+    rows: Rows
+    V: torch.Tensor
+    K_rope: torch.Tensor | None
+
+    def c(self) -> gva_cache:
+        return gva_cache(self.rows.c(), _ptr(self.V, None, "V"),
+                         _ptr(self.K_rope, None, "K_rope") if self.K_rope is not None
+                         and self.K_rope.numel() > 0 else None)
+
+
+@dataclass
+class KVCache:
+    """GQA comparator cache: explicit K and V rows [G, d_h] (gva_kv_cache)."""
+    rows: Rows
+    K: torch.Tensor
+    V: torch.Tensor
+
+    def c(self) -> gva_kv_cache:
+        return gva_kv_cache(self.rows.c(), _ptr(self.K, None, "K"), _ptr(self.V, None, "V"))
+
+
+def _opts(path: str, num_ctas: int) -> gva_decode_opts:
+    return gva_decode_opts(PATHS[path], int(num_ctas), 0)
+
+
+# --------------------------------------------------------------------------- #
+# entry points (same names as the C ABI)
+# --------------------------------------------------------------------------- #
+def gva_status_string(status: int) -> str:
+    return _lib.gva_status_string(int(status)).decode()
+
+
+def gva_abi_version() -> int:
+    return int(_lib.gva_abi_version())
+
+
+def gva_num_sms() -> int:
+    return int(_lib.gva_num_sms())
+
+
+def gva_rope_table_fill(max_pos: int, d_r: int, base: float = 10000.0) -> torch.Tensor:
+    """Host fp32 table [max_pos, d_r/2, 2] of (cos, sin)(p * base^(-2i/d_r))."""
+    tab = torch.empty((max_pos, max(d_r // 2, 0), 2), dtype=torch.float32)
+    ptr = ctypes.c_void_p(tab.data_ptr()) if tab.numel() else None
+    _check(_lib.gva_rope_table_fill(ptr, int(max_pos), int(d_r), float(base)),
+           "gva_rope_table_fill")
+    return tab
+
+
+def gva_last_cuda_error() -> int:
+    return int(_lib.gva_last_cuda_error())
+
+
+def gva_absorb_query(dims: Dims, q_nope, q_rope, M, seq_len, rope_tab, scale: float,
+                     q_tilde, q_rope_rot, stream=None) -> None:
+    d = dims.c()
+    _check(_lib.gva_absorb_query(
+        _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
+        _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
+        _ptr(seq_len, torch.int32, "seq_len"),
+        _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(q_tilde, torch.float32, "q_tilde"),
+        _ptr(q_rope_rot, torch.float32, "q_rope_rot") if dims.d_r else None),
+        "gva_absorb_query")
+
+
+def gva_append_cache(dims: Dims, v_new, k_rope_new, pos, seq_len_out, cache: Cache,
+                     rope_tab, stream=None) -> None:
+    d = dims.c()
+    cc = cache.c()
+    _check(_lib.gva_append_cache(
+        _stream(stream), ctypes.byref(d), _ptr(v_new, torch.float32, "v_new"),
+        _ptr(k_rope_new, torch.float32, "k_rope_new") if dims.d_r else None,
+        _ptr(pos, torch.int32, "pos"), _ptr(seq_len_out, torch.int32, "seq_len_out"),
+        ctypes.byref(cc), _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0), "gva_append_cache")
+
+
+def gva_decode_workspace_size(dims: Dims) -> int:
+    d = dims.c()
+    return int(_lib.gva_decode_workspace_size(ctypes.byref(d)))
+
+
+def gva_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, rope_tab,
+                         scale: float, out, lse, workspace, path: str = "auto",
+                         num_ctas: int = 0, stream=None) -> None:
+    d = dims.c()
+    cc = cache.c()
+    o = _opts(path, num_ctas)
+    _check(_lib.gva_decode_attention_ex(
+        _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
+        _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
+        _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc),
+        _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+        ctypes.byref(o)), "gva_decode_attention")
+
+
+def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: float, out, lse,
+                             workspace, path: str = "auto", num_ctas: int = 0,
+                             stream=None) -> None:
+    d = dims.c()
+    cc = cache.c()
+    o = _opts(path, num_ctas)
+    _check(_lib.gva_gqa_decode_attention(
+        _stream(stream), ctypes.byref(d), _ptr(q, None, "q"),
+        _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc), float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+        ctypes.byref(o)), "gva_gqa_decode_attention")
+
+
+def gva_get_device_status() -> int:
+    """Read and clear the device status word (synchronises the device)."""
+    code = ctypes.c_int(0)
+    st = _lib.gva_get_device_status(ctypes.byref(code))
+    if st not in (GVA_OK, GVA_ERR_DEVICE_CHECK):
+        raise GvaError(st, "gva_get_device_status")
+    return int(code.value)
+
+
+def workspace(dims: Dims, device=None) -> torch.Tensor:
+    """Allocate a decode workspace (uint8, 256-byte aligned by the caching allocator)."""
+    n = gva_decode_workspace_size(dims)
+    if n == 0:
+        raise GvaError(GVA_ERR_ARG, "gva_decode_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,143 @@
+// common.cuh -- device helpers shared by the GVA decode kernels (one translation unit).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gva.h"
+
+namespace gva {
+
+constexpr int SLAB = 16;              // tokens per slab: unit of the split-K partition
+constexpr int MAX_B = 4096;           // largest batch the in-kernel prefix scan handles
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// First device-side check code (gva_device_check), 0 when none tripped.
+__device__ int g_status;
+
+__device__ __forceinline__ void dev_report(int code) { atomicCAS(&g_status, 0, code); }
+
+// Programmatic dependent launch: wait until the preceding grid in the stream has
+// completed and its writes are visible; then let the next grid start its prologue.
+// Every kernel waits before its first global read, so a grid is only ever released
+// once everything before it has finished.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Where logical token j of sequence b lives (mirror of gva_rows plus the page count).
+struct RowsDev {
+    int layout;
+    long long num_rows;
+    long long T_cap;
+    const int *offsets;
+    const int *block_table;
+    int max_pages;
+    int page_size;
+    int num_pages;
+};
+
+__device__ __forceinline__ long long seq_capacity(const RowsDev &R, int b) {
+    if (R.layout == GVA_LAYOUT_CONTIGUOUS) return R.T_cap;
+    if (R.layout == GVA_LAYOUT_RAGGED) return (long long)R.offsets[b + 1] - R.offsets[b];
+    return (long long)R.max_pages * R.page_size;
+}
+
+// A length is usable when it fits the sequence's capacity and its rows exist.
+__device__ __forceinline__ bool length_ok(const RowsDev &R, int b, long long L) {
+    if (L < 0 || L > seq_capacity(R, b)) return false;
+    if (R.layout == GVA_LAYOUT_RAGGED)
+        return R.offsets[b] >= 0 && (long long)R.offsets[b] + L <= R.num_rows;
+    return true;
+}
+
+// Storage row of token j (0 <= j < capacity) of sequence b, or -1 when the page id
+// read from the block table is out of range.
+__device__ __forceinline__ long long row_of(const RowsDev &R, int b, long long j) {
+    if (R.layout == GVA_LAYOUT_CONTIGUOUS) return (long long)b * R.T_cap + j;
+    if (R.layout == GVA_LAYOUT_RAGGED) return (long long)R.offsets[b] + j;
+    const int page = R.block_table[(long long)b * R.max_pages + j / R.page_size];
+    if (page < 0 || page >= R.num_pages) return -1;
+    return (long long)page * R.page_size + j % R.page_size;
+}
+
+// Flat split-K partition over slabs.  Sequence b has n_b = ceil(L_b / 16) slabs
+// starting at flat index F[b] (exclusive prefix); S = F[B].  CTA c of n owns flat
+// slabs [c*S/n, (c+1)*S/n): equal shares of the whole batch's cache, whatever the
+// length mix.  Partials of (CTA c, sequence b) go to slot c + b, which is unique
+// along the monotone walk of (c, b) pairs.
+struct Part {
+    long long S;
+    int n;
+    __device__ __forceinline__ long long start(int c) const { return (long long)c * S / n; }
+    // the CTA that owns flat slab s (0 <= s < S)
+    __device__ __forceinline__ int cta_of(long long s) const {
+        return (int)(((s + 1) * (long long)n - 1) / S);
+    }
+};
+
+// Block-wide: validated lengths into Ls[0..B), exclusive slab prefix into F[0..B].
+// Invalid lengths count as 0 and set GVA_DEV_BAD_LENGTH when `report` is set.
+__device__ void build_prefix(const int *seq_len, const RowsDev &R, int B, int *Ls, int *F,
+                             bool report) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        int L = seq_len[b];
+        if (!length_ok(R, b, L)) {
+            if (report) dev_report(GVA_DEV_BAD_LENGTH);
+            L = 0;
+        }
+        Ls[b] = L;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (B + 31) / 32;
+        const int lo = lane * per, hi = min(lo + per, B);
+        int sum = 0;
+        for (int b = lo; b < hi; ++b) sum += (Ls[b] + SLAB - 1) / SLAB;
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int b = lo; b < hi; ++b) {
+            F[b] = run;
+            run += (Ls[b] + SLAB - 1) / SLAB;
+        }
+        if (lane == 31) F[B] = incl;
+    }
+    __syncthreads();
+}
+
+// Largest b with F[b] <= s (F non-decreasing, F[0] = 0 <= s < F[B]); that sequence
+// is non-empty and contains flat slab s.
+__device__ __forceinline__ int seq_of_slab(const int *F, int B, long long s) {
+    int lo = 0, hi = B;  // invariant: F[lo] <= s < F[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (F[mid] <= s) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) {
+    return (x + a - 1) / a * a;
+}
+
+}  // namespace gva

@@ -1,0 +1,316 @@
+// decode_simt.cuh -- split-K decode on CUDA cores (fp32 FMA), for every supported
+// shape and both cache dtypes, plus the log-sum-exp combine shared by all decode paths.
+#pragma once
+
+#include "common.cuh"
+
+namespace gva {
+
+// Parameters of one decode launch (GVA, or the GQA comparator when Kc != Vc).
+struct DecodeParams {
+    int B, H, G, r, d_h, d_r;
+    const int *seq_len;
+    RowsDev R;
+    const void *Kc;         // rows scored against the content query: V (GVA) or K (GQA)
+    const void *Vc;         // value rows [G][d_h]
+    const void *Krope;      // positional key rows [d_r] (GVA, d_r > 0)
+    const void *qc;         // content query [B][H][d_h]
+    int qc_f32;             // 1: fp32, 0: bf16
+    float qc_scale;         // multiplies qc when loaded (softmax scale in log2 units)
+    const float *qr;        // positional query [B][H][d_r], already scaled (GVA)
+    float *out;             // [B][H][d_h]
+    float *lse;             // [B][H] or null
+    float *part_o;          // [slots][H][d_h]
+    float *part_ml;         // [slots][H][2]  (running max in log2 units, sum)
+    int n_ctas;
+};
+
+constexpr int SIMT_THREADS = 256;
+constexpr int SIMT_MAXQ = 16;   // (H * d_h) / SIMT_THREADS outputs per thread, at most
+
+// Shared-memory plan of the SIMT kernel (bytes), padded rows for conflict-free reads.
+struct SimtSmem {
+    size_t ls, f, qc, qr, s, m, l, a, tk, tv, tr, total;
+    int rs_k, rs_r;  // row strides of the key/value tile and the positional tile, 4-byte words
+};
+
+__host__ __device__ inline SimtSmem simt_smem(int B, int H, int G, int d_h, int d_r,
+                                              int elem, bool gqa) {
+    SimtSmem s;
+    size_t o = 0;
+    s.ls = o; o += sizeof(int) * B;
+    s.f = o; o += sizeof(int) * (B + 1);
+    o = align_up(o, 16);
+    s.qc = o; o += sizeof(float) * H * d_h;
+    s.qr = o; o += sizeof(float) * H * (d_r > 0 ? d_r : 1);
+    s.s = o; o += sizeof(float) * H * SLAB;
+    s.m = o; o += sizeof(float) * H;
+    s.l = o; o += sizeof(float) * H;
+    s.a = o; o += sizeof(float) * H;
+    o = align_up(o, 16);
+    s.rs_k = (G * d_h * elem) / 4 + 1;
+    s.rs_r = (d_r * elem) / 4 + 1;
+    s.tk = o; o += sizeof(int) * SLAB * s.rs_k;
+    s.tv = s.tk;
+    if (gqa) { s.tv = o; o += sizeof(int) * SLAB * s.rs_k; }
+    s.tr = o; o += sizeof(int) * SLAB * (d_r > 0 ? s.rs_r : 1);
+    s.total = align_up(o, 16);
+    return s;
+}
+
+// Copy `nv` contiguous rows of `row_words` 4-byte words from global memory into a
+// tile with row stride `rs` words; rows nv..SLAB-1 are zeroed (a cache slot past a
+// sequence's end may hold anything, including NaN).
+__device__ __forceinline__ void load_rows(uint32_t *dst, const uint32_t *src, int nv,
+                                          int row_words, int rs) {
+    const int n4 = row_words / 4;  // 16-byte vectors per row
+    for (int e = threadIdx.x; e < SLAB * n4; e += blockDim.x) {
+        const int t = e / n4, c = e % n4;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (t < nv) v = reinterpret_cast<const uint4 *>(src + (long long)t * row_words)[c];
+        uint32_t *d = dst + t * rs + 4 * c;
+        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+    }
+}
+
+template <typename CT>
+__device__ __forceinline__ float tile_elem(const uint32_t *tile, int rs, int t, int e) {
+    return to_f<CT>(reinterpret_cast<const CT *>(tile + t * rs)[e]);
+}
+
+// One CTA walks its share [c*S/n, (c+1)*S/n) of the batch's slabs.  For each slab:
+// scores for all (head, token) pairs, an online-softmax update per head, then the
+// probability-weighted value sum per (head, dimension).  A sequence entirely inside
+// the CTA's share is finished here; otherwise its (o, m, l) partial goes to slot c+b.
+template <typename CT, bool GQA>
+__global__ void __launch_bounds__(SIMT_THREADS) decode_simt_kernel(const DecodeParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int B = p.B, H = p.H, d_h = p.d_h, r = p.r;
+    const int d_r = GQA ? 0 : p.d_r;
+    const int W = p.G * d_h;
+    const SimtSmem L = simt_smem(B, H, p.G, d_h, d_r, (int)sizeof(CT), GQA);
+    int *Ls = reinterpret_cast<int *>(smem + L.ls);
+    int *F = reinterpret_cast<int *>(smem + L.f);
+    float *qc_s = reinterpret_cast<float *>(smem + L.qc);
+    float *qr_s = reinterpret_cast<float *>(smem + L.qr);
+    float *S = reinterpret_cast<float *>(smem + L.s);
+    float *m_s = reinterpret_cast<float *>(smem + L.m);
+    float *l_s = reinterpret_cast<float *>(smem + L.l);
+    float *a_s = reinterpret_cast<float *>(smem + L.a);
+    uint32_t *tk = reinterpret_cast<uint32_t *>(smem + L.tk);
+    uint32_t *tv = reinterpret_cast<uint32_t *>(smem + L.tv);
+    uint32_t *tr = reinterpret_cast<uint32_t *>(smem + L.tr);
+
+    build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0);
+    const Part P{F[B], p.n_ctas};
+    if (P.S == 0) return;
+    const int c = blockIdx.x;
+    const long long s0 = P.start(c), s1 = P.start(c + 1);
+    if (s0 >= s1) return;
+
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int nq = (H * d_h + nthr - 1) / nthr;
+    const int row_words = W * (int)sizeof(CT) / 4;
+    const int rrow_words = d_r * (int)sizeof(CT) / 4;
+    const CT *Kg = reinterpret_cast<const CT *>(p.Kc);
+    const CT *Vg = reinterpret_cast<const CT *>(p.Vc);
+    const CT *Rg = reinterpret_cast<const CT *>(p.Krope);
+
+    int b = seq_of_slab(F, B, s0);
+    long long s = s0;
+    while (s < s1) {
+        while (F[b + 1] <= s) ++b;
+        const long long seg_end = min(s1, (long long)F[b + 1]);
+        const int Lb = Ls[b];
+        // ---- per-sequence state ----
+        for (int e = tid; e < H * d_h; e += nthr) {
+            const long long q = (long long)b * H * d_h + e;
+            qc_s[e] = p.qc_scale * (p.qc_f32 ? reinterpret_cast<const float *>(p.qc)[q]
+                                             : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.qc)[q]));
+        }
+        for (int e = tid; e < H * d_r; e += nthr) qr_s[e] = p.qr[(long long)b * H * d_r + e];
+        for (int h = tid; h < H; h += nthr) { m_s[h] = -INFINITY; l_s[h] = 0.f; }
+        float o[SIMT_MAXQ];
+#pragma unroll
+        for (int u = 0; u < SIMT_MAXQ; ++u) o[u] = 0.f;
+        __syncthreads();
+
+        for (; s < seg_end; ++s) {
+            const long long j0 = (long long)(s - F[b]) * SLAB;
+            int nv = (int)min((long long)SLAB, (long long)Lb - j0);
+            const long long row0 = row_of(p.R, b, j0);
+            if (row0 < 0) {  // corrupt block-table entry: skip the slab's tokens
+                if (tid == 0) dev_report(GVA_DEV_BAD_PAGE);
+                nv = 0;
+            }
+            const long long rr = row0 < 0 ? 0 : row0;
+            load_rows(tk, reinterpret_cast<const uint32_t *>(Kg + rr * W), nv, row_words, L.rs_k);
+            if (GQA) load_rows(tv, reinterpret_cast<const uint32_t *>(Vg + rr * W), nv, row_words, L.rs_k);
+            if (d_r > 0) load_rows(tr, reinterpret_cast<const uint32_t *>(Rg + rr * d_r), nv, rrow_words, L.rs_r);
+            __syncthreads();
+            // scores, log2 units
+            for (int e = tid; e < H * SLAB; e += nthr) {
+                const int h = e / SLAB, t = e % SLAB, g = h / r;
+                float z = -INFINITY;
+                if (t < nv) {
+                    float acc = 0.f;
+                    const float *q = qc_s + h * d_h;
+                    for (int i = 0; i < d_h; ++i) acc = fmaf(q[i], tile_elem<CT>(tk, L.rs_k, t, g * d_h + i), acc);
+                    const float *qr = qr_s + h * d_r;
+                    for (int i = 0; i < d_r; ++i) acc = fmaf(qr[i], tile_elem<CT>(tr, L.rs_r, t, i), acc);
+                    z = acc;
+                }
+                S[e] = z;
+            }
+            __syncthreads();
+            // online softmax, one thread per head
+            for (int h = tid; h < H; h += nthr) {
+                float mx = -INFINITY;
+                for (int t = 0; t < SLAB; ++t) mx = fmaxf(mx, S[h * SLAB + t]);
+                const float m_old = m_s[h];
+                const float m_new = fmaxf(m_old, mx);
+                const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+                float sum = 0.f;
+                for (int t = 0; t < SLAB; ++t) {
+                    const float zz = S[h * SLAB + t];
+                    const float pr = (zz == -INFINITY) ? 0.f : exp2f(zz - m_new);
+                    S[h * SLAB + t] = pr;
+                    sum += pr;
+                }
+                l_s[h] = l_s[h] * alpha + sum;
+                m_s[h] = m_new;
+                a_s[h] = alpha;
+            }
+            __syncthreads();
+            // probability-weighted values
+#pragma unroll
+            for (int u = 0; u < SIMT_MAXQ; ++u) {
+                if (u < nq) {
+                    const int e = tid + u * nthr;
+                    if (e < H * d_h) {
+                        const int h = e / d_h, i = e % d_h, g = h / r;
+                        float acc = o[u] * a_s[h];
+                        for (int t = 0; t < nv; ++t)
+                            acc = fmaf(S[h * SLAB + t], tile_elem<CT>(tv, L.rs_k, t, g * d_h + i), acc);
+                        o[u] = acc;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        // ---- segment end ----
+        const bool whole = F[b] >= s0 && F[b + 1] <= s1;
+        const long long slot = (long long)c + b;
+#pragma unroll
+        for (int u = 0; u < SIMT_MAXQ; ++u) {
+            if (u < nq) {
+                const int e = tid + u * nthr;
+                if (e < H * d_h) {
+                    const int h = e / d_h;
+                    if (whole) {
+                        const float l = l_s[h];
+                        p.out[(long long)b * H * d_h + e] = l > 0.f ? o[u] / l : 0.f;
+                    } else {
+                        p.part_o[slot * H * d_h + e] = o[u];
+                    }
+                }
+            }
+        }
+        for (int h = tid; h < H; h += nthr) {
+            if (whole) {
+                const float l = l_s[h];
+                if (p.lse) p.lse[(long long)b * H + h] = l > 0.f ? (m_s[h] + log2f(l)) * LN2 : -INFINITY;
+            } else {
+                p.part_ml[(slot * H + h) * 2] = m_s[h];
+                p.part_ml[(slot * H + h) * 2 + 1] = l_s[h];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// --------------------------------------------------------------------------- //
+// Log-sum-exp combine of split-K partials (flash-decoding):
+//   m* = max_s m_s,  o = sum_s 2^(m_s - m*) o_s / sum_s 2^(m_s - m*) l_s,
+//   lse = (m* + log2 sum_s 2^(m_s - m*) l_s) ln 2.
+// One CTA per (b, h), one thread per value dimension.  Sequences owned by a single
+// CTA were finished by the decode kernel; empty sequences get out = 0, lse = -inf.
+// --------------------------------------------------------------------------- //
+struct CombineParams {
+    int B, H, d_h;
+    const int *seq_len;
+    RowsDev R;
+    const float *part_o;
+    const float *part_ml;
+    float *out;
+    float *lse;
+    int n_ctas;
+};
+
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int i = threadIdx.x;
+    __shared__ long long red[4];
+    __shared__ long long tot_s;
+    // F_b and S: sums of the validated slab counts (same rule as build_prefix)
+    long long before = 0, total = 0;
+    for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
+        int L = p.seq_len[bb];
+        if (!length_ok(p.R, bb, L)) L = 0;
+        const long long n = (L + SLAB - 1) / SLAB;
+        total += n;
+        if (bb < b) before += n;
+    }
+    // block reduce (blockDim.x <= 128)
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    const int warp = threadIdx.x / 32, nw = (blockDim.x + 31) / 32;
+    __shared__ long long red2[4];
+    if ((threadIdx.x & 31) == 0) { red[warp] = before; red2[warp] = total; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long a = 0, t = 0;
+        for (int w = 0; w < nw; ++w) { a += red[w]; t += red2[w]; }
+        red[0] = a;
+        tot_s = t;
+    }
+    __syncthreads();
+    const long long Fb = red[0], S = tot_s;
+    int Lb = p.seq_len[b];
+    if (!length_ok(p.R, b, Lb)) Lb = 0;
+    const long long nb = (Lb + SLAB - 1) / SLAB;
+    float *out = p.out + ((long long)b * p.H + h) * p.d_h;
+    if (nb == 0) {
+        if (i < p.d_h) out[i] = 0.f;
+        if (i == 0 && p.lse) p.lse[(long long)b * p.H + h] = -INFINITY;
+        return;
+    }
+    const Part P{S, p.n_ctas};
+    const int c_lo = P.cta_of(Fb), c_hi = P.cta_of(Fb + nb - 1);
+    if (c_lo == c_hi) return;
+    float mstar = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        if (P.start(c) == P.start(c + 1)) continue;
+        mstar = fmaxf(mstar, p.part_ml[(((long long)c + b) * p.H + h) * 2]);
+    }
+    float acc = 0.f, den = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        if (P.start(c) == P.start(c + 1)) continue;
+        const long long slot = (long long)c + b;
+        const float m = p.part_ml[(slot * p.H + h) * 2];
+        const float l = p.part_ml[(slot * p.H + h) * 2 + 1];
+        const float w = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
+        den += w * l;
+        if (i < p.d_h) acc += w * p.part_o[(slot * p.H + h) * p.d_h + i];
+    }
+    if (i < p.d_h) out[i] = den > 0.f ? acc / den : 0.f;
+    if (i == 0 && p.lse) p.lse[(long long)b * p.H + h] = den > 0.f ? (mstar + log2f(den)) * LN2 : -INFINITY;
+}
+
+}  // namespace gva

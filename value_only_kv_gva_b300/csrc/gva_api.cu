@@ -1,0 +1,506 @@
+// gva_api.cu -- the C ABI of libgva.so (declared in include/gva.h): host-side
+// validation, workspace planning and kernel launches.  One translation unit holds
+// every kernel so that they share the device status word.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "gva.h"
+#include "common.cuh"
+#include "launch.cuh"
+#include "prep_kernels.cuh"
+#include "decode_simt.cuh"
+#include "decode_mma.cuh"
+
+using namespace gva;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr int CTAS_PER_SM_CAP = 8;   // the workspace is sized for this many CTAs per SM
+
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Make the stream's device current for this library's runtime (the caller's runtime
+// may be another copy of cudart).
+cudaError_t bind_stream_device(void *stream) {
+    if (stream == nullptr) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+    if (e != cudaSuccess) return e;
+    // a capturing stream belongs to the device current at capture; device queries on it
+    // are not needed (and not all are permitted while capturing)
+    if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
+    int dev = -1;
+    e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &dev);
+    if (e != cudaSuccess) return e;
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    return cur == dev ? cudaSuccess : cudaSetDevice(dev);
+}
+
+int bind_or_fail(void *stream) {
+    const cudaError_t e = bind_stream_device(stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return GVA_ERR_CUDA;
+    }
+    return GVA_OK;
+}
+
+// Once per device, on the first call that reaches it: the SM count, the shared-memory
+// opt-in of every kernel that may use more than 48 KB, and the register counts the
+// CUDA-core grid is sized from.  Later calls (including calls made during stream
+// capture) only read these values.
+struct DevState {
+    int ready;
+    int sms;
+    int simt_regs[4];   // decode_simt_kernel <f32,gva> <bf16,gva> <f32,gqa> <bf16,gqa>
+};
+DevState g_dev[MAX_DEVICES];
+std::mutex g_dev_mu;
+
+template <typename Kern>
+cudaError_t opt_in_smem(Kern k) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_LIMIT);
+}
+
+template <typename Kern>
+int kernel_regs(Kern k) {
+    cudaFuncAttributes a;
+    return cudaFuncGetAttributes(&a, k) == cudaSuccess ? a.numRegs : 255;
+}
+
+const DevState *device_state() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        if (e != cudaSuccess) g_last_cuda_error = (int)e;
+        return nullptr;
+    }
+    if (g_dev[dev].ready) return &g_dev[dev];
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevState &d = g_dev[dev];
+    if (d.ready) return &d;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = opt_in_smem(absorb_kernel<float>);
+    if (e == cudaSuccess) e = opt_in_smem(absorb_kernel<__nv_bfloat16>);
+    if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, false>);
+    if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, false>);
+    if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, true>);
+    if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, true>);
+    if (e == cudaSuccess) e = mma_opt_in_all();
+    if (e == cudaSuccess && !encode_fn()) e = cudaErrorSymbolNotFound;
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        cudaGetLastError();
+        return nullptr;
+    }
+    d.simt_regs[0] = kernel_regs(decode_simt_kernel<float, false>);
+    d.simt_regs[1] = kernel_regs(decode_simt_kernel<__nv_bfloat16, false>);
+    d.simt_regs[2] = kernel_regs(decode_simt_kernel<float, true>);
+    d.simt_regs[3] = kernel_regs(decode_simt_kernel<__nv_bfloat16, true>);
+    d.sms = n;
+    d.ready = 1;
+    return &d;
+}
+
+int num_sms_current() {
+    const DevState *d = device_state();
+    return d ? d->sms : 0;
+}
+
+bool dims_ok(const gva_dims *d, bool gva_shape) {
+    if (!d) return false;
+    if (d->B < 1 || d->B > MAX_B || d->H < 1 || d->G < 1 || d->H % d->G != 0) return false;
+    const int r = d->H / d->G;
+    if (r > 8) return false;
+    if (d->d_h != 32 && d->d_h != 64 && d->d_h != 128) return false;
+    if (d->cache_dtype != GVA_F32 && d->cache_dtype != GVA_BF16) return false;
+    if (d->q_dtype != GVA_F32 && d->q_dtype != GVA_BF16) return false;
+    if (d->H * d->d_h > SIMT_THREADS * SIMT_MAXQ) return false;
+    if (gva_shape) {
+        if (d->d_n < 8 || d->d_n > 256 || d->d_n % 8 != 0) return false;
+        if (d->d_r < 0 || d->d_r > 32 || d->d_r % 8 != 0) return false;
+    }
+    return true;
+}
+
+bool rows_ok(const gva_rows *R, int B) {
+    if (!R || R->num_rows < 0) return false;
+    switch (R->layout) {
+    case GVA_LAYOUT_CONTIGUOUS:
+        return R->T_cap >= 0 && (long long)B * R->T_cap <= R->num_rows;
+    case GVA_LAYOUT_RAGGED:
+        return R->offsets != nullptr;
+    case GVA_LAYOUT_PAGED:
+        return R->block_table != nullptr && R->page_size > 0 && R->page_size % SLAB == 0 &&
+               R->max_pages >= 1 && R->num_rows % R->page_size == 0;
+    default:
+        return false;
+    }
+}
+
+RowsDev to_dev(const gva_rows &R) {
+    RowsDev d;
+    d.layout = R.layout;
+    d.num_rows = R.num_rows;
+    d.T_cap = R.T_cap;
+    d.offsets = R.offsets;
+    d.block_table = R.block_table;
+    d.max_pages = R.max_pages;
+    d.page_size = R.page_size;
+    d.num_pages = R.layout == GVA_LAYOUT_PAGED ? (int)(R.num_rows / R.page_size) : 0;
+    return d;
+}
+
+// Workspace: [q_tilde B*H*d_h][q_hat B*H*d_r][part_o slots*H*d_h][part_ml slots*H*2]
+struct WsPlan {
+    size_t qt, qh, po, pm, total;
+    long long slots;
+};
+
+WsPlan plan_ws(const gva_dims *d, int sms) {
+    WsPlan w;
+    w.slots = (long long)sms * CTAS_PER_SM_CAP + d->B;
+    size_t o = 0;
+    w.qt = o; o = align_up(o + sizeof(float) * d->B * d->H * d->d_h, 256);
+    w.qh = o; o = align_up(o + sizeof(float) * d->B * d->H * (d->d_r > 0 ? d->d_r : 1), 256);
+    w.po = o; o = align_up(o + sizeof(float) * w.slots * d->H * d->d_h, 256);
+    w.pm = o; o = align_up(o + sizeof(float) * w.slots * d->H * 2, 256);
+    w.total = o;
+    return w;
+}
+
+// Grid of the SIMT decode kernel: resident CTAs per SM (shared memory, registers,
+// threads; B300 SM: 228 KB shared memory, 64K registers, 2048 threads) x SMs, capped.
+int simt_grid(int regs, size_t smem, int sms, int req) {
+    if (req > 0) return req < sms * CTAS_PER_SM_CAP ? req : sms * CTAS_PER_SM_CAP;
+    const int by_smem = (int)((228 * 1024) / (smem + 1024));
+    const int regs_warp = ((regs * 32 + 255) / 256) * 256;
+    const int by_regs = 65536 / (regs_warp * (SIMT_THREADS / 32));
+    int per = by_smem < by_regs ? by_smem : by_regs;
+    if (per > 2048 / SIMT_THREADS) per = 2048 / SIMT_THREADS;
+    if (per > CTAS_PER_SM_CAP) per = CTAS_PER_SM_CAP;
+    if (per < 1) per = 1;
+    return sms * per;
+}
+
+int launch_combine(void *stream, const DecodeParams &dp, const gva_rows &rows) {
+    CombineParams cp;
+    cp.B = dp.B;
+    cp.H = dp.H;
+    cp.d_h = dp.d_h;
+    cp.seq_len = dp.seq_len;
+    cp.R = to_dev(rows);
+    cp.part_o = dp.part_o;
+    cp.part_ml = dp.part_ml;
+    cp.out = dp.out;
+    cp.lse = dp.lse;
+    cp.n_ctas = dp.n_ctas;
+    return cuda_status(launch(combine_kernel, dim3(dp.B * dp.H), dim3(dp.d_h), 0, stream, cp));
+}
+
+// Sets dp.n_ctas (the combine kernel re-derives the partition from it) and launches.
+template <typename CT, bool GQA>
+int run_simt(void *stream, DecodeParams &dp, int sms, int req_ctas) {
+    const SimtSmem L = simt_smem(dp.B, dp.H, dp.G, dp.d_h, GQA ? 0 : dp.d_r, (int)sizeof(CT), GQA);
+    auto kern = decode_simt_kernel<CT, GQA>;
+    const DevState *ds = device_state();
+    if (!ds) return GVA_ERR_CUDA;
+    const int regs = ds->simt_regs[(sizeof(CT) == 2 ? 1 : 0) + (GQA ? 2 : 0)];
+    dp.n_ctas = simt_grid(regs, L.total, sms, req_ctas);
+    return cuda_status(launch(kern, dim3(dp.n_ctas), dim3(SIMT_THREADS), L.total, stream, dp));
+}
+
+int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                  const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
+                  float prescale, float *q_tilde, float *q_hat, int sms,
+                  const gva_rows *rows = nullptr) {
+    AbsorbParams p;
+    p.check_rows = rows != nullptr;
+    if (rows) p.R = to_dev(*rows);
+    else memset(&p.R, 0, sizeof(p.R));
+    p.B = d->B;
+    p.H = d->H;
+    p.d_h = d->d_h;
+    p.d_n = d->d_n;
+    p.d_r = d->d_r;
+    int bpb = (d->B * d->H) / (sms > 0 ? sms : 1);
+    bpb = bpb < 1 ? 1 : (bpb > 8 ? 8 : bpb);
+    p.bpb = bpb;
+    p.q_nope = q_nope;
+    p.q_rope = q_rope;
+    p.M = M;
+    p.seq_len = seq_len;
+    p.rope_tab = rope_tab;
+    p.rope_max_pos = rope_max_pos;
+    p.prescale = prescale;
+    p.q_tilde = q_tilde;
+    p.q_hat = q_hat;
+    const size_t smem = sizeof(float) * ((size_t)d->d_h * (d->d_n + 1) + (size_t)bpb * d->d_n);
+    dim3 grid(d->H, (d->B + bpb - 1) / bpb);
+    cudaError_t e;
+    if (d->q_dtype == GVA_F32) e = launch(absorb_kernel<float>, grid, dim3(128), smem, stream, p);
+    else e = launch(absorb_kernel<__nv_bfloat16>, grid, dim3(128), smem, stream, p);
+    return cuda_status(e);
+}
+
+const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0};
+
+}  // namespace
+
+// =========================================================================== //
+extern "C" {
+
+const char *gva_status_string(int s) {
+    switch (s) {
+    case GVA_OK: return "GVA_OK";
+    case GVA_ERR_ARG: return "GVA_ERR_ARG: invalid argument";
+    case GVA_ERR_UNSUPPORTED: return "GVA_ERR_UNSUPPORTED: shape or dtype not supported";
+    case GVA_ERR_CUDA: return "GVA_ERR_CUDA: CUDA runtime or launch failure";
+    case GVA_ERR_WORKSPACE: return "GVA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case GVA_ERR_DEVICE_CHECK: return "GVA_ERR_DEVICE_CHECK: a device-side check tripped";
+    case GVA_DEV_BAD_LENGTH: return "GVA_DEV_BAD_LENGTH: sequence length outside its capacity";
+    case GVA_DEV_BAD_PAGE: return "GVA_DEV_BAD_PAGE: block-table entry out of range";
+    case GVA_DEV_BAD_POSITION: return "GVA_DEV_BAD_POSITION: position outside capacity or RoPE table";
+    case GVA_DEV_TIMEOUT: return "GVA_DEV_TIMEOUT: a bounded in-kernel wait gave up";
+    default: return "unknown gva status";
+    }
+}
+
+int gva_abi_version(void) { return GVA_ABI_VERSION; }
+
+int gva_num_sms(void) { return num_sms_current(); }
+
+int gva_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gva_rope_table_fill(float *tab, int max_pos, int d_r, double base) {
+    if (max_pos < 1 || d_r < 0 || d_r % 2 != 0 || !(base > 0.0)) return GVA_ERR_ARG;
+    if (d_r == 0) return GVA_OK;
+    if (!tab) return GVA_ERR_ARG;
+    const int half = d_r / 2;
+    for (long long p = 0; p < max_pos; ++p) {
+        for (int i = 0; i < half; ++i) {
+            const double theta = std::pow(base, -(2.0 * (double)i) / (double)d_r);
+            const double ang = (double)p * theta;
+            tab[(p * half + i) * 2 + 0] = (float)std::cos(ang);
+            tab[(p * half + i) * 2 + 1] = (float)std::sin(ang);
+        }
+    }
+    return GVA_OK;
+}
+
+int gva_absorb_query(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                     const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
+                     float scale, float *q_tilde, float *q_rope_rot) {
+    if (!dims_ok(d, true)) return GVA_ERR_ARG;
+    if (!q_nope || !M || !seq_len || !q_tilde || !aligned16(q_nope) || !aligned16(M) ||
+        !aligned16(q_tilde))
+        return GVA_ERR_ARG;
+    if (d->d_r > 0 && (!q_rope || !rope_tab || !q_rope_rot || rope_max_pos < 1 ||
+                       !aligned16(q_rope) || !aligned16(q_rope_rot) || !aligned16(rope_tab)))
+        return GVA_ERR_ARG;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    return absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos, scale,
+                         q_tilde, q_rope_rot, num_sms_current());
+}
+
+int gva_append_cache(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
+                     const int *pos, int *seq_len_out, const gva_cache *cache,
+                     const float *rope_tab, int rope_max_pos) {
+    if (!dims_ok(d, true) || !cache || !rows_ok(&cache->rows, d->B)) return GVA_ERR_ARG;
+    if (!v_new || !pos || !cache->V || !aligned16(v_new) || !aligned16(cache->V)) return GVA_ERR_ARG;
+    if (d->d_r > 0 && (!k_new || !cache->K_rope || !rope_tab || rope_max_pos < 1 ||
+                       !aligned16(k_new) || !aligned16(cache->K_rope)))
+        return GVA_ERR_ARG;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    if (!device_state()) return GVA_ERR_CUDA;
+    AppendParams p;
+    p.B = d->B;
+    p.G = d->G;
+    p.d_h = d->d_h;
+    p.d_r = d->d_r;
+    p.v_new = v_new;
+    p.k_new = k_new;
+    p.pos = pos;
+    p.seq_len_out = seq_len_out;
+    p.R = to_dev(cache->rows);
+    p.V = cache->V;
+    p.Kr = cache->K_rope;
+    p.rope_tab = rope_tab;
+    p.rope_max_pos = rope_max_pos;
+    cudaError_t e = d->cache_dtype == GVA_F32
+                        ? launch(append_kernel<float>, dim3(d->B), dim3(128), 0, stream, p)
+                        : launch(append_kernel<__nv_bfloat16>, dim3(d->B), dim3(128), 0, stream, p);
+    return cuda_status(e);
+}
+
+size_t gva_decode_workspace_size(const gva_dims *d) {
+    if (!dims_ok(d, false)) return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    return plan_ws(d, sms).total;
+}
+
+// Host-only checks shared by both decode entry points (no CUDA call).
+static int decode_arg_checks(const gva_dims *d, const gva_rows *rows, float *out, float *lse,
+                             const gva_decode_opts *o, bool gva_shape) {
+    if (!dims_ok(d, gva_shape) || !rows_ok(rows, d->B)) return GVA_ERR_ARG;
+    if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
+    if (o->flags != 0 || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_MMA || o->num_ctas < 0)
+        return GVA_ERR_ARG;
+    return GVA_OK;
+}
+
+// Device binding, SM count and the workspace check.
+static int decode_device_checks(void *stream, const gva_dims *d, void *ws, size_t ws_bytes,
+                                WsPlan *plan, int *sms) {
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    *sms = num_sms_current();
+    if (*sms <= 0) return GVA_ERR_CUDA;
+    *plan = plan_ws(d, *sms);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < plan->total)
+        return GVA_ERR_WORKSPACE;
+    return GVA_OK;
+}
+
+int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
+                            const void *q_rope, const float *M, const int *seq_len,
+                            const gva_cache *cache, const float *rope_tab, int rope_max_pos,
+                            float scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                            const gva_decode_opts *opts) {
+    const gva_decode_opts *o = opts ? opts : &kDefaultOpts;
+    if (!cache) return GVA_ERR_ARG;
+    int st = decode_arg_checks(d, &cache->rows, out, lse, o, true);
+    if (st != GVA_OK) return st;
+    if (!q_nope || !M || !seq_len || !cache->V || !aligned16(q_nope) || !aligned16(M) ||
+        !aligned16(cache->V))
+        return GVA_ERR_ARG;
+    if (d->d_r > 0 && (!q_rope || !cache->K_rope || !rope_tab || rope_max_pos < 1 ||
+                       !aligned16(q_rope) || !aligned16(cache->K_rope) || !aligned16(rope_tab)))
+        return GVA_ERR_ARG;
+    const bool mma_ok = mma_supported(d);
+    if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
+    WsPlan plan;
+    int sms = 0;
+    st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
+    if (st != GVA_OK) return st;
+    const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
+
+    char *w = static_cast<char *>(ws);
+    float *qt = reinterpret_cast<float *>(w + plan.qt);
+    float *qh = reinterpret_cast<float *>(w + plan.qh);
+    st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                       scale * LOG2E, qt, qh, sms, &cache->rows);
+    if (st != GVA_OK) return st;
+
+    DecodeParams dp;
+    dp.B = d->B;
+    dp.H = d->H;
+    dp.G = d->G;
+    dp.r = d->H / d->G;
+    dp.d_h = d->d_h;
+    dp.d_r = d->d_r;
+    dp.seq_len = seq_len;
+    dp.R = to_dev(cache->rows);
+    dp.Kc = cache->V;
+    dp.Vc = cache->V;
+    dp.Krope = cache->K_rope;
+    dp.qc = qt;
+    dp.qc_f32 = 1;
+    dp.qc_scale = 1.f;
+    dp.qr = qh;
+    dp.out = out;
+    dp.lse = lse;
+    dp.part_o = reinterpret_cast<float *>(w + plan.po);
+    dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
+    dp.n_ctas = 0;
+    if (use_mma) {
+        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false);
+    } else if (d->cache_dtype == GVA_F32) {
+        st = run_simt<float, false>(stream, dp, sms, o->num_ctas);
+    } else {
+        st = run_simt<__nv_bfloat16, false>(stream, dp, sms, o->num_ctas);
+    }
+    if (st != GVA_OK) return st;
+    return launch_combine(stream, dp, cache->rows);
+}
+
+int gva_decode_attention(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                         const float *M, const int *seq_len, const gva_cache *cache,
+                         const float *rope_tab, int rope_max_pos, float scale, float *out,
+                         float *lse, void *ws, size_t ws_bytes) {
+    return gva_decode_attention_ex(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab,
+                                   rope_max_pos, scale, out, lse, ws, ws_bytes, nullptr);
+}
+
+int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, const int *seq_len,
+                             const gva_kv_cache *cache, float scale, float *out, float *lse,
+                             void *ws, size_t ws_bytes, const gva_decode_opts *opts) {
+    const gva_decode_opts *o = opts ? opts : &kDefaultOpts;
+    if (!cache) return GVA_ERR_ARG;
+    int st = decode_arg_checks(d, &cache->rows, out, lse, o, false);
+    if (st != GVA_OK) return st;
+    if (!q || !seq_len || !cache->K || !cache->V || !aligned16(q) || !aligned16(cache->K) ||
+        !aligned16(cache->V))
+        return GVA_ERR_ARG;
+    gva_dims dg = *d;
+    dg.d_r = 0;
+    const bool mma_ok = mma_supported(&dg);
+    if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
+    WsPlan plan;
+    int sms = 0;
+    st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
+    if (st != GVA_OK) return st;
+    const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
+    char *w = static_cast<char *>(ws);
+    DecodeParams dp;
+    dp.B = d->B;
+    dp.H = d->H;
+    dp.G = d->G;
+    dp.r = d->H / d->G;
+    dp.d_h = d->d_h;
+    dp.d_r = 0;
+    dp.seq_len = seq_len;
+    dp.R = to_dev(cache->rows);
+    dp.Kc = cache->K;
+    dp.Vc = cache->V;
+    dp.Krope = nullptr;
+    dp.qc = q;
+    dp.qc_f32 = d->q_dtype == GVA_F32;
+    dp.qc_scale = scale * LOG2E;
+    dp.qr = nullptr;
+    dp.out = out;
+    dp.lse = lse;
+    dp.part_o = reinterpret_cast<float *>(w + plan.po);
+    dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
+    dp.n_ctas = 0;
+    if (use_mma) {
+        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, true);
+    } else if (d->cache_dtype == GVA_F32) {
+        st = run_simt<float, true>(stream, dp, sms, o->num_ctas);
+    } else {
+        st = run_simt<__nv_bfloat16, true>(stream, dp, sms, o->num_ctas);
+    }
+    if (st != GVA_OK) return st;
+    return launch_combine(stream, dp, cache->rows);
+}
+
+int gva_get_device_status(int *code_out) {
+    int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+    const int zero = 0;
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    if (code_out) *code_out = v;
+    if (e != cudaSuccess) return GVA_ERR_CUDA;
+    return v == 0 ? GVA_OK : GVA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"
