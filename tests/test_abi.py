@@ -17,8 +17,8 @@ HEADER = os.path.join(ROOT, "include", "gva.h")
 
 @pytest.fixture(scope="module")
 def gva():
-    from value_only_kv_gva_b300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import value_only_kv_gva_b300 as m
     return m
 
