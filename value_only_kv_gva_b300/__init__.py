@@ -79,11 +79,12 @@ _lib.gva_decode_attention_ex.argtypes = _lib.gva_decode_attention.argtypes + [_P
 _lib.gva_gqa_decode_attention.argtypes = [_P, _PD, _P, _P, _PKV, _F, _P, _P, _P, _Z, _PO]
 _lib.gva_get_device_status.argtypes = [ctypes.POINTER(_I)]
 _lib.gva_last_cuda_error.restype = _I
+_lib.gva_decode_attention_static.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I, _F, _P, _P]
 
 EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_table_fill",
            "gva_absorb_query", "gva_append_cache", "gva_decode_workspace_size",
            "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
-           "gva_get_device_status", "gva_last_cuda_error"]
+           "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static"]
 
 
 class GvaError(RuntimeError):
@@ -283,6 +284,22 @@ def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: floa
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
         ctypes.byref(o)), "gva_gqa_decode_attention")
+
+
+def gva_decode_attention_static(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, rope_tab,
+                                scale: float, out, lse, stream=None) -> None:
+    """gva_decode_attention for callers that cannot allocate device memory: the
+    library's fixed device scratch array stands in for the workspace (see gva.h)."""
+    d = dims.c()
+    cc = cache.c()
+    _check(_lib.gva_decode_attention_static(
+        _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
+        _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
+        _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc),
+        _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse")),
+        "gva_decode_attention_static")
 
 
 def gva_get_device_status() -> int:

@@ -492,6 +492,60 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     return launch_combine(stream, dp, cache->rows);
 }
 
+// ---------------------------------------------------------------------------- //
+// Decode without a caller-provided workspace.
+//
+// For callers that cannot allocate device memory at the point where they decode:
+// code running while a stream is being captured into a CUDA graph (allocation calls
+// are refused there), plugins and embedded runtimes that are handed no allocator or
+// scratch buffer, and latency-critical loops that forbid allocator calls because they
+// can block or synchronise the device.  The scratch lives in one fixed-size array in
+// device memory that every GPU loading this library holds until the process exits.
+// ---------------------------------------------------------------------------- //
+static __device__ __align__(256) unsigned char g_static_scratch[GVA_STATIC_SCRATCH_BYTES];
+
+static void *g_static_scratch_ptr[MAX_DEVICES];   // device address, per device
+static std::mutex g_static_scratch_mu;
+
+// Resolve the array's device address once per device, with that device current.
+// Host code must not hand `g_static_scratch` itself to a kernel: on the host the name
+// is a stand-in, not a device address.
+static void *static_scratch_for_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+    if (!g_static_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) {
+            g_last_cuda_error = (int)e;
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_static_scratch_ptr[dev] = ptr;
+    }
+    return g_static_scratch_ptr[dev];
+}
+
+int gva_decode_attention_static(void *stream, const gva_dims *d, const void *q_nope,
+                                const void *q_rope, const float *M, const int *seq_len,
+                                const gva_cache *cache, const float *rope_tab, int rope_max_pos,
+                                float scale, float *out, float *lse) {
+    if (!dims_ok(d, true)) return GVA_ERR_ARG;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    const size_t need = gva_decode_workspace_size(d);
+    if (need == 0) return GVA_ERR_CUDA;
+    if (need > (size_t)GVA_STATIC_SCRATCH_BYTES) return GVA_ERR_WORKSPACE;  // beyond the fixed maximum
+    void *ws = static_scratch_for_current_device();
+    if (!ws) return GVA_ERR_CUDA;
+    return gva_decode_attention_ex(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab,
+                                   rope_max_pos, scale, out, lse, ws,
+                                   (size_t)GVA_STATIC_SCRATCH_BYTES, nullptr);
+}
+
 int gva_get_device_status(int *code_out) {
     int v = 0;
     cudaError_t e = cudaDeviceSynchronize();
