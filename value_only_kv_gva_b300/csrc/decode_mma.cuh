@@ -49,7 +49,26 @@ struct MmaParams {
     int off_bar;       // barriers, from the aligned dynamic smem base
     int off_f;         // Ls[B], F[B+1]
     int off_merge;     // group-merge buffer
+    int v3d;           // 1: one 3D TMA box per slab covers every value column
+    int early;         // 1: the preceding kernel only writes the queries, so the cache
+                       //    may be streamed before the grid dependency resolves
 };
+
+// Optional timeline of a few CTAs (compiled in only with -DGVA_TRACE; a debugging aid
+// for measuring where a CTA spends its cycles, read back by gva_debug_trace_read).
+#ifdef GVA_TRACE
+constexpr int TRACE_CTAS = 4, TRACE_SLOTS = 512;
+__device__ long long g_trace[TRACE_CTAS * TRACE_SLOTS];
+#define GVA_TRACE_AT(slot)                                                          \
+    do {                                                                            \
+        if (blockIdx.x < TRACE_CTAS && (slot) < TRACE_SLOTS)                        \
+            g_trace[blockIdx.x * TRACE_SLOTS + (slot)] = clock64();                 \
+    } while (0)
+#else
+#define GVA_TRACE_AT(slot) \
+    do {                   \
+    } while (0)
+#endif
 
 // ---------------------------------------------------------------------------- //
 // PTX wrappers
@@ -106,6 +125,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
@@ -205,9 +232,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (GQA) prefetch_tmap(&tm_k);
         if (DR > 0) prefetch_tmap(&tm_r);
     }
-    pdl_wait();
+    if (threadIdx.x == 0) GVA_TRACE_AT(0);
+    // Lengths, row maps and the cache are final before the preceding grid (the query
+    // absorption) was allowed to start, so with `early` they are read at once and the
+    // cache streams while that grid still runs; the queries are read after the wait.
+    if (!mp.early) pdl_wait();
     pdl_launch_dependents();
     build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0);   // includes __syncthreads
+    if (threadIdx.x == 0) GVA_TRACE_AT(1);
     const Part P{F[B], p.n_ctas};
     if (P.S == 0) return;
     const int c = blockIdx.x;
@@ -219,16 +251,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (lane == 0) {
             unsigned int last_phase_mask = 0, issued_mask = 0;  // per stage (NS <= 32)
             int b = seq_of_slab(F, B, s0);
-            long long q = 0;
-            bool ok = true;
-            for (long long s = s0; s < s1 && ok; ++s, ++q) {
+            int stage = 0;
+            uint32_t round = 0;                 // times the ring has wrapped
+            const int nbox = G * (DH / 64);
+            const int nslab = (int)(s1 - s0);
+            for (int i = 0; i < nslab; ++i) {
+                const long long s = s0 + i;
                 while (F[b + 1] <= s) ++b;
-                const int stage = (int)(q % NS);
-                const uint32_t round = (uint32_t)(q / NS);
-                if (round > 0 && !mbar_wait(bar_empty + 8 * stage, (round - 1) & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
+                if (round > 0 && !mbar_wait(bar_empty + 8 * stage, (round - 1) & 1u, abort)) break;
                 const long long j0 = (long long)(s - F[b]) * SLAB;
                 long long row = row_of(p.R, b, j0);
                 if (row < 0) row = 0;  // consumers mask a slab behind a bad page id
@@ -236,15 +266,25 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 const uint32_t st = base_u32 + stage * mp.stage_bytes;
                 const uint32_t fb = bar_full + 8 * stage;
                 mbar_expect_tx(fb, (uint32_t)mp.tx_bytes);
-                const int nbox = G * (DH / 64);
-                for (int bx = 0; bx < nbox; ++bx) {
-                    tma_load_2d(st + bx * 2048, &tm_v, bx * 64, y, fb);
-                    if (GQA) tma_load_2d(st + mp.off_k + bx * 2048, &tm_k, bx * 64, y, fb);
+                if (mp.v3d) {
+                    tma_load_3d(st, &tm_v, 0, y, 0, fb);
+                    if (GQA) tma_load_3d(st + mp.off_k, &tm_k, 0, y, 0, fb);
+                } else {
+                    for (int bx = 0; bx < nbox; ++bx) {
+                        tma_load_2d(st + bx * 2048, &tm_v, bx * 64, y, fb);
+                        if (GQA) tma_load_2d(st + mp.off_k + bx * 2048, &tm_k, bx * 64, y, fb);
+                    }
                 }
                 if (DR > 0) tma_load_2d(st + mp.off_r, &tm_r, 0, y, fb);
                 issued_mask |= 1u << stage;
                 last_phase_mask = (last_phase_mask & ~(1u << stage)) | ((round & 1u) << stage);
+                if (i == 0) GVA_TRACE_AT(2);
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
+                }
             }
+            GVA_TRACE_AT(3);
             // never leave with copies in flight: wait (bounded) for each stage's last load
             for (int s = 0; s < NS; ++s) {
                 if (!(issued_mask & (1u << s))) continue;
@@ -273,8 +313,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     // ldmatrix lane roles
     const int lm_mat = lane >> 3, lm_row = lane & 7;
 
+    if (mp.early) pdl_wait();         // the absorbed queries come from the preceding grid
     int b = seq_of_slab(F, B, s0);
-    long long q = 0;
+    int stage = 0, wsel = 0;          // ring stage and slab-owner counter of the next slab
+    uint32_t phase = 0;
+    int tslab = 0;                    // trace index
     long long s = s0;
     bool alive = true;
     while (s < s1) {
@@ -338,20 +381,26 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
 
-        for (; s < seg_end; ++s, ++q) {
-            if ((int)(q % wpg) != w || !alive) continue;
-            const int stage = (int)(q % NS);
-            if (!mbar_wait(bar_full + 8 * stage, (uint32_t)((q / NS) & 1), abort)) {
+        if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(4);
+        for (; s < seg_end; ++s) {
+            const int my_stage = stage;
+            const uint32_t my_phase = phase;
+            const bool mine = wsel == w;
+            if (++stage == NS) { stage = 0; phase ^= 1u; }
+            if (++wsel == wpg) wsel = 0;
+            if (!mine || !alive) continue;
+            if (!mbar_wait(bar_full + 8 * my_stage, my_phase, abort)) {
                 alive = false;
                 continue;
             }
+            if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(8 + 2 * tslab);
             const long long j0 = (long long)(s - F[b]) * SLAB;
             int nv = (int)min((long long)SLAB, (long long)Lb - j0);
             if (row_of(p.R, b, j0) < 0) {
                 if (lane == 0 && g == 0) dev_report(GVA_DEV_BAD_PAGE);
                 nv = 0;
             }
-            const uint32_t st = base_u32 + stage * mp.stage_bytes;
+            const uint32_t st = base_u32 + my_stage * mp.stage_bytes;
             const uint32_t kst = GQA ? st + mp.off_k : st;
 
             // ---- scores S^T = Q . K^T for tokens 8nt .. 8nt+7 ----
@@ -448,7 +497,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 mma16816(oacc[2 * np + 1], pa, b2, b3);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+            if (lane == 0) mbar_arrive(bar_empty + 8 * my_stage);
+            if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(9 + 2 * tslab);
+            ++tslab;
         }
 
         // ---- segment end: fold hi/lo rows, reduce l over the quad, merge the group's warps ----
@@ -491,6 +542,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             }
             named_bar(1 + g, wpg * 32);
         }
+        if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(5);
         if (w == 0 && real_row) {
             const bool whole = F[b] >= s0 && F[b + 1] <= s1;
             if (whole) {
@@ -558,6 +610,21 @@ inline bool make_map(CUtensorMap *m, const void *ptr, long long rows, int width,
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D bf16 map viewing each row of `width` elements as width/64 chunks of 64: dims
+// {64, rows, width/64}, strides {row pitch, 128 B}; one box {64, 16, width/64} lands
+// in shared memory chunk-major ([chunk][16 rows][64]), each chunk 128-byte swizzled.
+inline bool make_map3(CUtensorMap *m, const void *ptr, long long rows, int width) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(width / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)width * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)SLAB, (cuuint32_t)(width / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -644,7 +711,7 @@ inline int launch_mma_dr(void *stream, MmaParams &mp, const CUtensorMap &tv, con
 
 // Sets dp.n_ctas and launches the tensor-core decode (one CTA per SM by default).
 inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms, int req_ctas,
-                   bool gqa) {
+                   bool gqa, bool early) {
     if (rows.num_rows > 0x7fffffffLL) return GVA_ERR_UNSUPPORTED;   // TMA row coordinate is int32
     MmaParams mp;
     mp.d = dp;
@@ -652,10 +719,15 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
     if (!plan_mma(mp, DH, DR, gqa)) return GVA_ERR_UNSUPPORTED;
     const long long nrows = rows.num_rows > 0 ? rows.num_rows : 1;
     CUtensorMap tv, tk, tr;
-    if (!make_map(&tv, dp.Vc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
-    tk = tv;
+    mp.early = early ? 1 : 0;
+    mp.v3d = make_map3(&tv, dp.Vc, nrows, dp.G * DH) &&
+             (!gqa || make_map3(&tk, dp.Kc, nrows, dp.G * DH));
+    if (!mp.v3d) {
+        if (!make_map(&tv, dp.Vc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
+        if (gqa && !make_map(&tk, dp.Kc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
+    }
+    if (!gqa) tk = tv;
     tr = tv;
-    if (gqa && !make_map(&tk, dp.Kc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
     if (DR > 0 && !make_map(&tr, dp.Krope, nrows, DR, DR, false)) return GVA_ERR_CUDA;
     int grid = req_ctas > 0 ? req_ctas : sms;
     if (grid > sms * 8) grid = sms * 8;

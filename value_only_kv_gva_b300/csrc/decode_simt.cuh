@@ -235,8 +235,10 @@ __global__ void __launch_bounds__(SIMT_THREADS) decode_simt_kernel(const DecodeP
 // Log-sum-exp combine of split-K partials (flash-decoding):
 //   m* = max_s m_s,  o = sum_s 2^(m_s - m*) o_s / sum_s 2^(m_s - m*) l_s,
 //   lse = (m* + log2 sum_s 2^(m_s - m*) l_s) ln 2.
-// One CTA per (b, h), one thread per value dimension.  Sequences owned by a single
-// CTA were finished by the decode kernel; empty sequences get out = 0, lse = -inf.
+// Grid (B*H, ceil(d_h/32)), 128 threads = 4 part lanes x 32 dimensions.  Every global
+// load of a phase is independent of the others, so a phase costs one memory round
+// trip: lengths, then the parts' (m, l), then the parts' o slices.  Sequences owned by
+// a single CTA were finished by the decode kernel; empty ones get out = 0, lse = -inf.
 // --------------------------------------------------------------------------- //
 struct CombineParams {
     int B, H, d_h;
@@ -249,68 +251,109 @@ struct CombineParams {
     int n_ctas;
 };
 
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+constexpr int COMBINE_THREADS = 128;
+constexpr int COMBINE_MAX_PARTS = 4096;   // >= the largest decode grid
+
+__global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineParams p) {
+    __shared__ float w_s[COMBINE_MAX_PARTS];   // part weight 2^(m - m*), 0 for no part
+    __shared__ float l_s[COMBINE_MAX_PARTS];
+    __shared__ long long red_ll[2][COMBINE_THREADS / 32];
+    __shared__ float red_f[COMBINE_THREADS / 32];
+    __shared__ float acc_s[4][32];
     pdl_wait();
     pdl_launch_dependents();
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
-    const int i = threadIdx.x;
-    __shared__ long long red[4];
-    __shared__ long long tot_s;
-    // F_b and S: sums of the validated slab counts (same rule as build_prefix)
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // ---- F_b and S: the validated slab counts (same rule as build_prefix) ----
     long long before = 0, total = 0;
-    for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
+    for (int bb = tid; bb < p.B; bb += COMBINE_THREADS) {
         int L = p.seq_len[bb];
         if (!length_ok(p.R, bb, L)) L = 0;
         const long long n = (L + SLAB - 1) / SLAB;
         total += n;
         if (bb < b) before += n;
     }
-    // block reduce (blockDim.x <= 128)
+#pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         before += __shfl_xor_sync(0xffffffffu, before, o);
         total += __shfl_xor_sync(0xffffffffu, total, o);
     }
-    const int warp = threadIdx.x / 32, nw = (blockDim.x + 31) / 32;
-    __shared__ long long red2[4];
-    if ((threadIdx.x & 31) == 0) { red[warp] = before; red2[warp] = total; }
+    if (lane == 0) { red_ll[0][wid] = before; red_ll[1][wid] = total; }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        long long a = 0, t = 0;
-        for (int w = 0; w < nw; ++w) { a += red[w]; t += red2[w]; }
-        red[0] = a;
-        tot_s = t;
-    }
-    __syncthreads();
-    const long long Fb = red[0], S = tot_s;
+    long long Fb = 0, S = 0;
+#pragma unroll
+    for (int w = 0; w < COMBINE_THREADS / 32; ++w) { Fb += red_ll[0][w]; S += red_ll[1][w]; }
     int Lb = p.seq_len[b];
     if (!length_ok(p.R, b, Lb)) Lb = 0;
     const long long nb = (Lb + SLAB - 1) / SLAB;
+    const int d0 = blockIdx.y * 32;
     float *out = p.out + ((long long)b * p.H + h) * p.d_h;
     if (nb == 0) {
-        if (i < p.d_h) out[i] = 0.f;
-        if (i == 0 && p.lse) p.lse[(long long)b * p.H + h] = -INFINITY;
+        if (tid < 32 && d0 + tid < p.d_h) out[d0 + tid] = 0.f;
+        if (tid == 0 && blockIdx.y == 0 && p.lse) p.lse[(long long)b * p.H + h] = -INFINITY;
         return;
     }
     const Part P{S, p.n_ctas};
     const int c_lo = P.cta_of(Fb), c_hi = P.cta_of(Fb + nb - 1);
     if (c_lo == c_hi) return;
+    const int n = c_hi - c_lo + 1;
+    // ---- parts' (m, l) and the running maximum ----
+    float mloc = -INFINITY;
+    for (int k = tid; k < n; k += COMBINE_THREADS) {
+        const int c = c_lo + k;
+        float m = -INFINITY, l = 0.f;
+        if (P.start(c) != P.start(c + 1)) {
+            const float2 ml = *reinterpret_cast<const float2 *>(
+                p.part_ml + (((long long)c + b) * p.H + h) * 2);
+            m = ml.x;
+            l = ml.y;
+        }
+        w_s[k] = m;
+        l_s[k] = l;
+        mloc = fmaxf(mloc, m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if (lane == 0) red_f[wid] = mloc;
+    __syncthreads();
     float mstar = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) {
-        if (P.start(c) == P.start(c + 1)) continue;
-        mstar = fmaxf(mstar, p.part_ml[(((long long)c + b) * p.H + h) * 2]);
+#pragma unroll
+    for (int w = 0; w < COMBINE_THREADS / 32; ++w) mstar = fmaxf(mstar, red_f[w]);
+    __syncthreads();
+    float dloc = 0.f;
+    for (int k = tid; k < n; k += COMBINE_THREADS) {
+        const float m = w_s[k];
+        const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
+        w_s[k] = wgt;
+        dloc += wgt * l_s[k];
     }
-    float acc = 0.f, den = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-        if (P.start(c) == P.start(c + 1)) continue;
-        const long long slot = (long long)c + b;
-        const float m = p.part_ml[(slot * p.H + h) * 2];
-        const float l = p.part_ml[(slot * p.H + h) * 2 + 1];
-        const float w = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
-        den += w * l;
-        if (i < p.d_h) acc += w * p.part_o[(slot * p.H + h) * p.d_h + i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dloc += __shfl_xor_sync(0xffffffffu, dloc, o);
+    if (lane == 0) red_f[wid] = dloc;
+    __syncthreads();
+    float den = 0.f;
+#pragma unroll
+    for (int w = 0; w < COMBINE_THREADS / 32; ++w) den += red_f[w];
+    // ---- weighted sum of this CTA's 32-dimension slice: part lane wid, dimension lane ----
+    const int i = d0 + lane;
+    float acc = 0.f;
+    if (i < p.d_h) {
+        const float *po = p.part_o + (((long long)c_lo + b) * p.H + h) * p.d_h + i;
+        const long long step = (long long)p.H * p.d_h;   // next slot (c + 1 + b)
+#pragma unroll 4
+        for (int k = wid; k < n; k += 4) {
+            const float wgt = w_s[k];
+            if (wgt != 0.f) acc += wgt * po[(long long)k * step];
+        }
     }
-    if (i < p.d_h) out[i] = den > 0.f ? acc / den : 0.f;
-    if (i == 0 && p.lse) p.lse[(long long)b * p.H + h] = den > 0.f ? (mstar + log2f(den)) * LN2 : -INFINITY;
+    acc_s[wid][lane] = acc;
+    __syncthreads();
+    if (wid == 0 && i < p.d_h) {
+        const float a = acc_s[0][lane] + acc_s[1][lane] + acc_s[2][lane] + acc_s[3][lane];
+        out[i] = den > 0.f ? a / den : 0.f;
+    }
+    if (tid == 0 && blockIdx.y == 0 && p.lse)
+        p.lse[(long long)b * p.H + h] = den > 0.f ? (mstar + log2f(den)) * LN2 : -INFINITY;
 }
 
 }  // namespace gva

@@ -203,7 +203,8 @@ int launch_combine(void *stream, const DecodeParams &dp, const gva_rows &rows) {
     cp.out = dp.out;
     cp.lse = dp.lse;
     cp.n_ctas = dp.n_ctas;
-    return cuda_status(launch(combine_kernel, dim3(dp.B * dp.H), dim3(dp.d_h), 0, stream, cp));
+    return cuda_status(launch(combine_kernel, dim3(dp.B * dp.H, (dp.d_h + 31) / 32),
+                              dim3(COMBINE_THREADS), 0, stream, cp));
 }
 
 // Sets dp.n_ctas (the combine kernel re-derives the partition from it) and launches.
@@ -231,7 +232,9 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     p.d_h = d->d_h;
     p.d_n = d->d_n;
     p.d_r = d->d_r;
-    int bpb = (d->B * d->H) / (sms > 0 ? sms : 1);
+    // sequences per CTA: enough CTAs to cover the GPU, at most 8 query rows per CTA
+    const int zs = (d->d_h + 31) / 32;
+    int bpb = (d->B * d->H * zs) / (sms > 0 ? 2 * sms : 1);
     bpb = bpb < 1 ? 1 : (bpb > 8 ? 8 : bpb);
     p.bpb = bpb;
     p.q_nope = q_nope;
@@ -243,11 +246,11 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     p.prescale = prescale;
     p.q_tilde = q_tilde;
     p.q_hat = q_hat;
-    const size_t smem = sizeof(float) * ((size_t)d->d_h * (d->d_n + 1) + (size_t)bpb * d->d_n);
-    dim3 grid(d->H, (d->B + bpb - 1) / bpb);
+    const size_t smem = sizeof(float) * ((size_t)32 * (d->d_n + 4) + (size_t)bpb * d->d_n);
+    dim3 grid(d->H, (d->B + bpb - 1) / bpb, zs);
     cudaError_t e;
-    if (d->q_dtype == GVA_F32) e = launch(absorb_kernel<float>, grid, dim3(128), smem, stream, p);
-    else e = launch(absorb_kernel<__nv_bfloat16>, grid, dim3(128), smem, stream, p);
+    if (d->q_dtype == GVA_F32) e = launch(absorb_kernel<float>, grid, dim3(ABSORB_THREADS), smem, stream, p);
+    else e = launch(absorb_kernel<__nv_bfloat16>, grid, dim3(ABSORB_THREADS), smem, stream, p);
     return cuda_status(e);
 }
 
@@ -422,7 +425,7 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
     if (use_mma) {
-        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false);
+        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, true);
     } else if (d->cache_dtype == GVA_F32) {
         st = run_simt<float, false>(stream, dp, sms, o->num_ctas);
     } else {
@@ -482,7 +485,7 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
     if (use_mma) {
-        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, true);
+        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, true, false);
     } else if (d->cache_dtype == GVA_F32) {
         st = run_simt<float, true>(stream, dp, sms, o->num_ctas);
     } else {
@@ -545,6 +548,19 @@ int gva_decode_attention_static(void *stream, const gva_dims *d, const void *q_n
                                    rope_max_pos, scale, out, lse, ws,
                                    (size_t)GVA_STATIC_SCRATCH_BYTES, nullptr);
 }
+
+#ifdef GVA_TRACE
+// Debug builds only: copy / clear the per-CTA cycle timeline of the tensor-core decode.
+int gva_debug_trace_read(long long *host, int n) {
+    if (n > TRACE_CTAS * TRACE_SLOTS) n = TRACE_CTAS * TRACE_SLOTS;
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(long long) * n) == cudaSuccess ? GVA_OK
+                                                                                    : GVA_ERR_CUDA;
+}
+int gva_debug_trace_clear(void) {
+    static long long zeros[TRACE_CTAS * TRACE_SLOTS];
+    return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) == cudaSuccess ? GVA_OK : GVA_ERR_CUDA;
+}
+#endif
 
 int gva_get_device_status(int *code_out) {
     int v = 0;

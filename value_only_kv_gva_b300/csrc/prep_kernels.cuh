@@ -79,41 +79,57 @@ struct AbsorbParams {
     RowsDev R;                     //    (the decode kernel reports it); used when check_rows
 };
 
-// Grid (H, ceil(B / bpb)).  M_h is staged in shared memory with a padded row so
-// that thread i reading row i is bank-conflict free; each output is a plain fp32
-// dot product over d_n.
+// Grid (H, ceil(B / bpb), d_h / 32), 256 threads.  A CTA owns 32 rows of M_h (at most
+// 32 x 256 fp32 = 32 KB) and issues all of its 16-byte loads of them at once (one
+// memory round trip, even while the decode streams the cache); each output row is
+// split over 8 threads (k strided by 8) and reduced with shuffles.
+constexpr int ABSORB_THREADS = 256;
+
 template <typename QT>
-__global__ void __launch_bounds__(128) absorb_kernel(const AbsorbParams p) {
+__global__ void __launch_bounds__(ABSORB_THREADS) absorb_kernel(const AbsorbParams p) {
     extern __shared__ __align__(16) float sm_abs[];
     pdl_wait();
     pdl_launch_dependents();
     const int h = blockIdx.x;
     const int b0 = blockIdx.y * p.bpb;
     const int nb = min(p.bpb, p.B - b0);
-    const int d_n = p.d_n, d_h = p.d_h, ldm = d_n + 1;
-    float *Ms = sm_abs;                 // [d_h][d_n + 1]
-    float *qs = Ms + d_h * ldm;         // [bpb][d_n]
-    const float *Mh = p.M + (long long)h * d_h * d_n;
-    for (int e = threadIdx.x; e < d_h * d_n; e += blockDim.x)
-        Ms[(e / d_n) * ldm + (e % d_n)] = Mh[e];
+    const int i0 = blockIdx.z * 32;
+    const int d_n = p.d_n, d_h = p.d_h;
+    const int ldm = d_n + 4;                 // padded row (16-byte aligned)
+    float *Ms = sm_abs;                      // [32][d_n + 4]
+    float *qs = Ms + 32 * ldm;               // [bpb][d_n]
+    const float *Mh = p.M + ((long long)h * d_h + i0) * d_n;
+    const int rows = min(32, d_h - i0);
+    const int n4 = rows * d_n / 4;
+    for (int e = threadIdx.x; e < n4; e += ABSORB_THREADS) {
+        const float4 v = reinterpret_cast<const float4 *>(Mh)[e];
+        const int i = (4 * e) / d_n, k = (4 * e) % d_n;
+        *reinterpret_cast<float4 *>(Ms + i * ldm + k) = v;
+    }
     const QT *qn = reinterpret_cast<const QT *>(p.q_nope);
-    for (int e = threadIdx.x; e < nb * d_n; e += blockDim.x) {
+    for (int e = threadIdx.x; e < nb * d_n; e += ABSORB_THREADS) {
         const int bl = e / d_n, k = e % d_n;
         qs[e] = to_f<QT>(qn[((long long)(b0 + bl) * p.H + h) * d_n + k]);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < nb * d_h; e += blockDim.x) {
-        const int bl = e / d_h, i = e % d_h;
-        const float *mrow = Ms + i * ldm;
-        const float *q = qs + bl * d_n;
+    const int o = threadIdx.x >> 3, kl = threadIdx.x & 7;   // output row, k lane
+    for (int bl = 0; bl < nb; ++bl) {
         float acc = 0.f;
-        for (int k = 0; k < d_n; ++k) acc = fmaf(q[k], mrow[k], acc);
-        p.q_tilde[((long long)(b0 + bl) * p.H + h) * d_h + i] = p.prescale * acc;
+        if (o < rows) {
+            const float *mrow = Ms + o * ldm;
+            const float *q = qs + bl * d_n;
+            for (int k = kl; k < d_n; k += 8) acc = fmaf(q[k], mrow[k], acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (kl == 0 && o < rows)
+            p.q_tilde[((long long)(b0 + bl) * p.H + h) * d_h + i0 + o] = p.prescale * acc;
     }
-    if (p.d_r > 0) {
+    if (p.d_r > 0 && blockIdx.z == 0) {
         const QT *qr = reinterpret_cast<const QT *>(p.q_rope);
         const int half = p.d_r / 2;
-        for (int e = threadIdx.x; e < nb * half; e += blockDim.x) {
+        for (int e = threadIdx.x; e < nb * half; e += ABSORB_THREADS) {
             const int bl = e / half, i = e % half, b = b0 + bl;
             const int L = p.seq_len[b];
             int t = L - 1;
