@@ -19,6 +19,43 @@ __device__ int g_status;
 
 __device__ __forceinline__ void dev_report(int code) { atomicCAS(&g_status, 0, code); }
 
+// Optional kernel timeline (compiled in only with -DGVA_TRACE, a debugging aid): the
+// earliest (g_kt_min) and latest (g_kt_max) global-timer reading of thread 0 of any CTA
+// at marked points of each kernel.
+#ifdef GVA_TRACE
+__device__ unsigned long long g_kt_min[16];
+__device__ unsigned long long g_kt_max[16];
+__device__ __forceinline__ unsigned long long kt_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ unsigned long long g_cta_t[4096][4];   // decode CTA: start, queries ready, end, SM
+__device__ __forceinline__ unsigned smid() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+#define GVA_CTA_T(k)                                                          \
+    do {                                                                      \
+        if (blockIdx.x < 4096) g_cta_t[blockIdx.x][(k)] = kt_now();           \
+        if ((k) == 2 && blockIdx.x < 4096) g_cta_t[blockIdx.x][3] = smid();  \
+    } while (0)
+#define GVA_KT(slot)                                   \
+    do {                                               \
+        const unsigned long long t_ = kt_now();        \
+        atomicMin(&g_kt_min[(slot)], t_);              \
+        atomicMax(&g_kt_max[(slot)], t_);              \
+    } while (0)
+#else
+#define GVA_KT(slot) \
+    do {             \
+    } while (0)
+#define GVA_CTA_T(k) \
+    do {             \
+    } while (0)
+#endif
+
 // Programmatic dependent launch: wait until the preceding grid in the stream has
 // completed and its writes are visible; then let the next grid start its prologue.
 // Every kernel waits before its first global read, so a grid is only ever released
@@ -70,23 +107,40 @@ __device__ __forceinline__ bool length_ok(const RowsDev &R, int b, long long L) 
 __device__ __forceinline__ long long row_of(const RowsDev &R, int b, long long j) {
     if (R.layout == GVA_LAYOUT_CONTIGUOUS) return (long long)b * R.T_cap + j;
     if (R.layout == GVA_LAYOUT_RAGGED) return (long long)R.offsets[b] + j;
-    const int page = R.block_table[(long long)b * R.max_pages + j / R.page_size];
+    const int jj = (int)j;   // positions are below 2^31 (lengths are int): 32-bit division
+    const int page = R.block_table[(long long)b * R.max_pages + jj / R.page_size];
     if (page < 0 || page >= R.num_pages) return -1;
-    return (long long)page * R.page_size + j % R.page_size;
+    return (long long)page * R.page_size + jj % R.page_size;
 }
 
 // Flat split-K partition over slabs.  Sequence b has n_b = ceil(L_b / 16) slabs
 // starting at flat index F[b] (exclusive prefix); S = F[B].  CTA c of n owns flat
-// slabs [c*S/n, (c+1)*S/n): equal shares of the whole batch's cache, whatever the
-// length mix.  Partials of (CTA c, sequence b) go to slot c + b, which is unique
-// along the monotone walk of (c, b) pairs.
+// slabs [floor(c*S/n), floor((c+1)*S/n)): equal shares of the whole batch's cache,
+// whatever the length mix.  Partials of (CTA c, sequence b) go to slot c + b, which is
+// unique along the monotone walk of (c, b) pairs.
+//
+// The shares are computed with 32-bit divisions only (S < 2^31, c <= n < 2^12):
+// floor(c*S/n) = c*floor(S/n) + floor(c*(S mod n)/n), and c*(S mod n) < 2^23.  A 64-bit
+// integer division is a long dependent instruction sequence that sat on the path to
+// the first cache load.
 struct Part {
     long long S;
     int n;
-    __device__ __forceinline__ long long start(int c) const { return (long long)c * S / n; }
-    // the CTA that owns flat slab s (0 <= s < S)
+    __device__ __forceinline__ long long start(int c) const {
+        const unsigned su = (unsigned)S, nu = (unsigned)n, cu = (unsigned)c;
+        const unsigned q = su / nu, r = su - q * nu;
+        return (long long)cu * q + (long long)((cu * r) / nu);
+    }
+    // the CTA that owns flat slab s (0 <= s < S): the largest c with start(c) <= s,
+    // i.e. floor(((s + 1) n - 1) / S).  The quotient is below n < 2^12, so a single-
+    // precision estimate is within one of it and two integer checks make it exact (FP64
+    // arithmetic is slow on this GPU).
     __device__ __forceinline__ int cta_of(long long s) const {
-        return (int)(((s + 1) * (long long)n - 1) / S);
+        const long long a = (s + 1) * (long long)n - 1;
+        long long q = (long long)__fdiv_rn((float)a, (float)S);
+        while (q > 0 && q * S > a) --q;
+        while ((q + 1) * S <= a) ++q;
+        return (int)q;
     }
 };
 

@@ -31,11 +31,17 @@
 
 namespace gva {
 
-constexpr int MMA_CONSUMERS = 8;                      // consumer warps per CTA (G * warps per group)
-constexpr int MMA_THREADS = (MMA_CONSUMERS + 1) * 32; // + one producer warp
-constexpr int MMA_MAX_STAGES = 24;
+// Warp roles: warp 0 is the producer, warps 1 .. ncons the consumers (G x warps per
+// group, at most 8).  The launch bound caps a thread at 128 registers, so a CTA (at most
+// 9 warps) leaves a third of the SM's register file, and some of its shared memory, to
+// the small kernels around the decode: the query absorption before it and the
+// log-sum-exp combine after it are resident beside it under programmatic dependent
+// launch instead of waiting for the SM to drain.
+constexpr int MMA_CONSUMERS = 8;
+constexpr int MMA_THREADS = 16 * 32;                  // launch bound (-> <= 128 registers)
 constexpr float MMA_RESCALE_TH = 8.f;                 // log2 units
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MMA_MAX_STAGES = 24;
 
 struct MmaParams {
     DecodeParams d;
@@ -59,14 +65,26 @@ struct MmaParams {
 #ifdef GVA_TRACE
 constexpr int TRACE_CTAS = 4, TRACE_SLOTS = 512;
 __device__ long long g_trace[TRACE_CTAS * TRACE_SLOTS];
+// stamps go to shared memory (a global store before an mbarrier arrive would delay the
+// arrive until the store completes) and are copied out when the stamping thread exits
+#define GVA_TRACE_DECL __shared__ long long s_trace[TRACE_SLOTS]
 #define GVA_TRACE_AT(slot)                                                          \
     do {                                                                            \
-        if (blockIdx.x < TRACE_CTAS && (slot) < TRACE_SLOTS)                        \
-            g_trace[blockIdx.x * TRACE_SLOTS + (slot)] = clock64();                 \
+        if ((slot) < TRACE_SLOTS) s_trace[(slot)] = clock64();                      \
+    } while (0)
+#define GVA_TRACE_FLUSH(lo, hi)                                                     \
+    do {                                                                            \
+        if (blockIdx.x < TRACE_CTAS)                                                \
+            for (int i_ = (lo); i_ < (hi) && i_ < TRACE_SLOTS; ++i_)               \
+                g_trace[blockIdx.x * TRACE_SLOTS + i_] = s_trace[i_];               \
     } while (0)
 #else
+#define GVA_TRACE_DECL
 #define GVA_TRACE_AT(slot) \
     do {                   \
+    } while (0)
+#define GVA_TRACE_FLUSH(lo, hi) \
+    do {                        \
     } while (0)
 #endif
 
@@ -102,15 +120,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but the thread may be suspended in hardware for up to `ns`
+// nanoseconds while the phase is incomplete, so waiting warps leave the issue slots
+// to the warps that have work (the producer shares its scheduler with consumers).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t a, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t WAIT_SLEEP_NS = 1000000u;   // per try; the overall limit is WAIT_LIMIT_NS
 // Bounded wait for the phase with the given parity.  Gives up (returns false) when
 // another warp raised `abort` or after WAIT_LIMIT_NS, raising abort and the status.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int *abort) {
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait_sleep(a, parity, WAIT_SLEEP_NS)) return true;
         if (*abort) return false;
         if (global_ns() - t0 > WAIT_LIMIT_NS) {
             *abort = 1;
@@ -135,6 +166,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
+// Plain (non-tensor) bulk copy of `bytes` contiguous bytes: 16-byte aligned addresses,
+// a multiple of 16 bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -155,15 +195,18 @@ __device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t &r0, uint32_t &r1) 
                  : "=r"(r0), "=r"(r1)
                  : "r"(a));
 }
+// The MMA wrappers are not volatile: they only read their operands and accumulators, so
+// the compiler may interleave independent products; the ldmatrix wrappers above stay
+// volatile so that no shared-memory read moves above the barrier wait that guards it.
 __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ void mma1688(float c[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -185,6 +228,16 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uin
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
+// One part of the bf16 hi/lo split of (x0, x1), packed: the hi part rn(x), or the
+// remainder rn(x - hi) when `lo` is set.
+__device__ __forceinline__ uint32_t part_bf16x2(float x0, float x1, bool lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    if (!lo) return *reinterpret_cast<const uint32_t *>(&h);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    return *reinterpret_cast<const uint32_t *>(&l);
+}
+
 // Byte address of the 16-byte chunk c (8 bf16 along d) of token row t of group g's
 // tile within a stage: one TMA box of 16 rows x 128 bytes per 64 columns, swizzled
 // by XOR-ing the chunk index with (row mod 8).
@@ -197,12 +250,12 @@ __device__ __forceinline__ uint32_t vtile_addr(uint32_t base, int g, int t, int 
 // ---------------------------------------------------------------------------- //
 // the kernel
 // ---------------------------------------------------------------------------- //
-template <int DH, int DR, bool GQA>
+template <int DH, int DR, bool GQA, int NT>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_r, const MmaParams mp) {
+                      const __grid_constant__ CUtensorMap tm_k, const MmaParams mp) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
+    GVA_TRACE_DECL;
     const DecodeParams &p = mp.d;
     // 1024-byte aligned base for the swizzled stages
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -212,6 +265,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     const uint32_t bar_full = base_u32 + mp.off_bar;          // NS x 8 bytes
     const uint32_t bar_empty = bar_full + 8 * NS;             // NS x 8 bytes
     volatile int *abort = reinterpret_cast<volatile int *>(base + mp.off_bar + 16 * NS);
+    // per stage: 1 when the slab's block-table entry was out of range (its tokens are skipped)
+    int *stage_bad = reinterpret_cast<int *>(base + mp.off_bar + 16 * NS + 16);
     int *Ls = reinterpret_cast<int *>(base + mp.off_f);
     int *F = Ls + p.B;
     float *merge = reinterpret_cast<float *>(base + mp.off_merge);
@@ -227,12 +282,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == mp.ncons && lane == 0) {
+    if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_v);
         if (GQA) prefetch_tmap(&tm_k);
-        if (DR > 0) prefetch_tmap(&tm_r);
     }
     if (threadIdx.x == 0) GVA_TRACE_AT(0);
+    if (threadIdx.x == 0) GVA_KT(5);
+    if (threadIdx.x == 0) GVA_CTA_T(0);
     // Lengths, row maps and the cache are final before the preceding grid (the query
     // absorption) was allowed to start, so with `early` they are read at once and the
     // cache streams while that grid still runs; the queries are read after the wait.
@@ -247,50 +303,108 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     if (s0 >= s1) return;
 
     // ============================= producer warp ============================= //
-    if (warp == mp.ncons) {
-        if (lane == 0) {
-            unsigned int last_phase_mask = 0, issued_mask = 0;  // per stage (NS <= 32)
-            int b = seq_of_slab(F, B, s0);
-            int stage = 0;
-            uint32_t round = 0;                 // times the ring has wrapped
-            const int nbox = G * (DH / 64);
-            const int nslab = (int)(s1 - s0);
-            for (int i = 0; i < nslab; ++i) {
-                const long long s = s0 + i;
-                while (F[b + 1] <= s) ++b;
-                if (round > 0 && !mbar_wait(bar_empty + 8 * stage, (round - 1) & 1u, abort)) break;
-                const long long j0 = (long long)(s - F[b]) * SLAB;
-                long long row = row_of(p.R, b, j0);
-                if (row < 0) row = 0;  // consumers mask a slab behind a bad page id
-                const int y = (int)row;
-                const uint32_t st = base_u32 + stage * mp.stage_bytes;
-                const uint32_t fb = bar_full + 8 * stage;
-                mbar_expect_tx(fb, (uint32_t)mp.tx_bytes);
-                if (mp.v3d) {
-                    tma_load_3d(st, &tm_v, 0, y, 0, fb);
-                    if (GQA) tma_load_3d(st + mp.off_k, &tm_k, 0, y, 0, fb);
-                } else {
-                    for (int bx = 0; bx < nbox; ++bx) {
-                        tma_load_2d(st + bx * 2048, &tm_v, bx * 64, y, fb);
-                        if (GQA) tma_load_2d(st + mp.off_k + bx * 2048, &tm_k, bx * 64, y, fb);
-                    }
-                }
-                if (DR > 0) tma_load_2d(st + mp.off_r, &tm_r, 0, y, fb);
-                issued_mask |= 1u << stage;
-                last_phase_mask = (last_phase_mask & ~(1u << stage)) | ((round & 1u) << stage);
-                if (i == 0) GVA_TRACE_AT(2);
-                if (++stage == NS) {
-                    stage = 0;
-                    ++round;
+    // The warp's lanes find the storage rows of the next 32 slabs together (for a paged
+    // cache the 32 block-table reads are in flight at once).  Copies are then issued
+    // `il` slabs per step, one slab per lane (lanes 0 .. il-1, consecutive slabs,
+    // consecutive ring stages), which divides the per-copy instruction overhead by il.
+    if (warp == 0) {
+        const int il = NS >= 4 ? 4 : (NS >= 2 ? 2 : 1);
+        unsigned int last_phase_mask = 0, issued_mask = 0;  // per stage (NS <= 32)
+        int stage = 0;                      // stage of the next slab to issue
+        uint32_t round = 0;                 // times the ring has wrapped at that slab
+        bool dead = false;
+        int b = seq_of_slab(F, B, s0);
+        if (lane == 0) GVA_TRACE_AT(6);
+        for (long long sb = s0; sb < s1 && !dead; sb += 32) {
+            const long long s = sb + lane;
+            int y = 0, bad = 0;
+            if (s < s1) {
+                int bl = b;
+                while (F[bl + 1] <= s) ++bl;
+                const long long row = row_of(p.R, bl, (s - F[bl]) * SLAB);
+                if (row < 0) bad = 1;       // consumers mask the slab's tokens
+                else y = (int)row;
+            }
+            {   // sequence of the first slab of the next batch of 32
+                const long long sn = sb + 32;
+                if (sn < s1) {
+                    int bl = b;
+                    while (F[bl + 1] <= sn) ++bl;
+                    b = bl;
                 }
             }
+            const int cnt = (int)min(32LL, s1 - sb);
+            if (lane == 0 && sb == s0) GVA_TRACE_AT(7);
+            for (int k0 = 0; k0 < cnt; k0 += il) {
+                const int j = lane % il;
+                const int k = k0 + j;
+                const int yk = __shfl_sync(0xffffffffu, y, k & 31);
+                const int badk = __shfl_sync(0xffffffffu, bad, k & 31);
+                const bool act = lane < il && k < cnt;
+                int st_j = stage + j;
+                uint32_t rd_j = round;
+                if (st_j >= NS) { st_j -= NS; ++rd_j; }
+                bool ok = true;
+                if (act) {
+                    if (rd_j > 0 && !mbar_wait(bar_empty + 8 * st_j, (rd_j - 1) & 1u, abort)) {
+                        ok = false;
+                    } else {
+                        const uint32_t stb = base_u32 + st_j * mp.stage_bytes;
+                        const uint32_t fb = bar_full + 8 * st_j;
+                        stage_bad[st_j] = badk;   // published by the arrive below
+                        // the positional keys of the slab are one contiguous run of rows;
+                        // rows past the end of the cache storage are not copied (their
+                        // tokens are past every sequence's end, and masked)
+                        long long rrows = p.R.num_rows - (long long)yk;
+                        rrows = rrows < SLAB ? (rrows < 0 ? 0 : rrows) : SLAB;
+                        const uint32_t rbytes = (uint32_t)rrows * (DR * 2);
+                        mbar_expect_tx(fb, (uint32_t)mp.off_r + rbytes);
+                        if (mp.v3d) {
+                            tma_load_3d(stb, &tm_v, 0, yk, 0, fb);
+                            if (GQA) tma_load_3d(stb + mp.off_k, &tm_k, 0, yk, 0, fb);
+                        } else {
+                            for (int bx = 0; bx < G * (DH / 64); ++bx) {
+                                tma_load_2d(stb + bx * 2048, &tm_v, bx * 64, yk, fb);
+                                if (GQA) tma_load_2d(stb + mp.off_k + bx * 2048, &tm_k, bx * 64, yk, fb);
+                            }
+                        }
+                        if (DR > 0 && rbytes > 0)
+                            bulk_load(stb + mp.off_r,
+                                      reinterpret_cast<const unsigned char *>(p.Krope) +
+                                          (size_t)yk * (DR * 2),
+                                      rbytes, fb);
+                        const int ti = (int)(sb - s0) + k;
+                        if (ti == 0) GVA_TRACE_AT(2);
+                        if (ti < 64) GVA_TRACE_AT(300 + ti);
+                    }
+                }
+                // bookkeeping of what is in flight (for the drain), the same in every lane
+                const unsigned done = __ballot_sync(0xffffffffu, act && ok);
+                for (int jj = 0; jj < il; ++jj) {
+                    if (!(done & (1u << jj))) continue;
+                    int sj = stage + jj;
+                    uint32_t rj = round;
+                    if (sj >= NS) { sj -= NS; ++rj; }
+                    issued_mask |= 1u << sj;
+                    last_phase_mask = (last_phase_mask & ~(1u << sj)) | ((rj & 1u) << sj);
+                }
+                dead = __any_sync(0xffffffffu, act && !ok);
+                if (dead) break;
+                stage += min(il, cnt - k0);
+                if (stage >= NS) { stage -= NS; ++round; }
+            }
+        }
+        if (lane == 0) {
             GVA_TRACE_AT(3);
+            GVA_TRACE_FLUSH(2, 4);
+            GVA_TRACE_FLUSH(6, 8);
+            GVA_TRACE_FLUSH(300, 364);
             // never leave with copies in flight: wait (bounded) for each stage's last load
-            for (int s = 0; s < NS; ++s) {
-                if (!(issued_mask & (1u << s))) continue;
-                const uint32_t par = (last_phase_mask >> s) & 1u;
+            for (int st = 0; st < NS; ++st) {
+                if (!(issued_mask & (1u << st))) continue;
+                const uint32_t par = (last_phase_mask >> st) & 1u;
                 const unsigned long long t0 = global_ns();
-                while (!mbar_try_wait(bar_full + 8 * s, par)) {
+                while (!mbar_try_wait(bar_full + 8 * st, par)) {
                     if (global_ns() - t0 > WAIT_LIMIT_NS) {
                         dev_report(GVA_DEV_TIMEOUT);
                         break;
@@ -302,18 +416,31 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
 
     // ============================= consumer warps ============================ //
-    if (warp > mp.ncons) return;      // spare warps when G does not divide the consumer count
-    const int g = warp % G;           // value group of this warp
-    const int w = warp / G;           // rank among the group's warps
+    // Products with the slab's 16 tokens on the MMA rows and the group's heads on the
+    // columns, two columns per head (the bf16 "hi" part of the query or probability and
+    // its "lo" remainder), so r <= 4 heads fill one 8-column tile with no padding:
+    //   S[16 tok x 8]    = V_g[16 tok x d_h] . Q^T[d_h x 8]  (+ K_rope . Q_r^T)
+    //   O^T[d_h x 8]    += V_g^T[d_h x 16 tok] . P^T[16 tok x 8]
+    // Lane (gid, tig) holds the scores of head 4nt + tig for tokens gid and gid + 8, and
+    // the output of the same head for dimensions 16mt + gid (+ 8).
+    const int ci = warp - 1;          // consumer index
+    if (ci >= mp.ncons) return;       // spare warps
+    const int g = ci % G;             // value group of this warp
+    const int w = ci / G;             // rank among the group's warps
     const int wpg = mp.wpg;
     const int gid = lane >> 2, tig = lane & 3;
-    const bool real_row = gid < r;    // lanes whose row (gid) is a real head of the group
-    const int h = g * r + gid;        // head of this lane's rows (when real_row)
-
+    constexpr int KD = DH / 16;       // k16 steps over d_h (and 16-row tiles of O^T)
+    constexpr int DRK16 = DR / 16;    // full k16 steps over the positional slice
+    constexpr bool DR_K8 = (DR % 16) == 8;  // one trailing k8 step
     // ldmatrix lane roles
     const int lm_mat = lane >> 3, lm_row = lane & 7;
+    // P^T exchange: the lanes holding tokens 2tig and 2tig+1 of this lane's column head
+    const int srcA = (2 * tig) * 4 + (gid >> 1), srcB = (2 * tig + 1) * 4 + (gid >> 1);
+    const bool lo_col = (gid & 1) != 0;
 
     if (mp.early) pdl_wait();         // the absorbed queries come from the preceding grid
+    if (w == 0 && g == 0 && lane == 0) GVA_KT(6);
+    if (w == 0 && g == 0 && lane == 0) GVA_CTA_T(1);
     int b = seq_of_slab(F, B, s0);
     int stage = 0, wsel = 0;          // ring stage and slab-owner counter of the next slab
     uint32_t phase = 0;
@@ -324,62 +451,104 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         while (F[b + 1] <= s) ++b;
         const long long seg_end = min(s1, (long long)F[b + 1]);
         const int Lb = Ls[b];
+        const int Fb = F[b];
 
-        // ---- query fragments for (b, g): hi part in row gid, lo part in row gid + 8 ----
-        uint32_t qa[DH / 16][4];
-        {
-            const long long qoff = ((long long)b * H + h) * DH;
+        // ---- Q^T fragments: column gid = head 4nt + gid/2, hi (gid even) or lo part ----
+        uint32_t bq[KD][NT][2];
+        uint32_t bqr[DRK16 > 0 ? DRK16 : 1][NT][2];
+        uint32_t bqr8[NT];
 #pragma unroll
-            for (int kk = 0; kk < DH / 16; ++kk) {
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                if (real_row) {
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hl = 4 * nt + (gid >> 1);
+            const bool real = hl < r;
+            const long long qoff = ((long long)b * H + g * r + hl) * DH;
+            float x[KD][4];
+#pragma unroll
+            for (int kk = 0; kk < KD; ++kk) {
+                x[kk][0] = x[kk][1] = x[kk][2] = x[kk][3] = 0.f;
+                if (real) {
                     const int d0 = kk * 16 + tig * 2;
                     if (p.qc_f32) {
                         const float *qf = reinterpret_cast<const float *>(p.qc) + qoff;
-                        x[0] = qf[d0]; x[1] = qf[d0 + 1]; x[2] = qf[d0 + 8]; x[3] = qf[d0 + 9];
+                        const float2 u = *reinterpret_cast<const float2 *>(qf + d0);
+                        const float2 v = *reinterpret_cast<const float2 *>(qf + d0 + 8);
+                        x[kk][0] = u.x; x[kk][1] = u.y; x[kk][2] = v.x; x[kk][3] = v.y;
                     } else {
                         const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(p.qc) + qoff;
-                        x[0] = __bfloat162float(qb[d0]); x[1] = __bfloat162float(qb[d0 + 1]);
-                        x[2] = __bfloat162float(qb[d0 + 8]); x[3] = __bfloat162float(qb[d0 + 9]);
+                        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qb + d0));
+                        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qb + d0 + 8));
+                        x[kk][0] = u.x; x[kk][1] = u.y; x[kk][2] = v.x; x[kk][3] = v.y;
                     }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) x[e] *= p.qc_scale;
                 }
-                split_bf16(x[0], x[1], qa[kk][0], qa[kk][1]);
-                split_bf16(x[2], x[3], qa[kk][2], qa[kk][3]);
             }
-        }
-        constexpr int DRK16 = DR / 16;          // full k16 steps over the positional slice
-        constexpr bool DR_K8 = (DR % 16) == 8;  // one trailing k8 step
-        uint32_t ra[DRK16 > 0 ? DRK16 : 1][4];
-        uint32_t ra8[2];
-        if (DR > 0) {
-            const float *qr = p.qr + ((long long)b * H + h) * DR;
+            float xr[DRK16 > 0 ? DRK16 : 1][4], xr8[2] = {0.f, 0.f};
+            if (DR > 0) {
+                // this lane's positional query pairs (d0, d0+1), (d0+8, d0+9) are RoPE
+                // pairs d0/2 and d0/2 + 4: either rotated by the absorption kernel
+                // (p.qr), or rotated here by Rot(L_b - 1) from the raw q_rope
+                const long long qo = ((long long)b * H + g * r + hl) * DR;
+                int t = Lb - 1;
+                if (t < 0) t = 0;
+                if (t >= p.rope_max_pos) {
+                    if (p.qr == nullptr && real && tig == 0 && (gid & 1) == 0)
+                        dev_report(GVA_DEV_BAD_POSITION);
+                    t = 0;
+                }
+                const float2 *cs = reinterpret_cast<const float2 *>(p.rope_tab) + (long long)t * (DR / 2);
+                auto pair = [&](int d) -> float2 {   // rotated, scaled pair (d, d + 1)
+                    if (p.qr != nullptr) return *reinterpret_cast<const float2 *>(p.qr + qo + d);
+                    float2 x;
+                    if (p.qr_f32) {
+                        x = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(p.q_rope) + qo + d);
+                    } else {
+                        x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
+                            reinterpret_cast<const __nv_bfloat16 *>(p.q_rope) + qo + d));
+                    }
+                    const float2 c = cs[d / 2];
+                    return make_float2(p.qr_scale * (x.x * c.x - x.y * c.y),
+                                       p.qr_scale * (x.x * c.y + x.y * c.x));
+                };
 #pragma unroll
-            for (int kk = 0; kk < DRK16; ++kk) {
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                if (real_row) {
-                    const int d0 = kk * 16 + tig * 2;
-                    x[0] = qr[d0]; x[1] = qr[d0 + 1]; x[2] = qr[d0 + 8]; x[3] = qr[d0 + 9];
+                for (int kk = 0; kk < DRK16; ++kk) {
+                    xr[kk][0] = xr[kk][1] = xr[kk][2] = xr[kk][3] = 0.f;
+                    if (real) {
+                        const int d0 = kk * 16 + tig * 2;
+                        const float2 u = pair(d0);
+                        const float2 v = pair(d0 + 8);
+                        xr[kk][0] = u.x; xr[kk][1] = u.y; xr[kk][2] = v.x; xr[kk][3] = v.y;
+                    }
                 }
-                split_bf16(x[0], x[1], ra[kk][0], ra[kk][1]);
-                split_bf16(x[2], x[3], ra[kk][2], ra[kk][3]);
+                if (DR_K8 && real) {
+                    const float2 u = pair(DRK16 * 16 + tig * 2);
+                    xr8[0] = u.x; xr8[1] = u.y;
+                }
             }
-            if (DR_K8) {
-                float x0 = 0.f, x1 = 0.f;
-                if (real_row) {
-                    const int d0 = DRK16 * 16 + tig * 2;
-                    x0 = qr[d0]; x1 = qr[d0 + 1];
+#pragma unroll
+            for (int kk = 0; kk < KD; ++kk) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[kk][e] *= p.qc_scale;
+                bq[kk][nt][0] = part_bf16x2(x[kk][0], x[kk][1], lo_col);
+                bq[kk][nt][1] = part_bf16x2(x[kk][2], x[kk][3], lo_col);
+            }
+            if (DR > 0) {
+#pragma unroll
+                for (int kk = 0; kk < DRK16; ++kk) {
+                    bqr[kk][nt][0] = part_bf16x2(xr[kk][0], xr[kk][1], lo_col);
+                    bqr[kk][nt][1] = part_bf16x2(xr[kk][2], xr[kk][3], lo_col);
                 }
-                split_bf16(x0, x1, ra8[0], ra8[1]);
+                if (DR_K8) bqr8[nt] = part_bf16x2(xr8[0], xr8[1], lo_col);
             }
         }
 
-        float oacc[DH / 8][4];
+        float oacc[KD][NT][4];
 #pragma unroll
-        for (int nd = 0; nd < DH / 8; ++nd)
-            oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
-        float m_run = -INFINITY, l_run = 0.f;
+        for (int mt = 0; mt < KD; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
+        float m_run[NT], l_run[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) { m_run[nt] = -INFINITY; l_run[nt] = 0.f; }
 
         if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(4);
         for (; s < seg_end; ++s) {
@@ -394,178 +563,230 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 continue;
             }
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(8 + 2 * tslab);
-            const long long j0 = (long long)(s - F[b]) * SLAB;
-            int nv = (int)min((long long)SLAB, (long long)Lb - j0);
-            if (row_of(p.R, b, j0) < 0) {
+            const int j0 = (int)(s - Fb) * SLAB;
+            int nv = min(SLAB, Lb - j0);
+            if (stage_bad[my_stage]) {
                 if (lane == 0 && g == 0) dev_report(GVA_DEV_BAD_PAGE);
                 nv = 0;
             }
             const uint32_t st = base_u32 + my_stage * mp.stage_bytes;
             const uint32_t kst = GQA ? st + mp.off_k : st;
 
-            // ---- scores S^T = Q . K^T for tokens 8nt .. 8nt+7 ----
-            float sc[2][4];
+            // ---- scores: A = the key tile (tokens x d), B = Q^T ----
+            float sc[NT][2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int kp = 0; kp < DH / 32; ++kp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(vtile_addr<DH>(kst, g, nt * 8 + lm_row, kp * 4 + lm_mat), b0, b1, b2, b3);
-                    mma16816(sc[nt], qa[2 * kp], b0, b1);
-                    mma16816(sc[nt], qa[2 * kp + 1], b2, b3);
+                for (int a2 = 0; a2 < 2; ++a2)
+                    sc[nt][a2][0] = sc[nt][a2][1] = sc[nt][a2][2] = sc[nt][a2][3] = 0.f;
+            {
+                uint32_t av[KD][4];
+#pragma unroll
+                for (int kk = 0; kk < KD; ++kk)
+                    ldsm_x4(vtile_addr<DH>(kst, g, lm_row + 8 * (lm_mat & 1), 2 * kk + (lm_mat >> 1)),
+                            av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
+                uint32_t ar[DRK16 > 0 ? DRK16 : 1][4], ar8[2];
+                if (DR > 0) {
+                    const uint32_t rbase = st + mp.off_r;
+#pragma unroll
+                    for (int kk = 0; kk < DRK16; ++kk)
+                        ldsm_x4(rbase + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + (2 * kk + (lm_mat >> 1)) * 16,
+                                ar[kk][0], ar[kk][1], ar[kk][2], ar[kk][3]);
+                    if (DR_K8)
+                        ldsm_x2(rbase + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + DRK16 * 32, ar8[0], ar8[1]);
+                }
+#pragma unroll
+                for (int kk = 0; kk < KD; ++kk)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816(sc[nt][kk & 1], av[kk], bq[kk][nt][0], bq[kk][nt][1]);
+                if (DR > 0) {
+#pragma unroll
+                    for (int kk = 0; kk < DRK16; ++kk)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816(sc[nt][(KD + kk) & 1], ar[kk], bqr[kk][nt][0], bqr[kk][nt][1]);
+                    if (DR_K8) {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma1688(sc[nt][(KD + DRK16) & 1], ar8[0], ar8[1], bqr8[nt]);
+                    }
                 }
             }
-            if (DR > 0) {
-                const uint32_t rbase = st + mp.off_r;
+            // value tiles for the weighted sum (V^T as the A operand): loaded now,
+            // consumed after the softmax
+            uint32_t apv[KD][4];
 #pragma unroll
-                for (int kk = 0; kk < DRK16; ++kk) {
-                    // matrices: (nt0, chunk 2kk), (nt0, 2kk+1), (nt1, 2kk), (nt1, 2kk+1)
-                    const int t = (lm_mat >> 1) * 8 + lm_row;
-                    const int ch = 2 * kk + (lm_mat & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(rbase + t * (DR * 2) + ch * 16, b0, b1, b2, b3);
-                    mma16816(sc[0], ra[kk], b0, b1);
-                    mma16816(sc[1], ra[kk], b2, b3);
-                }
-                if (DR_K8) {
-                    const int t = (lm_mat & 1) * 8 + lm_row;
-                    uint32_t b0, b1;
-                    ldsm_x2(rbase + t * (DR * 2) + DRK16 * 32, b0, b1);
-                    mma1688(sc[0], ra8[0], ra8[1], b0);
-                    mma1688(sc[1], ra8[0], ra8[1], b1);
+            for (int mt = 0; mt < KD; ++mt)
+                ldsm_x4_t(vtile_addr<DH>(st, g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
+                          apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
+
+            // ---- per head: hi + lo columns -> score of tokens gid, gid + 8 ----
+            float z[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                z[nt][0] = (sc[nt][0][0] + sc[nt][0][1]) + (sc[nt][1][0] + sc[nt][1][1]);
+                z[nt][1] = (sc[nt][0][2] + sc[nt][0][3]) + (sc[nt][1][2] + sc[nt][1][3]);
+                if (gid >= nv) z[nt][0] = -INFINITY;
+                if (gid + 8 >= nv) z[nt][1] = -INFINITY;
+            }
+            float mloc[NT];
+            bool raise_any = false;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float m = fmaxf(z[nt][0], z[nt][1]);
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                mloc[nt] = m;
+                raise_any |= m > m_run[nt] + MMA_RESCALE_TH;
+            }
+            if (__any_sync(0xffffffffu, raise_any)) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const bool raise = mloc[nt] > m_run[nt] + MMA_RESCALE_TH;
+                    const float alpha = raise ? exp2f(m_run[nt] - mloc[nt]) : 1.f;  // 0 when m_run = -inf
+                    if (raise) m_run[nt] = mloc[nt];
+                    l_run[nt] *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < KD; ++mt) {
+                        oacc[mt][nt][0] *= alpha; oacc[mt][nt][1] *= alpha;
+                        oacc[mt][nt][2] *= alpha; oacc[mt][nt][3] *= alpha;
+                    }
                 }
             }
-            // ---- hi + lo rows -> one score per (head gid, token) ----
-            // lane holds tokens 8nt + 2tig + {0,1}
-            float z[2][2];
+            // ---- probabilities, then P^T as the B operand (column gid: head 4nt + gid/2) ----
+            uint32_t bp[NT][2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                z[nt][0] = sc[nt][0] + sc[nt][2];
-                z[nt][1] = sc[nt][1] + sc[nt][3];
+            for (int nt = 0; nt < NT; ++nt) {
+                const float p0 = z[nt][0] == -INFINITY ? 0.f : exp2f(z[nt][0] - m_run[nt]);
+                const float p1 = z[nt][1] == -INFINITY ? 0.f : exp2f(z[nt][1] - m_run[nt]);
+                l_run[nt] += p0 + p1;
+                const float a0 = __shfl_sync(0xffffffffu, p0, srcA);   // token 2tig
+                const float a1 = __shfl_sync(0xffffffffu, p1, srcA);   // token 2tig + 8
+                const float b0 = __shfl_sync(0xffffffffu, p0, srcB);   // token 2tig + 1
+                const float b1 = __shfl_sync(0xffffffffu, p1, srcB);   // token 2tig + 9
+                bp[nt][0] = part_bf16x2(a0, b0, lo_col);
+                bp[nt][1] = part_bf16x2(a1, b1, lo_col);
             }
+            // ---- O^T += V^T . P^T ----
             if (nv < SLAB) {
+                // zero the values of tokens past the end (they may hold NaN)
+                const int ta = 2 * tig, tb = 8 + 2 * tig;
+                const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
+                const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        if (nt * 8 + 2 * tig + e >= nv) z[nt][e] = -INFINITY;
-            }
-            float mloc = fmaxf(fmaxf(z[0][0], z[0][1]), fmaxf(z[1][0], z[1][1]));
-            mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-            mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-            const bool raise = mloc > m_run + MMA_RESCALE_TH;
-            if (__any_sync(0xffffffffu, raise)) {
-                const float alpha = raise ? exp2f(m_run - mloc) : 1.f;  // 0 when m_run = -inf
-                if (raise) m_run = mloc;
-                l_run *= alpha;
-#pragma unroll
-                for (int nd = 0; nd < DH / 8; ++nd) {
-                    oacc[nd][0] *= alpha; oacc[nd][1] *= alpha;
-                    oacc[nd][2] *= alpha; oacc[nd][3] *= alpha;
+                for (int mt = 0; mt < KD; ++mt) {
+                    apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
                 }
             }
-            float pr[2][2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int mt = 0; mt < KD; ++mt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float v = exp2f(z[nt][e] - m_run);
-                    pr[nt][e] = (z[nt][e] == -INFINITY) ? 0.f : v;
-                }
-            l_run += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-            // ---- P as the A operand: rows gid (hi) / gid + 8 (lo), k = token ----
-            uint32_t pa[4];
-            split_bf16(pr[0][0], pr[0][1], pa[0], pa[1]);
-            split_bf16(pr[1][0], pr[1][1], pa[2], pa[3]);
-            // ---- O += P . V ----
-#pragma unroll
-            for (int np = 0; np < DH / 16; ++np) {
-                // matrices: (tok 0-7, chunk 2np), (tok 8-15, 2np), (tok 0-7, 2np+1), (tok 8-15, 2np+1)
-                const int t = (lm_mat & 1) * 8 + lm_row;
-                const int ch = 2 * np + (lm_mat >> 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vtile_addr<DH>(st, g, t, ch), b0, b1, b2, b3);
-                if (nv < SLAB) {
-                    // zero the values of tokens past the end (they may hold NaN)
-                    const int ta = 2 * tig, tb = 8 + 2 * tig;
-                    const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
-                    const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
-                    b0 &= ma; b1 &= mb; b2 &= ma; b3 &= mb;
-                }
-                mma16816(oacc[2 * np], pa, b0, b1);
-                mma16816(oacc[2 * np + 1], pa, b2, b3);
-            }
+                for (int nt = 0; nt < NT; ++nt)
+                    mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
+            // the products above consumed every tile register, so all of the warp's
+            // shared-memory reads of the stage are complete: release it to the producer
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * my_stage);
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(9 + 2 * tslab);
             ++tslab;
         }
 
-        // ---- segment end: fold hi/lo rows, reduce l over the quad, merge the group's warps ----
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-        float o2[DH / 8][2];
+        // ---- segment end: fold hi/lo columns, reduce l over the 8 token lanes, merge
+        //      the group's warps ----
+        float o2[KD][NT][2];   // O[head 4nt + tig][16mt + gid (+8)]
 #pragma unroll
-        for (int nd = 0; nd < DH / 8; ++nd) {
-            o2[nd][0] = oacc[nd][0] + oacc[nd][2];
-            o2[nd][1] = oacc[nd][1] + oacc[nd][3];
+        for (int mt = 0; mt < KD; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                o2[mt][nt][0] = oacc[mt][nt][0] + oacc[mt][nt][1];
+                o2[mt][nt][1] = oacc[mt][nt][2] + oacc[mt][nt][3];
+            }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 4);
+            l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 8);
+            l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], 16);
         }
         if (wpg > 1) {
-            // slot per (extra warp, group): 8 heads x (DH + 2) floats
-            const int stride = 8 * (DH + 2);
+            // slot per (extra warp, group): 4 NT heads x (DH + 2) floats
+            const int stride = 4 * NT * (DH + 2);
             if (w > 0) {
-                float *mb = merge + ((w - 1) * G + g) * stride + gid * (DH + 2);
 #pragma unroll
-                for (int nd = 0; nd < DH / 8; ++nd) {
-                    mb[nd * 8 + 2 * tig] = o2[nd][0];
-                    mb[nd * 8 + 2 * tig + 1] = o2[nd][1];
+                for (int nt = 0; nt < NT; ++nt) {
+                    float *mb = merge + ((w - 1) * G + g) * stride + (4 * nt + tig) * (DH + 2);
+#pragma unroll
+                    for (int mt = 0; mt < KD; ++mt) {
+                        mb[16 * mt + gid] = o2[mt][nt][0];
+                        mb[16 * mt + gid + 8] = o2[mt][nt][1];
+                    }
+                    if (gid == 0) { mb[DH] = m_run[nt]; mb[DH + 1] = l_run[nt]; }
                 }
-                if (tig == 0) { mb[DH] = m_run; mb[DH + 1] = l_run; }
             }
             named_bar(1 + g, wpg * 32);
             if (w == 0) {
                 for (int ww = 1; ww < wpg; ++ww) {
-                    const float *mb = merge + ((ww - 1) * G + g) * stride + gid * (DH + 2);
-                    const float m2 = mb[DH], l2 = mb[DH + 1];
-                    const float mn = fmaxf(m_run, m2);
-                    const float a1 = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mn);
-                    const float a2 = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mn);
 #pragma unroll
-                    for (int nd = 0; nd < DH / 8; ++nd) {
-                        o2[nd][0] = o2[nd][0] * a1 + mb[nd * 8 + 2 * tig] * a2;
-                        o2[nd][1] = o2[nd][1] * a1 + mb[nd * 8 + 2 * tig + 1] * a2;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const float *mb = merge + ((ww - 1) * G + g) * stride + (4 * nt + tig) * (DH + 2);
+                        const float m2 = mb[DH], l2 = mb[DH + 1];
+                        const float mn = fmaxf(m_run[nt], m2);
+                        const float a1 = (m_run[nt] == -INFINITY) ? 0.f : exp2f(m_run[nt] - mn);
+                        const float a2 = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mn);
+#pragma unroll
+                        for (int mt = 0; mt < KD; ++mt) {
+                            o2[mt][nt][0] = o2[mt][nt][0] * a1 + mb[16 * mt + gid] * a2;
+                            o2[mt][nt][1] = o2[mt][nt][1] * a1 + mb[16 * mt + gid + 8] * a2;
+                        }
+                        l_run[nt] = l_run[nt] * a1 + l2 * a2;
+                        m_run[nt] = mn;
                     }
-                    l_run = l_run * a1 + l2 * a2;
-                    m_run = mn;
                 }
             }
             named_bar(1 + g, wpg * 32);
         }
         if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(5);
-        if (w == 0 && real_row) {
-            const bool whole = F[b] >= s0 && F[b + 1] <= s1;
-            if (whole) {
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                float *o = p.out + ((long long)b * H + h) * DH;
+        if (w == 0) {
+            const bool whole = Fb >= s0 && F[b + 1] <= s1;
 #pragma unroll
-                for (int nd = 0; nd < DH / 8; ++nd)
-                    *reinterpret_cast<float2 *>(o + nd * 8 + 2 * tig) =
-                        make_float2(o2[nd][0] * inv, o2[nd][1] * inv);
-                if (tig == 0 && p.lse)
-                    p.lse[(long long)b * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
-            } else {
-                const long long slot = (long long)c + b;
-                float *o = p.part_o + (slot * H + h) * DH;
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hl = 4 * nt + tig;
+                if (hl >= r) continue;
+                const int h = g * r + hl;
+                if (whole) {
+                    const float inv = l_run[nt] > 0.f ? 1.f / l_run[nt] : 0.f;
+                    float *o = p.out + ((long long)b * H + h) * DH;
 #pragma unroll
-                for (int nd = 0; nd < DH / 8; ++nd)
-                    *reinterpret_cast<float2 *>(o + nd * 8 + 2 * tig) = make_float2(o2[nd][0], o2[nd][1]);
-                if (tig == 0) {
-                    p.part_ml[(slot * H + h) * 2] = m_run;
-                    p.part_ml[(slot * H + h) * 2 + 1] = l_run;
+                    for (int mt = 0; mt < KD; ++mt) {
+                        o[16 * mt + gid] = o2[mt][nt][0] * inv;
+                        o[16 * mt + gid + 8] = o2[mt][nt][1] * inv;
+                    }
+                    if (gid == 0 && p.lse)
+                        p.lse[(long long)b * H + h] =
+                            l_run[nt] > 0.f ? (m_run[nt] + log2f(l_run[nt])) * LN2 : -INFINITY;
+                } else {
+                    const long long slot = (long long)c + b;
+                    float *o = p.part_o + (slot * H + h) * DH;
+#pragma unroll
+                    for (int mt = 0; mt < KD; ++mt) {
+                        o[16 * mt + gid] = o2[mt][nt][0];
+                        o[16 * mt + gid + 8] = o2[mt][nt][1];
+                    }
+                    if (gid == 0) {
+                        p.part_ml[(slot * H + h) * 2] = m_run[nt];
+                        p.part_ml[(slot * H + h) * 2 + 1] = l_run[nt];
+                    }
                 }
             }
         }
+    }
+    if (w == 0 && g == 0 && lane == 0) {
+        GVA_KT(7);
+        GVA_CTA_T(2);
+        GVA_TRACE_FLUSH(0, 2);
+        GVA_TRACE_FLUSH(4, 6);
+        GVA_TRACE_FLUSH(8, 8 + 2 * tslab);
     }
 }
 
@@ -628,9 +849,24 @@ inline bool make_map3(CUtensorMap *m, const void *ptr, long long rows, int width
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+#ifdef GVA_TRACE
+constexpr int MMA_SMEM_LIMIT = 227 * 1024 - TRACE_SLOTS * 8;   // the trace buffer is static
+#else
 constexpr int MMA_SMEM_LIMIT = 227 * 1024;
+#endif
+// The stage ring is sized to leave room on the SM for the query-absorption grid that
+// precedes the decode: with programmatic dependent launch the decode's CTAs start
+// while that grid's CTAs are still resident, and stream the cache meanwhile.
+constexpr int MMA_SMEM_TARGET = 196 * 1024;
 
-inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa) {
+inline int bar_region_bytes(int ns) { return (int)align_up(16 * ns + 16 + 4 * ns, 16); }
+
+// Merge buffer of the group's extra warps: per (extra warp, group) 4 NT heads x (DH + 2).
+inline int merge_bytes_of(int wpg, int G, int DH, int NT) {
+    return (wpg - 1) * G * 4 * NT * (DH + 2) * 4;
+}
+
+inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
     const DecodeParams &d = mp.d;
     const int vbytes = d.G * DH * SLAB * 2;
     mp.off_k = vbytes;
@@ -641,33 +877,33 @@ inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa) {
     mp.wpg = MMA_CONSUMERS / d.G;
     if (mp.wpg < 1) mp.wpg = 1;
     mp.ncons = d.G * mp.wpg;
-    const int merge_bytes = (mp.wpg - 1) * d.G * 8 * (DH + 2) * 4;
+    const int merge_bytes = merge_bytes_of(mp.wpg, d.G, DH, NT);
     const int fixed = 1024 /* alignment slack */ + (int)align_up(sizeof(int) * (2 * d.B + 1), 16) +
-                      merge_bytes + 16 * MMA_MAX_STAGES + 16;
-    int ns = (MMA_SMEM_LIMIT - fixed) / mp.stage_bytes;
+                      merge_bytes + bar_region_bytes(MMA_MAX_STAGES);
+    int ns = (MMA_SMEM_TARGET - fixed) / mp.stage_bytes;
+    if (ns < 4) ns = (MMA_SMEM_LIMIT - fixed) / mp.stage_bytes;
     if (ns > MMA_MAX_STAGES) ns = MMA_MAX_STAGES;
     if (ns < 2) return false;
     mp.nstages = ns;
     mp.off_bar = ns * mp.stage_bytes;
-    mp.off_f = mp.off_bar + (int)align_up(16 * ns + 16, 16);
+    mp.off_f = mp.off_bar + bar_region_bytes(ns);
     mp.off_merge = mp.off_f + (int)align_up(sizeof(int) * (2 * d.B + 1), 16);
     return true;
 }
 
-inline size_t mma_smem_bytes(const MmaParams &mp, int DH) {
-    const int merge_bytes = (mp.wpg - 1) * mp.d.G * 8 * (DH + 2) * 4;
-    return 1024 + (size_t)mp.off_merge + merge_bytes;
+inline size_t mma_smem_bytes(const MmaParams &mp, int DH, int NT) {
+    return 1024 + (size_t)mp.off_merge + merge_bytes_of(mp.wpg, mp.d.G, DH, NT);
 }
 
-template <int DH, int DR, bool GQA>
+template <int DH, int DR, bool GQA, int NT>
 inline int launch_mma_t(void *stream, MmaParams &mp, const CUtensorMap &tv, const CUtensorMap &tk,
-                        const CUtensorMap &tr, int grid) {
-    auto kern = decode_mma_kernel<DH, DR, GQA>;
-    const size_t smem = mma_smem_bytes(mp, DH);
+                        int grid) {
+    auto kern = decode_mma_kernel<DH, DR, GQA, NT>;
+    const size_t smem = mma_smem_bytes(mp, DH, NT);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(MMA_THREADS);
+    cfg.blockDim = dim3((mp.ncons + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -675,18 +911,16 @@ inline int launch_mma_t(void *stream, MmaParams &mp, const CUtensorMap &tv, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_allowed(cfg.stream) ? 1 : 0;
-    return cuda_status(cudaLaunchKernelEx(&cfg, kern, tv, tk, tr, mp));
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, tv, tk, mp));
 }
 
 // Shared-memory opt-in of every instantiation (once per device, before any launch).
-inline cudaError_t mma_opt_in_all() {
+template <int DH, int NT>
+inline cudaError_t mma_opt_in_dh() {
     const void *ks[] = {
-        (const void *)decode_mma_kernel<64, 0, false>, (const void *)decode_mma_kernel<64, 8, false>,
-        (const void *)decode_mma_kernel<64, 16, false>, (const void *)decode_mma_kernel<64, 24, false>,
-        (const void *)decode_mma_kernel<64, 32, false>, (const void *)decode_mma_kernel<64, 0, true>,
-        (const void *)decode_mma_kernel<128, 0, false>, (const void *)decode_mma_kernel<128, 8, false>,
-        (const void *)decode_mma_kernel<128, 16, false>, (const void *)decode_mma_kernel<128, 24, false>,
-        (const void *)decode_mma_kernel<128, 32, false>, (const void *)decode_mma_kernel<128, 0, true>};
+        (const void *)decode_mma_kernel<DH, 0, false, NT>, (const void *)decode_mma_kernel<DH, 8, false, NT>,
+        (const void *)decode_mma_kernel<DH, 16, false, NT>, (const void *)decode_mma_kernel<DH, 24, false, NT>,
+        (const void *)decode_mma_kernel<DH, 32, false, NT>, (const void *)decode_mma_kernel<DH, 0, true, NT>};
     for (const void *k : ks) {
         const cudaError_t e =
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_LIMIT);
@@ -694,17 +928,24 @@ inline cudaError_t mma_opt_in_all() {
     }
     return cudaSuccess;
 }
+inline cudaError_t mma_opt_in_all() {
+    cudaError_t e = mma_opt_in_dh<64, 1>();
+    if (e == cudaSuccess) e = mma_opt_in_dh<64, 2>();
+    if (e == cudaSuccess) e = mma_opt_in_dh<128, 1>();
+    if (e == cudaSuccess) e = mma_opt_in_dh<128, 2>();
+    return e;
+}
 
-template <int DH>
+template <int DH, int NT>
 inline int launch_mma_dr(void *stream, MmaParams &mp, const CUtensorMap &tv, const CUtensorMap &tk,
-                         const CUtensorMap &tr, int grid, int DR, bool gqa) {
-    if (gqa) return launch_mma_t<DH, 0, true>(stream, mp, tv, tk, tr, grid);
+                         int grid, int DR, bool gqa) {
+    if (gqa) return launch_mma_t<DH, 0, true, NT>(stream, mp, tv, tk, grid);
     switch (DR) {
-    case 0: return launch_mma_t<DH, 0, false>(stream, mp, tv, tk, tr, grid);
-    case 8: return launch_mma_t<DH, 8, false>(stream, mp, tv, tk, tr, grid);
-    case 16: return launch_mma_t<DH, 16, false>(stream, mp, tv, tk, tr, grid);
-    case 24: return launch_mma_t<DH, 24, false>(stream, mp, tv, tk, tr, grid);
-    case 32: return launch_mma_t<DH, 32, false>(stream, mp, tv, tk, tr, grid);
+    case 0: return launch_mma_t<DH, 0, false, NT>(stream, mp, tv, tk, grid);
+    case 8: return launch_mma_t<DH, 8, false, NT>(stream, mp, tv, tk, grid);
+    case 16: return launch_mma_t<DH, 16, false, NT>(stream, mp, tv, tk, grid);
+    case 24: return launch_mma_t<DH, 24, false, NT>(stream, mp, tv, tk, grid);
+    case 32: return launch_mma_t<DH, 32, false, NT>(stream, mp, tv, tk, grid);
     default: return GVA_ERR_UNSUPPORTED;
     }
 }
@@ -716,9 +957,10 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
     MmaParams mp;
     mp.d = dp;
     const int DH = dp.d_h, DR = gqa ? 0 : dp.d_r;
-    if (!plan_mma(mp, DH, DR, gqa)) return GVA_ERR_UNSUPPORTED;
+    const int NT = dp.r <= 4 ? 1 : 2;   // 8-column tiles holding the group's heads (hi, lo)
+    if (!plan_mma(mp, DH, DR, gqa, NT)) return GVA_ERR_UNSUPPORTED;
     const long long nrows = rows.num_rows > 0 ? rows.num_rows : 1;
-    CUtensorMap tv, tk, tr;
+    CUtensorMap tv, tk;
     mp.early = early ? 1 : 0;
     mp.v3d = make_map3(&tv, dp.Vc, nrows, dp.G * DH) &&
              (!gqa || make_map3(&tk, dp.Kc, nrows, dp.G * DH));
@@ -727,14 +969,15 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
         if (gqa && !make_map(&tk, dp.Kc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
     }
     if (!gqa) tk = tv;
-    tr = tv;
-    if (DR > 0 && !make_map(&tr, dp.Krope, nrows, DR, DR, false)) return GVA_ERR_CUDA;
     int grid = req_ctas > 0 ? req_ctas : sms;
     if (grid > sms * 8) grid = sms * 8;
     dp.n_ctas = grid;
     mp.d.n_ctas = grid;
-    return DH == 64 ? launch_mma_dr<64>(stream, mp, tv, tk, tr, grid, DR, gqa)
-                    : launch_mma_dr<128>(stream, mp, tv, tk, tr, grid, DR, gqa);
+    if (DH == 64)
+        return NT == 1 ? launch_mma_dr<64, 1>(stream, mp, tv, tk, grid, DR, gqa)
+                       : launch_mma_dr<64, 2>(stream, mp, tv, tk, grid, DR, gqa);
+    return NT == 1 ? launch_mma_dr<128, 1>(stream, mp, tv, tk, grid, DR, gqa)
+                   : launch_mma_dr<128, 2>(stream, mp, tv, tk, grid, DR, gqa);
 }
 
 }  // namespace gva

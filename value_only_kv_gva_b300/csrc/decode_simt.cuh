@@ -17,7 +17,13 @@ struct DecodeParams {
     const void *qc;         // content query [B][H][d_h]
     int qc_f32;             // 1: fp32, 0: bf16
     float qc_scale;         // multiplies qc when loaded (softmax scale in log2 units)
-    const float *qr;        // positional query [B][H][d_r], already scaled (GVA)
+    const float *qr;        // positional query [B][H][d_r], already rotated and scaled (GVA)
+    // the raw positional query, rotated in the tensor-core decode when qr is null
+    const void *q_rope;     // [B][H][d_r], q_dtype
+    int qr_f32;             // 1: q_rope fp32, 0: bf16
+    const float *rope_tab;  // [rope_max_pos][d_r/2][2] (cos, sin)
+    int rope_max_pos;
+    float qr_scale;         // multiplies the rotated q_rope (softmax scale in log2 units)
     float *out;             // [B][H][d_h]
     float *lse;             // [B][H] or null
     float *part_o;          // [slots][H][d_h]
@@ -235,10 +241,11 @@ __global__ void __launch_bounds__(SIMT_THREADS) decode_simt_kernel(const DecodeP
 // Log-sum-exp combine of split-K partials (flash-decoding):
 //   m* = max_s m_s,  o = sum_s 2^(m_s - m*) o_s / sum_s 2^(m_s - m*) l_s,
 //   lse = (m* + log2 sum_s 2^(m_s - m*) l_s) ln 2.
-// Grid (B*H, ceil(d_h/32)), 128 threads = 4 part lanes x 32 dimensions.  Every global
-// load of a phase is independent of the others, so a phase costs one memory round
-// trip: lengths, then the parts' (m, l), then the parts' o slices.  Sequences owned by
-// a single CTA were finished by the decode kernel; empty ones get out = 0, lse = -inf.
+// Grid (B*H, ceil(d_h/32)), 128 threads = 4 part lanes x 32 dimensions.  Two memory
+// round trips after the grid dependency: the lengths (final before the decode call,
+// so they are read while the decode kernel still runs), then every part's (m, l) and
+// o slice at once; the weights are applied in registers.  Sequences owned by a single
+// CTA were finished by the decode kernel; empty ones get out = 0, lse = -inf.
 // --------------------------------------------------------------------------- //
 struct CombineParams {
     int B, H, d_h;
@@ -252,15 +259,21 @@ struct CombineParams {
 };
 
 constexpr int COMBINE_THREADS = 128;
-constexpr int COMBINE_MAX_PARTS = 4096;   // >= the largest decode grid
+constexpr int COMBINE_BATCH = 16;         // o loads in flight per thread
+
+// Dynamic shared memory: 2 x n_ctas floats (a sequence spans at most n_ctas parts).  It
+// is kept small so that the combine's CTAs fit beside the decode's on an SM and start
+// (then wait on the grid dependency) while the decode still runs.
+inline size_t combine_smem_bytes(int n_ctas) { return sizeof(float) * 2 * (size_t)n_ctas; }
 
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineParams p) {
-    __shared__ float w_s[COMBINE_MAX_PARTS];   // part weight 2^(m - m*), 0 for no part
-    __shared__ float l_s[COMBINE_MAX_PARTS];
+    extern __shared__ float comb_dyn[];
+    float *w_s = comb_dyn;                 // part weight 2^(m - m*), 0 for no part
+    float *l_s = comb_dyn + p.n_ctas;
     __shared__ long long red_ll[2][COMBINE_THREADS / 32];
     __shared__ float red_f[COMBINE_THREADS / 32];
     __shared__ float acc_s[4][32];
-    pdl_wait();
+    if (threadIdx.x == 0) GVA_KT(8);
     pdl_launch_dependents();
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -288,6 +301,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     const long long nb = (Lb + SLAB - 1) / SLAB;
     const int d0 = blockIdx.y * 32;
     float *out = p.out + ((long long)b * p.H + h) * p.d_h;
+    // the partials (and the outputs the decode kernel writes) come from the preceding grid
+    pdl_wait();
+    if (threadIdx.x == 0) GVA_KT(9);
     if (nb == 0) {
         if (tid < 32 && d0 + tid < p.d_h) out[d0 + tid] = 0.f;
         if (tid == 0 && blockIdx.y == 0 && p.lse) p.lse[(long long)b * p.H + h] = -INFINITY;
@@ -297,14 +313,23 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     const int c_lo = P.cta_of(Fb), c_hi = P.cta_of(Fb + nb - 1);
     if (c_lo == c_hi) return;
     const int n = c_hi - c_lo + 1;
-    // ---- parts' (m, l) and the running maximum ----
+    const int i = d0 + lane;
+    const long long step = (long long)p.H * p.d_h;   // next slot (c + 1 + b)
+    const float *po = p.part_o + (((long long)c_lo + b) * p.H + h) * p.d_h + i;
+    // ---- every part's (m, l), and this thread's first batch of o values, in one trip ----
+    float ov[COMBINE_BATCH];
+#pragma unroll
+    for (int u = 0; u < COMBINE_BATCH; ++u) {
+        const int k = wid + 4 * u;
+        ov[u] = (k < n && i < p.d_h) ? po[(long long)k * step] : 0.f;
+    }
     float mloc = -INFINITY;
     for (int k = tid; k < n; k += COMBINE_THREADS) {
-        const int c = c_lo + k;
+        // a CTA with an empty share (more CTAs than slabs) wrote no partial: weight 0
         float m = -INFINITY, l = 0.f;
-        if (P.start(c) != P.start(c + 1)) {
+        if (P.start(c_lo + k) != P.start(c_lo + k + 1)) {
             const float2 ml = *reinterpret_cast<const float2 *>(
-                p.part_ml + (((long long)c + b) * p.H + h) * 2);
+                p.part_ml + (((long long)c_lo + k + b) * p.H + h) * 2);
             m = ml.x;
             l = ml.y;
         }
@@ -335,15 +360,22 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
 #pragma unroll
     for (int w = 0; w < COMBINE_THREADS / 32; ++w) den += red_f[w];
     // ---- weighted sum of this CTA's 32-dimension slice: part lane wid, dimension lane ----
-    const int i = d0 + lane;
     float acc = 0.f;
-    if (i < p.d_h) {
-        const float *po = p.part_o + (((long long)c_lo + b) * p.H + h) * p.d_h + i;
-        const long long step = (long long)p.H * p.d_h;   // next slot (c + 1 + b)
-#pragma unroll 4
-        for (int k = wid; k < n; k += 4) {
-            const float wgt = w_s[k];
-            if (wgt != 0.f) acc += wgt * po[(long long)k * step];
+#pragma unroll
+    for (int u = 0; u < COMBINE_BATCH; ++u) {
+        const int k = wid + 4 * u;
+        if (k < n && w_s[k] != 0.f) acc += w_s[k] * ov[u];
+    }
+    for (int k0 = wid + 4 * COMBINE_BATCH; k0 < n; k0 += 4 * COMBINE_BATCH) {
+#pragma unroll
+        for (int u = 0; u < COMBINE_BATCH; ++u) {
+            const int k = k0 + 4 * u;
+            ov[u] = (k < n && i < p.d_h) ? po[(long long)k * step] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < COMBINE_BATCH; ++u) {
+            const int k = k0 + 4 * u;
+            if (k < n && w_s[k] != 0.f) acc += w_s[k] * ov[u];
         }
     }
     acc_s[wid][lane] = acc;
@@ -354,6 +386,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     }
     if (tid == 0 && blockIdx.y == 0 && p.lse)
         p.lse[(long long)b * p.H + h] = den > 0.f ? (mstar + log2f(den)) * LN2 : -INFINITY;
+    if (tid == 0) GVA_KT(10);
 }
 
 }  // namespace gva

@@ -204,7 +204,7 @@ int launch_combine(void *stream, const DecodeParams &dp, const gva_rows &rows) {
     cp.lse = dp.lse;
     cp.n_ctas = dp.n_ctas;
     return cuda_status(launch(combine_kernel, dim3(dp.B * dp.H, (dp.d_h + 31) / 32),
-                              dim3(COMBINE_THREADS), 0, stream, cp));
+                              dim3(COMBINE_THREADS), combine_smem_bytes(dp.n_ctas), stream, cp));
 }
 
 // Sets dp.n_ctas (the combine kernel re-derives the partition from it) and launches.
@@ -222,8 +222,9 @@ int run_simt(void *stream, DecodeParams &dp, int sms, int req_ctas) {
 int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
                   const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
                   float prescale, float *q_tilde, float *q_hat, int sms,
-                  const gva_rows *rows = nullptr) {
+                  const gva_rows *rows = nullptr, bool skip_rope = false) {
     AbsorbParams p;
+    p.skip_rope = skip_rope ? 1 : 0;
     p.check_rows = rows != nullptr;
     if (rows) p.R = to_dev(*rows);
     else memset(&p.R, 0, sizeof(p.R));
@@ -399,8 +400,11 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     char *w = static_cast<char *>(ws);
     float *qt = reinterpret_cast<float *>(w + plan.qt);
     float *qh = reinterpret_cast<float *>(w + plan.qh);
+    // the tensor-core decode rotates the positional query itself (its inputs are final
+    // before the call, so it overlaps the absorption), leaving the absorption a single
+    // memory round trip
     st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                       scale * LOG2E, qt, qh, sms, &cache->rows);
+                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma);
     if (st != GVA_OK) return st;
 
     DecodeParams dp;
@@ -418,7 +422,12 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     dp.qc = qt;
     dp.qc_f32 = 1;
     dp.qc_scale = 1.f;
-    dp.qr = qh;
+    dp.qr = use_mma ? nullptr : qh;
+    dp.q_rope = q_rope;
+    dp.qr_f32 = d->q_dtype == GVA_F32;
+    dp.rope_tab = rope_tab;
+    dp.rope_max_pos = rope_max_pos;
+    dp.qr_scale = scale * LOG2E;
     dp.out = out;
     dp.lse = lse;
     dp.part_o = reinterpret_cast<float *>(w + plan.po);
@@ -479,6 +488,11 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     dp.qc_f32 = d->q_dtype == GVA_F32;
     dp.qc_scale = scale * LOG2E;
     dp.qr = nullptr;
+    dp.q_rope = nullptr;
+    dp.qr_f32 = 1;
+    dp.rope_tab = nullptr;
+    dp.rope_max_pos = 0;
+    dp.qr_scale = 0.f;
     dp.out = out;
     dp.lse = lse;
     dp.part_o = reinterpret_cast<float *>(w + plan.po);
@@ -558,7 +572,23 @@ int gva_debug_trace_read(long long *host, int n) {
 }
 int gva_debug_trace_clear(void) {
     static long long zeros[TRACE_CTAS * TRACE_SLOTS];
-    return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) == cudaSuccess ? GVA_OK : GVA_ERR_CUDA;
+    unsigned long long lo[16], hi[16];
+    for (int i = 0; i < 16; ++i) { lo[i] = ~0ull; hi[i] = 0ull; }
+    const bool ok = cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) == cudaSuccess &&
+                    cudaMemcpyToSymbol(g_kt_min, lo, sizeof(lo)) == cudaSuccess &&
+                    cudaMemcpyToSymbol(g_kt_max, hi, sizeof(hi)) == cudaSuccess;
+    return ok ? GVA_OK : GVA_ERR_CUDA;
+}
+int gva_debug_cta_read(unsigned long long *host, int n) {
+    if (n > 4096) n = 4096;
+    return cudaMemcpyFromSymbol(host, g_cta_t, sizeof(unsigned long long) * 4 * n) == cudaSuccess
+               ? GVA_OK : GVA_ERR_CUDA;
+}
+// [0..16) earliest, [16..32) latest global-timer reading per timeline slot
+int gva_debug_kt_read(unsigned long long *host) {
+    const bool ok = cudaMemcpyFromSymbol(host, g_kt_min, 16 * 8) == cudaSuccess &&
+                    cudaMemcpyFromSymbol(host + 16, g_kt_max, 16 * 8) == cudaSuccess;
+    return ok ? GVA_OK : GVA_ERR_CUDA;
 }
 #endif
 
