@@ -114,29 +114,32 @@ __device__ __forceinline__ long long row_of(const RowsDev &R, int b, long long j
 }
 
 // Flat split-K partition over slabs.  Sequence b has n_b = ceil(L_b / 16) slabs
-// starting at flat index F[b] (exclusive prefix); S = F[B].  CTA c of n owns flat
-// slabs [floor(c*S/n), floor((c+1)*S/n)): equal shares of the whole batch's cache,
-// whatever the length mix.  Partials of (CTA c, sequence b) go to slot c + b, which is
-// unique along the monotone walk of (c, b) pairs.
+// starting at flat index F[b] (exclusive prefix); S = F[B].  The first
+// neff = min(n, S) CTAs of the grid share the slabs: CTA c < neff owns flat slabs
+// [floor(c*S/neff), floor((c+1)*S/neff)), at least one each, equal shares of the
+// whole batch's cache whatever the length mix; CTAs c >= neff own none.  Partials of
+// (CTA c, sequence b) go to slot c + b, which is unique along the monotone walk of
+// (c, b) pairs.
 //
-// The shares are computed with 32-bit divisions only (S < 2^31, c <= n < 2^12):
-// floor(c*S/n) = c*floor(S/n) + floor(c*(S mod n)/n), and c*(S mod n) < 2^23.  A 64-bit
-// integer division is a long dependent instruction sequence that sat on the path to
-// the first cache load.
+// The shares are computed with 32-bit divisions only (S < 2^31, c <= neff < 2^12):
+// floor(c*S/neff) = c*floor(S/neff) + floor(c*(S mod neff)/neff), c*(S mod neff) < 2^23.
 struct Part {
     long long S;
     int n;
+    __device__ __forceinline__ int neff() const { return S < (long long)n ? (int)S : n; }
     __device__ __forceinline__ long long start(int c) const {
-        const unsigned su = (unsigned)S, nu = (unsigned)n, cu = (unsigned)c;
+        const int ne = neff();
+        if (c >= ne) return S;
+        const unsigned su = (unsigned)S, nu = (unsigned)ne, cu = (unsigned)c;
         const unsigned q = su / nu, r = su - q * nu;
         return (long long)cu * q + (long long)((cu * r) / nu);
     }
     // the CTA that owns flat slab s (0 <= s < S): the largest c with start(c) <= s,
-    // i.e. floor(((s + 1) n - 1) / S).  The quotient is below n < 2^12, so a single-
-    // precision estimate is within one of it and two integer checks make it exact (FP64
-    // arithmetic is slow on this GPU).
+    // i.e. floor(((s + 1) neff - 1) / S).  The quotient is below neff < 2^12, so a
+    // single-precision estimate is within one of it and two integer checks make it
+    // exact (FP64 arithmetic is slow on this GPU).
     __device__ __forceinline__ int cta_of(long long s) const {
-        const long long a = (s + 1) * (long long)n - 1;
+        const long long a = (s + 1) * (long long)neff() - 1;
         long long q = (long long)__fdiv_rn((float)a, (float)S);
         while (q > 0 && q * S > a) --q;
         while ((q + 1) * S <= a) ++q;

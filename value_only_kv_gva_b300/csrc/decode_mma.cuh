@@ -109,6 +109,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t a) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
 }
+// Arrive without release semantics, for a consumer giving a stage back: every read of
+// the stage has already returned its data (the values were consumed by the products),
+// so there is nothing for a release to order.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t a) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -135,10 +141,22 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t a, uint32_t parity,
     return ok != 0;
 }
 constexpr uint32_t WAIT_SLEEP_NS = 1000000u;   // per try; the overall limit is WAIT_LIMIT_NS
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t a, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase with the given parity.  Gives up (returns false) when
 // another warp raised `abort` or after WAIT_LIMIT_NS, raising abort and the status.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int *abort) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_test_wait(a, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_sleep(a, parity, WAIT_SLEEP_NS)) return true;
@@ -150,29 +168,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile 
         }
     }
 }
+// The cache is streamed once per step: its loads carry an L2 evict-first policy, so
+// that they do not push out of L2 what is reused (the kernels' code, the maps M, the
+// queries and the split partials).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(pol)
         : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
-                                            int z, uint32_t bar) {
+                                            int z, uint32_t bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
         : "memory");
 }
 // Plain (non-tensor) bulk copy of `bytes` contiguous bytes: 16-byte aligned addresses,
 // a multiple of 16 bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar) {
+                                          uint32_t bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
@@ -297,116 +324,97 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0);   // includes __syncthreads
     if (threadIdx.x == 0) GVA_TRACE_AT(1);
     const Part P{F[B], p.n_ctas};
-    if (P.S == 0) return;
     const int c = blockIdx.x;
+    if (P.S == 0) return;
     const long long s0 = P.start(c), s1 = P.start(c + 1);
     if (s0 >= s1) return;
 
     // ============================= producer warp ============================= //
-    // The warp's lanes find the storage rows of the next 32 slabs together (for a paged
-    // cache the 32 block-table reads are in flight at once).  Copies are then issued
-    // `il` slabs per step, one slab per lane (lanes 0 .. il-1, consecutive slabs,
-    // consecutive ring stages), which divides the per-copy instruction overhead by il.
+    // One step issues up to il = min(NS, 32) consecutive slabs, one per lane: lane j
+    // finds its slab's storage row (for a paged cache the block-table reads of the step
+    // are in flight together), waits until its ring stage is free, and issues the copies.
+    // The stages of one step are distinct, so no lane waits on another lane's copy.  A
+    // short cache (the whole share fits in the ring) is issued in a single step.
     if (warp == 0) {
-        const int il = NS >= 4 ? 4 : (NS >= 2 ? 2 : 1);
-        unsigned int last_phase_mask = 0, issued_mask = 0;  // per stage (NS <= 32)
-        int stage = 0;                      // stage of the next slab to issue
-        uint32_t round = 0;                 // times the ring has wrapped at that slab
+        const int il = NS < 32 ? NS : 32;
+        const uint64_t pol = l2_evict_first_policy();
+        int stage = 0;                      // stage of the step's first slab
+        uint32_t round = 0;                 // ring wraps before the step's first slab
         bool dead = false;
-        int b = seq_of_slab(F, B, s0);
+        long long n_tried = 0;              // slabs of the steps attempted
+        int b = seq_of_slab(F, B, s0);      // sequence of the step's first slab
         if (lane == 0) GVA_TRACE_AT(6);
-        for (long long sb = s0; sb < s1 && !dead; sb += 32) {
+        for (long long sb = s0; sb < s1; sb += il) {
             const long long s = sb + lane;
-            int y = 0, bad = 0;
-            if (s < s1) {
+            const bool act = lane < il && s < s1;
+            int st = stage + lane;
+            uint32_t rd = round;
+            if (st >= NS) { st -= NS; ++rd; }
+            bool ok = true;
+            if (act) {
                 int bl = b;
                 while (F[bl + 1] <= s) ++bl;
                 const long long row = row_of(p.R, bl, (s - F[bl]) * SLAB);
-                if (row < 0) bad = 1;       // consumers mask the slab's tokens
-                else y = (int)row;
-            }
-            {   // sequence of the first slab of the next batch of 32
-                const long long sn = sb + 32;
-                if (sn < s1) {
-                    int bl = b;
-                    while (F[bl + 1] <= sn) ++bl;
-                    b = bl;
-                }
-            }
-            const int cnt = (int)min(32LL, s1 - sb);
-            if (lane == 0 && sb == s0) GVA_TRACE_AT(7);
-            for (int k0 = 0; k0 < cnt; k0 += il) {
-                const int j = lane % il;
-                const int k = k0 + j;
-                const int yk = __shfl_sync(0xffffffffu, y, k & 31);
-                const int badk = __shfl_sync(0xffffffffu, bad, k & 31);
-                const bool act = lane < il && k < cnt;
-                int st_j = stage + j;
-                uint32_t rd_j = round;
-                if (st_j >= NS) { st_j -= NS; ++rd_j; }
-                bool ok = true;
-                if (act) {
-                    if (rd_j > 0 && !mbar_wait(bar_empty + 8 * st_j, (rd_j - 1) & 1u, abort)) {
-                        ok = false;
-                    } else {
-                        const uint32_t stb = base_u32 + st_j * mp.stage_bytes;
-                        const uint32_t fb = bar_full + 8 * st_j;
-                        stage_bad[st_j] = badk;   // published by the arrive below
-                        // the positional keys of the slab are one contiguous run of rows;
-                        // rows past the end of the cache storage are not copied (their
-                        // tokens are past every sequence's end, and masked)
-                        long long rrows = p.R.num_rows - (long long)yk;
-                        rrows = rrows < SLAB ? (rrows < 0 ? 0 : rrows) : SLAB;
-                        const uint32_t rbytes = (uint32_t)rrows * (DR * 2);
-                        mbar_expect_tx(fb, (uint32_t)mp.off_r + rbytes);
-                        if (mp.v3d) {
-                            tma_load_3d(stb, &tm_v, 0, yk, 0, fb);
-                            if (GQA) tma_load_3d(stb + mp.off_k, &tm_k, 0, yk, 0, fb);
-                        } else {
-                            for (int bx = 0; bx < G * (DH / 64); ++bx) {
-                                tma_load_2d(stb + bx * 2048, &tm_v, bx * 64, yk, fb);
-                                if (GQA) tma_load_2d(stb + mp.off_k + bx * 2048, &tm_k, bx * 64, yk, fb);
-                            }
-                        }
-                        if (DR > 0 && rbytes > 0)
-                            bulk_load(stb + mp.off_r,
-                                      reinterpret_cast<const unsigned char *>(p.Krope) +
-                                          (size_t)yk * (DR * 2),
-                                      rbytes, fb);
-                        const int ti = (int)(sb - s0) + k;
-                        if (ti == 0) GVA_TRACE_AT(2);
-                        if (ti < 64) GVA_TRACE_AT(300 + ti);
+                const int yk = row < 0 ? 0 : (int)row;
+                if (rd > 0 && !mbar_wait(bar_empty + 8 * st, (rd - 1) & 1u, abort)) {
+                    ok = false;
+                } else {
+                    const uint32_t stb = base_u32 + st * mp.stage_bytes;
+                    const uint32_t fb = bar_full + 8 * st;
+                    stage_bad[st] = row < 0;   // published by the arrive below
+                    // the positional keys of the slab are one contiguous run of rows;
+                    // rows past the end of the cache storage are not copied (their
+                    // tokens are past every sequence's end, and masked)
+                    int rrows = SLAB;
+                    if ((long long)yk + SLAB > p.R.num_rows) {
+                        const long long left = p.R.num_rows - (long long)yk;
+                        rrows = left < 0 ? 0 : (int)left;
                     }
+                    const uint32_t rbytes = (uint32_t)rrows * (DR * 2);
+                    mbar_expect_tx(fb, (uint32_t)mp.off_r + rbytes);
+                    if (mp.v3d) {
+                        tma_load_3d(stb, &tm_v, 0, yk, 0, fb, pol);
+                        if (GQA) tma_load_3d(stb + mp.off_k, &tm_k, 0, yk, 0, fb, pol);
+                    } else {
+                        for (int bx = 0; bx < G * (DH / 64); ++bx) {
+                            tma_load_2d(stb + bx * 2048, &tm_v, bx * 64, yk, fb, pol);
+                            if (GQA) tma_load_2d(stb + mp.off_k + bx * 2048, &tm_k, bx * 64, yk, fb, pol);
+                        }
+                    }
+                    if (DR > 0 && rbytes > 0)
+                        bulk_load(stb + mp.off_r,
+                                  reinterpret_cast<const unsigned char *>(p.Krope) + (size_t)yk * (DR * 2),
+                                  rbytes, fb, pol);
+                    const int ti = (int)(s - s0);
+                    if (ti == 0) GVA_TRACE_AT(2);
+                    if (ti < 64) GVA_TRACE_AT(300 + ti);
                 }
-                // bookkeeping of what is in flight (for the drain), the same in every lane
-                const unsigned done = __ballot_sync(0xffffffffu, act && ok);
-                for (int jj = 0; jj < il; ++jj) {
-                    if (!(done & (1u << jj))) continue;
-                    int sj = stage + jj;
-                    uint32_t rj = round;
-                    if (sj >= NS) { sj -= NS; ++rj; }
-                    issued_mask |= 1u << sj;
-                    last_phase_mask = (last_phase_mask & ~(1u << sj)) | ((rj & 1u) << sj);
-                }
-                dead = __any_sync(0xffffffffu, act && !ok);
-                if (dead) break;
-                stage += min(il, cnt - k0);
-                if (stage >= NS) { stage -= NS; ++round; }
             }
+            n_tried += min((long long)il, s1 - sb);
+            dead = __any_sync(0xffffffffu, act && !ok);
+            if (dead) break;
+            {   // sequence of the next step's first slab
+                const long long sn = sb + il;
+                while (b < B - 1 && F[b + 1] <= sn) ++b;
+            }
+            stage += il;
+            if (stage >= NS) { stage -= NS; ++round; }
         }
         if (lane == 0) {
             GVA_TRACE_AT(3);
             GVA_TRACE_FLUSH(2, 4);
             GVA_TRACE_FLUSH(6, 8);
             GVA_TRACE_FLUSH(300, 364);
-            // never leave with copies in flight: wait (bounded) for each stage's last load
-            for (int st = 0; st < NS; ++st) {
-                if (!(issued_mask & (1u << st))) continue;
-                const uint32_t par = (last_phase_mask >> st) & 1u;
+            // Never leave with copies in flight: wait (bounded) for the last copy of each
+            // stage used.  Slab i used stage i % NS in round i / NS.  After an abort a
+            // stage's last slab may not have been issued: those waits are kept short.
+            const unsigned long long limit = dead ? 1000000ull : WAIT_LIMIT_NS;
+            for (int st = 0; st < NS && st < n_tried; ++st) {
+                const uint32_t par = (uint32_t)((n_tried - 1 - st) / NS) & 1u;
                 const unsigned long long t0 = global_ns();
                 while (!mbar_try_wait(bar_full + 8 * st, par)) {
-                    if (global_ns() - t0 > WAIT_LIMIT_NS) {
-                        dev_report(GVA_DEV_TIMEOUT);
+                    if (global_ns() - t0 > limit) {
+                        if (!dead) dev_report(GVA_DEV_TIMEOUT);
                         break;
                     }
                 }
@@ -430,6 +438,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     const int wpg = mp.wpg;
     const int gid = lane >> 2, tig = lane & 3;
     constexpr int KD = DH / 16;       // k16 steps over d_h (and 16-row tiles of O^T)
+    constexpr int NSL = 1;            // own slabs per loop trip (2 measured no faster)
     constexpr int DRK16 = DR / 16;    // full k16 steps over the positional slice
     constexpr bool DR_K8 = (DR % 16) == 8;  // one trailing k8 step
     // ldmatrix lane roles
@@ -551,35 +560,70 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         for (int nt = 0; nt < NT; ++nt) { m_run[nt] = -INFINITY; l_run[nt] = 0.f; }
 
         if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(4);
-        for (; s < seg_end; ++s) {
-            const int my_stage = stage;
-            const uint32_t my_phase = phase;
-            const bool mine = wsel == w;
-            if (++stage == NS) { stage = 0; phase ^= 1u; }
-            if (++wsel == wpg) wsel = 0;
-            if (!mine || !alive) continue;
-            if (!mbar_wait(bar_full + 8 * my_stage, my_phase, abort)) {
+        // The warp's own slabs of the segment are taken NSL at a time: their chains of
+        // dependent latencies overlap and share one max reduction and rescale test.
+        // A missing partner (odd tail) is a copy of the first slab with no valid token.
+        while (s < seg_end) {
+            int my_stage[NSL];
+            uint32_t my_phase[NSL];
+            int j0[NSL];
+            int cnt = 0;
+            while (s < seg_end && cnt < NSL) {
+                const bool mine = wsel == w;
+                if (mine) {
+#pragma unroll
+                    for (int u = 0; u < NSL; ++u)   // constant indices: the arrays stay in registers
+                        if (cnt == u) {
+                            my_stage[u] = stage;
+                            my_phase[u] = phase;
+                            j0[u] = (int)(s - Fb) * SLAB;
+                        }
+                    ++cnt;
+                }
+                if (++stage == NS) { stage = 0; phase ^= 1u; }
+                if (++wsel == wpg) wsel = 0;
+                ++s;
+            }
+            if (cnt == 0 || !alive) continue;
+#pragma unroll
+            for (int u = 1; u < NSL; ++u)
+                if (u >= cnt) { my_stage[u] = my_stage[0]; my_phase[u] = my_phase[0]; j0[u] = Lb; }
+            bool waited = true;
+#pragma unroll
+            for (int u = 0; u < NSL; ++u)
+                if (u < cnt && waited && !mbar_wait(bar_full + 8 * my_stage[u], my_phase[u], abort))
+                    waited = false;
+            // one decision for the warp (the code below is warp-synchronous)
+            waited = __all_sync(0xffffffffu, waited);
+            if (!waited) {
                 alive = false;
                 continue;
             }
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(8 + 2 * tslab);
-            const int j0 = (int)(s - Fb) * SLAB;
-            int nv = min(SLAB, Lb - j0);
-            if (stage_bad[my_stage]) {
-                if (lane == 0 && g == 0) dev_report(GVA_DEV_BAD_PAGE);
-                nv = 0;
+            int nv[NSL];
+            uint32_t st[NSL];
+#pragma unroll
+            for (int u = 0; u < NSL; ++u) {
+                nv[u] = min(SLAB, Lb - j0[u]);
+                if (u < cnt && stage_bad[my_stage[u]]) {
+                    if (lane == 0 && g == 0) dev_report(GVA_DEV_BAD_PAGE);
+                    nv[u] = 0;
+                }
+                st[u] = base_u32 + my_stage[u] * mp.stage_bytes;
             }
-            const uint32_t st = base_u32 + my_stage * mp.stage_bytes;
-            const uint32_t kst = GQA ? st + mp.off_k : st;
 
             // ---- scores: A = the key tile (tokens x d), B = Q^T ----
-            float sc[NT][2][4];
+            float sc[NSL][NT][2][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int u = 0; u < NSL; ++u)
 #pragma unroll
-                for (int a2 = 0; a2 < 2; ++a2)
-                    sc[nt][a2][0] = sc[nt][a2][1] = sc[nt][a2][2] = sc[nt][a2][3] = 0.f;
-            {
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int a2 = 0; a2 < 2; ++a2)
+                        sc[u][nt][a2][0] = sc[u][nt][a2][1] = sc[u][nt][a2][2] = sc[u][nt][a2][3] = 0.f;
+#pragma unroll
+            for (int u = 0; u < NSL; ++u) {
+                const uint32_t kst = GQA ? st[u] + mp.off_k : st[u];
                 uint32_t av[KD][4];
 #pragma unroll
                 for (int kk = 0; kk < KD; ++kk)
@@ -587,7 +631,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                             av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
                 uint32_t ar[DRK16 > 0 ? DRK16 : 1][4], ar8[2];
                 if (DR > 0) {
-                    const uint32_t rbase = st + mp.off_r;
+                    const uint32_t rbase = st[u] + mp.off_r;
 #pragma unroll
                     for (int kk = 0; kk < DRK16; ++kk)
                         ldsm_x4(rbase + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + (2 * kk + (lm_mat >> 1)) * 16,
@@ -599,42 +643,39 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 for (int kk = 0; kk < KD; ++kk)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16816(sc[nt][kk & 1], av[kk], bq[kk][nt][0], bq[kk][nt][1]);
+                        mma16816(sc[u][nt][kk & 1], av[kk], bq[kk][nt][0], bq[kk][nt][1]);
                 if (DR > 0) {
 #pragma unroll
                     for (int kk = 0; kk < DRK16; ++kk)
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma16816(sc[nt][(KD + kk) & 1], ar[kk], bqr[kk][nt][0], bqr[kk][nt][1]);
+                            mma16816(sc[u][nt][(KD + kk) & 1], ar[kk], bqr[kk][nt][0], bqr[kk][nt][1]);
                     if (DR_K8) {
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma1688(sc[nt][(KD + DRK16) & 1], ar8[0], ar8[1], bqr8[nt]);
+                            mma1688(sc[u][nt][(KD + DRK16) & 1], ar8[0], ar8[1], bqr8[nt]);
                     }
                 }
             }
-            // value tiles for the weighted sum (V^T as the A operand): loaded now,
-            // consumed after the softmax
-            uint32_t apv[KD][4];
-#pragma unroll
-            for (int mt = 0; mt < KD; ++mt)
-                ldsm_x4_t(vtile_addr<DH>(st, g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
-                          apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
 
             // ---- per head: hi + lo columns -> score of tokens gid, gid + 8 ----
-            float z[NT][2];
+            float z[NSL][NT][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                z[nt][0] = (sc[nt][0][0] + sc[nt][0][1]) + (sc[nt][1][0] + sc[nt][1][1]);
-                z[nt][1] = (sc[nt][0][2] + sc[nt][0][3]) + (sc[nt][1][2] + sc[nt][1][3]);
-                if (gid >= nv) z[nt][0] = -INFINITY;
-                if (gid + 8 >= nv) z[nt][1] = -INFINITY;
-            }
+            for (int u = 0; u < NSL; ++u)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    z[u][nt][0] = (sc[u][nt][0][0] + sc[u][nt][0][1]) + (sc[u][nt][1][0] + sc[u][nt][1][1]);
+                    z[u][nt][1] = (sc[u][nt][0][2] + sc[u][nt][0][3]) + (sc[u][nt][1][2] + sc[u][nt][1][3]);
+                    if (gid >= nv[u]) z[u][nt][0] = -INFINITY;
+                    if (gid + 8 >= nv[u]) z[u][nt][1] = -INFINITY;
+                }
             float mloc[NT];
             bool raise_any = false;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float m = fmaxf(z[nt][0], z[nt][1]);
+                float m = fmaxf(z[0][nt][0], z[0][nt][1]);
+#pragma unroll
+                for (int u = 1; u < NSL; ++u) m = fmaxf(m, fmaxf(z[u][nt][0], z[u][nt][1]));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
@@ -655,40 +696,53 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     }
                 }
             }
-            // ---- probabilities, then P^T as the B operand (column gid: head 4nt + gid/2) ----
-            uint32_t bp[NT][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float p0 = z[nt][0] == -INFINITY ? 0.f : exp2f(z[nt][0] - m_run[nt]);
-                const float p1 = z[nt][1] == -INFINITY ? 0.f : exp2f(z[nt][1] - m_run[nt]);
-                l_run[nt] += p0 + p1;
-                const float a0 = __shfl_sync(0xffffffffu, p0, srcA);   // token 2tig
-                const float a1 = __shfl_sync(0xffffffffu, p1, srcA);   // token 2tig + 8
-                const float b0 = __shfl_sync(0xffffffffu, p0, srcB);   // token 2tig + 1
-                const float b1 = __shfl_sync(0xffffffffu, p1, srcB);   // token 2tig + 9
-                bp[nt][0] = part_bf16x2(a0, b0, lo_col);
-                bp[nt][1] = part_bf16x2(a1, b1, lo_col);
-            }
-            // ---- O^T += V^T . P^T ----
-            if (nv < SLAB) {
-                // zero the values of tokens past the end (they may hold NaN)
-                const int ta = 2 * tig, tb = 8 + 2 * tig;
-                const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
-                const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
+            for (int u = 0; u < NSL; ++u) {
+                // value tiles for the weighted sum (V^T as the A operand)
+                uint32_t apv[KD][4];
 #pragma unroll
-                for (int mt = 0; mt < KD; ++mt) {
-                    apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
+                for (int mt = 0; mt < KD; ++mt)
+                    ldsm_x4_t(vtile_addr<DH>(st[u], g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
+                              apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
+                // ---- probabilities, then P^T as the B operand (column gid: head 4nt + gid/2) ----
+                uint32_t bp[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float p0 = z[u][nt][0] == -INFINITY ? 0.f : exp2f(z[u][nt][0] - m_run[nt]);
+                    const float p1 = z[u][nt][1] == -INFINITY ? 0.f : exp2f(z[u][nt][1] - m_run[nt]);
+                    l_run[nt] += p0 + p1;
+                    const float a0 = __shfl_sync(0xffffffffu, p0, srcA);   // token 2tig
+                    const float a1 = __shfl_sync(0xffffffffu, p1, srcA);   // token 2tig + 8
+                    const float b0 = __shfl_sync(0xffffffffu, p0, srcB);   // token 2tig + 1
+                    const float b1 = __shfl_sync(0xffffffffu, p1, srcB);   // token 2tig + 9
+                    bp[nt][0] = part_bf16x2(a0, b0, lo_col);
+                    bp[nt][1] = part_bf16x2(a1, b1, lo_col);
                 }
+                // ---- O^T += V^T . P^T ----
+                if (nv[u] < SLAB) {
+                    // zero the values of tokens past the end (they may hold NaN)
+                    const int ta = 2 * tig, tb = 8 + 2 * tig;
+                    const uint32_t ma = (ta >= nv[u] ? 0u : 0xffffu) | (ta + 1 >= nv[u] ? 0u : 0xffff0000u);
+                    const uint32_t mb = (tb >= nv[u] ? 0u : 0xffffu) | (tb + 1 >= nv[u] ? 0u : 0xffff0000u);
+#pragma unroll
+                    for (int mt = 0; mt < KD; ++mt) {
+                        apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < KD; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
             }
-#pragma unroll
-            for (int mt = 0; mt < KD; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
             // the products above consumed every tile register, so all of the warp's
-            // shared-memory reads of the stage are complete: release it to the producer
+            // shared-memory reads of its stages are complete: release them to the producer
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * my_stage);
+            if (lane == 0) {
+#pragma unroll
+                for (int u = 0; u < NSL; ++u)
+                    if (u < cnt) mbar_arrive_relaxed(bar_empty + 8 * my_stage[u]);
+            }
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(9 + 2 * tslab);
             ++tslab;
         }
@@ -907,10 +961,14 @@ inline int launch_mma_t(void *stream, MmaParams &mp, const CUtensorMap &tv, cons
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int na = 0;
+    if (pdl_allowed(cfg.stream)) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_allowed(cfg.stream) ? 1 : 0;
+    cfg.numAttrs = na;
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, tv, tk, mp));
 }
 
