@@ -172,8 +172,20 @@ def test_append_bit_exact(layout, cache, mode):
         assert_close(out, ref, cache, "decode after extend")
 
 
-def test_absorb_matches_oracle():
-    c = make_case(workload("350m", T=50, B=5))
+@pytest.mark.parametrize("over", [
+    dict(B=5),
+    # several 8-sequence groups per CTA and a partial last chunk (300 = 9 x 32 + 12)
+    dict(B=300, H=16, G=4, d_h=64, d_n=64, d_r=16),
+    # d_n = 256 (chunks of 32), fp32 queries: the per-CTA sequence cap of the staging
+    dict(B=400, H=8, G=2, d_h=32, d_n=256, d_r=8, cache_dtype="f32", q_dtype="f32"),
+    dict(B=70, H=4, G=2, d_h=128, d_n=256, d_r=32),
+    # chunk sizes that are not a multiple of 4 (padded chunks, per-element scatter)
+    dict(B=33, H=3, G=3, d_h=32, d_n=24, d_r=8, cache_dtype="f32", q_dtype="f32"),
+    dict(B=50, H=6, G=2, d_h=64, d_n=40, d_r=24),
+    dict(B=9, H=2, G=1, d_h=32, d_n=8, d_r=16),
+], ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_absorb_matches_oracle(over):
+    c = make_case(workload("350m", T=50, **over))
     D = Dev(c)
     w = c.w
     qt = torch.empty((w.B, w.H, w.d_h), device="cuda")

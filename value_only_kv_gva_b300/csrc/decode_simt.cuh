@@ -301,6 +301,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     const long long nb = (Lb + SLAB - 1) / SLAB;
     const int d0 = blockIdx.y * 32;
     float *out = p.out + ((long long)b * p.H + h) * p.d_h;
+    // the parts of the sequence depend on the lengths only: found before the wait
+    const Part P{S, p.n_ctas};
+    const int c_lo = nb > 0 ? P.cta_of(Fb) : 0, c_hi = nb > 0 ? P.cta_of(Fb + nb - 1) : 0;
     // the partials (and the outputs the decode kernel writes) come from the preceding grid
     pdl_wait();
     if (threadIdx.x == 0) GVA_KT(9);
@@ -309,8 +312,6 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
         if (tid == 0 && blockIdx.y == 0 && p.lse) p.lse[(long long)b * p.H + h] = -INFINITY;
         return;
     }
-    const Part P{S, p.n_ctas};
-    const int c_lo = P.cta_of(Fb), c_hi = P.cta_of(Fb + nb - 1);
     if (c_lo == c_hi) return;
     const int n = c_hi - c_lo + 1;
     const int i = d0 + lane;

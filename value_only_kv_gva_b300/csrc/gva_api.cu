@@ -88,8 +88,8 @@ const DevState *device_state() {
     if (d.ready) return &d;
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = opt_in_smem(absorb_kernel<float>);
-    if (e == cudaSuccess) e = opt_in_smem(absorb_kernel<__nv_bfloat16>);
+    if (e == cudaSuccess) e = opt_in_smem(absorb_kernel<float, 0>);
+    if (e == cudaSuccess) e = opt_in_smem(absorb_kernel<__nv_bfloat16, 0>);
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, false>);
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, false>);
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, true>);
@@ -233,10 +233,18 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     p.d_h = d->d_h;
     p.d_n = d->d_n;
     p.d_r = d->d_r;
-    // sequences per CTA: enough CTAs to cover the GPU, at most 8 query rows per CTA
+    // sequences per CTA: about one CTA per SM (the grid is resident at once and
+    // leaves room beside it for the dependent decode grid to start), no more
+    // sequences per CTA than the query staging holds
     const int zs = (d->d_h + 31) / 32;
-    int bpb = (d->B * d->H * zs) / (sms > 0 ? 2 * sms : 1);
-    bpb = bpb < 1 ? 1 : (bpb > 8 ? 8 : bpb);
+    const long long per_b = (long long)d->H * zs;   // CTAs per sequence chunk
+    const int qsize = d->q_dtype == GVA_F32 ? 4 : 2;
+    long long nbc = (long long)(sms > 0 ? sms : 1) / per_b;
+    if (nbc < 1) nbc = 1;
+    if (nbc > d->B) nbc = d->B;
+    int bpb = (int)((d->B + nbc - 1) / nbc);
+    const int lim = absorb_bpb_limit(d->d_n, qsize);
+    if (bpb > lim) bpb = lim;
     p.bpb = bpb;
     p.q_nope = q_nope;
     p.q_rope = q_rope;
@@ -247,11 +255,28 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     p.prescale = prescale;
     p.q_tilde = q_tilde;
     p.q_hat = q_hat;
-    const size_t smem = sizeof(float) * ((size_t)32 * (d->d_n + 4) + (size_t)bpb * d->d_n);
+    const size_t smem = (size_t)absorb_smem_bytes(d->d_n, bpb);
     dim3 grid(d->H, (d->B + bpb - 1) / bpb, zs);
     cudaError_t e;
-    if (d->q_dtype == GVA_F32) e = launch(absorb_kernel<float>, grid, dim3(ABSORB_THREADS), smem, stream, p);
-    else e = launch(absorb_kernel<__nv_bfloat16>, grid, dim3(ABSORB_THREADS), smem, stream, p);
+    const dim3 blk(ABSORB_THREADS);
+    const bool f32 = d->q_dtype == GVA_F32;
+    switch (d->d_n) {
+    case 64:
+        e = f32 ? launch(absorb_kernel<float, 8>, grid, blk, smem, stream, p)
+                : launch(absorb_kernel<__nv_bfloat16, 8>, grid, blk, smem, stream, p);
+        break;
+    case 128:
+        e = f32 ? launch(absorb_kernel<float, 16>, grid, blk, smem, stream, p)
+                : launch(absorb_kernel<__nv_bfloat16, 16>, grid, blk, smem, stream, p);
+        break;
+    case 256:
+        e = f32 ? launch(absorb_kernel<float, 32>, grid, blk, smem, stream, p)
+                : launch(absorb_kernel<__nv_bfloat16, 32>, grid, blk, smem, stream, p);
+        break;
+    default:
+        e = f32 ? launch(absorb_kernel<float, 0>, grid, blk, smem, stream, p)
+                : launch(absorb_kernel<__nv_bfloat16, 0>, grid, blk, smem, stream, p);
+    }
     return cuda_status(e);
 }
 

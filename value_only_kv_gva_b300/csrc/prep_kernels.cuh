@@ -105,14 +105,50 @@ struct AbsorbParams {
     int skip_rope;                 // 1: q_hat is not computed (the decode rotates q_rope)
 };
 
-// Grid (H, ceil(B / bpb), d_h / 32), 256 threads.  A CTA owns 32 rows of M_h (at most
-// 32 x 256 fp32 = 32 KB) and issues all of its 16-byte loads of them at once (one
-// memory round trip, even while the decode streams the cache); each output row is
-// split over 8 threads (k strided by 8) and reduced with shuffles.
+// Grid (H, ceil(B / bpb), d_h / 32), 256 threads, bpb <= 32 sequences per CTA.
+//
+// Warp w owns rows i0 + 4w .. i0 + 4w + 3 of M_h; lane (o = lane / 8, kl = lane % 8)
+// holds the kl-th contiguous chunk of cs = d_n / 8 entries of its row in registers for
+// the whole CTA.  The CTA's query rows are staged in shared memory as fp32 in the same
+// chunking, each chunk padded to cst floats (a multiple of 4 with cst / 4 odd), so that
+// the 8 lanes of a row read their chunks with conflict-free 16-byte loads, each one
+// broadcast to the 4 rows of the warp: one shared-memory wavefront feeds 128 FMAs.
+// The 8 chunk partials of a row are combined for 8 sequences at a time by a
+// reduce-scatter over the 8 lanes (7 shuffles), after which lane kl holds sequence kl.
+// Every global load of the CTA (its M rows, its query rows, the positional inputs) is
+// issued in one unrolled batch before the first use: one memory round trip.
 constexpr int ABSORB_THREADS = 256;
+constexpr int ABSORB_CSMAX = 32;   // d_n <= 256
+constexpr int ABSORB_QVEC = 4;     // 16-byte query vectors per thread (bpb is sized to fit)
+constexpr int ABSORB_BPB_MAX = 32;
 
-template <typename QT>
-__global__ void __launch_bounds__(ABSORB_THREADS) absorb_kernel(const AbsorbParams p) {
+__host__ __device__ constexpr int absorb_cst(int d_n) {
+    // chunk stride: cs rounded up to 4, plus 4 when that leaves an even number of float4
+    return (((d_n / 8 + 3) / 4) & 1) ? ((d_n / 8 + 3) / 4) * 4 : ((d_n / 8 + 3) / 4) * 4 + 4;
+}
+// sequences per CTA the query staging allows for one query row of d_n elements of qsize bytes
+__host__ __device__ constexpr int absorb_bpb_limit(int d_n, int qsize) {
+    return (ABSORB_QVEC * ABSORB_THREADS) / (d_n * qsize / 16) < ABSORB_BPB_MAX
+               ? (ABSORB_QVEC * ABSORB_THREADS) / (d_n * qsize / 16) : ABSORB_BPB_MAX;
+}
+__host__ __device__ constexpr int absorb_smem_bytes(int d_n, int bpb) {
+    return ((bpb + 7) / 8) * 8 * 8 * absorb_cst(d_n) * 4;
+}
+
+// Element t of a 16-byte vector of query values, widened exactly to fp32.
+template <typename QT> __device__ __forceinline__ float vec_elem(const uint4 &v, int t);
+template <> __device__ __forceinline__ float vec_elem<float>(const uint4 &v, int t) {
+    const unsigned w = t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w;
+    return __uint_as_float(w);
+}
+template <> __device__ __forceinline__ float vec_elem<__nv_bfloat16>(const uint4 &v, int t) {
+    const unsigned w = (t >> 1) == 0 ? v.x : (t >> 1) == 1 ? v.y : (t >> 1) == 2 ? v.z : v.w;
+    return __uint_as_float((t & 1) ? (w & 0xffff0000u) : (w << 16));   // bf16 = high half of fp32
+}
+
+// CSF: the chunk size d_n / 8 when it is fixed at compile time (8, 16, 32), 0 otherwise.
+template <typename QT, int CSF>
+__global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbParams p) {
     extern __shared__ __align__(16) float sm_abs[];
     if (threadIdx.x == 0) GVA_KT(2);
     pdl_wait();
@@ -123,68 +159,161 @@ __global__ void __launch_bounds__(ABSORB_THREADS) absorb_kernel(const AbsorbPara
     const int nb = min(p.bpb, p.B - b0);
     const int i0 = blockIdx.z * 32;
     const int d_n = p.d_n, d_h = p.d_h;
-    const int ldm = d_n + 4;                 // padded row (16-byte aligned)
-    float *Ms = sm_abs;                      // [32][d_n + 4]
-    float *qs = Ms + 32 * ldm;               // [bpb][d_n]
-    // Positional slice: one (sequence, pair) per thread (bpb * d_r / 2 <= 8 * 16 threads).
-    // Its inputs are read together with M and q_nope, and the rotation table entry right
-    // after, so the whole CTA costs two memory round trips.
-    const int half = p.d_r / 2;
-    const bool rot = p.d_r > 0 && !p.skip_rope && blockIdx.z == 0 && (int)threadIdx.x < nb * half;
-    int rb = 0, ri = 0, rL = 0;
-    float rx0 = 0.f, rx1 = 0.f;
-    long long qoff_r = 0;
-    if (rot) {
-        rb = b0 + threadIdx.x / half;
-        ri = threadIdx.x % half;
-        rL = p.seq_len[rb];
-        qoff_r = ((long long)rb * p.H + h) * p.d_r;
-        const QT *qr = reinterpret_cast<const QT *>(p.q_rope);
-        rx0 = to_f<QT>(qr[qoff_r + 2 * ri]);
-        rx1 = to_f<QT>(qr[qoff_r + 2 * ri + 1]);
-    }
-    const float *Mh = p.M + ((long long)h * d_h + i0) * d_n;
+    const int cs = CSF > 0 ? CSF : d_n / 8, cst = absorb_cst(8 * cs);
+    constexpr int CSMAX = CSF > 0 ? CSF : ABSORB_CSMAX;
+    const int lane = threadIdx.x & 31, kl = lane & 7;
+    const int o = (threadIdx.x >> 5) * 4 + (lane >> 3);   // row within the CTA's 32
     const int rows = min(32, d_h - i0);
-    const int n4 = rows * d_n / 4;
-    for (int e = threadIdx.x; e < n4; e += ABSORB_THREADS) {
-        const float4 v = reinterpret_cast<const float4 *>(Mh)[e];
-        const int i = (4 * e) / d_n, k = (4 * e) % d_n;
-        *reinterpret_cast<float4 *>(Ms + i * ldm + k) = v;
-    }
-    const QT *qn = reinterpret_cast<const QT *>(p.q_nope);
-    for (int e = threadIdx.x; e < nb * d_n; e += ABSORB_THREADS) {
-        const int bl = e / d_n, k = e % d_n;
-        qs[e] = to_f<QT>(qn[((long long)(b0 + bl) * p.H + h) * d_n + k]);
-    }
-    float rc = 1.f, rs = 0.f;
-    if (rot) {
-        int t = rL - 1;
-        if (t < 0) t = 0;
-        if (t >= p.rope_max_pos) {
-            if (!p.check_rows || length_ok(p.R, rb, rL)) dev_report(GVA_DEV_BAD_POSITION);
-            t = 0;
+    const int nbr = (nb + 7) & ~7;                        // staged rows (zero past nb)
+
+    // Positional slice: one (sequence, pair) per thread and pass, two passes at most
+    // (bpb * d_r / 2 <= 32 * 16).  Its inputs are loaded with the rest; the rotation
+    // table entries, which depend on the lengths, right after.
+    const int half = p.d_r / 2;
+    const bool rope = p.d_r > 0 && !p.skip_rope && blockIdx.z == 0;
+    constexpr int RPT = 2;
+    int rL[RPT];
+    float rx0[RPT], rx1[RPT];
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+        const int e = threadIdx.x + u * ABSORB_THREADS;
+        if (rope && e < nb * half) {
+            const int rb = b0 + e / half, ri = e % half;
+            const QT *qr = reinterpret_cast<const QT *>(p.q_rope) + ((long long)rb * p.H + h) * p.d_r;
+            rL[u] = p.seq_len[rb];
+            rx0[u] = to_f<QT>(qr[2 * ri]);
+            rx1[u] = to_f<QT>(qr[2 * ri + 1]);
         }
-        rc = p.rope_tab[((long long)t * half + ri) * 2];
-        rs = p.rope_tab[((long long)t * half + ri) * 2 + 1];
+    }
+
+    // 1. this thread's chunk of M row i0 + o
+    float mr[CSMAX];
+    {
+        const float *mrow = p.M + ((long long)h * d_h + i0 + o) * d_n + kl * cs;
+        const bool own = o < rows;
+        if ((cs & 3) == 0) {
+#pragma unroll
+            for (int u = 0; u < CSMAX / 4; ++u) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (own && 4 * u < cs) v = __ldg(reinterpret_cast<const float4 *>(mrow) + u);
+                mr[4 * u] = v.x; mr[4 * u + 1] = v.y; mr[4 * u + 2] = v.z; mr[4 * u + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < CSMAX; ++j) mr[j] = (own && j < cs) ? __ldg(mrow + j) : 0.f;
+        }
+    }
+    // 2. the query rows of the CTA's sequences, as raw 16-byte vectors
+    constexpr int EPV = 16 / (int)sizeof(QT);   // elements per vector
+    const int vrow = d_n / EPV;                 // vectors per query row
+    uint4 qv[ABSORB_QVEC];
+#pragma unroll
+    for (int u = 0; u < ABSORB_QVEC; ++u) {
+        const int e = threadIdx.x + u * ABSORB_THREADS;
+        if (e < nb * vrow) {
+            const int r = e / vrow, vi = e % vrow;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const QT *>(p.q_nope) + ((long long)(b0 + r) * p.H + h) * d_n);
+            qv[u] = __ldg(src + vi);
+        }
+    }
+    // 3. stage: zero what the dot products read but no query fills (the rows past nb
+    // and, for a chunk size that is not a multiple of 4, the chunk tails), then scatter
+    {
+        float4 *z = reinterpret_cast<float4 *>(sm_abs);
+        for (int e = nb * 2 * cst + threadIdx.x; e < nbr * 2 * cst; e += ABSORB_THREADS)
+            z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cs & 3) {
+            const int pad = 4 - (cs & 3);
+            for (int e = threadIdx.x; e < nb * 8 * pad; e += ABSORB_THREADS)
+                sm_abs[(e / pad) * cst + cs + e % pad] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < ABSORB_QVEC; ++u) {
+        const int e = threadIdx.x + u * ABSORB_THREADS;
+        if (e < nb * vrow) {
+            const int r = e / vrow, k0 = (e % vrow) * EPV;
+            if (cs % EPV == 0) {
+                // the vector lies in one chunk: EPV / 4 aligned 16-byte stores
+                float *dst = sm_abs + (r * 8 + k0 / cs) * cst + k0 % cs;
+#pragma unroll
+                for (int t = 0; t < EPV; t += 4)
+                    *reinterpret_cast<float4 *>(dst + t) =
+                        make_float4(vec_elem<QT>(qv[u], t), vec_elem<QT>(qv[u], t + 1),
+                                    vec_elem<QT>(qv[u], t + 2), vec_elem<QT>(qv[u], t + 3));
+            } else {
+#pragma unroll
+                for (int t = 0; t < EPV; ++t) {
+                    const int k = k0 + t;
+                    sm_abs[(r * 8 + k / cs) * cst + k % cs] = vec_elem<QT>(qv[u], t);
+                }
+            }
+        }
     }
     __syncthreads();
-    const int o = threadIdx.x >> 3, kl = threadIdx.x & 7;   // output row, k lane
-    for (int bl = 0; bl < nb; ++bl) {
-        float acc = 0.f;
-        if (o < rows) {
-            const float *mrow = Ms + o * ldm;
-            const float *q = qs + bl * d_n;
-            for (int k = kl; k < d_n; k += 8) acc = fmaf(q[k], mrow[k], acc);
+    // 4. eight sequences at a time: chunk dot products, then the reduce-scatter
+    for (int g0 = 0; g0 < nb; g0 += 8) {
+        float acc[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const float4 *qc = reinterpret_cast<const float4 *>(sm_abs + ((g0 + s) * 8 + kl) * cst);
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < CSMAX / 4; ++u) {
+                if (4 * u < cs) {
+                    const float4 q = qc[u];
+                    a0 = fmaf(q.x, mr[4 * u], a0);
+                    a1 = fmaf(q.y, mr[4 * u + 1], a1);
+                    a0 = fmaf(q.z, mr[4 * u + 2], a0);
+                    a1 = fmaf(q.w, mr[4 * u + 3], a1);
+                }
+            }
+            acc[s] = a0 + a1;
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        if (kl == 0 && o < rows)
-            p.q_tilde[((long long)(b0 + bl) * p.H + h) * d_h + i0 + o] = p.prescale * acc;
+        // lanes kl and kl ^ 4 swap halves: each keeps 4 sequences, then 2, then 1
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool up = kl & 4;
+            const float send = up ? acc[i] : acc[i + 4];
+            const float keep = up ? acc[i + 4] : acc[i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const bool up = kl & 2;
+            const float send = up ? acc[i] : acc[i + 2];
+            const float keep = up ? acc[i + 2] : acc[i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        {
+            const bool up = kl & 1;
+            const float send = up ? acc[0] : acc[1];
+            const float keep = up ? acc[1] : acc[0];
+            acc[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        }
+        const int s = g0 + kl;   // the sequence this lane now holds
+        if (o < rows && s < nb)
+            p.q_tilde[((long long)(b0 + s) * p.H + h) * d_h + i0 + o] = p.prescale * acc[0];
     }
-    if (rot) {
-        p.q_hat[qoff_r + 2 * ri] = p.prescale * (rx0 * rc - rx1 * rs);
-        p.q_hat[qoff_r + 2 * ri + 1] = p.prescale * (rx0 * rs + rx1 * rc);
+    // 5. the positional queries: Rot(t) q_rope with t = L_b - 1
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+        const int e = threadIdx.x + u * ABSORB_THREADS;
+        if (rope && e < nb * half) {
+            const int rb = b0 + e / half, ri = e % half;
+            int t = rL[u] - 1;
+            if (t < 0) t = 0;
+            if (t >= p.rope_max_pos) {
+                if (!p.check_rows || length_ok(p.R, rb, rL[u])) dev_report(GVA_DEV_BAD_POSITION);
+                t = 0;
+            }
+            const float rc = p.rope_tab[((long long)t * half + ri) * 2];
+            const float rs = p.rope_tab[((long long)t * half + ri) * 2 + 1];
+            float *qh = p.q_hat + ((long long)rb * p.H + h) * p.d_r;
+            qh[2 * ri] = p.prescale * (rx0[u] * rc - rx1[u] * rs);
+            qh[2 * ri + 1] = p.prescale * (rx0[u] * rs + rx1[u] * rc);
+        }
     }
     if (threadIdx.x == 0) GVA_KT(4);
 }
