@@ -37,7 +37,10 @@ namespace gva {
 // the small kernels around the decode: the query absorption before it and the
 // log-sum-exp combine after it are resident beside it under programmatic dependent
 // launch instead of waiting for the SM to drain.
-constexpr int MMA_CONSUMERS = 8;
+#ifndef GVA_MMA_CONSUMERS
+#define GVA_MMA_CONSUMERS 8
+#endif
+constexpr int MMA_CONSUMERS = GVA_MMA_CONSUMERS;   // at most 15 (launch bound)
 constexpr int MMA_THREADS = 16 * 32;                  // launch bound (-> <= 128 registers)
 constexpr float MMA_RESCALE_TH = 8.f;                 // log2 units
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
@@ -67,7 +70,8 @@ constexpr int TRACE_CTAS = 4, TRACE_SLOTS = 512;
 __device__ long long g_trace[TRACE_CTAS * TRACE_SLOTS];
 // stamps go to shared memory (a global store before an mbarrier arrive would delay the
 // arrive until the store completes) and are copied out when the stamping thread exits
-#define GVA_TRACE_DECL __shared__ long long s_trace[TRACE_SLOTS]
+__shared__ long long s_trace[TRACE_SLOTS];
+#define GVA_TRACE_DECL
 #define GVA_TRACE_AT(slot)                                                          \
     do {                                                                            \
         if ((slot) < TRACE_SLOTS) s_trace[(slot)] = clock64();                      \
@@ -438,7 +442,6 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     const int wpg = mp.wpg;
     const int gid = lane >> 2, tig = lane & 3;
     constexpr int KD = DH / 16;       // k16 steps over d_h (and 16-row tiles of O^T)
-    constexpr int NSL = 1;            // own slabs per loop trip (2 measured no faster)
     constexpr int DRK16 = DR / 16;    // full k16 steps over the positional slice
     constexpr bool DR_K8 = (DR % 16) == 8;  // one trailing k8 step
     // ldmatrix lane roles
@@ -450,11 +453,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     if (mp.early) pdl_wait();         // the absorbed queries come from the preceding grid
     if (w == 0 && g == 0 && lane == 0) GVA_KT(6);
     if (w == 0 && g == 0 && lane == 0) GVA_CTA_T(1);
+    // The slabs of the share go round-robin to the group's warps: this warp takes
+    // s0 + w, s0 + w + wpg, ...; slab s0 + i sits in ring stage i mod NS, phase (i / NS) & 1.
+    long long my_s = s0 + w;
+    int my_stage = w % NS;
+    uint32_t my_phase = (uint32_t)(w / NS) & 1u;
     int b = seq_of_slab(F, B, s0);
-    int stage = 0, wsel = 0;          // ring stage and slab-owner counter of the next slab
-    uint32_t phase = 0;
     int tslab = 0;                    // trace index
-    long long s = s0;
+    long long s = s0;                 // start of the current segment (one sequence's slabs)
     bool alive = true;
     while (s < s1) {
         while (F[b + 1] <= s) ++b;
@@ -560,70 +566,31 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         for (int nt = 0; nt < NT; ++nt) { m_run[nt] = -INFINITY; l_run[nt] = 0.f; }
 
         if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(4);
-        // The warp's own slabs of the segment are taken NSL at a time: their chains of
-        // dependent latencies overlap and share one max reduction and rescale test.
-        // A missing partner (odd tail) is a copy of the first slab with no valid token.
-        while (s < seg_end) {
-            int my_stage[NSL];
-            uint32_t my_phase[NSL];
-            int j0[NSL];
-            int cnt = 0;
-            while (s < seg_end && cnt < NSL) {
-                const bool mine = wsel == w;
-                if (mine) {
-#pragma unroll
-                    for (int u = 0; u < NSL; ++u)   // constant indices: the arrays stay in registers
-                        if (cnt == u) {
-                            my_stage[u] = stage;
-                            my_phase[u] = phase;
-                            j0[u] = (int)(s - Fb) * SLAB;
-                        }
-                    ++cnt;
-                }
-                if (++stage == NS) { stage = 0; phase ^= 1u; }
-                if (++wsel == wpg) wsel = 0;
-                ++s;
-            }
-            if (cnt == 0 || !alive) continue;
-#pragma unroll
-            for (int u = 1; u < NSL; ++u)
-                if (u >= cnt) { my_stage[u] = my_stage[0]; my_phase[u] = my_phase[0]; j0[u] = Lb; }
-            bool waited = true;
-#pragma unroll
-            for (int u = 0; u < NSL; ++u)
-                if (u < cnt && waited && !mbar_wait(bar_full + 8 * my_stage[u], my_phase[u], abort))
-                    waited = false;
+        while (my_s < seg_end && alive) {
             // one decision for the warp (the code below is warp-synchronous)
-            waited = __all_sync(0xffffffffu, waited);
+            const bool waited = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * my_stage, my_phase, abort));
             if (!waited) {
                 alive = false;
-                continue;
+                break;
             }
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(8 + 2 * tslab);
-            int nv[NSL];
-            uint32_t st[NSL];
-#pragma unroll
-            for (int u = 0; u < NSL; ++u) {
-                nv[u] = min(SLAB, Lb - j0[u]);
-                if (u < cnt && stage_bad[my_stage[u]]) {
-                    if (lane == 0 && g == 0) dev_report(GVA_DEV_BAD_PAGE);
-                    nv[u] = 0;
-                }
-                st[u] = base_u32 + my_stage[u] * mp.stage_bytes;
+            const int j0 = (int)(my_s - Fb) * SLAB;
+            int nv = min(SLAB, Lb - j0);
+            if (stage_bad[my_stage]) {
+                if (lane == 0 && g == 0) dev_report(GVA_DEV_BAD_PAGE);
+                nv = 0;
             }
+            const uint32_t st = base_u32 + my_stage * mp.stage_bytes;
 
             // ---- scores: A = the key tile (tokens x d), B = Q^T ----
-            float sc[NSL][NT][2][4];
+            float sc[NT][2][4];
 #pragma unroll
-            for (int u = 0; u < NSL; ++u)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int a2 = 0; a2 < 2; ++a2)
-                        sc[u][nt][a2][0] = sc[u][nt][a2][1] = sc[u][nt][a2][2] = sc[u][nt][a2][3] = 0.f;
-#pragma unroll
-            for (int u = 0; u < NSL; ++u) {
-                const uint32_t kst = GQA ? st[u] + mp.off_k : st[u];
+                for (int a2 = 0; a2 < 2; ++a2)
+                    sc[nt][a2][0] = sc[nt][a2][1] = sc[nt][a2][2] = sc[nt][a2][3] = 0.f;
+            {
+                const uint32_t kst = GQA ? st + mp.off_k : st;
                 uint32_t av[KD][4];
 #pragma unroll
                 for (int kk = 0; kk < KD; ++kk)
@@ -631,7 +598,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                             av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
                 uint32_t ar[DRK16 > 0 ? DRK16 : 1][4], ar8[2];
                 if (DR > 0) {
-                    const uint32_t rbase = st[u] + mp.off_r;
+                    const uint32_t rbase = st + mp.off_r;
 #pragma unroll
                     for (int kk = 0; kk < DRK16; ++kk)
                         ldsm_x4(rbase + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + (2 * kk + (lm_mat >> 1)) * 16,
@@ -643,51 +610,53 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 for (int kk = 0; kk < KD; ++kk)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16816(sc[u][nt][kk & 1], av[kk], bq[kk][nt][0], bq[kk][nt][1]);
+                        mma16816(sc[nt][kk & 1], av[kk], bq[kk][nt][0], bq[kk][nt][1]);
                 if (DR > 0) {
 #pragma unroll
                     for (int kk = 0; kk < DRK16; ++kk)
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma16816(sc[u][nt][(KD + kk) & 1], ar[kk], bqr[kk][nt][0], bqr[kk][nt][1]);
+                            mma16816(sc[nt][(KD + kk) & 1], ar[kk], bqr[kk][nt][0], bqr[kk][nt][1]);
                     if (DR_K8) {
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma1688(sc[u][nt][(KD + DRK16) & 1], ar8[0], ar8[1], bqr8[nt]);
+                            mma1688(sc[nt][(KD + DRK16) & 1], ar8[0], ar8[1], bqr8[nt]);
                     }
                 }
             }
+            // value tiles for the weighted sum (V^T as the A operand), read while the
+            // softmax below runs
+            uint32_t apv[KD][4];
+#pragma unroll
+            for (int mt = 0; mt < KD; ++mt)
+                ldsm_x4_t(vtile_addr<DH>(st, g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
+                          apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
 
             // ---- per head: hi + lo columns -> score of tokens gid, gid + 8 ----
-            float z[NSL][NT][2];
-#pragma unroll
-            for (int u = 0; u < NSL; ++u)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    z[u][nt][0] = (sc[u][nt][0][0] + sc[u][nt][0][1]) + (sc[u][nt][1][0] + sc[u][nt][1][1]);
-                    z[u][nt][1] = (sc[u][nt][0][2] + sc[u][nt][0][3]) + (sc[u][nt][1][2] + sc[u][nt][1][3]);
-                    if (gid >= nv[u]) z[u][nt][0] = -INFINITY;
-                    if (gid + 8 >= nv[u]) z[u][nt][1] = -INFINITY;
-                }
-            float mloc[NT];
-            bool raise_any = false;
+            float z[NT][2];
+            bool over = false;   // a score above the running maximum by more than the threshold
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float m = fmaxf(z[0][nt][0], z[0][nt][1]);
-#pragma unroll
-                for (int u = 1; u < NSL; ++u) m = fmaxf(m, fmaxf(z[u][nt][0], z[u][nt][1]));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                mloc[nt] = m;
-                raise_any |= m > m_run[nt] + MMA_RESCALE_TH;
+                z[nt][0] = (sc[nt][0][0] + sc[nt][0][1]) + (sc[nt][1][0] + sc[nt][1][1]);
+                z[nt][1] = (sc[nt][0][2] + sc[nt][0][3]) + (sc[nt][1][2] + sc[nt][1][3]);
+                if (gid >= nv) z[nt][0] = -INFINITY;
+                if (gid + 8 >= nv) z[nt][1] = -INFINITY;
+                over |= fmaxf(z[nt][0], z[nt][1]) > m_run[nt] + MMA_RESCALE_TH;
             }
-            if (__any_sync(0xffffffffu, raise_any)) {
+            // Lazy rescale: the running maximum moves only when a score exceeds it by
+            // more than the threshold (always on a head's first valid token); otherwise
+            // the probabilities are taken against the stale maximum (at most 2^threshold)
+            // and the max reduction over the token lanes is skipped.
+            if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const bool raise = mloc[nt] > m_run[nt] + MMA_RESCALE_TH;
-                    const float alpha = raise ? exp2f(m_run[nt] - mloc[nt]) : 1.f;  // 0 when m_run = -inf
-                    if (raise) m_run[nt] = mloc[nt];
+                    float m = fmaxf(z[nt][0], z[nt][1]);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    const bool raise = m > m_run[nt] + MMA_RESCALE_TH;
+                    const float alpha = raise ? exp2f(m_run[nt] - m) : 1.f;  // 0 when m_run = -inf
+                    if (raise) m_run[nt] = m;
                     l_run[nt] *= alpha;
 #pragma unroll
                     for (int mt = 0; mt < KD; ++mt) {
@@ -696,56 +665,47 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     }
                 }
             }
+            // ---- probabilities, then P^T as the B operand (column gid: head 4nt + gid/2) ----
+            uint32_t bp[NT][2];
 #pragma unroll
-            for (int u = 0; u < NSL; ++u) {
-                // value tiles for the weighted sum (V^T as the A operand)
-                uint32_t apv[KD][4];
-#pragma unroll
-                for (int mt = 0; mt < KD; ++mt)
-                    ldsm_x4_t(vtile_addr<DH>(st[u], g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
-                              apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
-                // ---- probabilities, then P^T as the B operand (column gid: head 4nt + gid/2) ----
-                uint32_t bp[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float p0 = z[u][nt][0] == -INFINITY ? 0.f : exp2f(z[u][nt][0] - m_run[nt]);
-                    const float p1 = z[u][nt][1] == -INFINITY ? 0.f : exp2f(z[u][nt][1] - m_run[nt]);
-                    l_run[nt] += p0 + p1;
-                    const float a0 = __shfl_sync(0xffffffffu, p0, srcA);   // token 2tig
-                    const float a1 = __shfl_sync(0xffffffffu, p1, srcA);   // token 2tig + 8
-                    const float b0 = __shfl_sync(0xffffffffu, p0, srcB);   // token 2tig + 1
-                    const float b1 = __shfl_sync(0xffffffffu, p1, srcB);   // token 2tig + 9
-                    bp[nt][0] = part_bf16x2(a0, b0, lo_col);
-                    bp[nt][1] = part_bf16x2(a1, b1, lo_col);
-                }
-                // ---- O^T += V^T . P^T ----
-                if (nv[u] < SLAB) {
-                    // zero the values of tokens past the end (they may hold NaN)
-                    const int ta = 2 * tig, tb = 8 + 2 * tig;
-                    const uint32_t ma = (ta >= nv[u] ? 0u : 0xffffu) | (ta + 1 >= nv[u] ? 0u : 0xffff0000u);
-                    const uint32_t mb = (tb >= nv[u] ? 0u : 0xffffu) | (tb + 1 >= nv[u] ? 0u : 0xffff0000u);
-#pragma unroll
-                    for (int mt = 0; mt < KD; ++mt) {
-                        apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
-                    }
-                }
-#pragma unroll
-                for (int mt = 0; mt < KD; ++mt)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+                const float p0 = z[nt][0] == -INFINITY ? 0.f : exp2f(z[nt][0] - m_run[nt]);
+                const float p1 = z[nt][1] == -INFINITY ? 0.f : exp2f(z[nt][1] - m_run[nt]);
+                l_run[nt] += p0 + p1;
+                const float a0 = __shfl_sync(0xffffffffu, p0, srcA);   // token 2tig
+                const float a1 = __shfl_sync(0xffffffffu, p1, srcA);   // token 2tig + 8
+                const float b0 = __shfl_sync(0xffffffffu, p0, srcB);   // token 2tig + 1
+                const float b1 = __shfl_sync(0xffffffffu, p1, srcB);   // token 2tig + 9
+                bp[nt][0] = part_bf16x2(a0, b0, lo_col);
+                bp[nt][1] = part_bf16x2(a1, b1, lo_col);
             }
+            // ---- O^T += V^T . P^T ----
+            if (nv < SLAB) {
+                // zero the values of tokens past the end (they may hold NaN)
+                const int ta = 2 * tig, tb = 8 + 2 * tig;
+                const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
+                const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
+#pragma unroll
+                for (int mt = 0; mt < KD; ++mt) {
+                    apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < KD; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
             // the products above consumed every tile register, so all of the warp's
-            // shared-memory reads of its stages are complete: release them to the producer
+            // shared-memory reads of the stage are complete: release it to the producer
             __syncwarp();
-            if (lane == 0) {
-#pragma unroll
-                for (int u = 0; u < NSL; ++u)
-                    if (u < cnt) mbar_arrive_relaxed(bar_empty + 8 * my_stage[u]);
-            }
+            if (lane == 0) mbar_arrive_relaxed(bar_empty + 8 * my_stage);
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(9 + 2 * tslab);
             ++tslab;
+            my_s += wpg;
+            my_stage += wpg;
+            while (my_stage >= NS) { my_stage -= NS; my_phase ^= 1u; }
         }
+        s = seg_end;
 
         // ---- segment end: fold hi/lo columns, reduce l over the 8 token lanes, merge
         //      the group's warps ----
