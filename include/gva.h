@@ -116,9 +116,12 @@ typedef struct {
 } gva_kv_cache;
 
 typedef enum {
-    GVA_PATH_AUTO = 0,       /* tensor-core kernel where it applies, else CUDA cores */
+    GVA_PATH_AUTO = 0,       /* tensor-core kernels where they apply, else CUDA cores */
     GVA_PATH_SIMT = 1,       /* CUDA-core kernel (fp32 FMA); every supported shape */
-    GVA_PATH_MMA = 2         /* bf16 tensor-core kernel (bf16 cache only) */
+    GVA_PATH_MMA = 2,        /* separate absorb, bf16 tensor-core split-K and combine
+                                kernels (bf16 cache only) */
+    GVA_PATH_FUSED = 3       /* absorb, then one kernel for the tensor-core split-K and
+                                the merge of the splits (bf16 cache, GVA decode only) */
 } gva_path;
 
 typedef struct {
@@ -181,9 +184,13 @@ size_t gva_decode_workspace_size(const gva_dims *dims);
  *   out[b,h,:] = sum_j softmax(z)_j v_{j,g(h)}     (device fp32 [B][H][d_h])
  *   lse[b,h]   = ln sum_j exp(z_j)                 (device fp32 [B][H], or NULL)
  * L_b = 0 gives out = 0 and lse = -inf.  Runs absorb, a split-K partial kernel
- * (flash-decoding over 16-token slabs spread evenly over the GPU) and a
- * log-sum-exp combine.  The workspace (device, >= gva_decode_workspace_size(dims),
- * 256-byte aligned) is scratch, overwritten by each call.  q_nope/q_rope/M/seq_len/
+ * (flash-decoding over 16-token slabs spread evenly over the GPU) and a log-sum-exp
+ * combine; GVA_PATH_FUSED merges the splits inside the partial kernel instead.  The
+ * workspace (device,
+ * >= gva_decode_workspace_size(dims), 256-byte aligned) is scratch, except for a
+ * block of per-(group, sequence) tickets that must be zero before the first call
+ * and that every completed call leaves zero: zero-fill a new workspace once, and
+ * again after a call that reported GVA_DEV_TIMEOUT.  q_nope/q_rope/M/seq_len/
  * rope_tab as in gva_absorb_query. */
 int gva_decode_attention(void *stream, const gva_dims *dims, const void *q_nope,
                          const void *q_rope, const float *M, const int *seq_len,

@@ -19,8 +19,14 @@ def _mma_ok(c):
     return w.cache_dtype == "bf16" and w.d_h in (64, 128) and w.G <= 8
 
 
+def _fused_ok(c):
+    """The fused kernel's support matrix (include/gva.h: bf16 cache, d_h 64 or 128)."""
+    w = c.w
+    return w.cache_dtype == "bf16" and w.d_h in (64, 128)
+
+
 def paths_for(c):
-    return ["simt", "mma"] if _mma_ok(c) else ["simt"]
+    return (["simt"] + (["mma"] if _mma_ok(c) else []) + (["fused"] if _fused_ok(c) else []))
 
 
 # small variants of the five workloads: several slabs and CTAs, ragged tails
@@ -46,11 +52,13 @@ def _step(c, path, num_ctas=0):
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("path", ["simt", "mma", "auto"])
+@pytest.mark.parametrize("path", ["simt", "mma", "fused", "auto"])
 def test_step_small_workloads(name, path):
     c = make_case(workload(name, **SMALL[name]))
     if path == "mma" and not _mma_ok(c):
         pytest.skip("tensor-core path needs a bf16 cache")
+    if path == "fused" and not _fused_ok(c):
+        pytest.skip("fused path needs a bf16 cache")
     out, lse, ref, ref_lse, _ = _step(c, path)
     assert_close(out, ref, c.w.cache_dtype, f"{name}/{path} out")
     assert_close(lse, ref_lse, c.w.cache_dtype, f"{name}/{path} lse")
@@ -267,7 +275,7 @@ def test_gqa_comparator(name):
     w = c.w
     scale = 1.0 / np.sqrt(w.d_h)
     ref, ref_lse = oracle.gqa_decode(q, c.seq_len, oracle_rows(c), K, c.V, scale, w.G)
-    for path in paths_for(c):
+    for path in [p for p in paths_for(c) if p != "fused"]:
         out = torch.empty((w.B, w.H, w.d_h), device="cuda")
         lse = torch.empty((w.B, w.H), device="cuda")
         g.gva_gqa_decode_attention(D.dims, q.cuda(), D.seq_len, kv, scale, out, lse, D.ws,
@@ -277,10 +285,24 @@ def test_gqa_comparator(name):
         assert_close(lse.cpu().numpy(), ref_lse, "bf16", f"gqa {path} lse")
 
 
+def test_gqa_refuses_fused_path():
+    """The fused kernel decodes GVA caches only: the comparator reports UNSUPPORTED."""
+    c = make_case(workload("350m", **SMALL["350m"]))
+    D = Dev(c)
+    g = gva()
+    kv = g.KVCache(D.rows, make_gqa_keys(c).cuda(), D.V)
+    w = c.w
+    out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    with pytest.raises(g.GvaError) as e:
+        g.gva_gqa_decode_attention(D.dims, make_gqa_query(c).cuda(), D.seq_len, kv, 0.125,
+                                   out, None, D.ws, path="fused")
+    assert e.value.status == g.GVA_ERR_UNSUPPORTED
+
+
 # --------------------------------------------------------------------------- #
 # CUDA graphs: the calls can be captured (torch's default global capture mode)
 # --------------------------------------------------------------------------- #
-@pytest.mark.parametrize("path", ["simt", "mma"])
+@pytest.mark.parametrize("path", ["simt", "mma", "fused"])
 def test_graph_capture_and_replay(path):
     c = make_case(workload("350m", T=200, B=3))
     D = Dev(c)

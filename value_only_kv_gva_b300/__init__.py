@@ -33,7 +33,7 @@ GVA_DEV_OK, GVA_DEV_BAD_LENGTH, GVA_DEV_BAD_PAGE, GVA_DEV_BAD_POSITION, \
     GVA_DEV_TIMEOUT = 0, 1, 2, 3, 4
 GVA_F32, GVA_BF16 = 0, 1
 LAYOUTS = {"contiguous": 0, "ragged": 1, "paged": 2}
-PATHS = {"auto": 0, "simt": 1, "mma": 2}
+PATHS = {"auto": 0, "simt": 1, "mma": 2, "fused": 3}
 
 
 class gva_dims(ctypes.Structure):
@@ -312,8 +312,10 @@ def gva_get_device_status() -> int:
 
 
 def workspace(dims: Dims, device=None) -> torch.Tensor:
-    """Allocate a decode workspace (uint8, 256-byte aligned by the caching allocator)."""
+    """Allocate a decode workspace (uint8, 256-byte aligned by the caching allocator),
+    zero-filled: its per-pair tickets must start at zero (each completed call leaves
+    them zero)."""
     n = gva_decode_workspace_size(dims)
     if n == 0:
         raise GvaError(GVA_ERR_ARG, "gva_decode_workspace_size")
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")

@@ -13,6 +13,7 @@
 #include "prep_kernels.cuh"
 #include "decode_simt.cuh"
 #include "decode_mma.cuh"
+#include "decode_fused.cuh"
 
 using namespace gva;
 
@@ -95,6 +96,7 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, true>);
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, true>);
     if (e == cudaSuccess) e = mma_opt_in_all();
+    if (e == cudaSuccess) e = fused_opt_in_all();
     if (e == cudaSuccess && !encode_fn()) e = cudaErrorSymbolNotFound;
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
@@ -161,7 +163,7 @@ RowsDev to_dev(const gva_rows &R) {
 
 // Workspace: [q_tilde B*H*d_h][q_hat B*H*d_r][part_o slots*H*d_h][part_ml slots*H*2]
 struct WsPlan {
-    size_t qt, qh, po, pm, total;
+    size_t qt, qh, po, pm, tk, total;
     long long slots;
 };
 
@@ -173,6 +175,9 @@ WsPlan plan_ws(const gva_dims *d, int sms) {
     w.qh = o; o = align_up(o + sizeof(float) * d->B * d->H * (d->d_r > 0 ? d->d_r : 1), 256);
     w.po = o; o = align_up(o + sizeof(float) * w.slots * d->H * d->d_h, 256);
     w.pm = o; o = align_up(o + sizeof(float) * w.slots * d->H * 2, 256);
+    // fused path: one ticket per (group, sequence); its partial slots (CTA c + pair
+    // index, r heads each) fit in po / pm
+    w.tk = o; o = align_up(o + sizeof(int) * (size_t)d->G * d->B, 256);
     w.total = o;
     return w;
 }
@@ -382,7 +387,7 @@ static int decode_arg_checks(const gva_dims *d, const gva_rows *rows, float *out
                              const gva_decode_opts *o, bool gva_shape) {
     if (!dims_ok(d, gva_shape) || !rows_ok(rows, d->B)) return GVA_ERR_ARG;
     if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
-    if (o->flags != 0 || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_MMA || o->num_ctas < 0)
+    if (o->flags != 0 || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_FUSED || o->num_ctas < 0)
         return GVA_ERR_ARG;
     return GVA_OK;
 }
@@ -415,14 +420,45 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
                        !aligned16(q_rope) || !aligned16(cache->K_rope) || !aligned16(rope_tab)))
         return GVA_ERR_ARG;
     const bool mma_ok = mma_supported(d);
+    const bool fused_ok = fused_supported(d, cache->rows);
     if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
+    if (o->path == GVA_PATH_FUSED && !fused_ok) return GVA_ERR_UNSUPPORTED;
     WsPlan plan;
     int sms = 0;
     st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
     if (st != GVA_OK) return st;
+    char *w = static_cast<char *>(ws);
+    // AUTO takes the separate-kernel tensor-core path: on every measured workload it is
+    // faster than the fused kernel (whose per-group tiles read each cache row in
+    // d_h-wide pieces and whose in-kernel merge lengthens the tail)
+    if (o->path == GVA_PATH_FUSED) {
+        float *qt = reinterpret_cast<float *>(w + plan.qt);
+        float *qh = reinterpret_cast<float *>(w + plan.qh);
+        st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                           scale * LOG2E, qt, qh, sms, &cache->rows, false);
+        if (st != GVA_OK) return st;
+        FusedParams fp;
+        memset(&fp, 0, sizeof(fp));
+        fp.B = d->B;
+        fp.H = d->H;
+        fp.G = d->G;
+        fp.r = d->H / d->G;
+        fp.d_r = d->d_r;
+        fp.seq_len = seq_len;
+        fp.R = to_dev(cache->rows);
+        fp.Krope = cache->K_rope;
+        fp.qt = qt;
+        fp.qh = qh;
+        fp.out = out;
+        fp.lse = lse;
+        fp.part_o = reinterpret_cast<float *>(w + plan.po);
+        fp.part_ml = reinterpret_cast<float *>(w + plan.pm);
+        fp.ticket = reinterpret_cast<int *>(w + plan.tk);
+        fp.early = 1;
+        return run_fused(stream, fp, cache->V, cache->rows, d->d_h, sms, o->num_ctas);
+    }
     const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
 
-    char *w = static_cast<char *>(ws);
     float *qt = reinterpret_cast<float *>(w + plan.qt);
     float *qh = reinterpret_cast<float *>(w + plan.qh);
     // the tensor-core decode rotates the positional query itself (its inputs are final
@@ -487,6 +523,7 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     if (!q || !seq_len || !cache->K || !cache->V || !aligned16(q) || !aligned16(cache->K) ||
         !aligned16(cache->V))
         return GVA_ERR_ARG;
+    if (o->path == GVA_PATH_FUSED) return GVA_ERR_UNSUPPORTED;   // GVA decode only
     gva_dims dg = *d;
     dg.d_r = 0;
     const bool mma_ok = mma_supported(&dg);
