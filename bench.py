@@ -324,7 +324,7 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = oracle_baseline(w, c, budget_s=args.cpu_seconds)
 
-    launches_per_step = nl * 4
+    launches_per_step = nl * (3 if path == "fused" else 4)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -351,7 +351,8 @@ def run_ours(args, dist: Dist):
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
                      "peak_source": "measured" if peaks else "fallback",
-                     "traffic": None},
+                     "traffic": profiled_traffic(w.name) if path in ("auto", "mma") else None,
+                     "traffic_kernel": "decode_mma_kernel, DRAM bytes per launch (ncu)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -360,6 +361,35 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+# Sources of the tensor-core decode kernel: a DRAM-traffic figure recorded with ncu is
+# reported only while these files are unchanged since the capture.
+KERNEL_SOURCES = ["decode_mma.cuh", "decode_simt.cuh", "common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "value_only_kv_gva_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_mma_kernel on
+    this workload, from the ncu summary under profiles/, or None when there is none or
+    the kernel's sources changed since it was taken."""
+    import re
+    path = os.path.join(ROOT, "profiles", f"decode_mma_{workload}_ncu.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        m = re.search(r"traffic_bytes_per_launch=(\d+) source_hash=([0-9a-f]+)", f.read())
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
 
 
 def capture_list(torch, stream, items, fn):
@@ -508,7 +538,7 @@ def main():
                     choices=["tiny", "350m", "ragged", "long", "paged"])
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per step (0 = enough distinct caches to exceed L2)")
-    ap.add_argument("--path", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "mma", "fused"])
     ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing (s)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
