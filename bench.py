@@ -289,6 +289,7 @@ def run_ours(args, dist: Dist):
 
     peaks = measured_peaks()
     hbm_peak = peaks["hbm_gbs"] if peaks else FALLBACK_HBM_GBS
+    read_probe = read_probe_gbs(gva, torch, stream, dev)
 
     # GQA comparator of matched H, G, d_h reading explicit K and V
     gqa = None
@@ -340,6 +341,8 @@ def run_ours(args, dist: Dist):
             "us_per_decode": round(us_decode, 3),
             "pct_of_8tbs_spec": round(100 * value / dist.world / SPEC_HBM_GBS, 2),
             "pct_of_measured_copy": round(100 * value / dist.world / hbm_peak, 2),
+            "read_probe_gbs": read_probe,
+            "decode_pct_of_read_probe": round(100 * achieved / read_probe, 2) if read_probe else None,
             "seqs_steps_per_s": round(w.B * dist.world / (ms_per_step * 1e-3), 1),
             "l2": f"inputs larger than L2: {nl} distinct layer caches, "
                   f"{bytes_layer * nl / 1e6:.0f} MB",
@@ -451,14 +454,35 @@ def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, 
 # --------------------------------------------------------------------------- #
 # the oracle on the host cores
 # --------------------------------------------------------------------------- #
-def oracle_sample(w, c, budget_s):
+def read_probe_gbs(gva, torch, stream, dev, gib: float = 4.0, reps: int = 10):
+    """Read-only streaming ceiling of this GPU, measured in the same run: the library's
+    probe kernel over a buffer larger than L2, CUDA events on the launching stream."""
+    n = int(gib * (1 << 30)) // 16 * 16
+    buf = torch.ones(n // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            gva.gva_read_probe(buf, sink, stream=stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gva.gva_read_probe(buf, sink, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) * 1e-3 / reps
+    del buf
+    return round(n / secs / 1e9, 1)
+
+
+def oracle_sample(w, c, budget_s, threads=None):
     """Run the fp64 oracle over whole sequences of one layer until ~budget_s elapses;
     returns (seconds, cache bytes read, description, threads)."""
     import numpy as np
 
     import oracle
     rows_all = {"contiguous": None}
-    nthr = os.cpu_count() or 1
+    nthr = threads or os.cpu_count() or 1
     oracle.set_threads(nthr)
     V = oracle._np(c.V)
     K = oracle._np(c.Kr)
@@ -488,10 +512,13 @@ def oracle_sample(w, c, budget_s):
 
 def oracle_baseline(w, c, budget_s=10.0):
     secs, nbytes, nseq, thr = oracle_sample(w, c, budget_s)
+    s1, b1, n1, _ = oracle_sample(w, c, max(1.0, budget_s / 4), threads=1)
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": thr,
             "kind": "oracle",
             "sample": f"{nseq} whole sequences of one {w.name} layer (all {w.H} heads each), "
-                      f"fp64 C oracle with OpenMP over (b, h), {secs:.1f} s"}
+                      f"fp64 C oracle with OpenMP over (b, h), {secs:.1f} s",
+            "single_thread_value": round(b1 / s1 / 1e9, 4),
+            "single_thread_sample": f"{n1} whole sequences, 1 thread, {s1:.1f} s"}
 
 
 def run_reference(args, dist: Dist):

@@ -246,6 +246,14 @@ int gva_decode_attention_static(void *stream, const gva_dims *dims, const void *
  * a CUDA failure. */
 int gva_get_device_status(int *code_out);
 
+/* Measurement helper (not on the decode path): read `bytes` of device memory at `buf`
+ * once, as a pure read stream (16-byte non-allocating loads, about 16 loads in flight
+ * per thread, 2048 threads per SM), and fold the words into *sink (device unsigned,
+ * XOR of every 32-bit word of the buffer, overwritten) so that no load is dead.  Its
+ * throughput is the read-only ceiling the decode kernels are compared with.  `buf`
+ * 16-byte aligned, `bytes` a positive multiple of 16; otherwise GVA_ERR_ARG. */
+int gva_read_probe(void *stream, const void *buf, size_t bytes, unsigned *sink);
+
 /* Streaming multiprocessors of the current device (the decode grid is sized from it). */
 int gva_num_sms(void);
 

@@ -334,3 +334,18 @@ def test_graph_capture_and_replay(path):
     ref, ref_lse = oracle_decode(c, V, K)
     assert_close(out.cpu().numpy(), ref, "bf16", f"graph {path}")
     assert_close(lse.cpu().numpy(), ref_lse, "bf16", f"graph {path} lse")
+
+
+def test_read_probe_reads_every_word():
+    """The bandwidth probe folds every 32-bit word of its buffer: its XOR matches the
+    host's (odd size: the unrolled part and the tail both run)."""
+    g = gva()
+    n = 37 * 1024 * 1024 // 4 + 12   # words (a multiple of 4 words: 16-byte vectors)
+    gen = torch.Generator().manual_seed(7)
+    host = torch.randint(-2**31, 2**31 - 1, (n,), generator=gen, dtype=torch.int64).to(torch.int32)
+    buf = host.cuda()
+    sink = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    g.gva_read_probe(buf, sink)
+    torch.cuda.synchronize()
+    ref = int(np.bitwise_xor.reduce(host.numpy().view(np.uint32)))
+    assert int(sink.cpu().numpy().view(np.uint32)[0]) == ref

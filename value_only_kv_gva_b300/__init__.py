@@ -80,11 +80,13 @@ _lib.gva_gqa_decode_attention.argtypes = [_P, _PD, _P, _P, _PKV, _F, _P, _P, _P,
 _lib.gva_get_device_status.argtypes = [ctypes.POINTER(_I)]
 _lib.gva_last_cuda_error.restype = _I
 _lib.gva_decode_attention_static.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I, _F, _P, _P]
+_lib.gva_read_probe.argtypes = [_P, _P, _Z, _P]
 
 EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_table_fill",
            "gva_absorb_query", "gva_append_cache", "gva_decode_workspace_size",
            "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
-           "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static"]
+           "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static",
+           "gva_read_probe"]
 
 
 class GvaError(RuntimeError):
@@ -209,6 +211,14 @@ def gva_abi_version() -> int:
 
 def gva_num_sms() -> int:
     return int(_lib.gva_num_sms())
+
+
+def gva_read_probe(buf, sink, stream=None) -> None:
+    """Read every byte of the device tensor `buf` once (pure read stream) and fold its
+    32-bit words by XOR into the int32 device tensor `sink` (one element)."""
+    _check(_lib.gva_read_probe(_stream(stream), _ptr(buf, None, "buf"),
+                               buf.numel() * buf.element_size(), _ptr(sink, torch.int32, "sink")),
+           "gva_read_probe")
 
 
 def gva_rope_table_fill(max_pos: int, d_r: int, base: float = 10000.0) -> torch.Tensor:

@@ -289,6 +289,33 @@ const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0};
 
 }  // namespace
 
+// Read-only streaming probe: every thread issues PROBE_UNROLL independent 16-byte
+// non-allocating loads per trip and folds them into a XOR; one atomic per warp.
+constexpr int PROBE_THREADS = 512, PROBE_UNROLL = 16;
+__global__ void __launch_bounds__(PROBE_THREADS) read_probe_kernel(const uint4 *p, long long n16,
+                                                                   unsigned *sink) {
+    unsigned acc = 0;
+    const long long stride = (long long)gridDim.x * PROBE_THREADS;
+    long long i = (long long)blockIdx.x * PROBE_THREADS + threadIdx.x;
+    for (; i + (PROBE_UNROLL - 1) * stride < n16; i += PROBE_UNROLL * stride) {
+        uint4 v[PROBE_UNROLL];
+#pragma unroll
+        for (int u = 0; u < PROBE_UNROLL; ++u)
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                         : "l"(p + i + u * stride));
+#pragma unroll
+        for (int u = 0; u < PROBE_UNROLL; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+    }
+    for (; i < n16; i += stride) {
+        const uint4 v = p[i];
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) atomicXor(sink, acc);
+}
+
 // =========================================================================== //
 extern "C" {
 
@@ -311,6 +338,22 @@ const char *gva_status_string(int s) {
 int gva_abi_version(void) { return GVA_ABI_VERSION; }
 
 int gva_num_sms(void) { return num_sms_current(); }
+
+int gva_read_probe(void *stream, const void *buf, size_t bytes, unsigned *sink) {
+    if (!buf || !sink || bytes == 0 || bytes % 16 != 0 || !aligned16(buf)) return GVA_ERR_ARG;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    const int sms = num_sms_current();
+    if (sms <= 0) return GVA_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(sink, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) {
+        // a plain launch: the probe starts only after the preceding work has finished
+        read_probe_kernel<<<sms * (2048 / PROBE_THREADS), PROBE_THREADS, 0,
+                            static_cast<cudaStream_t>(stream)>>>(
+            reinterpret_cast<const uint4 *>(buf), (long long)(bytes / 16), sink);
+        e = cudaGetLastError();
+    }
+    return cuda_status(e);
+}
 
 int gva_last_cuda_error(void) { return g_last_cuda_error; }
 
