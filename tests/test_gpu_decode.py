@@ -349,3 +349,28 @@ def test_read_probe_reads_every_word():
     torch.cuda.synchronize()
     ref = int(np.bitwise_xor.reduce(host.numpy().view(np.uint32)))
     assert int(sink.cpu().numpy().view(np.uint32)[0]) == ref
+
+
+def test_prepared_calls_match_the_oracle():
+    """Prepared append + decode calls (arguments marshalled once, called twice) give the
+    oracle's result, like the plain entry points."""
+    c = make_case(workload("350m", T=200, B=3))
+    D = Dev(c)
+    w = c.w
+    g = gva()
+    pos = (c.seq_len - 1).to(torch.int32).cuda()
+    out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    lse = torch.empty((w.B, w.H), device="cuda")
+    app = g.prepare_append_cache(D.dims, D.v_new, D.k_new, pos, None, D.cache, D.tab)
+    dec = g.prepare_decode_attention(D.dims, D.q_nope, D.q_rope, D.M, D.seq_len, D.cache, D.tab,
+                                     w.scale, out, lse, D.ws)
+    for _ in range(2):
+        out.zero_()
+        app()
+        dec()
+    torch.cuda.synchronize()
+    assert g.gva_get_device_status() == 0
+    V, K = oracle_append(c, pos.cpu(), D.tab_h)
+    ref, ref_lse = oracle_decode(c, V, K)
+    assert_close(out.cpu().numpy(), ref, "bf16", "prepared")
+    assert_close(lse.cpu().numpy(), ref_lse, "bf16", "prepared lse")

@@ -282,6 +282,49 @@ def gva_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, r
         ctypes.byref(o)), "gva_decode_attention")
 
 
+class PreparedCall:
+    """One C-ABI call with its arguments validated and marshalled once, for loops that
+    repeat the same call on the same buffers (a decode step per layer): calling the
+    object issues the C function directly.  The tensors are kept alive by the object;
+    their contents may change between calls, their storage may not."""
+
+    def __init__(self, fn, args, what, keep):
+        self._fn, self._args, self._what, self._keep = fn, args, what, keep
+
+    def __call__(self) -> None:
+        _check(self._fn(*self._args), self._what)
+
+
+def prepare_append_cache(dims: Dims, v_new, k_rope_new, pos, seq_len_out, cache: Cache,
+                         rope_tab, stream=None) -> PreparedCall:
+    """gva_append_cache with fixed arguments (see PreparedCall)."""
+    d, cc = dims.c(), cache.c()
+    args = (_stream(stream), ctypes.byref(d), _ptr(v_new, torch.float32, "v_new"),
+            _ptr(k_rope_new, torch.float32, "k_rope_new") if dims.d_r else None,
+            _ptr(pos, torch.int32, "pos"), _ptr(seq_len_out, torch.int32, "seq_len_out"),
+            ctypes.byref(cc), _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+            int(rope_tab.shape[0]) if rope_tab is not None else 0)
+    return PreparedCall(_lib.gva_append_cache, args, "gva_append_cache",
+                        (d, cc, v_new, k_rope_new, pos, seq_len_out, cache, rope_tab))
+
+
+def prepare_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, rope_tab,
+                             scale: float, out, lse, workspace, path: str = "auto",
+                             num_ctas: int = 0, stream=None) -> PreparedCall:
+    """gva_decode_attention(_ex) with fixed arguments (see PreparedCall)."""
+    d, cc, o = dims.c(), cache.c(), _opts(path, num_ctas)
+    args = (_stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
+            _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
+            _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc),
+            _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+            int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+            _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+            _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+            ctypes.byref(o))
+    return PreparedCall(_lib.gva_decode_attention_ex, args, "gva_decode_attention",
+                        (d, cc, o, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse, workspace))
+
+
 def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: float, out, lse,
                              workspace, path: str = "auto", num_ctas: int = 0,
                              stream=None) -> None:
