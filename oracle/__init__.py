@@ -84,6 +84,7 @@ def lib():
             L.od_append.argtypes = ([_I] * 4 + [_P, _P, _P, ctypes.POINTER(_Rows), _I,
                                                 _P, _P, _P])
             L.od_rotate_keys_f64.argtypes = [_I, _I, _P, _P, _D, _P]
+            L.od_query_rmsnorm.argtypes = [_I, _I, _I, _P, _P, _D, _P]
             _lib = L
         return _lib
 
@@ -210,6 +211,19 @@ def bf16_rne(x) -> np.ndarray:
 # --------------------------------------------------------------------------- #
 # the method
 # --------------------------------------------------------------------------- #
+def query_rmsnorm(q_nope, gain=None, eps: float = 1e-6):
+    """Per-head RMSNorm of the content query, fp64 ([A] 实验 / [S] results table,
+    "scale-matched + query RMSNorm"; the formula is a reading, see od_query_rmsnorm):
+    y = gain * x / sqrt(mean(x^2) + eps) over each head's d_n values."""
+    x = f64(q_nope)
+    B, H, d_n = x.shape
+    y = np.empty_like(x)
+    g = None if gain is None else np.ascontiguousarray(f64(gain).reshape(d_n))
+    lib().od_query_rmsnorm(B, H, d_n, _ptr(x), _ptr(g) if g is not None else None,
+                           float(eps), _ptr(y))
+    return y
+
+
 def absorb(q_nope, q_rope, M, seq_len, scale: float, base: float):
     """q~_h = scale * q_h^nope M_h^T and q^_h = scale * Rot(L_b - 1) q_h^rope
     ([A] "关键技巧一" eq. q_h k_{j,h}^T = q~_h v_{j,g(h)}^T; [S] "absorption")."""

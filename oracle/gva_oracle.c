@@ -170,6 +170,29 @@ void od_absorb(int B, int H, int d_h, int d_n, int d_r,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Query RMSNorm  ([A] 实验: "GVA scale-matched + query RMSNorm"; [S] results   */
+/* table "GVA, scale-matched + query RMSNorm")                                  */
+/* ------------------------------------------------------------------------- */
+/* The pages name the variant without its formula.  Reading (listed in the design
+ * notes): each head's content query is divided by its root mean square over its
+ * d_n values, then multiplied by a per-dimension gain (ones when gain is NULL):
+ *   y[b,h,k] = gain[k] * x[b,h,k] / sqrt( (1/d_n) sum_k' x[b,h,k']^2 + eps )
+ * The positional query is not normalised. */
+void od_query_rmsnorm(int B, int H, int d_n, const double *x, const double *gain, double eps,
+                      double *y)
+{
+    long long bh;
+    int k;
+    for (bh = 0; bh < (long long)B * H; ++bh) {
+        const double *xr = x + bh * d_n;
+        double ss = 0.0, inv;
+        for (k = 0; k < d_n; ++k) ss += xr[k] * xr[k];
+        inv = 1.0 / sqrt(ss / (double)d_n + eps);
+        for (k = 0; k < d_n; ++k) y[bh * d_n + k] = (gain ? gain[k] : 1.0) * xr[k] * inv;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* exact widening of one stored cache element to double                        */
 /* ------------------------------------------------------------------------- */
 /* bf16 storage: the 16 bits are the top half of an fp32; fp32 storage as is.

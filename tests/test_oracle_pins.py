@@ -475,3 +475,56 @@ def test_cache_counts(golden):
         assert oracle.kv_bytes(1, 1, 1, nkv, Dh, 2) / 1024 == gx[kib]
         assert oracle.kv_bytes(L, 1, Tt, nkv, Dh, 2) / 2 ** 20 == gx[mib]
     assert oracle.n_mha(1, 8, 128) == 2 * 8 * 128
+
+
+# --------------------------------------------------------------------------- #
+# query RMSNorm (the "scale-matched + query RMSNorm" variant; formula is a reading)
+# --------------------------------------------------------------------------- #
+def test_query_rmsnorm_unit_rms_and_direction():
+    """With unit gain and eps = 0 each head's normalised query keeps its direction
+    (a positive multiple of the input) and has mean square exactly 1: together these
+    fix it uniquely (a wrong axis, a missing square root or a sum instead of a mean
+    each fails one of them)."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((3, 5, 24)) * rng.uniform(0.1, 30, (3, 5, 1))
+    y = oracle.query_rmsnorm(x, None, 0.0)
+    assert np.allclose(np.mean(y ** 2, axis=-1), 1.0, rtol=0, atol=1e-12)
+    ratio = y / x
+    assert np.all(ratio > 0)
+    assert np.allclose(ratio, ratio[..., :1], rtol=1e-12, atol=0)
+
+
+def test_query_rmsnorm_scale_invariance_gain_and_eps():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((2, 4, 32))
+    # eps = 0: invariant to a positive rescaling of the query
+    for c in (1e-3, 0.5, 7.0, 1e4):
+        assert np.allclose(oracle.query_rmsnorm(c * x, None, 0.0),
+                           oracle.query_rmsnorm(x, None, 0.0), rtol=0, atol=1e-12)
+    # the gain multiplies each dimension of the unit-gain result
+    g = rng.uniform(-2, 2, 32)
+    assert np.allclose(oracle.query_rmsnorm(x, g, 0.0) / oracle.query_rmsnorm(x, None, 0.0),
+                       np.broadcast_to(g, x.shape), rtol=1e-12, atol=0)
+    # eps: mean square of the output is ms / (ms + eps); a zero query stays zero
+    eps = 0.25
+    ms = np.mean(x ** 2, axis=-1)
+    y = oracle.query_rmsnorm(x, None, eps)
+    assert np.allclose(np.mean(y ** 2, axis=-1), ms / (ms + eps), rtol=1e-12, atol=0)
+    z = oracle.query_rmsnorm(np.zeros((1, 2, 8)), None, 1e-6)
+    assert np.all(z == 0.0)
+
+
+def test_query_rmsnorm_decode_reduces_to_plain_for_unit_rms_queries():
+    """A query that already has unit mean square (unit gain, eps = 0) decodes exactly as
+    the plain path."""
+    w = workload("350m", B=2, T=40, H=4, G=2, d_h=32, d_n=32, d_r=8)
+    c = make_case(w)
+    q = oracle.f64(c.q_nope)
+    q = q / np.sqrt(np.mean(q ** 2, axis=-1, keepdims=True))
+    qn = oracle.query_rmsnorm(q, None, 0.0)
+    R = oracle.Rows("contiguous", T_cap=c.T_cap)
+    a, la = oracle.gva_decode(q, c.q_rope, c.M, c.seq_len, R, oracle._np(c.V), oracle._np(c.Kr),
+                              w.scale, w.base, w.G)
+    b, lb = oracle.gva_decode(qn, c.q_rope, c.M, c.seq_len, R, oracle._np(c.V), oracle._np(c.Kr),
+                              w.scale, w.base, w.G)
+    assert np.max(np.abs(a - b)) < 1e-12 and np.max(np.abs(la - lb)) < 1e-12
