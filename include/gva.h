@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define GVA_ABI_VERSION 1
+#define GVA_ABI_VERSION 2
 
 typedef enum {
     GVA_OK = 0,
@@ -124,10 +124,19 @@ typedef enum {
                                 the merge of the splits (bf16 cache, GVA decode only) */
 } gva_path;
 
+/* Query RMSNorm before absorption (the "scale-matched + query RMSNorm" variant named
+ * in [A] 实验 and [S]'s results table; the pages give no formula, the reading is):
+ *   q_nope[b,h,:] <- gain * q_nope[b,h,:] / sqrt(mean_k q_nope[b,h,k]^2 + eps)
+ * per head over its d_n values; the positional query is not normalised. */
+#define GVA_FLAG_QUERY_RMSNORM 1
+
 typedef struct {
     int path;                /* gva_path */
     int num_ctas;            /* decode grid size; 0 = the library's choice for this GPU */
-    int flags;               /* reserved, must be 0 */
+    int flags;               /* 0 or GVA_FLAG_QUERY_RMSNORM; other bits: GVA_ERR_ARG */
+    float q_norm_eps;        /* with GVA_FLAG_QUERY_RMSNORM: eps >= 0 (finite) */
+    const float *q_norm_gain;/* with GVA_FLAG_QUERY_RMSNORM: device fp32 [d_n], shared by
+                                all heads, or NULL for ones */
 } gva_decode_opts;
 
 /* ------------------------------------------------------------------------- */
@@ -158,6 +167,13 @@ int gva_absorb_query(void *stream, const gva_dims *dims, const void *q_nope,
                      const void *q_rope, const float *M, const int *seq_len,
                      const float *rope_tab, int rope_max_pos, float scale,
                      float *q_tilde, float *q_rope_rot);
+
+/* gva_absorb_query with options: only opts->flags (GVA_FLAG_QUERY_RMSNORM), q_norm_eps
+ * and q_norm_gain are read; opts may be NULL. */
+int gva_absorb_query_ex(void *stream, const gva_dims *dims, const void *q_nope,
+                        const void *q_rope, const float *M, const int *seq_len,
+                        const float *rope_tab, int rope_max_pos, float scale,
+                        float *q_tilde, float *q_rope_rot, const gva_decode_opts *opts);
 
 /* Cache append ([S]: cached already rotated; [K] §1: append, then attend):
  *   V[row(b, pos[b])]      = v_new[b]                   (rounded once to cache_dtype)
@@ -198,8 +214,8 @@ int gva_decode_attention(void *stream, const gva_dims *dims, const void *q_nope,
                          float scale, float *out, float *lse, void *workspace,
                          size_t ws_bytes);
 
-/* gva_decode_attention with kernel options (path selection, grid size); opts may be
- * NULL.  GVA_ERR_UNSUPPORTED when the requested path cannot run `dims`. */
+/* gva_decode_attention with kernel options (path selection, grid size, query RMSNorm);
+ * opts may be NULL.  GVA_ERR_UNSUPPORTED when the requested path cannot run `dims`. */
 int gva_decode_attention_ex(void *stream, const gva_dims *dims, const void *q_nope,
                             const void *q_rope, const float *M, const int *seq_len,
                             const gva_cache *cache, const float *rope_tab,
@@ -209,7 +225,8 @@ int gva_decode_attention_ex(void *stream, const gva_dims *dims, const void *q_no
 /* Matched GQA decode, the comparator ([K] §4): out[b,h] = softmax(scale q_h K_g^T) V_g
  * with explicit K and V rows [G][d_h] (cache_dtype).  q device [B][H][d_h] (q_dtype);
  * dims.d_n and dims.d_r are ignored.  Same split-K design, workspace and outputs as
- * gva_decode_attention; opts may be NULL. */
+ * gva_decode_attention; opts may be NULL (GVA_PATH_FUSED and GVA_FLAG_QUERY_RMSNORM:
+ * GVA_ERR_UNSUPPORTED). */
 int gva_gqa_decode_attention(void *stream, const gva_dims *dims, const void *q,
                              const int *seq_len, const gva_kv_cache *cache, float scale,
                              float *out, float *lse, void *workspace, size_t ws_bytes,

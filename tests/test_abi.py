@@ -49,7 +49,7 @@ def test_every_declared_symbol_is_exported(gva):
 
 
 def test_abi_version_and_status_strings(gva):
-    assert gva.gva_abi_version() == 1
+    assert gva.gva_abi_version() == 2
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 3, 4):
         s = gva.gva_status_string(code)
         assert s and "unknown" not in s
@@ -128,3 +128,21 @@ def test_null_and_misaligned_pointers_rejected(gva):
     nokr = gva.gva_cache(rows, fake, None)
     assert lib.gva_append_cache(None, ctypes.byref(d), fake, fake, fake, None,
                                 ctypes.byref(nokr), fake, 100) == gva.GVA_ERR_ARG
+
+
+@pytest.mark.parametrize("flags,eps", [(2, 0.0), (1 | 4, 0.0), (1, -1.0), (1, float("inf")),
+                                       (1, float("nan"))])
+def test_bad_option_flags_rejected_before_cuda(gva, flags, eps):
+    """Only GVA_FLAG_QUERY_RMSNORM is a valid flag, and its eps is finite and >= 0."""
+    lib = gva._lib
+    d = _dims(gva)
+    fake = ctypes.c_void_p(0x10000)
+    cache = gva.gva_cache(gva.gva_rows(0, 2 * 1024, 1024, None, None, 0, 0), fake, fake)
+    o = gva.gva_decode_opts(0, 0, flags, eps, None)
+    st = lib.gva_decode_attention_ex(None, ctypes.byref(d), fake, fake, fake, fake,
+                                     ctypes.byref(cache), fake, 100, ctypes.c_float(0.1), fake,
+                                     None, fake, ctypes.c_size_t(1 << 30), ctypes.byref(o))
+    assert st == gva.GVA_ERR_ARG
+    st = lib.gva_absorb_query_ex(None, ctypes.byref(d), fake, fake, fake, fake, fake, 100,
+                                 ctypes.c_float(0.1), fake, fake, ctypes.byref(o))
+    assert st == gva.GVA_ERR_ARG

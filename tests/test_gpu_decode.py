@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
 seeded inputs.  Decode within the workloads' tolerances (bf16 cache: max-abs 2e-2 and
 relative L2 1e-3; fp32 cache: 1e-5 for both); append and paged gather bit-exact."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -374,3 +376,63 @@ def test_prepared_calls_match_the_oracle():
     ref, ref_lse = oracle_decode(c, V, K)
     assert_close(out.cpu().numpy(), ref, "bf16", "prepared")
     assert_close(lse.cpu().numpy(), ref_lse, "bf16", "prepared lse")
+
+
+# --------------------------------------------------------------------------- #
+# query RMSNorm variant (normalise each head's content query, then absorb)
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("name", ["350m", "ragged", "tiny", "paged"])
+@pytest.mark.parametrize("with_gain", [False, True])
+def test_query_rmsnorm_decode(name, with_gain):
+    c = make_case(workload(name, **SMALL[name]))
+    w = c.w
+    eps = 1e-5
+    gen = torch.Generator().manual_seed(99)
+    gain = torch.rand(w.d_n, generator=gen) * 2 + 0.25 if with_gain else None
+    qn = oracle.query_rmsnorm(c.q_nope, None if gain is None else gain.numpy(), eps)
+    for path in paths_for(c):
+        D = Dev(c)
+        out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+        lse = torch.empty((w.B, w.H), device="cuda")
+        gva().gva_decode_attention(D.dims, D.q_nope, D.q_rope, D.M, D.seq_len, D.cache, D.tab,
+                                   w.scale, out, lse, D.ws, path=path,
+                                   q_norm=(None if gain is None else gain.cuda(), eps))
+        torch.cuda.synchronize()
+        assert gva().gva_get_device_status() == 0
+        ref, ref_lse = oracle.gva_decode(qn, c.q_rope, c.M, c.seq_len, oracle_rows(c),
+                                         oracle._np(c.V), oracle._np(c.Kr), w.scale, w.base, w.G)
+        assert_close(out.cpu().numpy(), ref, w.cache_dtype, f"{name}/{path} q-norm out")
+        assert_close(lse.cpu().numpy(), ref_lse, w.cache_dtype, f"{name}/{path} q-norm lse")
+
+
+def test_query_rmsnorm_absorb():
+    c = make_case(workload("350m", T=50, B=37, d_n=128))
+    D = Dev(c)
+    w = c.w
+    gain = torch.linspace(0.5, 1.5, w.d_n)
+    qt = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    qh = torch.empty((w.B, w.H, w.d_r), device="cuda")
+    gva().gva_absorb_query(D.dims, D.q_nope, D.q_rope, D.M, D.seq_len, D.tab, w.scale, qt, qh,
+                           q_norm=(gain.cuda(), 1e-6))
+    torch.cuda.synchronize()
+    qn = oracle.query_rmsnorm(c.q_nope, gain.numpy(), 1e-6)
+    rt, rh = oracle.absorb(qn, c.q_rope, c.M, c.seq_len, w.scale, w.base)
+    for got, ref in ((qt, rt), (qh, rh)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g - ref)) <= 2e-6 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_gqa_refuses_query_rmsnorm():
+    c = make_case(workload("350m", **SMALL["350m"]))
+    D = Dev(c)
+    g = gva()
+    kv = g.KVCache(D.rows, make_gqa_keys(c).cuda(), D.V)
+    w = c.w
+    out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    o = g.gva_decode_opts(0, 0, g.GVA_FLAG_QUERY_RMSNORM, 1e-6, None)
+    st = g._lib.gva_gqa_decode_attention(None, ctypes.byref(D.dims.c()), ctypes.c_void_p(make_gqa_query(c).cuda().data_ptr()),
+                                         ctypes.c_void_p(D.seq_len.data_ptr()), ctypes.byref(kv.c()),
+                                         ctypes.c_float(0.125), ctypes.c_void_p(out.data_ptr()), None,
+                                         ctypes.c_void_p(D.ws.data_ptr()),
+                                         ctypes.c_size_t(D.ws.numel()), ctypes.byref(o))
+    assert st == g.GVA_ERR_UNSUPPORTED

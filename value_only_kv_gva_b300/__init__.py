@@ -58,7 +58,11 @@ class gva_kv_cache(ctypes.Structure):
 
 
 class gva_decode_opts(ctypes.Structure):
-    _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("flags", ctypes.c_int)]
+    _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("flags", ctypes.c_int),
+                ("q_norm_eps", ctypes.c_float), ("q_norm_gain", ctypes.c_void_p)]
+
+
+GVA_FLAG_QUERY_RMSNORM = 1
 
 
 _P, _I, _F, _D, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
@@ -71,6 +75,7 @@ _lib.gva_abi_version.restype = _I
 _lib.gva_num_sms.restype = _I
 _lib.gva_rope_table_fill.argtypes = [_P, _I, _I, _D]
 _lib.gva_absorb_query.argtypes = [_P, _PD, _P, _P, _P, _P, _P, _I, _F, _P, _P]
+_lib.gva_absorb_query_ex.argtypes = _lib.gva_absorb_query.argtypes + [ctypes.c_void_p]
 _lib.gva_append_cache.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I]
 _lib.gva_decode_workspace_size.restype = _Z
 _lib.gva_decode_workspace_size.argtypes = [_PD]
@@ -86,7 +91,7 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_absorb_query", "gva_append_cache", "gva_decode_workspace_size",
            "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
            "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static",
-           "gva_read_probe"]
+           "gva_read_probe", "gva_absorb_query_ex"]
 
 
 class GvaError(RuntimeError):
@@ -194,8 +199,14 @@ class KVCache:
         return gva_kv_cache(self.rows.c(), _ptr(self.K, None, "K"), _ptr(self.V, None, "V"))
 
 
-def _opts(path: str, num_ctas: int) -> gva_decode_opts:
-    return gva_decode_opts(PATHS[path], int(num_ctas), 0)
+def _opts(path: str, num_ctas: int, q_norm=None) -> gva_decode_opts:
+    """q_norm: None, or (gain, eps) for the query RMSNorm (gain: fp32 device tensor
+    [d_n] or None for ones)."""
+    if q_norm is None:
+        return gva_decode_opts(PATHS[path], int(num_ctas), 0, 0.0, None)
+    gain, eps = q_norm
+    return gva_decode_opts(PATHS[path], int(num_ctas), GVA_FLAG_QUERY_RMSNORM, float(eps),
+                           _ptr(gain, torch.float32, "q_norm gain"))
 
 
 # --------------------------------------------------------------------------- #
@@ -235,17 +246,19 @@ def gva_last_cuda_error() -> int:
 
 
 def gva_absorb_query(dims: Dims, q_nope, q_rope, M, seq_len, rope_tab, scale: float,
-                     q_tilde, q_rope_rot, stream=None) -> None:
+                     q_tilde, q_rope_rot, stream=None, q_norm=None) -> None:
+    """gva_absorb_query / gva_absorb_query_ex (q_norm as in _opts)."""
     d = dims.c()
-    _check(_lib.gva_absorb_query(
+    o = _opts("auto", 0, q_norm)
+    _check(_lib.gva_absorb_query_ex(
         _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
         _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
         _ptr(seq_len, torch.int32, "seq_len"),
         _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
         int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
         _ptr(q_tilde, torch.float32, "q_tilde"),
-        _ptr(q_rope_rot, torch.float32, "q_rope_rot") if dims.d_r else None),
-        "gva_absorb_query")
+        _ptr(q_rope_rot, torch.float32, "q_rope_rot") if dims.d_r else None,
+        ctypes.byref(o)), "gva_absorb_query")
 
 
 def gva_append_cache(dims: Dims, v_new, k_rope_new, pos, seq_len_out, cache: Cache,
@@ -267,10 +280,11 @@ def gva_decode_workspace_size(dims: Dims) -> int:
 
 def gva_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, rope_tab,
                          scale: float, out, lse, workspace, path: str = "auto",
-                         num_ctas: int = 0, stream=None) -> None:
+                         num_ctas: int = 0, stream=None, q_norm=None) -> None:
+    """gva_decode_attention_ex (q_norm as in _opts: the query RMSNorm variant)."""
     d = dims.c()
     cc = cache.c()
-    o = _opts(path, num_ctas)
+    o = _opts(path, num_ctas, q_norm)
     _check(_lib.gva_decode_attention_ex(
         _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
         _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
@@ -310,9 +324,9 @@ def prepare_append_cache(dims: Dims, v_new, k_rope_new, pos, seq_len_out, cache:
 
 def prepare_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, rope_tab,
                              scale: float, out, lse, workspace, path: str = "auto",
-                             num_ctas: int = 0, stream=None) -> PreparedCall:
+                             num_ctas: int = 0, stream=None, q_norm=None) -> PreparedCall:
     """gva_decode_attention(_ex) with fixed arguments (see PreparedCall)."""
-    d, cc, o = dims.c(), cache.c(), _opts(path, num_ctas)
+    d, cc, o = dims.c(), cache.c(), _opts(path, num_ctas, q_norm)
     args = (_stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
             _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
             _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc),
@@ -322,7 +336,8 @@ def prepare_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cach
             _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
             ctypes.byref(o))
     return PreparedCall(_lib.gva_decode_attention_ex, args, "gva_decode_attention",
-                        (d, cc, o, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse, workspace))
+                        (d, cc, o, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse, workspace,
+                         q_norm))
 
 
 def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: float, out, lse,

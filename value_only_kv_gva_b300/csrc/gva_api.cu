@@ -227,9 +227,13 @@ int run_simt(void *stream, DecodeParams &dp, int sms, int req_ctas) {
 int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
                   const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
                   float prescale, float *q_tilde, float *q_hat, int sms,
-                  const gva_rows *rows = nullptr, bool skip_rope = false) {
+                  const gva_rows *rows = nullptr, bool skip_rope = false,
+                  const gva_decode_opts *qn = nullptr) {
     AbsorbParams p;
     p.skip_rope = skip_rope ? 1 : 0;
+    p.qnorm = qn && (qn->flags & GVA_FLAG_QUERY_RMSNORM) ? 1 : 0;
+    p.qn_gain = p.qnorm ? qn->q_norm_gain : nullptr;
+    p.qn_eps = p.qnorm ? qn->q_norm_eps : 0.f;
     p.check_rows = rows != nullptr;
     if (rows) p.R = to_dev(*rows);
     else memset(&p.R, 0, sizeof(p.R));
@@ -285,7 +289,15 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     return cuda_status(e);
 }
 
-const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0};
+const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0, 0.f, nullptr};
+
+// Option flags: only the query RMSNorm, with a finite eps >= 0.
+bool flags_ok(const gva_decode_opts *o) {
+    if ((o->flags & ~GVA_FLAG_QUERY_RMSNORM) != 0) return false;
+    if (o->flags & GVA_FLAG_QUERY_RMSNORM)
+        return o->q_norm_eps >= 0.f && o->q_norm_eps < INFINITY;
+    return true;
+}
 
 }  // namespace
 
@@ -376,6 +388,16 @@ int gva_rope_table_fill(float *tab, int max_pos, int d_r, double base) {
 int gva_absorb_query(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
                      const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
                      float scale, float *q_tilde, float *q_rope_rot) {
+    return gva_absorb_query_ex(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                               scale, q_tilde, q_rope_rot, nullptr);
+}
+
+int gva_absorb_query_ex(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                        const float *M, const int *seq_len, const float *rope_tab,
+                        int rope_max_pos, float scale, float *q_tilde, float *q_rope_rot,
+                        const gva_decode_opts *opts) {
+    const gva_decode_opts *o = opts ? opts : &kDefaultOpts;
+    if (!flags_ok(o)) return GVA_ERR_ARG;
     if (!dims_ok(d, true)) return GVA_ERR_ARG;
     if (!q_nope || !M || !seq_len || !q_tilde || !aligned16(q_nope) || !aligned16(M) ||
         !aligned16(q_tilde))
@@ -385,7 +407,7 @@ int gva_absorb_query(void *stream, const gva_dims *d, const void *q_nope, const 
         return GVA_ERR_ARG;
     if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
     return absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos, scale,
-                         q_tilde, q_rope_rot, num_sms_current());
+                         q_tilde, q_rope_rot, num_sms_current(), nullptr, false, o);
 }
 
 int gva_append_cache(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
@@ -430,7 +452,7 @@ static int decode_arg_checks(const gva_dims *d, const gva_rows *rows, float *out
                              const gva_decode_opts *o, bool gva_shape) {
     if (!dims_ok(d, gva_shape) || !rows_ok(rows, d->B)) return GVA_ERR_ARG;
     if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
-    if (o->flags != 0 || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_FUSED || o->num_ctas < 0)
+    if (!flags_ok(o) || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_FUSED || o->num_ctas < 0)
         return GVA_ERR_ARG;
     return GVA_OK;
 }
@@ -478,7 +500,7 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
         float *qt = reinterpret_cast<float *>(w + plan.qt);
         float *qh = reinterpret_cast<float *>(w + plan.qh);
         st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                           scale * LOG2E, qt, qh, sms, &cache->rows, false);
+                           scale * LOG2E, qt, qh, sms, &cache->rows, false, o);
         if (st != GVA_OK) return st;
         FusedParams fp;
         memset(&fp, 0, sizeof(fp));
@@ -508,7 +530,7 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     // before the call, so it overlaps the absorption), leaving the absorption a single
     // memory round trip
     st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma);
+                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o);
     if (st != GVA_OK) return st;
 
     DecodeParams dp;
@@ -566,7 +588,8 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     if (!q || !seq_len || !cache->K || !cache->V || !aligned16(q) || !aligned16(cache->K) ||
         !aligned16(cache->V))
         return GVA_ERR_ARG;
-    if (o->path == GVA_PATH_FUSED) return GVA_ERR_UNSUPPORTED;   // GVA decode only
+    if (o->path == GVA_PATH_FUSED || (o->flags & GVA_FLAG_QUERY_RMSNORM))
+        return GVA_ERR_UNSUPPORTED;   // GVA decode only
     gva_dims dg = *d;
     dg.d_r = 0;
     const bool mma_ok = mma_supported(&dg);

@@ -103,6 +103,9 @@ struct AbsorbParams {
     int check_rows;                // 1: a length the cache cannot hold is skipped silently
     RowsDev R;                     //    (the decode kernel reports it); used when check_rows
     int skip_rope;                 // 1: q_hat is not computed (the decode rotates q_rope)
+    int qnorm;                     // 1: RMSNorm of each head's content query first
+    const float *qn_gain;          //    per-dimension gain [d_n] or null (ones)
+    float qn_eps;
 };
 
 // Grid (H, ceil(B / bpb), d_h / 32), 256 threads, bpb <= 32 sequences per CTA.
@@ -252,6 +255,26 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
         }
     }
     __syncthreads();
+    // 3b. query RMSNorm (the scale-matched + query RMSNorm variant): one warp per staged
+    //     row, y = gain * x / sqrt(mean(x^2) + eps) over the row's d_n values
+    if (p.qnorm) {
+        const int wq = threadIdx.x >> 5, lq = threadIdx.x & 31;
+        for (int r = wq; r < nb; r += ABSORB_THREADS / 32) {
+            float ss = 0.f;
+            for (int k = lq; k < d_n; k += 32) {
+                const float x = sm_abs[(r * 8 + k / cs) * cst + k % cs];
+                ss = fmaf(x, x, ss);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float inv = 1.f / sqrtf(ss / (float)d_n + p.qn_eps);
+            for (int k = lq; k < d_n; k += 32) {
+                float *xp = sm_abs + (r * 8 + k / cs) * cst + k % cs;
+                *xp = *xp * inv * (p.qn_gain ? __ldg(p.qn_gain + k) : 1.f);
+            }
+        }
+        __syncthreads();
+    }
     // 4. eight sequences at a time: chunk dot products, then the reduce-scatter
     for (int g0 = 0; g0 < nb; g0 += 8) {
         float acc[8];
