@@ -1,22 +1,25 @@
 // decode_mma.cuh -- split-K GVA decode on the tensor cores for bf16 caches.
 //
 // Per CTA (one per SM): one producer warp streams 16-token slabs of the cache into a
-// ring of shared-memory stages with TMA tensor copies (cp.async.bulk.tensor, 128-byte
-// swizzle, mbarrier completion); consumer warps, each bound to one value group, score
-// and accumulate with bf16 mma.sync (m16n8k16, fp32 accumulate):
+// ring of shared-memory stages with TMA tensor copies (one 3D box per slab covering
+// every value column, 128-byte swizzle, plus a bulk copy of the slab's positional keys;
+// mbarrier completion); consumer warps, each bound to one value group, score and
+// accumulate with bf16 mma.sync (m16n8k16, fp32 accumulate) with the slab's 16 tokens
+// on the MMA rows and the group's heads on the columns:
 //
-//   S^T[16 x 8 tok]  = Q[16 x d_h] . V_g^T[d_h x 8 tok] (+ Q_r[16 x d_r] . K_rope^T)
-//   O[16 x d_h]     += P[16 x 16 tok] . V_g[16 tok x d_h]
+//   S[16 tok x 8]    = V_g[16 tok x d_h] . Q^T[d_h x 8]   (+ K_rope . Q_r^T)
+//   O^T[d_h x 8]    += V_g^T[d_h x 16 tok] . P^T[16 tok x 8]
 //
-// The 16 rows hold the group's r <= 8 heads twice: row h carries the bf16 "hi" part
-// of the fp32 query / probability and row h + 8 its "lo" remainder (x - hi), so the
-// products keep about 16 mantissa bits; the two rows are summed in fp32 afterwards.
-// The V tile serves as the B operand of both products: plain ldmatrix for scores,
-// ldmatrix.trans for the weighted sum.  Each cache byte is read from HBM once.
+// Each 8-column tile holds up to 4 heads twice: column 2i carries the bf16 "hi" part
+// of head i's fp32 query / probability and column 2i + 1 its "lo" remainder (x - hi),
+// so the products keep about 16 mantissa bits; the two columns are summed in fp32
+// afterwards (r <= 4 heads per group: one tile, r <= 8: two).  The value tile is the A
+// operand of both products: plain ldmatrix for the scores, ldmatrix.trans for the
+// weighted sum.  Each cache byte is read from HBM once.
 //
-// Online softmax in log2 units with a lazy rescale: the running maximum is raised
-// only when a slab's maximum exceeds it by more than 8, so probabilities stay below
-// 2^8 and the accumulator rescale (a multiply of every O register) is rare.
+// Online softmax in log2 units with a lazy rescale: the running maximum moves only when
+// a score exceeds it by more than 8 (2^8 in probability), so the accumulator rescale
+// (a multiply of every O register) and the max reduction over the token lanes are rare.
 //
 // Every wait on an mbarrier is bounded by a wall-clock limit; on expiry the kernel
 // sets GVA_DEV_TIMEOUT, stops issuing work, waits (bounded) for the copies it has in
