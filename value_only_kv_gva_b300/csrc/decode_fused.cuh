@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
         if (lane == 0) {
             GVA_KT(8);
             GVA_TRACE_AT(22);
-            GVA_TRACE_FLUSH(20, 23);
+            GVA_TRACE_FLUSH(22, 23);
             // Never leave with copies in flight: wait (bounded) for the last use of each
             // stage (chunk i used stage i % NSS in round i / NSS).
             const unsigned long long limit = dead ? 1000000ull : WAIT_LIMIT_NS;
