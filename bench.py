@@ -241,26 +241,28 @@ def run_ours(args, dist: Dist):
     g_dec = capture(decode_only)
     assert gva.gva_get_device_status() == 0
 
+    step_ms = []   # per-step durations of the last timed region (events between steps)
+
     def timed(graph, K, W, sampler=None):
         for _ in range(W):
             graph.replay()
         torch.cuda.synchronize()
         dist.barrier()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
         if sampler:
             sampler.mark("t0")
         with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(K):
+            ev[0].record(stream)
+            for k in range(K):
                 graph.replay()
-            e1.record(stream)
+                ev[k + 1].record(stream)
         torch.cuda.synchronize()
         if sampler:
             sampler.mark("t1")
         dist.barrier()
-        return e0.elapsed_time(e1) / 1e3
+        step_ms[:] = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+        return ev[0].elapsed_time(ev[K]) / 1e3
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
@@ -281,10 +283,12 @@ def run_ours(args, dist: Dist):
     value = aggregate(step_bytes * args.steps * dist.world, max_secs) / 1e9   # GB/s, all ranks
     ms_per_step = max_secs / args.steps * 1e3
     us_layer = ms_per_step * 1e3 / nl
+    us_layer_median = statistics.median(step_ms) * 1e3 / nl   # this rank's per-step median
 
     # the decode op alone (absorb + split-K partial + combine), same stream, live
     dsecs = dist.max(timed(g_dec, args.steps, max(3, args.warmup)), dev)
     us_decode = dsecs / (args.steps * nl) * 1e6
+    us_decode_median = statistics.median(step_ms) * 1e3 / nl
     achieved = bytes_layer / (us_decode * 1e-6) / 1e9
 
     peaks = measured_peaks()
@@ -293,7 +297,12 @@ def run_ours(args, dist: Dist):
 
     # GQA comparator of matched H, G, d_h reading explicit K and V
     gqa = None
-    if not args.no_gqa:
+    if w.layout == "ragged" and not args.no_gqa:
+        # the graph replay of this comparator on the full ragged batch ended in a launch
+        # failure twice while the library was built (cause not found); it is not run
+        gqa = {"not_run": "ragged-layout comparator replay kept off the GPU (unresolved "
+                          "launch failure; see the design notes)"}
+    elif not args.no_gqa:
         Kq0 = gva_inputs.make_gqa_keys(c).to(dev)
         qq = gva_inputs.make_gqa_query(c).to(dev)
         glayers = []
@@ -339,6 +348,9 @@ def run_ours(args, dist: Dist):
             "layers": nl, "tokens_per_layer": int(sum(lengths)),
             "bytes_per_layer": bytes_layer, "us_per_layer_step": round(us_layer, 3),
             "us_per_decode": round(us_decode, 3),
+            "median_of_steps": {"us_per_layer_step": round(us_layer_median, 3),
+                                "us_per_decode": round(us_decode_median, 3),
+                                "reps": args.steps},
             "pct_of_8tbs_spec": round(100 * value / dist.world / SPEC_HBM_GBS, 2),
             "pct_of_measured_copy": round(100 * value / dist.world / hbm_peak, 2),
             "read_probe_gbs": read_probe,
@@ -590,7 +602,11 @@ def main():
         import gva_inputs
         w = gva_inputs.workload(args.workload)
         c_bytes = (w.B * (w.T or sum(w.len_range) // 2)) * (w.G * w.d_h + w.d_r) * 2
+        # a layer smaller than L2 (126 MB): at least 32 distinct layer caches, and four
+        # times L2 in all; a larger layer is already streamed from HBM on every call
         args.layers = max(1, min(64, math.ceil(4 * 126e6 / c_bytes)))
+        if c_bytes < 126e6:
+            args.layers = max(32, args.layers)
     dist = Dist()
     if args.impl == "reference":
         run_reference(args, dist)
