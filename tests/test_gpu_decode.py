@@ -436,3 +436,20 @@ def test_gqa_refuses_query_rmsnorm():
                                          ctypes.c_void_p(D.ws.data_ptr()),
                                          ctypes.c_size_t(D.ws.numel()), ctypes.byref(o))
     assert st == g.GVA_ERR_UNSUPPORTED
+
+
+def test_largest_batch():
+    """B = 4096, the largest batch the in-kernel prefix handles (its lengths and slab
+    offsets take 32 KB of shared memory, shrinking the ring): every path, mixed lengths
+    0..33 over a capacity of 40."""
+    B = 4096
+    gen = np.random.default_rng(5)
+    lengths = [int(x) for x in gen.integers(0, 34, B)]
+    c = make_case(workload("350m", B=B, T=40, H=4, G=2, d_h=64, d_n=64, d_r=16), lengths=lengths)
+    ref, ref_lse = oracle_decode(c)
+    for path in paths_for(c):
+        D = Dev(c)
+        out, lse = D.decode(path=path)
+        assert gva().gva_get_device_status() == 0
+        assert_close(out, ref, "bf16", f"B=4096 {path}")
+        assert_close(lse, ref_lse, "bf16", f"B=4096 {path} lse")
