@@ -149,8 +149,10 @@ struct Part {
 
 // Block-wide: validated lengths into Ls[0..B), exclusive slab prefix into F[0..B].
 // Invalid lengths count as 0 and set GVA_DEV_BAD_LENGTH when `report` is set.
+// When `prefix_out` is given, the CTA also stores F[0..B] there (one CTA of the grid
+// does, for the combine kernel's large-batch path).
 __device__ void build_prefix(const int *seq_len, const RowsDev &R, int B, int *Ls, int *F,
-                             bool report) {
+                             bool report, int *prefix_out = nullptr) {
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seq_len[b];
         if (!length_ok(R, b, L)) {
@@ -180,6 +182,8 @@ __device__ void build_prefix(const int *seq_len, const RowsDev &R, int B, int *L
         if (lane == 31) F[B] = incl;
     }
     __syncthreads();
+    if (prefix_out)
+        for (int b = threadIdx.x; b <= B; b += blockDim.x) prefix_out[b] = F[b];
 }
 
 // Largest b with F[b] <= s (F non-decreasing, F[0] = 0 <= s < F[B]); that sequence

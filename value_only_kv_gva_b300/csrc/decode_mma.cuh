@@ -328,7 +328,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     // cache streams while that grid still runs; the queries are read after the wait.
     if (!mp.early) pdl_wait();
     pdl_launch_dependents();
-    build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0);   // includes __syncthreads
+    build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0,   // includes __syncthreads
+                 blockIdx.x == 0 ? p.prefix_ws : nullptr);
     if (threadIdx.x == 0) GVA_TRACE_AT(1);
     const Part P{F[B], p.n_ctas};
     const int c = blockIdx.x;

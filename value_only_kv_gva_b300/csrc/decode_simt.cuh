@@ -29,6 +29,7 @@ struct DecodeParams {
     float *part_o;          // [slots][H][d_h]
     float *part_ml;         // [slots][H][2]  (running max in log2 units, sum)
     int n_ctas;
+    int *prefix_ws;         // [B + 1] slab offsets, written by CTA 0 (or null)
 };
 
 constexpr int SIMT_THREADS = 256;
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__(SIMT_THREADS) decode_simt_kernel(const DecodeP
     uint32_t *tv = reinterpret_cast<uint32_t *>(smem + L.tv);
     uint32_t *tr = reinterpret_cast<uint32_t *>(smem + L.tr);
 
-    build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0);
+    build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0, blockIdx.x == 0 ? p.prefix_ws : nullptr);
     const Part P{F[B], p.n_ctas};
     if (P.S == 0) return;
     const int c = blockIdx.x;
@@ -256,9 +257,13 @@ struct CombineParams {
     float *out;
     float *lse;
     int n_ctas;
+    const int *prefix_ws;   // [B + 1] slab offsets from the decode grid (large batches)
 };
 
 constexpr int COMBINE_THREADS = 128;
+// Above this batch the combine reads its sequence's slab offsets from the decode
+// grid's copy (after the grid wait) instead of scanning every length in every CTA.
+constexpr int COMBINE_SCAN_MAX = 256;
 constexpr int COMBINE_BATCH = 16;         // o loads in flight per thread
 
 // Dynamic shared memory: 2 x n_ctas floats (a sequence spans at most n_ctas parts).  It
@@ -278,8 +283,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     // ---- F_b and S: the validated slab counts (same rule as build_prefix) ----
+    const bool scan = p.B <= COMBINE_SCAN_MAX || p.prefix_ws == nullptr;
     long long before = 0, total = 0;
-    for (int bb = tid; bb < p.B; bb += COMBINE_THREADS) {
+    for (int bb = tid; scan && bb < p.B; bb += COMBINE_THREADS) {
         int L = p.seq_len[bb];
         if (!length_ok(p.R, bb, L)) L = 0;
         const long long n = (L + SLAB - 1) / SLAB;
@@ -298,14 +304,23 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     for (int w = 0; w < COMBINE_THREADS / 32; ++w) { Fb += red_ll[0][w]; S += red_ll[1][w]; }
     int Lb = p.seq_len[b];
     if (!length_ok(p.R, b, Lb)) Lb = 0;
-    const long long nb = (Lb + SLAB - 1) / SLAB;
+    long long nb = (Lb + SLAB - 1) / SLAB;
     const int d0 = blockIdx.y * 32;
     float *out = p.out + ((long long)b * p.H + h) * p.d_h;
     // the parts of the sequence depend on the lengths only: found before the wait
-    const Part P{S, p.n_ctas};
-    const int c_lo = nb > 0 ? P.cta_of(Fb) : 0, c_hi = nb > 0 ? P.cta_of(Fb + nb - 1) : 0;
+    // (large batches: from the decode grid's prefix, after the wait)
+    Part P{S, p.n_ctas};
+    int c_lo = nb > 0 ? P.cta_of(Fb) : 0, c_hi = nb > 0 ? P.cta_of(Fb + nb - 1) : 0;
     // the partials (and the outputs the decode kernel writes) come from the preceding grid
     pdl_wait();
+    if (!scan) {
+        Fb = p.prefix_ws[b];
+        nb = p.prefix_ws[b + 1] - Fb;
+        S = p.prefix_ws[p.B];
+        P = Part{S, p.n_ctas};
+        c_lo = nb > 0 ? P.cta_of(Fb) : 0;
+        c_hi = nb > 0 ? P.cta_of(Fb + nb - 1) : 0;
+    }
     if (threadIdx.x == 0) GVA_KT(9);
     if (nb == 0) {
         if (tid < 32 && d0 + tid < p.d_h) out[d0 + tid] = 0.f;

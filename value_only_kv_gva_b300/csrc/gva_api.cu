@@ -163,7 +163,7 @@ RowsDev to_dev(const gva_rows &R) {
 
 // Workspace: [q_tilde B*H*d_h][q_hat B*H*d_r][part_o slots*H*d_h][part_ml slots*H*2]
 struct WsPlan {
-    size_t qt, qh, po, pm, tk, total;
+    size_t qt, qh, po, pm, tk, pf, total;
     long long slots;
 };
 
@@ -178,6 +178,7 @@ WsPlan plan_ws(const gva_dims *d, int sms) {
     // fused path: one ticket per (group, sequence); its partial slots (CTA c + pair
     // index, r heads each) fit in po / pm
     w.tk = o; o = align_up(o + sizeof(int) * (size_t)d->G * d->B, 256);
+    w.pf = o; o = align_up(o + sizeof(int) * ((size_t)d->B + 1), 256);   // slab offsets
     w.total = o;
     return w;
 }
@@ -206,6 +207,7 @@ int launch_combine(void *stream, const DecodeParams &dp, const gva_rows &rows) {
     cp.part_o = dp.part_o;
     cp.part_ml = dp.part_ml;
     cp.out = dp.out;
+    cp.prefix_ws = dp.prefix_ws;
     cp.lse = dp.lse;
     cp.n_ctas = dp.n_ctas;
     return cuda_status(launch(combine_kernel, dim3(dp.B * dp.H, (dp.d_h + 31) / 32),
@@ -559,6 +561,7 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     dp.part_o = reinterpret_cast<float *>(w + plan.po);
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
+    dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
     if (use_mma) {
         st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, true);
     } else if (d->cache_dtype == GVA_F32) {
@@ -626,6 +629,7 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     dp.part_o = reinterpret_cast<float *>(w + plan.po);
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
+    dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
     if (use_mma) {
         st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, true, false);
     } else if (d->cache_dtype == GVA_F32) {
