@@ -85,6 +85,8 @@ def lib():
                                                 _P, _P, _P])
             L.od_rotate_keys_f64.argtypes = [_I, _I, _P, _P, _D, _P]
             L.od_query_rmsnorm.argtypes = [_I, _I, _I, _P, _P, _D, _P]
+            L.od_gva_decode_rope_keys.argtypes = ([_I] * 5 + [_P, _P, _P, ctypes.POINTER(_Rows)]
+                                                  + [_P, _I, _D, _D, _LL, _P, _P])
             _lib = L
         return _lib
 
@@ -275,6 +277,25 @@ def gva_decode_explicit(q_nope, q_rope, M, seq_len, rows: Rows, V, Kr, scale: fl
     concatenated with the rotated positional key, then ordinary softmax attention."""
     return _decode(lib().od_gva_decode_explicit, q_nope, q_rope, M, seq_len, rows, V,
                    Kr, scale, base, G)
+
+
+def gva_decode_rope_keys(q, M, seq_len, rows: Rows, V, scale: float, base: float, G: int,
+                         pos_offset: int = 0):
+    """GVA with ordinary RoPE on the reconstructed key (the non-absorbable variant; [S]
+    results discussion, [A] 关键技巧二; formula is a reading, see od_gva_decode_rope_keys):
+    z_j = scale * (Rot(t) q_h) . (Rot(j) v_{j,g} M_h), out = softmax(z) V_g."""
+    qq, Mm = f64(q), f64(M)
+    B, H, d_n = qq.shape
+    d_h = Mm.shape[1]
+    sl = np.ascontiguousarray(_np(seq_len).astype(np.int64))
+    Vs, vb = _storage(V)
+    out = np.zeros((B, H, d_h))
+    lse = np.zeros((B, H))
+    rc = rows.c()
+    lib().od_gva_decode_rope_keys(B, H, G, d_h, d_n, _ptr(qq), _ptr(Mm), _ptr(sl),
+                                  ctypes.byref(rc), _ptr(Vs), vb, float(scale), float(base),
+                                  int(pos_offset), _ptr(out), _ptr(lse))
+    return out, lse
 
 
 def gqa_decode(q, seq_len, rows: Rows, K, V, scale: float, G: int):

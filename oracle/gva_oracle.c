@@ -332,6 +332,56 @@ void od_gva_decode_explicit(int B, int H, int G, int d_h, int d_n, int d_r,
 }
 
 /* ------------------------------------------------------------------------- */
+/* GVA with ordinary RoPE on the reconstructed key (the non-absorbable variant) */
+/* ------------------------------------------------------------------------- */
+/* [S] (results discussion): the scale-matched row "still applies ordinary RoPE to
+ * the reconstructed key and cannot absorb M"; [A] 关键技巧二: the relative rotation
+ * R_{j-t} sits between q and M^T, so no single transformed query serves every cached
+ * position.  Reading (listed in the design notes): the key of token j for head h is
+ * K_h[j] = v_{j,g(h)} M_h (width d_n), rotated by its own position j; the query q_h
+ * (width d_n, the whole query) is rotated by t = L_b - 1 with the same pairing;
+ *   z_j = scale * (Rot(t) q_h) . (Rot(j) K_h[j]),   out = softmax(z) V_g (unrotated);
+ * there is no separate positional key.  pos_offset adds a constant to every position
+ * (t and all j), for the relative-position check. */
+void od_gva_decode_rope_keys(int B, int H, int G, int d_h, int d_n, const double *q,
+                             const double *M, const long long *seq_len, const od_rows *R,
+                             const void *V, int cache_bf16, double scale, double base,
+                             long long pos_offset, double *out, double *lse)
+{
+    int r = H / G;
+    long long bh;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (bh = 0; bh < (long long)B * H; ++bh) {
+        int b = (int)(bh / H), h = (int)(bh % H), g = h / r, i, k;
+        long long L = seq_len[b], t = L > 0 ? L - 1 : 0, j;
+        const double *Mh = M + (long long)h * d_h * d_n;
+        double *key = (double *)malloc(sizeof(double) * (size_t)d_n);
+        double *keyr = (double *)malloc(sizeof(double) * (size_t)d_n);
+        double *qr = (double *)malloc(sizeof(double) * (size_t)d_n);
+        double *z = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        od_rotate(q + bh * d_n, qr, d_n, t + pos_offset, base);
+        for (j = 0; j < L; ++j) {
+            long long v0 = (od_row(R, b, j) * G + g) * d_h;
+            double s = 0.0;
+            for (k = 0; k < d_n; ++k) {          /* (v M_h)[k] = sum_i v[i] M_h[i,k] */
+                double acc = 0.0;
+                for (i = 0; i < d_h; ++i) acc += od_load(V, v0 + i, cache_bf16) * Mh[(long long)i * d_n + k];
+                key[k] = acc;
+            }
+            od_rotate(key, keyr, d_n, j + pos_offset, base);
+            for (k = 0; k < d_n; ++k) s += qr[k] * keyr[k];
+            z[j] = scale * s;
+        }
+        softmax_sum(z, L, R, b, V, cache_bf16, (long long)G * d_h, (long long)g * d_h, d_h,
+                    out + bh * d_h, lse + bh);
+        free(key);
+        free(keyr);
+        free(qr);
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* GQA decode (the matched comparator)  ([K] §4, [C] §2.2)                     */
 /* ------------------------------------------------------------------------- */
 /* head_h = softmax(scale * q_h K_g^T) V_g with explicit K and V rows [G][d_h]. */

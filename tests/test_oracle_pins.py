@@ -528,3 +528,66 @@ def test_query_rmsnorm_decode_reduces_to_plain_for_unit_rms_queries():
     b, lb = oracle.gva_decode(qn, c.q_rope, c.M, c.seq_len, R, oracle._np(c.V), oracle._np(c.Kr),
                               w.scale, w.base, w.G)
     assert np.max(np.abs(a - b)) < 1e-12 and np.max(np.abs(la - lb)) < 1e-12
+
+
+# --------------------------------------------------------------------------- #
+# the non-absorbable variant: ordinary RoPE on the reconstructed key (a reading)
+# --------------------------------------------------------------------------- #
+def _rope_complex(x: torch.Tensor, pos: torch.Tensor, base: float) -> torch.Tensor:
+    """RoPE as complex multiplication: pair (x[2i], x[2i+1]) -> (x0 + i x1) e^{i p theta_i},
+    theta_i = base^(-2i/d) -- an independent formulation of the rotation."""
+    d = x.shape[-1]
+    theta = base ** (-2.0 * torch.arange(d // 2, dtype=torch.float64) / d)
+    ang = pos.to(torch.float64)[..., None] * theta
+    xc = torch.view_as_complex(x.reshape(*x.shape[:-1], d // 2, 2).contiguous())
+    return torch.view_as_real(xc * torch.polar(torch.ones_like(ang), ang)).reshape(x.shape)
+
+
+@pytest.mark.parametrize("shape", [dict(B=2, H=4, G=2, d_h=16, d_n=24, T=29),
+                                   dict(B=3, H=6, G=3, d_h=32, d_n=16, T=41)])
+def test_rope_keys_variant_equals_explicit_torch_attention(shape):
+    """Explicit keys K = V_g M_h (torch einsum), rotated by complex multiplication, the
+    whole query rotated to t = L - 1, then fp64 scaled-dot-product attention."""
+    T = shape.pop("T")
+    w = workload("350m", d_r=0, T=T, cache_dtype="f32", q_dtype="f32", **shape)
+    c = make_case(w, lengths=[T - 3 * b for b in range(w.B)])
+    q = torch.randn(w.B, w.H, w.d_n, generator=torch.Generator().manual_seed(31),
+                    dtype=torch.float64)
+    scale = 1.0 / math.sqrt(w.d_n)
+    R = oracle.Rows("contiguous", T_cap=c.T_cap)
+    out, lse = oracle.gva_decode_rope_keys(q, c.M, c.seq_len, R, c.V, scale, w.base, w.G)
+    V = c.V.to(torch.float64).reshape(w.B, c.T_cap, w.G, w.d_h)
+    M = c.M.to(torch.float64)
+    r = w.H // w.G
+    for b in range(w.B):
+        L = int(c.seq_len[b])
+        pos = torch.arange(L)
+        for h in range(w.H):
+            g = h // r
+            K = _rope_complex(V[b, :L, g] @ M[h], pos, w.base)               # [L, d_n]
+            qr = _rope_complex(q[b, h][None], torch.tensor([L - 1]), w.base)  # [1, d_n]
+            ref = F.scaled_dot_product_attention(qr[None], K[None], V[b, :L, g][None],
+                                                 scale=scale)[0, 0]
+            assert np.max(np.abs(out[b, h] - ref.numpy())) < 1e-12
+            z = scale * (K @ qr[0])
+            assert abs(lse[b, h] - torch.logsumexp(z, 0).item()) < 1e-12
+
+
+def test_rope_keys_variant_relative_position_and_one_token():
+    """Shifting every position by a constant leaves the output unchanged (the score
+    depends on j - t only); a one-token cache returns that token's value."""
+    w = workload("350m", d_r=0, T=33, B=2, H=4, G=2, d_h=32, d_n=32, cache_dtype="f32",
+                 q_dtype="f32")
+    c = make_case(w)
+    q = oracle.f64(c.q_nope)
+    R = oracle.Rows("contiguous", T_cap=c.T_cap)
+    a, la = oracle.gva_decode_rope_keys(q, c.M, c.seq_len, R, c.V, 0.2, w.base, w.G)
+    b_, lb = oracle.gva_decode_rope_keys(q, c.M, c.seq_len, R, c.V, 0.2, w.base, w.G,
+                                         pos_offset=77)
+    assert np.max(np.abs(a - b_)) < 1e-12 and np.max(np.abs(la - lb)) < 1e-12
+    one = np.ones(w.B, dtype=np.int64)
+    o1, _ = oracle.gva_decode_rope_keys(q, c.M, one, R, c.V, 0.2, w.base, w.G)
+    V = oracle.f64(c.V).reshape(w.B, c.T_cap, w.G, w.d_h)
+    for b in range(w.B):
+        for h in range(w.H):
+            assert np.array_equal(o1[b, h], V[b, 0, h // 2])
