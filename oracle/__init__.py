@@ -87,6 +87,8 @@ def lib():
             L.od_query_rmsnorm.argtypes = [_I, _I, _I, _P, _P, _D, _P]
             L.od_gva_decode_rope_keys.argtypes = ([_I] * 5 + [_P, _P, _P, ctypes.POINTER(_Rows)]
                                                   + [_P, _I, _D, _D, _LL, _P, _P])
+            L.od_mla_decode.argtypes = ([_I] * 6 + [_P, _P, _P, _P, _P, ctypes.POINTER(_Rows)]
+                                        + [_P, _P, _I, _D, _D, _P, _P])
             _lib = L
         return _lib
 
@@ -295,6 +297,33 @@ def gva_decode_rope_keys(q, M, seq_len, rows: Rows, V, scale: float, base: float
     lib().od_gva_decode_rope_keys(B, H, G, d_h, d_n, _ptr(qq), _ptr(Mm), _ptr(sl),
                                   ctypes.byref(rc), _ptr(Vs), vb, float(scale), float(base),
                                   int(pos_offset), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def mla_decode(q_nope, q_rope, Wuk, Wuv, seq_len, rows: Rows, C, Kr, scale: float,
+               base: float):
+    """MLA-shaped decode, explicit path ([A] 问题 / 对 MLA 的优势: T(d_c + d_r) cache;
+    [C] 3.1.2-3.1.3): keys [c_j Wuk_h ; k_rope_j], values c_j Wuv_h, query
+    [q_nope ; Rot(t) q_rope].  C rows [d_c], K_rope rows [d_r] (shared); Wuk [H, d_c, d_n],
+    Wuv [H, d_c, d_h]."""
+    qn, qr = f64(q_nope), f64(q_rope)
+    Wk, Wv = f64(Wuk), f64(Wuv)
+    B, H, d_n = qn.shape
+    d_r = qr.shape[2]
+    d_c, d_h = Wk.shape[1], Wv.shape[2]
+    sl = np.ascontiguousarray(_np(seq_len).astype(np.int64))
+    Cs, cb = _storage(C)
+    if d_r > 0:
+        Ks, kb = _storage(Kr)
+        assert kb == cb, "C and K_rope share the cache dtype"
+    else:
+        Ks = np.zeros(1, dtype=Cs.dtype)
+    out = np.zeros((B, H, d_h))
+    lse = np.zeros((B, H))
+    rc = rows.c()
+    lib().od_mla_decode(B, H, d_c, d_n, d_h, d_r, _ptr(qn), _ptr(qr), _ptr(Wk), _ptr(Wv),
+                        _ptr(sl), ctypes.byref(rc), _ptr(Cs), _ptr(Ks), cb, float(scale),
+                        float(base), _ptr(out), _ptr(lse))
     return out, lse
 
 

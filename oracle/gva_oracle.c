@@ -382,6 +382,69 @@ void od_gva_decode_rope_keys(int B, int H, int G, int d_h, int d_n, const double
 }
 
 /* ------------------------------------------------------------------------- */
+/* MLA-shaped decode (a second comparator; [A] 问题 and 对 MLA 的优势: a joint latent   */
+/* of width d_c plus one shared RoPE channel, T(d_c + d_r) cached scalars; [C]    */
+/* 3.1.2-3.1.3: per-head up-projections of the latent to K and V, decoupled RoPE)  */
+/* ------------------------------------------------------------------------- */
+/* Explicit path.  Cache rows: latent c_j [d_c], shared positional key k_rope_j [d_r]
+ * (already rotated, as for GVA).  For head h, with row-vector products as for GVA's
+ * K_h = V M_h:
+ *   K_h[j] = c_j Wuk_h  (Wuk_h in R^{d_c x d_n}),   V_h[j] = c_j Wuv_h  (Wuv_h in R^{d_c x d_h})
+ *   key_j = [K_h[j] ; k_rope_j],  query = [q_nope ; Rot(t) q_rope],  t = L_b - 1
+ *   z_j = scale * query . key_j,  out[b,h] = sum_j softmax(z)_j V_h[j],  lse = logsumexp(z)
+ * Reading (listed in the design notes): the positional key is one shared stream
+ * ([A]; [C] describes per-head positional keys, which is DeepSeek's MLA, not the
+ * T(d_c + d_r) count the GVA pages compare with). */
+void od_mla_decode(int B, int H, int d_c, int d_n, int d_h, int d_r, const double *q_nope,
+                   const double *q_rope, const double *Wuk, const double *Wuv,
+                   const long long *seq_len, const od_rows *R, const void *C, const void *Kr,
+                   int cache_bf16, double scale, double base, double *out, double *lse)
+{
+    long long bh;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (bh = 0; bh < (long long)B * H; ++bh) {
+        int b = (int)(bh / H), h = (int)(bh % H), i, k, c;
+        long long L = seq_len[b], t = L > 0 ? L - 1 : 0, j;
+        const double *Wk = Wuk + (long long)h * d_c * d_n;
+        const double *Wv = Wuv + (long long)h * d_c * d_h;
+        double *qh = (double *)malloc(sizeof(double) * (size_t)(d_r > 0 ? d_r : 1));
+        double *z = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double zmax = -INFINITY, den = 0.0;
+        if (d_r > 0) od_rotate(q_rope + bh * d_r, qh, d_r, t, base);
+        for (j = 0; j < L; ++j) {
+            long long row = od_row(R, b, j);
+            double s = 0.0;
+            for (k = 0; k < d_n; ++k) {          /* (c_j Wuk_h)[k] */
+                double acc = 0.0;
+                for (c = 0; c < d_c; ++c) acc += od_load(C, row * d_c + c, cache_bf16) * Wk[(long long)c * d_n + k];
+                s += q_nope[bh * d_n + k] * acc;
+            }
+            for (c = 0; c < d_r; ++c) s += qh[c] * od_load(Kr, row * d_r + c, cache_bf16);
+            z[j] = scale * s;
+            if (z[j] > zmax) zmax = z[j];
+        }
+        for (i = 0; i < d_h; ++i) out[bh * d_h + i] = 0.0;
+        if (L == 0) {
+            lse[bh] = -INFINITY;
+        } else {
+            for (j = 0; j < L; ++j) den += exp(z[j] - zmax);
+            for (j = 0; j < L; ++j) {
+                long long row = od_row(R, b, j);
+                double p = exp(z[j] - zmax) / den;
+                for (i = 0; i < d_h; ++i) {      /* (c_j Wuv_h)[i] */
+                    double acc = 0.0;
+                    for (c = 0; c < d_c; ++c) acc += od_load(C, row * d_c + c, cache_bf16) * Wv[(long long)c * d_h + i];
+                    out[bh * d_h + i] += p * acc;
+                }
+            }
+            lse[bh] = zmax + log(den);
+        }
+        free(qh);
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* GQA decode (the matched comparator)  ([K] §4, [C] §2.2)                     */
 /* ------------------------------------------------------------------------- */
 /* head_h = softmax(scale * q_h K_g^T) V_g with explicit K and V rows [G][d_h]. */

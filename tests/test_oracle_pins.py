@@ -591,3 +591,64 @@ def test_rope_keys_variant_relative_position_and_one_token():
     for b in range(w.B):
         for h in range(w.H):
             assert np.array_equal(o1[b, h], V[b, 0, h // 2])
+
+
+# --------------------------------------------------------------------------- #
+# the MLA-shaped comparator: latent cache c [d_c] + shared positional key [d_r]
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("dims", [dict(B=2, H=4, d_c=32, d_n=16, d_h=24, d_r=8, T=37),
+                                  dict(B=3, H=2, d_c=48, d_n=32, d_h=32, d_r=0, T=20)])
+def test_mla_decode_equals_absorbed_gva_then_up_projection(dims):
+    """MLA's attention weights are GVA's with one value group (G = 1), values the latent
+    (d_h = d_c) and M_h = Wuk_h; its output is that result times Wuv_h.  The MLA oracle
+    materialises every key and value explicitly, the GVA oracle absorbs: they must agree
+    (the absorption identity for MLA, with the up-projection moved past the sum)."""
+    T = dims.pop("T")
+    B, H, d_c, d_n, d_h, d_r = (dims[k] for k in ("B", "H", "d_c", "d_n", "d_h", "d_r"))
+    gen = torch.Generator().manual_seed(41)
+    Cc = torch.randn(B * T, d_c, generator=gen)
+    Kr = torch.randn(B * T, max(d_r, 1), generator=gen)[:, :d_r].contiguous()
+    qn = torch.randn(B, H, d_n, generator=gen)
+    qr = torch.randn(B, H, d_r, generator=gen)
+    Wuk = torch.randn(H, d_c, d_n, generator=gen) / math.sqrt(d_c)
+    Wuv = torch.randn(H, d_c, d_h, generator=gen) / math.sqrt(d_c)
+    L = torch.tensor([T - 5 * b for b in range(B)])
+    R = oracle.Rows("contiguous", T_cap=T)
+    scale = 1.0 / math.sqrt(d_n + d_r)
+    out, lse = oracle.mla_decode(qn, qr, Wuk, Wuv, L, R, Cc, Kr, scale, 10000.0)
+    # GVA with one group: cache rows [1][d_c], M_h = Wuk_h (d_h := d_c, d_n)
+    o_lat, lse_g = oracle.gva_decode(qn, qr, Wuk, L, R, Cc.reshape(B * T, 1, d_c), Kr, scale,
+                                     10000.0, 1)
+    ref = np.einsum("bhc,hcd->bhd", o_lat, oracle.f64(Wuv))
+    assert np.max(np.abs(out - ref)) < 1e-12
+    assert np.max(np.abs(lse - lse_g)) < 1e-12
+
+
+def test_mla_decode_equals_explicit_torch_attention():
+    """An independent construction: torch einsum keys and values from the latent, the
+    positional query rotated by complex multiplication, fp64 SDPA."""
+    B, H, d_c, d_n, d_h, d_r, T = 2, 3, 24, 16, 8, 8, 19
+    gen = torch.Generator().manual_seed(43)
+    Cc = torch.randn(B * T, d_c, generator=gen, dtype=torch.float64).to(torch.float32)
+    Kr = torch.randn(B * T, d_r, generator=gen, dtype=torch.float64).to(torch.float32)
+    qn = torch.randn(B, H, d_n, generator=gen, dtype=torch.float64)
+    qr = torch.randn(B, H, d_r, generator=gen, dtype=torch.float64)
+    Wuk = torch.randn(H, d_c, d_n, generator=gen, dtype=torch.float64)
+    Wuv = torch.randn(H, d_c, d_h, generator=gen, dtype=torch.float64)
+    L = torch.tensor([T, T - 6])
+    scale = 0.3
+    out, lse = oracle.mla_decode(qn, qr, Wuk, Wuv, L, oracle.Rows("contiguous", T_cap=T), Cc, Kr,
+                                 scale, 10000.0)
+    C64 = Cc.to(torch.float64).reshape(B, T, d_c)
+    K64 = Kr.to(torch.float64).reshape(B, T, d_r)
+    for b in range(B):
+        n = int(L[b])
+        for h in range(H):
+            keys = torch.cat([C64[b, :n] @ Wuk[h], K64[b, :n]], dim=1)
+            vals = C64[b, :n] @ Wuv[h]
+            q = torch.cat([qn[b, h], _rope_complex(qr[b, h][None], torch.tensor([n - 1]),
+                                                   10000.0)[0]])
+            ref = F.scaled_dot_product_attention(q[None, None], keys[None], vals[None],
+                                                 scale=scale)[0, 0]
+            assert np.max(np.abs(out[b, h] - ref.numpy())) < 1e-12
+            assert abs(lse[b, h] - torch.logsumexp(scale * (keys @ q), 0).item()) < 1e-12
