@@ -327,6 +327,28 @@ def mla_decode(q_nope, q_rope, Wuk, Wuv, seq_len, rows: Rows, C, Kr, scale: floa
     return out, lse
 
 
+def gva_prefill(q_nope, q_rope, M, L0, T_cap: int, V, Kr, scale: float, base: float, G: int):
+    """Chunked prefill, causal ([K] §1: every new token attends to all history up to and
+    including itself; [S] notes that prefill stays matrix-heavy).  Contiguous cache of
+    capacity T_cap per sequence that already holds the chunk: sequence b's n new tokens sit
+    at positions L0[b] .. L0[b] + n - 1.  Query i of sequence b (position p = L0[b] + i)
+    is scored exactly as a decode query of a sequence of length p + 1 (absorbed content
+    part, positional query rotated by p).  q_nope [B, n, H, d_n], q_rope [B, n, H, d_r];
+    returns out [B, n, H, d_h], lse [B, n, H].  Each query is one entry of a decode over
+    a ragged view of the same storage (one entry per (b, i))."""
+    qn, qr = f64(q_nope), f64(q_rope)
+    B, n, H, d_n = qn.shape
+    d_r = qr.shape[3]
+    L0 = np.asarray(_np(L0), dtype=np.int64)
+    offs = np.repeat(np.arange(B, dtype=np.int64) * T_cap, n)
+    lens = (L0[:, None] + np.arange(n)[None, :] + 1).reshape(-1)
+    assert np.all(L0 + n <= T_cap), "the chunk must fit the capacity"
+    R = Rows("ragged", offsets=np.append(offs, 0))
+    out, lse = gva_decode(qn.reshape(B * n, H, d_n), qr.reshape(B * n, H, d_r), M, lens, R, V,
+                          Kr, scale, base, G)
+    return out.reshape(B, n, H, -1), lse.reshape(B, n, H)
+
+
 def gqa_decode(q, seq_len, rows: Rows, K, V, scale: float, G: int):
     """GQA decode, head_h = softmax(scale * q_h K_g^T) V_g ([K] §4; [C] §2.2)."""
     qq = f64(q)

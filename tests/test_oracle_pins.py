@@ -652,3 +652,39 @@ def test_mla_decode_equals_explicit_torch_attention():
                                                  scale=scale)[0, 0]
             assert np.max(np.abs(out[b, h] - ref.numpy())) < 1e-12
             assert abs(lse[b, h] - torch.logsumexp(scale * (keys @ q), 0).item()) < 1e-12
+
+
+# --------------------------------------------------------------------------- #
+# chunked prefill (causal), composed from the decode oracle
+# --------------------------------------------------------------------------- #
+def test_prefill_equals_causal_torch_attention():
+    """Each new token attends causally to the history and the chunk up to itself:
+    compared with fp64 SDPA over explicitly materialised keys [V_g M_h ; k_rope] and a
+    boolean causal mask offset by the history length."""
+    w = workload("350m", B=2, H=4, G=2, d_h=32, d_n=16, d_r=8, T=40, cache_dtype="f32",
+                 q_dtype="f32")
+    c = make_case(w)
+    n = 5
+    L0 = torch.tensor([30, 17])
+    gen = torch.Generator().manual_seed(53)
+    qn = torch.randn(w.B, n, w.H, w.d_n, generator=gen, dtype=torch.float64)
+    qr = torch.randn(w.B, n, w.H, w.d_r, generator=gen, dtype=torch.float64)
+    out, lse = oracle.gva_prefill(qn, qr, c.M, L0, c.T_cap, c.V, c.Kr, w.scale, w.base, w.G)
+    V = c.V.to(torch.float64).reshape(w.B, c.T_cap, w.G, w.d_h)
+    Kr = c.Kr.to(torch.float64).reshape(w.B, c.T_cap, w.d_r)
+    M = c.M.to(torch.float64)
+    r = w.H // w.G
+    for b in range(w.B):
+        P = int(L0[b]) + n                        # positions 0 .. P-1 hold history + chunk
+        pos_q = torch.arange(int(L0[b]), P)
+        mask = torch.arange(P)[None, :] <= pos_q[:, None]          # [n, P] causal
+        for h in range(w.H):
+            g = h // r
+            keys = torch.cat([V[b, :P, g] @ M[h], Kr[b, :P]], dim=1)   # K_h = V_g M_h
+            q = torch.cat([qn[b, :, h], _rope_complex(qr[b, :, h], pos_q, w.base)], dim=1)
+            ref = F.scaled_dot_product_attention(q[None], keys[None], V[b, :P, g][None],
+                                                 attn_mask=mask[None], scale=w.scale)[0]
+            assert np.max(np.abs(out[b, :, h] - ref.numpy())) < 1e-12
+            z = w.scale * (q @ keys.T)
+            z = z.masked_fill(~mask, float("-inf"))
+            assert np.max(np.abs(lse[b, :, h] - torch.logsumexp(z, 1).numpy())) < 1e-12
