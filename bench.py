@@ -378,6 +378,193 @@ def run_ours(args, dist: Dist):
     dist.close()
 
 
+def prefill_work(w, L0, n: int):
+    """Algorithmic work of one chunked-prefill call on one layer: every sequence's rows
+    (history and chunk) read once, sum_b (L0_b + n)(G d_h + d_r) x elem bytes; and the
+    flops of scoring and weighting, each query at position p covering p + 1 positions
+    with H (2 d_h + d_r) multiply-adds (the absorption excluded)."""
+    elem = 2 if w.cache_dtype == "bf16" else 4
+    nbytes = sum(int(l0) + n for l0 in L0) * (w.G * w.d_h + w.d_r) * elem
+    pairs = sum(n * (int(l0) + 1) + n * (n - 1) // 2 for l0 in L0)
+    return nbytes, 2 * w.H * (2 * w.d_h + w.d_r) * pairs
+
+
+def run_prefill(args, dist: Dist):
+    """Causal chunked prefill: one step = gva_prefill_attention (append of n tokens per
+    sequence, then the attention of each new token over the history and the chunk up to
+    itself) on every layer, the chunk being the last n tokens of each sequence of the
+    workload."""
+    import numpy as np
+    import torch
+
+    import gva_inputs
+    import value_only_kv_gva_b300 as gva
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    w = gva_inputs.workload(args.workload)
+    c = gva_inputs.make_case(w)
+    n = args.prefill
+    ch = gva_inputs.make_prefill_chunk(c, n)
+    L0 = ch.L0.tolist()
+    nl = args.layers
+    dims = gva.Dims(w.B, w.H, w.G, w.d_h, w.d_n, w.d_r,
+                    gva.GVA_F32 if w.cache_dtype == "f32" else gva.GVA_BF16,
+                    gva.GVA_F32 if w.q_dtype == "f32" else gva.GVA_BF16)
+    offs = c.offsets.to(dev) if c.offsets is not None else None
+    bt = c.block_table.to(dev) if c.block_table is not None else None
+    rows = gva.Rows(w.layout, c.num_rows, T_cap=c.T_cap, offsets=offs, block_table=bt,
+                    page_size=w.page_size)
+    V0, K0 = c.V.to(dev), c.Kr.to(dev)
+    d_in = [t.to(dev).unsqueeze(0).expand((nl,) + tuple(t.shape)).contiguous()
+            for t in (ch.q_nope, ch.q_rope, ch.v_new, ch.k_new)]
+    layers = []
+    for li in range(nl):
+        V = V0.clone() if li else V0
+        K = K0.clone() if li else K0
+        layers.append(dict(cache=gva.Cache(rows, V, K), M=c.M.to(dev).clone(), li=li))
+    d_out = torch.empty((nl, w.B, n, w.H, w.d_h), device=dev)
+    d_lse = torch.empty((nl, w.B, n, w.H), device=dev)
+    L0d = ch.L0.to(dev)
+    tab = gva.gva_rope_table_fill(int(c.seq_len.max()) + 1, w.d_r, w.base).to(dev)
+    ws = gva.prefill_workspace(dims, n, rows, dev)
+    path = args.path
+    log(f"[bench] prefill {w.name}: B={w.B} n={n} history={sum(L0)} tokens layers={nl}")
+
+    def call(L, stream=None):
+        li = L["li"]
+        gva.gva_prefill_attention(dims, d_in[0][li], d_in[1][li], L["M"], L0d, d_in[2][li],
+                                  d_in[3][li], L["cache"], tab, w.scale, d_out[li], d_lse[li],
+                                  ws, path=path, stream=stream)
+
+    stream = torch.cuda.Stream(device=dev)
+    graph = capture_list(torch, stream, layers, call)
+    assert gva.gva_get_device_status() == 0
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    soak_t = time.time()
+    while time.time() - soak_t < args.soak:
+        for _ in range(5):
+            graph.replay()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for k in range(args.steps):
+            graph.replay()
+            ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    dist.barrier()
+    clocks = sampler.summary(sampler.t_marks["t0"] - args.soak, sampler.t_marks["t1"])
+    sampler.stop()
+    secs = dist.max(ev[0].elapsed_time(ev[args.steps]) / 1e3, dev)
+    step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
+    us_call = secs / (args.steps * nl) * 1e6
+    nbytes, flops = prefill_work(w, L0, n)
+    tokens = w.B * n * nl * args.steps * dist.world
+    value = tokens / secs
+    peaks = measured_peaks()
+    hbm_peak = peaks["hbm_gbs"] if peaks else FALLBACK_HBM_GBS
+    tc_peak = peaks.get("bf16_tflops") if peaks else 1800.0
+    gbs = nbytes / (us_call * 1e-6) / 1e9
+    tflops = flops / (us_call * 1e-6) / 1e12
+
+    # end to end: pinned host chunk inputs in, every layer's outputs out, eager calls
+    h_in = [t.unsqueeze(0).expand((nl,) + tuple(t.shape)).contiguous().pin_memory()
+            for t in (ch.q_nope, ch.q_rope, ch.v_new, ch.k_new)]
+    h_out = torch.empty(tuple(d_out.shape), dtype=torch.float32).pin_memory()
+    cur = torch.cuda.current_stream()
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one_step():
+        for dst, src in zip(d_in, h_in):
+            dst.copy_(src, non_blocking=True)
+        for L in layers:
+            call(L, stream=cur)
+        h_out.copy_(d_out, non_blocking=True)
+        cur.synchronize()
+
+    for _ in range(3):
+        one_step()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        one_step()
+    te = dist.max(time.perf_counter() - t0, dev)
+    e2e = {"value": round(w.B * n * nl * e2e_steps * dist.world / te, 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+           "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": e2e_steps,
+           "how": "eager C-ABI prefill call per layer; pinned host chunk inputs and every "
+                  "layer's outputs copied inside the timed region"}
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        nthr = os.cpu_count() or 1
+        oracle.set_threads(nthr)
+        Vh, Kh = oracle._np(c.V), oracle._np(c.Kr)
+        done = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds or done == 0:
+            b = done % w.B
+            if w.layout == "contiguous":
+                Rb = oracle.Rows("ragged", offsets=np.array([b * c.T_cap, (b + 1) * c.T_cap]))
+            else:
+                Rb = oracle.Rows("paged", block_table=c.block_table.numpy()[[b]],
+                                 page_size=w.page_size)
+            oracle.gva_prefill(ch.q_nope[[b]], ch.q_rope[[b]], c.M, ch.L0[[b]], Rb, Vh, Kh,
+                               w.scale, w.base, w.G)
+            done += 1
+        cs = time.perf_counter() - t0
+        cpu = {"value": round(done * n / cs, 2), "unit": "tokens/s", "cores": oracle.get_threads(),
+               "kind": "oracle",
+               "sample": f"{done} whole chunks of one sequence ({n} queries, all {w.H} heads) "
+                         f"of one {w.name} layer, fp64 C oracle with OpenMP over (b, h), "
+                         f"{cs:.1f} s"}
+
+    line = {
+        "metric": f"GVA causal chunked prefill, new tokens/s ({w.name} layer, n={n} per "
+                  f"sequence)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.cache_dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: GVA chunked prefill B={w.B} n={n} H={w.H} G={w.G} "
+                        f"d_h={w.d_h} d_n={w.d_n} d_r={w.d_r}, chunk = the last {n} tokens "
+                        f"of each sequence; step = one prefill call on each of {nl} layers",
+            "layers": nl, "history_tokens": int(sum(L0)), "us_per_layer_call": round(us_call, 3),
+            "median_us_per_layer_call": round(statistics.median(step_ms) * 1e3 / nl, 3),
+            "bytes_per_layer": nbytes, "flops_per_layer": flops,
+            "achieved_tflops": round(tflops, 3),
+            "tensor_frac_of_bf16_peak": round(tflops / tc_peak, 5) if tc_peak else None,
+            "l2": f"inputs larger than L2: {nl} distinct layer caches", "path": path,
+            "design": "each new token is one entry of a decode batch of B*n entries over a "
+                      "paged view of the cache (history re-read per query, mostly from L2)"},
+        "roofline": {"bound": "hbm", "kernel": "gva_prefill_attention (view + append + absorb + "
+                     "split-K partial + combine), per call", "achieved": round(gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                     "peak_source": "measured" if peaks else "fallback", "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": nl * (4 if path == "fused" else 5) * args.steps,
+        "clocks": clocks,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
 # Sources of the tensor-core decode kernel: a DRAM-traffic figure recorded with ncu is
 # reported only while these files are unchanged since the capture.
 KERNEL_SOURCES = ["decode_mma.cuh", "decode_simt.cuh", "common.cuh"]
@@ -595,6 +782,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-gqa", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="time the causal chunked prefill of this many new tokens per "
+                         "sequence instead of the decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -610,6 +800,8 @@ def main():
     dist = Dist()
     if args.impl == "reference":
         run_reference(args, dist)
+    elif args.prefill > 0:
+        run_prefill(args, dist)
     else:
         run_ours(args, dist)
 

@@ -199,3 +199,33 @@ def make_gqa_query(case: Case) -> torch.Tensor:
     g = torch.Generator().manual_seed(case.w.seed + 2000)
     q = torch.randn((case.w.B, case.w.H, case.w.d_h), generator=g, dtype=torch.float32)
     return q.to(_dt(case.w.q_dtype))
+
+
+@dataclass
+class Chunk:
+    """A prefill chunk of n new tokens per sequence, all on the CPU: the history L0
+    [B] int32, queries q_nope [B,n,H,d_n] and q_rope [B,n,H,d_r] (query dtype), new
+    values v_new [B,n,G,d_h] and unrotated positional keys k_new [B,n,d_r] (fp32)."""
+    n: int
+    L0: torch.Tensor
+    q_nope: torch.Tensor
+    q_rope: torch.Tensor
+    v_new: torch.Tensor
+    k_new: torch.Tensor
+
+
+def make_prefill_chunk(case: Case, n: int) -> Chunk:
+    """The chunk that ends at the case's lengths: L0[b] = L_b - n (every L_b >= n), drawn
+    N(0, 1) from a third generator (seed + 3000) in the order q_nope, q_rope, v_new,
+    k_new."""
+    w = case.w
+    L0 = case.seq_len.to(torch.int64) - n
+    assert bool((L0 >= 0).all()), "every sequence must hold at least n tokens"
+    g = torch.Generator().manual_seed(w.seed + 3000)
+    qd = _dt(w.q_dtype)
+    q_nope = torch.randn((w.B, n, w.H, w.d_n), generator=g, dtype=torch.float32).to(qd)
+    q_rope = torch.randn((w.B, n, w.H, w.d_r), generator=g, dtype=torch.float32).to(qd)
+    v_new = torch.randn((w.B, n, w.G, w.d_h), generator=g, dtype=torch.float32)
+    k_new = torch.randn((w.B, n, w.d_r), generator=g, dtype=torch.float32)
+    return Chunk(n=n, L0=L0.to(torch.int32), q_nope=q_nope, q_rope=q_rope, v_new=v_new,
+                 k_new=k_new)

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define GVA_ABI_VERSION 2
+#define GVA_ABI_VERSION 3
 
 typedef enum {
     GVA_OK = 0,
@@ -221,6 +221,36 @@ int gva_decode_attention_ex(void *stream, const gva_dims *dims, const void *q_no
                             const gva_cache *cache, const float *rope_tab,
                             int rope_max_pos, float scale, float *out, float *lse,
                             void *workspace, size_t ws_bytes, const gva_decode_opts *opts);
+
+/* Bytes of device workspace gva_prefill_attention needs for a chunk of n queries per
+ * sequence over `rows` on the current device.  0 on invalid arguments or a layout the
+ * prefill does not take. */
+size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *rows);
+
+/* Causal chunked prefill ([K] §1: every new token attends to the cached history and to
+ * the chunk up to and including itself; [A] 关键技巧一/二 for the scores).  Sequence b
+ * holds L0[b] tokens (device int [B]); its n new tokens go to positions
+ * p = L0[b] + i, i < n.  The call appends all of them, exactly as gva_append_cache
+ * would one by one (v_new device fp32 [B][n][G][d_h], k_rope_new device fp32
+ * [B][n][d_r], unrotated), then for query i of sequence b computes the decode of
+ * gva_decode_attention over positions 0..p with the positional query rotated by p:
+ *   out[b,i,h,:] (device fp32 [B][n][H][d_h]), lse[b,i,h] (device fp32 [B][n][H] or NULL).
+ * q_nope [B][n][H][d_n], q_rope [B][n][H][d_r] (q_dtype); M, rope_tab, scale and opts
+ * as in gva_decode_attention_ex.  L0 is not updated (the caller adds n).
+ * Each query is run as one entry of a decode batch of B*n entries that read sequence
+ * b's rows (a paged view of the cache; the cached history is read once per query,
+ * the repeats mostly from L2).
+ * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged returns
+ * GVA_ERR_UNSUPPORTED.  B*n <= 4096 (else GVA_ERR_ARG).  Workspace: device, 256-byte
+ * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), zero-filled once as
+ * for gva_decode_attention.  A chunk that does not fit the capacity or the RoPE table
+ * sets GVA_DEV_BAD_POSITION / GVA_DEV_BAD_LENGTH for the queries concerned. */
+int gva_prefill_attention(void *stream, const gva_dims *dims, int n, const void *q_nope,
+                          const void *q_rope, const float *M, const int *L0,
+                          const float *v_new, const float *k_rope_new,
+                          const gva_cache *cache, const float *rope_tab, int rope_max_pos,
+                          float scale, float *out, float *lse, void *workspace,
+                          size_t ws_bytes, const gva_decode_opts *opts);
 
 /* Matched GQA decode, the comparator ([K] §4): out[b,h] = softmax(scale q_h K_g^T) V_g
  * with explicit K and V rows [G][d_h] (cache_dtype).  q device [B][H][d_h] (q_dtype);

@@ -327,23 +327,33 @@ def mla_decode(q_nope, q_rope, Wuk, Wuv, seq_len, rows: Rows, C, Kr, scale: floa
     return out, lse
 
 
-def gva_prefill(q_nope, q_rope, M, L0, T_cap: int, V, Kr, scale: float, base: float, G: int):
+def gva_prefill(q_nope, q_rope, M, L0, rows, V, Kr, scale: float, base: float, G: int):
     """Chunked prefill, causal ([K] §1: every new token attends to all history up to and
-    including itself; [S] notes that prefill stays matrix-heavy).  Contiguous cache of
-    capacity T_cap per sequence that already holds the chunk: sequence b's n new tokens sit
-    at positions L0[b] .. L0[b] + n - 1.  Query i of sequence b (position p = L0[b] + i)
-    is scored exactly as a decode query of a sequence of length p + 1 (absorbed content
-    part, positional query rotated by p).  q_nope [B, n, H, d_n], q_rope [B, n, H, d_r];
-    returns out [B, n, H, d_h], lse [B, n, H].  Each query is one entry of a decode over
-    a ragged view of the same storage (one entry per (b, i))."""
+    including itself; [S] notes that prefill stays matrix-heavy).  The cache already
+    holds the chunk: sequence b's n new tokens sit at positions L0[b] .. L0[b] + n - 1.
+    `rows` is the cache's row map: an int T_cap (contiguous), or a Rows of any kind.
+    Query i of sequence b (position p = L0[b] + i) is scored exactly as a decode query
+    of a sequence of length p + 1 (absorbed content part, positional query rotated by
+    p).  q_nope [B, n, H, d_n], q_rope [B, n, H, d_r]; returns out [B, n, H, d_h],
+    lse [B, n, H].  Each query is one entry of a decode over a view of the same
+    storage (one entry per (b, i), all reading sequence b's rows)."""
     qn, qr = f64(q_nope), f64(q_rope)
     B, n, H, d_n = qn.shape
     d_r = qr.shape[3]
     L0 = np.asarray(_np(L0), dtype=np.int64)
-    offs = np.repeat(np.arange(B, dtype=np.int64) * T_cap, n)
     lens = (L0[:, None] + np.arange(n)[None, :] + 1).reshape(-1)
-    assert np.all(L0 + n <= T_cap), "the chunk must fit the capacity"
-    R = Rows("ragged", offsets=np.append(offs, 0))
+    if isinstance(rows, Rows) and rows.kind == "paged":
+        bt = np.asarray(_np(rows.block_table), dtype=np.int64)
+        assert np.all(L0 + n <= bt.shape[1] * rows.page_size), "the chunk must fit the capacity"
+        R = Rows("paged", block_table=np.repeat(bt[:B], n, axis=0), page_size=rows.page_size)
+    elif isinstance(rows, Rows) and rows.kind == "ragged":
+        offs = np.asarray(_np(rows.offsets), dtype=np.int64)
+        assert np.all(L0 + n <= offs[1:B + 1] - offs[:B]), "the chunk must fit the capacity"
+        R = Rows("ragged", offsets=np.append(np.repeat(offs[:B], n), 0))
+    else:
+        T_cap = rows.T_cap if isinstance(rows, Rows) else int(rows)
+        assert np.all(L0 + n <= T_cap), "the chunk must fit the capacity"
+        R = Rows("ragged", offsets=np.append(np.repeat(np.arange(B, dtype=np.int64) * T_cap, n), 0))
     out, lse = gva_decode(qn.reshape(B * n, H, d_n), qr.reshape(B * n, H, d_r), M, lens, R, V,
                           Kr, scale, base, G)
     return out.reshape(B, n, H, -1), lse.reshape(B, n, H)

@@ -49,7 +49,7 @@ def test_every_declared_symbol_is_exported(gva):
 
 
 def test_abi_version_and_status_strings(gva):
-    assert gva.gva_abi_version() == 2
+    assert gva.gva_abi_version() == 3
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 3, 4):
         s = gva.gva_status_string(code)
         assert s and "unknown" not in s
@@ -146,3 +146,27 @@ def test_bad_option_flags_rejected_before_cuda(gva, flags, eps):
     st = lib.gva_absorb_query_ex(None, ctypes.byref(d), fake, fake, fake, fake, fake, 100,
                                  ctypes.c_float(0.1), fake, fake, ctypes.byref(o))
     assert st == gva.GVA_ERR_ARG
+
+
+def test_prefill_arguments_rejected_before_cuda(gva):
+    """Ragged caches and contiguous capacities that are not a multiple of 16 are not
+    taken (GVA_ERR_UNSUPPORTED); an empty chunk or more than 4096 decode entries is an
+    argument error."""
+    lib = gva._lib
+    d = _dims(gva)
+    fake = ctypes.c_void_p(0x10000)
+
+    def call(rows, n):
+        cache = gva.gva_cache(rows, fake, fake)
+        return lib.gva_prefill_attention(None, ctypes.byref(d), n, fake, fake, fake, fake, fake,
+                                         fake, ctypes.byref(cache), fake, 100,
+                                         ctypes.c_float(0.1), fake, None, fake,
+                                         ctypes.c_size_t(1 << 30), None)
+
+    contig = gva.gva_rows(0, 2 * 1024, 1024, None, None, 0, 0)
+    assert call(gva.gva_rows(1, 640, 0, fake, None, 0, 0), 4) == gva.GVA_ERR_UNSUPPORTED
+    assert call(gva.gva_rows(0, 2 * 1000, 1000, None, None, 0, 0), 4) == gva.GVA_ERR_UNSUPPORTED
+    assert call(contig, 0) == gva.GVA_ERR_ARG
+    assert call(contig, 2049) == gva.GVA_ERR_ARG          # B = 2: 4098 entries
+    for rows in (contig, gva.gva_rows(1, 640, 0, fake, None, 0, 0)):
+        assert lib.gva_prefill_workspace_size(ctypes.byref(d), 0, ctypes.byref(rows)) == 0

@@ -1,0 +1,183 @@
+"""GPU parity of the causal chunked prefill (gva_prefill_attention, through the C ABI)
+against the fp64 oracle on the same seeded inputs: the appended rows bit-exact, the
+outputs within the decode tolerances (bf16 cache: max-abs 2e-2 and relative L2 1e-3;
+fp32 cache: 1e-5)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gva_inputs import make_case, make_prefill_chunk, workload
+from helpers import assert_close, dims_of, gva, oracle_rows, rope_tab
+
+pytestmark = pytest.mark.gpu
+
+
+def _supported(c, path):
+    w = c.w
+    if path in ("mma", "fused"):
+        return w.cache_dtype == "bf16" and w.d_h in (64, 128) and (path == "fused" or w.G <= 8)
+    return True
+
+
+class Run:
+    """One prefill call on the GPU and the oracle's answer for the same chunk."""
+
+    def __init__(self, c, n, path="auto", q_norm=None, L0=None):
+        g = gva()
+        w = c.w
+        d = torch.device("cuda")
+        ch = make_prefill_chunk(c, n)
+        if L0 is not None:
+            ch.L0 = torch.tensor(L0, dtype=torch.int32)
+        self.c, self.ch = c, ch
+        self.V, self.Kr = c.V.to(d), c.Kr.to(d)
+        rows = g.Rows(w.layout, c.num_rows, T_cap=c.T_cap,
+                      offsets=c.offsets.to(d) if c.offsets is not None else None,
+                      block_table=c.block_table.to(d) if c.block_table is not None else None,
+                      page_size=w.page_size)
+        cache = g.Cache(rows, self.V, self.Kr)
+        dims = dims_of(c)
+        self.tab_h = rope_tab(c)
+        ws = g.prefill_workspace(dims, n, rows, d)
+        self.out = torch.full((w.B, n, w.H, w.d_h), float("nan"), device=d)
+        self.lse = torch.full((w.B, n, w.H), float("nan"), device=d)
+        gq = None
+        if q_norm is not None:
+            gq = (None if q_norm[0] is None else q_norm[0].to(d), q_norm[1])
+        g.gva_prefill_attention(dims, ch.q_nope.to(d), ch.q_rope.to(d), c.M.to(d),
+                                ch.L0.to(d), ch.v_new.to(d), ch.k_new.to(d), cache,
+                                self.tab_h.to(d), w.scale, self.out, self.lse, ws, path=path,
+                                q_norm=gq)
+        torch.cuda.synchronize()
+        self.status = g.gva_get_device_status()
+
+    def oracle_cache(self, n=None):
+        """Host storage with the oracle's append of the chunk's first n tokens."""
+        c, ch = self.c, self.ch
+        n = ch.n if n is None else n
+        Vh, Kh = oracle._np(c.V).copy(), oracle._np(c.Kr).copy()
+        R = oracle_rows(c)
+        for i in range(n):
+            oracle.append(ch.v_new[:, i], ch.k_new[:, i], ch.L0.to(torch.int64) + i, R, Vh, Kh,
+                          self.tab_h.numpy())
+        return Vh, Kh
+
+    def oracle_out(self, Vh, Kh, q_nope=None, n=None):
+        c, ch, w = self.c, self.ch, self.c.w
+        n = ch.n if n is None else n
+        qn = ch.q_nope if q_nope is None else q_nope
+        return oracle.gva_prefill(qn[:, :n], ch.q_rope[:, :n], c.M, ch.L0, oracle_rows(c), Vh,
+                                  Kh, w.scale, w.base, w.G)
+
+    def got(self):
+        return (self.out.cpu().numpy().astype(np.float64),
+                self.lse.cpu().numpy().astype(np.float64))
+
+
+def _check_cache(r, Vh, Kh):
+    assert np.array_equal(oracle._np(r.V.cpu()), Vh), "appended values differ"
+    assert np.array_equal(oracle._np(r.Kr.cpu()), Kh), "appended positional keys differ"
+
+
+# small variants: several slabs and CTAs, ragged tails, chunks crossing slab and page
+# boundaries
+SMALL = {
+    "tiny": (dict(), 5),
+    "350m": (dict(T=320, B=3), 9),
+    "long": (dict(B=2, T=1200), 3),
+    "paged": (dict(B=5, len_range=(64, 900)), 17),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("path", ["simt", "mma", "fused", "auto"])
+def test_prefill_small_workloads(name, path):
+    over, n = SMALL[name]
+    c = make_case(workload(name, **over))
+    if not _supported(c, path):
+        pytest.skip(f"{path} path needs a bf16 cache")
+    r = Run(c, n, path)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, c.w.cache_dtype, f"{name}/{path} out")
+    assert_close(lse, ref_lse, c.w.cache_dtype, f"{name}/{path} lse")
+
+
+@pytest.mark.parametrize("n", [1, 16, 33])
+def test_prefill_chunk_lengths(n):
+    """One token (a decode step), one slab, and a chunk with a ragged tail, from an
+    empty history for one sequence."""
+    c = make_case(workload("350m", T=128, B=3), lengths=[128, 100, n])
+    r = Run(c, n)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, "bf16", f"n={n}")
+    assert_close(lse, ref_lse, "bf16", f"n={n} lse")
+
+
+def test_prefill_largest_batch():
+    """B * n = 4096 decode entries, the largest the library takes."""
+    c = make_case(workload("350m", T=160, B=64))
+    r = Run(c, 64)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, "bf16", "B*n=4096")
+    assert_close(lse, ref_lse, "bf16", "B*n=4096 lse")
+
+
+@pytest.mark.parametrize("cache", ["bf16", "f32"])
+def test_prefill_query_rmsnorm(cache):
+    w = workload("350m", T=192, B=2, cache_dtype=cache,
+                 q_dtype="f32" if cache == "f32" else "bf16")
+    c = make_case(w)
+    gain = torch.randn(w.d_n, generator=torch.Generator().manual_seed(9)) * 0.5 + 1.0
+    r = Run(c, 6, q_norm=(gain, 1e-6))
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    n = r.ch.n
+    qn = oracle.query_rmsnorm(r.ch.q_nope.reshape(w.B * n, w.H, w.d_n), gain.numpy(), 1e-6)
+    ref, ref_lse = r.oracle_out(Vh, Kh, q_nope=qn.reshape(w.B, n, w.H, w.d_n))
+    out, lse = r.got()
+    assert_close(out, ref, cache, "q-norm out")
+    assert_close(lse, ref_lse, cache, "q-norm lse")
+
+
+def test_prefill_past_capacity_is_reported():
+    """A chunk running past the capacity: its tokens beyond it are skipped with a status
+    code, their queries return out = 0 and lse = -inf, and the queries that fit are
+    right."""
+    c = make_case(workload("350m", T=64, B=2), lengths=[64, 30])
+    r = Run(c, 8, L0=[60, 22])
+    assert r.status == gva().GVA_DEV_BAD_POSITION
+    Vh, Kh = r.oracle_cache(n=4)          # sequence 0 keeps 4 tokens, sequence 1 all 8
+    seq1 = oracle.Rows("ragged", offsets=np.array([c.T_cap, 2 * c.T_cap]))
+    for i in range(4, 8):
+        oracle.append(r.ch.v_new[1:, i], r.ch.k_new[1:, i], [22 + i], seq1, Vh, Kh,
+                      r.tab_h.numpy())
+    _check_cache(r, Vh, Kh)
+    out, lse = r.got()
+    ref, ref_lse = r.oracle_out(Vh, Kh, n=4)
+    assert_close(out[0, :4], ref[0], "bf16", "b=0 fitting queries")
+    assert np.all(out[0, 4:] == 0) and np.isneginf(lse[0, 4:]).all()
+    ref1, _ = oracle.gva_prefill(r.ch.q_nope[1:], r.ch.q_rope[1:], c.M, r.ch.L0[1:], seq1, Vh,
+                                 Kh, c.w.scale, c.w.base, c.w.G)
+    assert_close(out[1], ref1[0], "bf16", "b=1")
+    assert gva().gva_get_device_status() == 0
+
+
+def test_prefill_refuses_ragged_layout():
+    c = make_case(workload("ragged", B=3, len_range=(20, 60)))
+    g = gva()
+    with pytest.raises(g.GvaError) as e:
+        Run(c, 4)
+    assert e.value.status in (g.GVA_ERR_ARG, g.GVA_ERR_UNSUPPORTED)

@@ -688,3 +688,44 @@ def test_prefill_equals_causal_torch_attention():
             z = w.scale * (q @ keys.T)
             z = z.masked_fill(~mask, float("-inf"))
             assert np.max(np.abs(lse[b, :, h] - torch.logsumexp(z, 1).numpy())) < 1e-12
+
+
+def test_prefill_views_of_paged_and_ragged_storage_match_contiguous():
+    """Where rows live moves bytes, not maths ([K] §7): the same history and chunk stored
+    in permuted pages, or at ragged offsets with gaps, give the contiguous prefill bit
+    for bit."""
+    w = workload("350m", B=3, H=4, G=2, d_h=32, d_n=16, d_r=8, T=64, cache_dtype="f32",
+                 q_dtype="f32")
+    c = make_case(w)
+    n = 7
+    L0 = np.array([40, 9, 57])
+    gen = torch.Generator().manual_seed(71)
+    qn = torch.randn(w.B, n, w.H, w.d_n, generator=gen, dtype=torch.float64)
+    qr = torch.randn(w.B, n, w.H, w.d_r, generator=gen, dtype=torch.float64)
+    T = c.T_cap
+    Vc = c.V.numpy().reshape(w.B, T, w.G, w.d_h)
+    Kc = c.Kr.numpy().reshape(w.B, T, w.d_r)
+    ref, ref_lse = oracle.gva_prefill(qn, qr, c.M, L0, T, c.V, c.Kr, w.scale, w.base, w.G)
+    # paged: 16-row pages at a random permutation of physical pages
+    ps, mp = 16, T // 16
+    bt = np.random.default_rng(5).permutation(w.B * mp).reshape(w.B, mp)
+    Vp = np.zeros((w.B * mp * ps, w.G, w.d_h), dtype=np.float32)
+    Kp = np.zeros((w.B * mp * ps, w.d_r), dtype=np.float32)
+    for b in range(w.B):
+        for p in range(mp):
+            Vp[bt[b, p] * ps:(bt[b, p] + 1) * ps] = Vc[b, p * ps:(p + 1) * ps]
+            Kp[bt[b, p] * ps:(bt[b, p] + 1) * ps] = Kc[b, p * ps:(p + 1) * ps]
+    out, lse = oracle.gva_prefill(qn, qr, c.M, L0, oracle.Rows("paged", block_table=bt,
+                                                                page_size=ps),
+                                  Vp, Kp, w.scale, w.base, w.G)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
+    # ragged: sequences at offsets with unused rows between them
+    offs = np.array([3, 3 + T + 5, 3 + 2 * T + 11, 3 + 3 * T + 11])
+    Vr = np.full((int(offs[-1]), w.G, w.d_h), np.nan, dtype=np.float32)
+    Kr = np.full((int(offs[-1]), w.d_r), np.nan, dtype=np.float32)
+    for b in range(w.B):
+        Vr[offs[b]:offs[b] + T] = Vc[b]
+        Kr[offs[b]:offs[b] + T] = Kc[b]
+    out, lse = oracle.gva_prefill(qn, qr, c.M, L0, oracle.Rows("ragged", offsets=offs),
+                                  Vr, Kr, w.scale, w.base, w.G)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)

@@ -86,12 +86,17 @@ _lib.gva_get_device_status.argtypes = [ctypes.POINTER(_I)]
 _lib.gva_last_cuda_error.restype = _I
 _lib.gva_decode_attention_static.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I, _F, _P, _P]
 _lib.gva_read_probe.argtypes = [_P, _P, _Z, _P]
+_lib.gva_prefill_workspace_size.restype = _Z
+_lib.gva_prefill_workspace_size.argtypes = [_PD, _I, ctypes.POINTER(gva_rows)]
+_lib.gva_prefill_attention.argtypes = [_P, _PD, _I, _P, _P, _P, _P, _P, _P, _PC, _P, _I, _F,
+                                       _P, _P, _P, _Z, _PO]
 
 EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_table_fill",
            "gva_absorb_query", "gva_append_cache", "gva_decode_workspace_size",
            "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
            "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static",
-           "gva_read_probe", "gva_absorb_query_ex"]
+           "gva_read_probe", "gva_absorb_query_ex", "gva_prefill_workspace_size",
+           "gva_prefill_attention"]
 
 
 class GvaError(RuntimeError):
@@ -296,6 +301,34 @@ def gva_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, r
         ctypes.byref(o)), "gva_decode_attention")
 
 
+def gva_prefill_workspace_size(dims: Dims, n: int, rows: Rows) -> int:
+    d, r = dims.c(), rows.c()
+    return int(_lib.gva_prefill_workspace_size(ctypes.byref(d), int(n), ctypes.byref(r)))
+
+
+def gva_prefill_attention(dims: Dims, q_nope, q_rope, M, L0, v_new, k_rope_new, cache: Cache,
+                          rope_tab, scale: float, out, lse, workspace, path: str = "auto",
+                          num_ctas: int = 0, stream=None, q_norm=None) -> None:
+    """gva_prefill_attention: append the chunk q_nope.shape[1] = n tokens per sequence
+    after L0[b] cached ones, then causal attention of each new token (q_nope
+    [B, n, H, d_n], v_new [B, n, G, d_h], k_rope_new [B, n, d_r], out [B, n, H, d_h],
+    lse [B, n, H]; q_norm as in _opts)."""
+    d = dims.c()
+    cc = cache.c()
+    o = _opts(path, num_ctas, q_norm)
+    n = int(q_nope.shape[1])
+    _check(_lib.gva_prefill_attention(
+        _stream(stream), ctypes.byref(d), n, _ptr(q_nope, None, "q_nope"),
+        _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
+        _ptr(L0, torch.int32, "L0"), _ptr(v_new, torch.float32, "v_new"),
+        _ptr(k_rope_new, torch.float32, "k_rope_new") if dims.d_r else None, ctypes.byref(cc),
+        _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+        ctypes.byref(o)), "gva_prefill_attention")
+
+
 class PreparedCall:
     """One C-ABI call with its arguments validated and marshalled once, for loops that
     repeat the same call on the same buffers (a decode step per layer): calling the
@@ -387,3 +420,11 @@ def workspace(dims: Dims, device=None) -> torch.Tensor:
     if n == 0:
         raise GvaError(GVA_ERR_ARG, "gva_decode_workspace_size")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def prefill_workspace(dims: Dims, n: int, rows: Rows, device=None) -> torch.Tensor:
+    """Allocate a zero-filled prefill workspace for chunks of n tokens per sequence."""
+    size = gva_prefill_workspace_size(dims, n, rows)
+    if size == 0:
+        raise GvaError(GVA_ERR_ARG, "gva_prefill_workspace_size")
+    return torch.zeros(size, dtype=torch.uint8, device=device or "cuda")

@@ -291,6 +291,61 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     return cuda_status(e);
 }
 
+// One CTA per entry of the batch d->B (arguments validated by the caller).
+int append_launch(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
+                  const int *pos, int *seq_len_out, const gva_rows &rows, void *V, void *Kr,
+                  const float *rope_tab, int rope_max_pos) {
+    AppendParams p;
+    p.B = d->B;
+    p.G = d->G;
+    p.d_h = d->d_h;
+    p.d_r = d->d_r;
+    p.v_new = v_new;
+    p.k_new = k_new;
+    p.pos = pos;
+    p.seq_len_out = seq_len_out;
+    p.R = to_dev(rows);
+    p.V = V;
+    p.Kr = Kr;
+    p.rope_tab = rope_tab;
+    p.rope_max_pos = rope_max_pos;
+    cudaError_t e = d->cache_dtype == GVA_F32
+                        ? launch(append_kernel<float>, dim3(d->B), dim3(128), 0, stream, p)
+                        : launch(append_kernel<__nv_bfloat16>, dim3(d->B), dim3(128), 0, stream, p);
+    return cuda_status(e);
+}
+
+// Chunked prefill over n queries per sequence: the view's tables, then the decode
+// batch of B*n entries.  Workspace: [view block table][positions][lengths][decode].
+struct PrefillPlan {
+    size_t bt, pos, len, dec, total;
+    int max_pages;
+    gva_dims dv;   // the decode batch: B*n entries
+};
+
+// False when the chunk cannot be viewed as a decode batch of this library.
+bool plan_prefill(const gva_dims *d, int n, const gva_rows &R, int sms, PrefillPlan *p) {
+    if (n < 1 || (long long)d->B * n > MAX_B) return false;
+    p->dv = *d;
+    p->dv.B = d->B * n;
+    p->max_pages = R.layout == GVA_LAYOUT_PAGED ? R.max_pages : 1;
+    size_t o = 0;
+    p->bt = o;  o = align_up(o + sizeof(int) * (size_t)p->dv.B * p->max_pages, 256);
+    p->pos = o; o = align_up(o + sizeof(int) * (size_t)p->dv.B, 256);
+    p->len = o; o = align_up(o + sizeof(int) * (size_t)p->dv.B, 256);
+    p->dec = o; o += plan_ws(&p->dv, sms).total;
+    p->total = o;
+    return true;
+}
+
+// Layouts the view supports: paged, and contiguous with a capacity that is a
+// multiple of the 16-token slab (read as one page per sequence).
+bool prefill_layout_ok(const gva_rows &R) {
+    if (R.layout == GVA_LAYOUT_PAGED) return true;
+    return R.layout == GVA_LAYOUT_CONTIGUOUS && R.T_cap >= SLAB && R.T_cap % SLAB == 0 &&
+           R.T_cap <= 0x7fffffffLL;
+}
+
 const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0, 0.f, nullptr};
 
 // Option flags: only the query RMSNorm, with a finite eps >= 0.
@@ -422,24 +477,8 @@ int gva_append_cache(void *stream, const gva_dims *d, const float *v_new, const 
         return GVA_ERR_ARG;
     if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
     if (!device_state()) return GVA_ERR_CUDA;
-    AppendParams p;
-    p.B = d->B;
-    p.G = d->G;
-    p.d_h = d->d_h;
-    p.d_r = d->d_r;
-    p.v_new = v_new;
-    p.k_new = k_new;
-    p.pos = pos;
-    p.seq_len_out = seq_len_out;
-    p.R = to_dev(cache->rows);
-    p.V = cache->V;
-    p.Kr = cache->K_rope;
-    p.rope_tab = rope_tab;
-    p.rope_max_pos = rope_max_pos;
-    cudaError_t e = d->cache_dtype == GVA_F32
-                        ? launch(append_kernel<float>, dim3(d->B), dim3(128), 0, stream, p)
-                        : launch(append_kernel<__nv_bfloat16>, dim3(d->B), dim3(128), 0, stream, p);
-    return cuda_status(e);
+    return append_launch(stream, d, v_new, k_new, pos, seq_len_out, cache->rows, cache->V,
+                         cache->K_rope, rope_tab, rope_max_pos);
 }
 
 size_t gva_decode_workspace_size(const gva_dims *d) {
@@ -579,6 +618,82 @@ int gva_decode_attention(void *stream, const gva_dims *d, const void *q_nope, co
                          float *lse, void *ws, size_t ws_bytes) {
     return gva_decode_attention_ex(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab,
                                    rope_max_pos, scale, out, lse, ws, ws_bytes, nullptr);
+}
+
+size_t gva_prefill_workspace_size(const gva_dims *d, int n, const gva_rows *rows) {
+    if (!dims_ok(d, true) || !rows || !rows_ok(rows, d->B) || !prefill_layout_ok(*rows))
+        return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    PrefillPlan pp;
+    return plan_prefill(d, n, *rows, sms, &pp) ? pp.total : 0;
+}
+
+int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_nope,
+                          const void *q_rope, const float *M, const int *L0,
+                          const float *v_new, const float *k_new, const gva_cache *cache,
+                          const float *rope_tab, int rope_max_pos, float scale, float *out,
+                          float *lse, void *ws, size_t ws_bytes, const gva_decode_opts *opts) {
+    const gva_decode_opts *o = opts ? opts : &kDefaultOpts;
+    if (!cache || n < 1 || !dims_ok(d, true) || (long long)d->B * n > MAX_B) return GVA_ERR_ARG;
+    if (!rows_ok(&cache->rows, d->B)) return GVA_ERR_ARG;
+    if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
+    if (!flags_ok(o) || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_FUSED || o->num_ctas < 0)
+        return GVA_ERR_ARG;
+    if (!q_nope || !M || !L0 || !v_new || !cache->V || !aligned16(q_nope) || !aligned16(M) ||
+        !aligned16(v_new) || !aligned16(cache->V))
+        return GVA_ERR_ARG;
+    if (d->d_r > 0 && (!q_rope || !k_new || !cache->K_rope || !rope_tab || rope_max_pos < 1 ||
+                       !aligned16(q_rope) || !aligned16(k_new) || !aligned16(cache->K_rope) ||
+                       !aligned16(rope_tab)))
+        return GVA_ERR_ARG;
+    const gva_rows &R = cache->rows;
+    if (!prefill_layout_ok(R)) return GVA_ERR_UNSUPPORTED;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    const int sms = num_sms_current();
+    if (sms <= 0) return GVA_ERR_CUDA;
+    PrefillPlan pp;
+    if (!plan_prefill(d, n, R, sms, &pp)) return GVA_ERR_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < pp.total)
+        return GVA_ERR_WORKSPACE;
+    char *w = static_cast<char *>(ws);
+    PrefillViewParams vp;
+    vp.B = d->B;
+    vp.n = n;
+    vp.L0 = L0;
+    vp.block_table = R.layout == GVA_LAYOUT_PAGED ? R.block_table : nullptr;
+    vp.max_pages = pp.max_pages;
+    vp.bt = reinterpret_cast<int *>(w + pp.bt);
+    vp.pos = reinterpret_cast<int *>(w + pp.pos);
+    vp.len = reinterpret_cast<int *>(w + pp.len);
+    gva_rows vr;
+    memset(&vr, 0, sizeof(vr));
+    vr.layout = GVA_LAYOUT_PAGED;
+    vr.block_table = vp.bt;
+    vr.max_pages = pp.max_pages;
+    if (R.layout == GVA_LAYOUT_PAGED) {
+        vr.page_size = R.page_size;
+        vr.num_rows = R.num_rows;
+    } else {
+        vr.page_size = (int)R.T_cap;
+        vr.num_rows = (long long)d->B * R.T_cap;
+    }
+    // a path that cannot run the chunk is refused before anything is appended
+    if (o->path == GVA_PATH_MMA && !mma_supported(d)) return GVA_ERR_UNSUPPORTED;
+    if (o->path == GVA_PATH_FUSED && !fused_supported(&pp.dv, vr)) return GVA_ERR_UNSUPPORTED;
+    int st = cuda_status(launch(prefill_view_kernel, dim3(d->B, (n + PV_ROWS - 1) / PV_ROWS),
+                                dim3(128), 0, stream, vp));
+    if (st != GVA_OK) return st;
+    st = append_launch(stream, &pp.dv, v_new, k_new, vp.pos, nullptr, vr, cache->V,
+                       cache->K_rope, rope_tab, rope_max_pos);
+    if (st != GVA_OK) return st;
+    gva_cache vc;
+    vc.rows = vr;
+    vc.V = cache->V;
+    vc.K_rope = cache->K_rope;
+    return gva_decode_attention_ex(stream, &pp.dv, q_nope, q_rope, M, vp.len, &vc, rope_tab,
+                                   rope_max_pos, scale, out, lse, w + pp.dec, ws_bytes - pp.dec,
+                                   o);
 }
 
 int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, const int *seq_len,

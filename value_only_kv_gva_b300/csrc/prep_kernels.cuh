@@ -87,6 +87,52 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
 }
 
 // --------------------------------------------------------------------------- //
+// Chunked-prefill view  (MQA/GQA page §1: each new token attends to the cached history
+// and to the chunk up to and including itself)
+// --------------------------------------------------------------------------- //
+// Query i of sequence b becomes entry v = b*n + i of a decode batch: a sequence of
+// length L0[b] + i + 1 stored in sequence b's rows.  The append then writes the token
+// at position L0[b] + i and the decode of entry v attends over positions 0..L0[b]+i,
+// which is the causal mask.  Every entry reads b's rows through its own copy of b's
+// block-table row; a contiguous cache is read as pages of T_cap rows (page b holds
+// sequence b), so the view is a paged one for both layouts.
+struct PrefillViewParams {
+    int B, n;
+    const int *L0;            // [B] tokens cached before the chunk
+    const int *block_table;   // paged: the caller's [B][max_pages]; contiguous: null
+    int max_pages;            // columns of both tables (1 for a contiguous cache)
+    int *bt;                  // [B*n][max_pages] block table of the view
+    int *pos;                 // [B*n] append position of entry v: L0[b] + i, or -1
+    int *len;                 // [B*n] decode length of entry v: L0[b] + i + 1, or -1
+};
+constexpr int PV_ROWS = 32;   // chunk queries per CTA (grid: B x ceil(n / PV_ROWS))
+
+__global__ void __launch_bounds__(128) prefill_view_kernel(const PrefillViewParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int b = blockIdx.x;
+    const int i0 = blockIdx.y * PV_ROWS;
+    const int i1 = min(p.n, i0 + PV_ROWS);
+    const long long l0 = p.L0[b];
+    // a negative history or a position past the int range is marked -1: the append
+    // reports a bad position and the decode a bad length for that entry
+    for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
+        const long long v = (long long)b * p.n + i;
+        const long long end = l0 + i + 1;
+        const bool ok = l0 >= 0 && end <= 0x7fffffffLL;
+        p.pos[v] = ok ? (int)(end - 1) : -1;
+        p.len[v] = ok ? (int)end : -1;
+    }
+    const long long W = (long long)(i1 - i0) * p.max_pages;
+    for (long long e = threadIdx.x; e < W; e += blockDim.x) {
+        const long long v = (long long)b * p.n + i0 + e / p.max_pages;
+        const long long col = e % p.max_pages;
+        p.bt[v * p.max_pages + col] =
+            p.block_table ? p.block_table[(long long)b * p.max_pages + col] : b;
+    }
+}
+
+// --------------------------------------------------------------------------- //
 // Absorb  (GVA analysis page, 关键技巧一: q_h k_{j,h}^T = (q_h M_h^T) v_{j,g(h)}^T)
 // --------------------------------------------------------------------------- //
 struct AbsorbParams {
