@@ -181,3 +181,41 @@ def test_prefill_refuses_ragged_layout():
     with pytest.raises(g.GvaError) as e:
         Run(c, 4)
     assert e.value.status in (g.GVA_ERR_ARG, g.GVA_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("H,G,d_h,d_n,d_r", [
+    (8, 8, 64, 64, 16), (8, 4, 64, 32, 8), (8, 2, 128, 128, 24), (8, 1, 64, 64, 32),
+    (16, 2, 64, 32, 0), (4, 4, 128, 64, 16), (32, 4, 64, 128, 16), (3, 3, 64, 64, 16),
+    (16, 8, 128, 128, 32),
+])
+@pytest.mark.parametrize("n", [3, 21])
+def test_prefill_shapes(H, G, d_h, d_n, d_r, n):
+    """The default path (the tensor-core prefill kernel for bf16 caches) over head
+    groupings r = 1..8, every positional width, both value widths."""
+    w = workload("350m", B=2, T=160, H=H, G=G, d_h=d_h, d_n=d_n, d_r=d_r)
+    c = make_case(w, lengths=[160, 45])
+    r = Run(c, n)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, "bf16", f"{H},{G},{d_h},{d_n},{d_r} n={n}")
+    assert_close(lse, ref_lse, "bf16", f"{H},{G},{d_h},{d_n},{d_r} n={n} lse")
+
+
+def test_prefill_paths_agree_on_a_paged_batch():
+    """Every path on the same paged chunk: the tensor-core prefill kernel (auto) and the
+    decode-entry compositions (simt, mma, fused), each against the oracle."""
+    c = make_case(workload("paged", B=3, len_range=(100, 700)))
+    refs = None
+    for path in ("auto", "simt", "mma", "fused"):
+        r = Run(c, 12, path)
+        assert r.status == 0
+        if refs is None:
+            Vh, Kh = r.oracle_cache()
+            refs = r.oracle_out(Vh, Kh), (Vh, Kh)
+        _check_cache(r, *refs[1])
+        out, lse = r.got()
+        assert_close(out, refs[0][0], "bf16", f"{path} out")
+        assert_close(lse, refs[0][1], "bf16", f"{path} lse")

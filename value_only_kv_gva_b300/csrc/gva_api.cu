@@ -14,6 +14,7 @@
 #include "decode_simt.cuh"
 #include "decode_mma.cuh"
 #include "decode_fused.cuh"
+#include "prefill_mma.cuh"
 
 using namespace gva;
 
@@ -97,6 +98,7 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, true>);
     if (e == cudaSuccess) e = mma_opt_in_all();
     if (e == cudaSuccess) e = fused_opt_in_all();
+    if (e == cudaSuccess) e = prefill_opt_in_all();
     if (e == cudaSuccess && !encode_fn()) e = cudaErrorSymbolNotFound;
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
@@ -315,12 +317,17 @@ int append_launch(void *stream, const gva_dims *d, const float *v_new, const flo
     return cuda_status(e);
 }
 
-// Chunked prefill over n queries per sequence: the view's tables, then the decode
-// batch of B*n entries.  Workspace: [view block table][positions][lengths][decode].
+// Chunked prefill over n queries per sequence: the view's tables, the decode workspace
+// of the B*n-entry batch (its absorbed-query regions also feed the tensor-core prefill
+// kernel), then that kernel's split partials.
+// Workspace: [view block table][positions][lengths][decode][prefill partials o][m, l].
 struct PrefillPlan {
-    size_t bt, pos, len, dec, total;
+    size_t bt, pos, len, dec, po, pml, total;
     int max_pages;
-    gva_dims dv;   // the decode batch: B*n entries
+    gva_dims dv;        // the decode batch: B*n entries
+    WsPlan dws;         // its workspace plan (offsets relative to dec)
+    bool mq;            // the tensor-core prefill kernel takes this shape
+    PrefillMmaPlan mp;
 };
 
 // False when the chunk cannot be viewed as a decode batch of this library.
@@ -333,7 +340,11 @@ bool plan_prefill(const gva_dims *d, int n, const gva_rows &R, int sms, PrefillP
     p->bt = o;  o = align_up(o + sizeof(int) * (size_t)p->dv.B * p->max_pages, 256);
     p->pos = o; o = align_up(o + sizeof(int) * (size_t)p->dv.B, 256);
     p->len = o; o = align_up(o + sizeof(int) * (size_t)p->dv.B, 256);
-    p->dec = o; o += plan_ws(&p->dv, sms).total;
+    p->dws = plan_ws(&p->dv, sms);
+    p->dec = o; o += p->dws.total;
+    p->mq = prefill_mma_plan(d, n, sms, &p->mp);
+    p->po = o;  o += p->mq ? p->mp.part_o_bytes : 0;
+    p->pml = o; o += p->mq ? p->mp.part_ml_bytes : 0;
     p->total = o;
     return true;
 }
@@ -687,6 +698,39 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     st = append_launch(stream, &pp.dv, v_new, k_new, vp.pos, nullptr, vr, cache->V,
                        cache->K_rope, rope_tab, rope_max_pos);
     if (st != GVA_OK) return st;
+    if (o->path == GVA_PATH_AUTO && pp.mq) {
+        // tensor-core prefill: absorb every (query, head) of the chunk, then one pass
+        // over each sequence's rows shared by all its queries, then the merge
+        float *qt = reinterpret_cast<float *>(w + pp.dec + pp.dws.qt);
+        float *qh = reinterpret_cast<float *>(w + pp.dec + pp.dws.qh);
+        st = absorb_launch(stream, &pp.dv, q_nope, q_rope, M, vp.len, rope_tab, rope_max_pos,
+                           scale * LOG2E, qt, qh, sms, &vr, false, o);
+        if (st != GVA_OK) return st;
+        PrefillMmaParams mp;
+        mp.B = d->B;
+        mp.n = n;
+        mp.H = d->H;
+        mp.G = d->G;
+        mp.r = d->H / d->G;
+        mp.L0 = L0;
+        mp.R = to_dev(R);
+        mp.V = cache->V;
+        mp.Kr = cache->K_rope;
+        mp.qt = qt;
+        mp.qh = qh;
+        mp.part_o = reinterpret_cast<float *>(w + pp.po);
+        mp.part_ml = reinterpret_cast<float *>(w + pp.pml);
+        mp.out = out;
+        mp.lse = lse;
+        mp.splits = pp.mp.splits;
+        mp.wpg = pp.mp.wpg;
+        mp.rows_pad = pp.mp.rows_pad;
+        mp.vpitch = pp.mp.vpitch;
+        mp.stage_bytes = pp.mp.stage_bytes;
+        const cudaError_t e = d->d_h == 64 ? prefill_launch_dh<64>(stream, d->d_r, pp.mp, mp)
+                                           : prefill_launch_dh<128>(stream, d->d_r, pp.mp, mp);
+        return cuda_status(e);
+    }
     gva_cache vc;
     vc.rows = vr;
     vc.V = cache->V;
