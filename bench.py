@@ -549,10 +549,14 @@ def run_prefill(args, dist: Dist):
             "achieved_tflops": round(tflops, 3),
             "tensor_frac_of_bf16_peak": round(tflops / tc_peak, 5) if tc_peak else None,
             "l2": f"inputs larger than L2: {nl} distinct layer caches", "path": path,
-            "design": "each new token is one entry of a decode batch of B*n entries over a "
-                      "paged view of the cache (history re-read per query, mostly from L2)"},
+            "design": ("tensor-core prefill kernel: each 16-token slab of a sequence's rows "
+                       "loaded once per CTA and scored against all the chunk's (query, head) "
+                       "rows, split over the history and merged by log-sum-exp"
+                       if path == "auto" and w.cache_dtype == "bf16" and w.d_h in (64, 128)
+                       else "each new token run as one entry of a decode batch of B*n entries "
+                            "over a paged view of the cache")},
         "roofline": {"bound": "hbm", "kernel": "gva_prefill_attention (view + append + absorb + "
-                     "split-K partial + combine), per call", "achieved": round(gbs, 1),
+                     "prefill partial + combine), per call", "achieved": round(gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                      "peak_source": "measured" if peaks else "fallback", "traffic": None},
         "cpu_baseline": cpu,

@@ -24,7 +24,7 @@
 
 namespace gva {
 
-constexpr int PF_STAGES = 4;
+constexpr int PF_STAGES = 6;
 constexpr int PF_SMEM_LIMIT = 227 * 1024;
 
 struct PrefillMmaParams {
@@ -197,9 +197,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) prefill_mma_kernel(const Prefil
         const long long j0 = (s_begin + k) * SLAB;
         if (j0 > wlim) continue;   // no row of this warp sees any token of the slab
         const uint32_t sv = sbase + (k % PF_STAGES) * p.stage_bytes;
-        float s[2][4];
+        // the hi and lo query parts accumulate separately (two independent MMA chains
+        // per score tile), summed before the mask
+        float s[2][4], sl[2][4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+        for (int t = 0; t < 2; ++t) {
+            s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+            sl[t][0] = sl[t][1] = sl[t][2] = sl[t][3] = 0.f;
+        }
         // S = Q~ V_g^T: matrices (tokens 0-7 | 8-15) x (dims lo | hi) of a 16-dim step
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
@@ -207,9 +212,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) prefill_mma_kernel(const Prefil
             uint32_t b0, b1, b2, b3;
             ldsm_x4(sv + tok * p.vpitch + (g * DH + dim) * 2, b0, b1, b2, b3);
             mma16816(s[0], qhi[kk], b0, b1);
-            mma16816(s[0], qlo[kk], b0, b1);
+            mma16816(sl[0], qlo[kk], b0, b1);
             mma16816(s[1], qhi[kk], b2, b3);
-            mma16816(s[1], qlo[kk], b2, b3);
+            mma16816(sl[1], qlo[kk], b2, b3);
         }
         if (DR > 0) {
             const uint32_t sk = sv + SLAB * p.vpitch;
@@ -219,19 +224,26 @@ __global__ void __launch_bounds__(WARPS * 32, 1) prefill_mma_kernel(const Prefil
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(sk + tok * (DR * 2) + dim * 2, b0, b1, b2, b3);
                 mma16816(s[0], rhi[kk], b0, b1);
-                mma16816(s[0], rlo[kk], b0, b1);
+                mma16816(sl[0], rlo[kk], b0, b1);
                 mma16816(s[1], rhi[kk], b2, b3);
-                mma16816(s[1], rlo[kk], b2, b3);
+                mma16816(sl[1], rlo[kk], b2, b3);
             }
             if (KR8) {
                 const int tok = (mi & 1) * 8 + rr;
                 uint32_t b0, b1;
                 ldsm_x2(sk + tok * (DR * 2) + KR16 * 16 * 2, b0, b1);
                 mma1688(s[0], r8hi[0], r8hi[1], b0);
-                mma1688(s[0], r8lo[0], r8lo[1], b0);
+                mma1688(sl[0], r8lo[0], r8lo[1], b0);
                 mma1688(s[1], r8hi[0], r8hi[1], b1);
-                mma1688(s[1], r8lo[0], r8lo[1], b1);
+                mma1688(sl[1], r8lo[0], r8lo[1], b1);
             }
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            s[t][0] += sl[t][0];
+            s[t][1] += sl[t][1];
+            s[t][2] += sl[t][2];
+            s[t][3] += sl[t][3];
         }
         // causal mask: column (tile t, pair element e) is token j0 + 8t + 2tig + e
 #pragma unroll
@@ -310,7 +322,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) prefill_mma_kernel(const Prefil
     }
 }
 
-// Log-sum-exp merge of the slab ranges: one warp per (b, i, h).
+// Log-sum-exp merge of the slab ranges: one warp per (b, i, h).  The lanes read the
+// ranges' (max, sum) 32 at a time, so every load of a row is independent of the others.
 constexpr int PF_COMBINE_WARPS = 8;
 
 template <int DH>
@@ -326,24 +339,41 @@ __global__ void __launch_bounds__(PF_COMBINE_WARPS * 32)
     const int i = (int)(bi % p.n), b = (int)(bi / p.n);
     const int g = h / p.r;
     const long long prow = (long long)g * p.wpg * 16 + (long long)i * p.r + (h - g * p.r);
+    const long long at0 = (long long)b * p.splits * p.rows_pad + prow;   // range 0's row
     float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s)
-        M = fmaxf(M, p.part_ml[(((long long)b * p.splits + s) * p.rows_pad + prow) * 2]);
+    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+        const int s = s0 + lane;
+        if (s < p.splits) M = fmaxf(M, p.part_ml[(at0 + (long long)s * p.rows_pad) * 2]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[DH / 32];
 #pragma unroll
     for (int u = 0; u < DH / 32; ++u) acc[u] = 0.f;
     float den = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < p.splits; ++s) {
-            const long long at = ((long long)b * p.splits + s) * p.rows_pad + prow;
-            const float m = p.part_ml[at * 2];
-            if (m == -INFINITY) continue;
-            const float w = exp2f(m - M);
-            den += w * p.part_ml[at * 2 + 1];
+        for (int s0 = 0; s0 < p.splits; s0 += 32) {
+            const int s = s0 + lane;
+            float w = 0.f;
+            if (s < p.splits) {
+                const float2 ml =
+                    *reinterpret_cast<const float2 *>(p.part_ml + (at0 + (long long)s * p.rows_pad) * 2);
+                w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+                den += w * ml.y;
+            }
+            const int cnt = min(32, p.splits - s0);
+#pragma unroll 4
+            for (int k = 0; k < cnt; ++k) {
+                // a range whose rows saw nothing wrote zeros, so its weight 0 adds 0
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                const float *src = p.part_o + (at0 + (long long)(s0 + k) * p.rows_pad) * DH;
 #pragma unroll
-            for (int u = 0; u < DH / 32; ++u) acc[u] += w * p.part_o[at * DH + lane + 32 * u];
+                for (int u = 0; u < DH / 32; ++u) acc[u] += wk * src[lane + 32 * u];
+            }
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     float *dst = p.out + row * DH;
 #pragma unroll
     for (int u = 0; u < DH / 32; ++u) dst[lane + 32 * u] = den > 0.f ? acc[u] / den : 0.f;
