@@ -237,9 +237,11 @@ size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *r
  *   out[b,i,h,:] (device fp32 [B][n][H][d_h]), lse[b,i,h] (device fp32 [B][n][H] or NULL).
  * q_nope [B][n][H][d_n], q_rope [B][n][H][d_r] (q_dtype); M, rope_tab, scale and opts
  * as in gva_decode_attention_ex.  L0 is not updated (the caller adds n).
- * Each query is run as one entry of a decode batch of B*n entries that read sequence
- * b's rows (a paged view of the cache; the cached history is read once per query,
- * the repeats mostly from L2).
+ * Paths: GVA_PATH_AUTO runs, for bf16 caches with d_h 64 or 128, a tensor-core prefill
+ * kernel that loads each 16-token slab of a sequence's rows once and scores it against
+ * all of the chunk's queries (split over the history, merged by log-sum-exp); every
+ * other case, and GVA_PATH_SIMT / _MMA / _FUSED, runs each query as one entry of a
+ * decode batch of B*n entries reading sequence b's rows (a paged view of the cache).
  * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged returns
  * GVA_ERR_UNSUPPORTED.  B*n <= 4096 (else GVA_ERR_ARG).  Workspace: device, 256-byte
  * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), zero-filled once as

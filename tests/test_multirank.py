@@ -71,3 +71,17 @@ def test_algorithmic_bytes_match_cache_count():
     assert bench.gqa_bytes(w, [4096] * 8) == 8 * oracle.n_gqa(4096, 4, 64) * 2
     wl = workload("long")
     assert bench.algorithmic_bytes(wl, [131072] * 2) == 545259520
+
+
+def test_prefill_work_counts_by_brute_force():
+    """The prefill line's algorithmic work: every row of history and chunk read once, and
+    H (2 d_h + d_r) multiply-adds for each (query, visible token) pair, counted here by
+    enumerating the causal pairs."""
+    import bench
+    from gva_inputs import workload
+    w = workload("350m")
+    L0, n = [4080, 0, 17], 16
+    nbytes, flops = bench.prefill_work(w, L0, n)
+    assert nbytes == sum(l0 + n for l0 in L0) * (w.G * w.d_h + w.d_r) * 2
+    pairs = sum(1 for l0 in L0 for i in range(n) for j in range(l0 + n) if j <= l0 + i)
+    assert flops == 2 * w.H * (2 * w.d_h + w.d_r) * pairs

@@ -312,7 +312,9 @@ def gva_prefill_attention(dims: Dims, q_nope, q_rope, M, L0, v_new, k_rope_new, 
     """gva_prefill_attention: append the chunk q_nope.shape[1] = n tokens per sequence
     after L0[b] cached ones, then causal attention of each new token (q_nope
     [B, n, H, d_n], v_new [B, n, G, d_h], k_rope_new [B, n, d_r], out [B, n, H, d_h],
-    lse [B, n, H]; q_norm as in _opts)."""
+    lse [B, n, H]; q_norm as in _opts).  path "auto" takes the tensor-core prefill
+    kernel where it applies; "simt", "mma" and "fused" run each query as a decode
+    entry."""
     d = dims.c()
     cc = cache.c()
     o = _opts(path, num_ctas, q_norm)
