@@ -219,3 +219,18 @@ def test_prefill_paths_agree_on_a_paged_batch():
         out, lse = r.got()
         assert_close(out, refs[0][0], "bf16", f"{path} out")
         assert_close(lse, refs[0][1], "bf16", f"{path} lse")
+
+
+def test_prefill_full_size_350m():
+    """The bench's prefill workload in its launch configuration (350M layer, B = 8,
+    T = 4096, the last 16 tokens of every sequence as the chunk, default path), every
+    output against the oracle."""
+    c = make_case(workload("350m"))
+    r = Run(c, 16)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, "bf16", "350m full size")
+    assert_close(lse, ref_lse, "bf16", "350m full size lse")
