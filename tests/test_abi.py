@@ -170,3 +170,16 @@ def test_prefill_arguments_rejected_before_cuda(gva):
     assert call(contig, 2049) == gva.GVA_ERR_ARG          # B = 2: 4098 entries
     for rows in (contig, gva.gva_rows(1, 640, 0, fake, None, 0, 0)):
         assert lib.gva_prefill_workspace_size(ctypes.byref(d), 0, ctypes.byref(rows)) == 0
+
+
+def test_plain_c_consumer(gva, tmp_path):
+    """libgva.so as a C library: a C program that includes only include/gva.h, compiled
+    with gcc and linked against the library, runs its host-only checks."""
+    src = os.path.join(ROOT, "tests", "c", "abi_host_check.c")
+    exe = str(tmp_path / "abi_host_check")
+    libdir = os.path.dirname(gva.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    src, "-o", exe, "-L", libdir, "-lgva", "-Wl,-rpath," + libdir, "-lm"],
+                   check=True, capture_output=True, text=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
