@@ -76,7 +76,8 @@ typedef enum {
 } gva_layout;
 
 /* Problem shape.  Supported: H % G == 0 with r = H/G in 1..8; d_h in {32, 64, 128};
- * d_n in 8..256, a multiple of 8; d_r in {0, 8, 16, 24, 32}; 1 <= B <= 4096. */
+ * H * d_h <= 4096; d_n in 8..256, a multiple of 8; d_r in {0, 8, 16, 24, 32};
+ * 1 <= B <= 4096; cache_dtype and q_dtype each GVA_F32 or GVA_BF16. */
 typedef struct {
     int B;            /* sequences in the batch */
     int H;            /* query heads */

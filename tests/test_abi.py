@@ -183,3 +183,62 @@ def test_plain_c_consumer(gva, tmp_path):
                    check=True, capture_output=True, text=True)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def _documented_valid(B, H, G, d_h, d_n, d_r, cd, qd):
+    """The support matrix include/gva.h states for gva_dims."""
+    return (1 <= B <= 4096 and H >= 1 and G >= 1 and H % G == 0 and H // G <= 8
+            and d_h in (32, 64, 128) and H * d_h <= 4096 and 8 <= d_n <= 256
+            and d_n % 8 == 0 and d_r in (0, 8, 16, 24, 32) and cd in (0, 1) and qd in (0, 1))
+
+
+def test_dims_validation_follows_the_header(gva):
+    """Random shapes: the library refuses exactly those the header's support matrix
+    excludes.  The probe is gva_prefill_attention on a ragged cache, which returns
+    before any CUDA call either way: GVA_ERR_ARG for unsupported dims,
+    GVA_ERR_UNSUPPORTED (ragged layouts are not taken) for supported ones."""
+    from hypothesis import given, settings, strategies as st
+
+    lib = gva._lib
+    fake = ctypes.c_void_p(0x10000)
+    rag = gva.gva_cache(gva.gva_rows(1, 640, 0, fake, None, 0, 0), fake, fake)
+
+    seen = {gva.GVA_ERR_ARG: 0, gva.GVA_ERR_UNSUPPORTED: 0}
+
+    # a supported shape, then zero, one or two fields replaced by values drawn from a
+    # wider range (often unsupported), so that both outcomes are common
+    wide = dict(B=st.sampled_from([-1, 0, 4097, 5000, 1, 4096]), G=st.integers(0, 20),
+                r=st.sampled_from([0, 9, 10, 1, 8]), skew=st.just(1),
+                d_h=st.sampled_from([16, 48, 96, 256, 32, 128]),
+                d_n=st.sampled_from([-8, 0, 4, 12, 257, 264, 8, 256]),
+                d_r=st.sampled_from([-8, 2, 12, 40, 0, 32]), cd=st.just(2), qd=st.just(2))
+
+    @st.composite
+    def shapes(draw):
+        v = dict(B=draw(st.integers(1, 4096)), G=draw(st.integers(1, 8)),
+                 r=draw(st.integers(1, 8)), skew=0,
+                 d_h=draw(st.sampled_from([32, 64, 128])),
+                 d_n=8 * draw(st.integers(1, 32)),
+                 d_r=draw(st.sampled_from([0, 8, 16, 24, 32])),
+                 cd=draw(st.sampled_from([0, 1])), qd=draw(st.sampled_from([0, 1])))
+        for k in draw(st.lists(st.sampled_from(sorted(wide)), max_size=2)):
+            v[k] = draw(wide[k])
+        return v
+
+    @settings(max_examples=600, deadline=None, derandomize=True)
+    @given(v=shapes())
+    def check(v):
+        B, G, r, skew, d_h, d_n, d_r, cd, qd = (v[k] for k in ("B", "G", "r", "skew", "d_h",
+                                                               "d_n", "d_r", "cd", "qd"))
+        H = G * r + skew                  # skew 1 usually breaks H % G == 0
+        d = gva.gva_dims(B, H, G, d_h, d_n, d_r, cd, qd)
+        st_ = lib.gva_prefill_attention(None, ctypes.byref(d), 1, fake, fake, fake, fake, fake,
+                                        fake, ctypes.byref(rag), fake, 100, ctypes.c_float(0.1),
+                                        fake, None, fake, ctypes.c_size_t(1 << 30), None)
+        want = gva.GVA_ERR_UNSUPPORTED if _documented_valid(B, H, G, d_h, d_n, d_r, cd, qd) \
+            else gva.GVA_ERR_ARG
+        assert st_ == want, (B, H, G, d_h, d_n, d_r, cd, qd, st_)
+        seen[want] += 1
+
+    check()
+    assert seen[gva.GVA_ERR_UNSUPPORTED] >= 20 and seen[gva.GVA_ERR_ARG] >= 20, seen
