@@ -229,7 +229,8 @@ int gva_decode_attention_ex(void *stream, const gva_dims *dims, const void *q_no
 size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *rows);
 
 /* Causal chunked prefill ([K] §1: every new token attends to the cached history and to
- * the chunk up to and including itself; [A] 关键技巧一/二 for the scores).  Sequence b
+ * the chunk up to and including itself; [K] §6.1: the chunk's tokens enter together and
+ * a group's query heads share its rows; [A] 关键技巧一/二 for the scores).  Sequence b
  * holds L0[b] tokens (device int [B]); its n new tokens go to positions
  * p = L0[b] + i, i < n.  The call appends all of them, exactly as gva_append_cache
  * would one by one (v_new device fp32 [B][n][G][d_h], k_rope_new device fp32

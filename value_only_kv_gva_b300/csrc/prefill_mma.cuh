@@ -2,10 +2,12 @@
 //
 // Every new token of a chunk attends to the cached history and to the chunk up to and
 // including itself (MQA/GQA page §1; GVA analysis page, 关键技巧一/二 for the scores:
-// z = q~_h . v_{j,g(h)} + q^_h . k_rope_j).  Unlike a decode, all n queries of a
-// sequence read the same rows, so a CTA loads each 16-token slab of the rows once and
-// scores it against every query row it holds: the chunk's (query, head) pairs of one
-// value group are the MMA rows (16 per warp), the slab's tokens the columns.
+// z = q~_h . v_{j,g(h)} + q^_h . k_rope_j).  The prompt's tokens enter together and a
+// group's query heads share its cached rows without copying them (MQA/GQA page §6.1).
+// Unlike a decode, all n queries of a sequence read the same rows, so a CTA loads each
+// 16-token slab of the rows once and scores it against every query row it holds: the
+// chunk's (query, head) pairs of one value group are the MMA rows (16 per warp), the
+// slab's tokens the columns.
 //
 // Per slab and warp: S[16 x 16] = Q~ V_g^T (+ Q^ K_rope^T), a causal mask (token j is
 // visible to the query at position p when j <= p), an online softmax in log2 units,
