@@ -404,6 +404,9 @@ def run_prefill(args, dist: Dist):
     torch.cuda.set_device(dev)
     dist.init("nccl")
     w = gva_inputs.workload(args.workload)
+    if w.layout == "ragged":
+        raise SystemExit("--prefill takes contiguous or paged caches (gva_prefill_attention "
+                         "refuses ragged layouts)")
     c = gva_inputs.make_case(w)
     n = args.prefill
     ch = gva_inputs.make_prefill_chunk(c, n)
