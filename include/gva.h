@@ -270,21 +270,23 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *dims, const void *q,
 #define GVA_STATIC_SCRATCH_BYTES (24u << 20)
 
 /* gva_decode_attention without a caller-provided workspace, for callers that cannot
- * allocate device memory where they decode: code recording a CUDA graph (allocations
- * are refused while a stream is being captured), plugins or embedded runtimes given no
- * allocator or scratch buffer, and latency-critical loops that forbid allocator calls
- * because those can block or synchronise the device.  The source pages have no
- * counterpart to this entry point; it exists for deployment only.
+ * allocate device memory where they decode: plugins or embedded runtimes handed no
+ * allocator and no scratch buffer, engines whose device memory is planned once at
+ * start-up and may not grow afterwards, and latency-critical loops that forbid
+ * allocator calls because those can block or synchronise the device.  The source pages
+ * have no counterpart to this entry point; it exists for deployment only.
  *   - Scratch is one fixed array of GVA_STATIC_SCRATCH_BYTES in device memory, held by
  *     every GPU that loads the library until the process exits.  Shapes whose
  *     workspace (gva_decode_workspace_size) exceeds it return GVA_ERR_WORKSPACE.
  *   - Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device resolves the array's device address (set-up); make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  `stream` must belong to the current
+ *     device (else GVA_ERR_CUDA).
  *   - Every call on a device shares the one array, and its contents persist from the
- *     previous call.  No part of it needs to start at zero: each call writes every
- *     scratch value it later reads.  Calls that may overlap on the GPU (different
- *     streams, or work not ordered by the caller) race on the array; order them.
+ *     previous call.  No part of it needs to start at zero: the call always takes the
+ *     automatic path, which writes every scratch value before reading it.  Calls that
+ *     may overlap on the GPU (different streams, or work not ordered by the caller)
+ *     race on the array; order them.
  * Arguments, outputs and errors otherwise as gva_decode_attention. */
 int gva_decode_attention_static(void *stream, const gva_dims *dims, const void *q_nope,
                                 const void *q_rope, const float *M, const int *seq_len,

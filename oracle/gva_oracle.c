@@ -18,7 +18,7 @@
  * no blocking, no fusion, no online softmax.  All floating point is double except
  * the append path, whose stored bf16/fp32 code is decided in fp32 (see od_append).
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings taken where the pages are silent:
  *   - RoPE pairs are interleaved (x[2i], x[2i+1]), theta_i = base^(-2i/d_r),
  *     angle = p * theta_i with 0-based position p; Rot(p): y0 = x0 c - x1 s,
  *     y1 = x0 s + x1 c.  ([A] "关键技巧二" names only the relative rotation R_{j-t}.)
@@ -334,10 +334,10 @@ void od_gva_decode_explicit(int B, int H, int G, int d_h, int d_n, int d_r,
 /* ------------------------------------------------------------------------- */
 /* GVA with ordinary RoPE on the reconstructed key (the non-absorbable variant) */
 /* ------------------------------------------------------------------------- */
-/* [S] (results discussion): the scale-matched row "still applies ordinary RoPE to
- * the reconstructed key and cannot absorb M"; [A] 关键技巧二: the relative rotation
+/* [S] (results discussion): the scale-matched row rotates the rebuilt key itself with
+ * plain RoPE, so M cannot be folded into the query there; [A] 关键技巧二: the relative rotation
  * R_{j-t} sits between q and M^T, so no single transformed query serves every cached
- * position.  Reading (listed in the design notes): the key of token j for head h is
+ * position.  The pages give no formula; the reading taken: the key of token j for head h is
  * K_h[j] = v_{j,g(h)} M_h (width d_n), rotated by its own position j; the query q_h
  * (width d_n, the whole query) is rotated by t = L_b - 1 with the same pairing;
  *   z_j = scale * (Rot(t) q_h) . (Rot(j) K_h[j]),   out = softmax(z) V_g (unrotated);
@@ -392,7 +392,7 @@ void od_gva_decode_rope_keys(int B, int H, int G, int d_h, int d_n, const double
  *   K_h[j] = c_j Wuk_h  (Wuk_h in R^{d_c x d_n}),   V_h[j] = c_j Wuv_h  (Wuv_h in R^{d_c x d_h})
  *   key_j = [K_h[j] ; k_rope_j],  query = [q_nope ; Rot(t) q_rope],  t = L_b - 1
  *   z_j = scale * query . key_j,  out[b,h] = sum_j softmax(z)_j V_h[j],  lse = logsumexp(z)
- * Reading (listed in the design notes): the positional key is one shared stream
+ * The reading taken where the pages differ: the positional key is one shared stream
  * ([A]; [C] describes per-head positional keys, which is DeepSeek's MLA, not the
  * T(d_c + d_r) count the GVA pages compare with). */
 void od_mla_decode(int B, int H, int d_c, int d_n, int d_h, int d_r, const double *q_nope,

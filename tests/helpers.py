@@ -90,11 +90,19 @@ class Dev:
         return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
+def oracle_table(c: Case, max_pos: int) -> np.ndarray:
+    """The oracle's own fp32 (cos, sin) table, built by the oracle (not the library)."""
+    return oracle.rope_table_f32(int(max_pos), c.w.d_r, c.w.base)
+
+
 def oracle_append(c: Case, pos, tab_h: torch.Tensor):
-    """Host copies of the cache storage with the oracle's append applied."""
+    """Host copies of the cache storage with the oracle's append applied.  The oracle
+    builds its own rotation table (as many positions as the library's table `tab_h`,
+    whose length only bounds which positions are valid)."""
     V = oracle._np(c.V).copy()
     K = oracle._np(c.Kr).copy()
-    oracle.append(c.v_new, c.k_new, pos, oracle_rows(c), V, K, tab_h.numpy())
+    oracle.append(c.v_new, c.k_new, pos, oracle_rows(c), V, K,
+                  oracle_table(c, int(tab_h.shape[0])))
     return V, K
 
 

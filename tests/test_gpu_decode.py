@@ -263,6 +263,37 @@ def test_host_argument_errors():
     assert e.value.status == g.GVA_ERR_UNSUPPORTED
 
 
+def test_binding_refuses_undersized_tensors():
+    """The binding checks every tensor against what the C call touches and raises
+    GVA_ERR_ARG before any launch (the C ABI sees plain pointers, not sizes)."""
+    c = make_case(workload("350m", T=32, B=2))
+    D = Dev(c)
+    g = gva()
+    w = c.w
+    out = torch.empty((w.B, w.H, w.d_h), device="cuda")
+    cases = {
+        "out": dict(out=out[:, :, :8].contiguous()),
+        "q_nope": dict(q_nope=D.q_nope[:1].contiguous()),
+        "M": dict(M=D.M[:3].contiguous()),
+        "seq_len": dict(seq_len=D.seq_len[:1].contiguous()),
+        "V": dict(cache=g.Cache(D.rows, D.V[:5].contiguous(), D.Kr)),
+        "K_rope dtype": dict(cache=g.Cache(D.rows, D.V, D.Kr.float())),
+    }
+    for what, over in cases.items():
+        a = dict(q_nope=D.q_nope, M=D.M, seq_len=D.seq_len, cache=D.cache, out=out)
+        a.update(over)
+        with pytest.raises(g.GvaError) as e:
+            g.gva_decode_attention(D.dims, a["q_nope"], D.q_rope, a["M"], a["seq_len"],
+                                   a["cache"], D.tab, w.scale, a["out"], None, D.ws)
+        assert e.value.status == g.GVA_ERR_ARG, what
+    with pytest.raises(g.GvaError) as e:
+        g.gva_append_cache(D.dims, D.v_new[:1].contiguous(), D.k_new,
+                           torch.zeros(2, dtype=torch.int32, device="cuda"), None, D.cache, D.tab)
+    assert e.value.status == g.GVA_ERR_ARG
+    torch.cuda.synchronize()
+    assert g.gva_get_device_status() == 0
+
+
 # --------------------------------------------------------------------------- #
 # GQA comparator
 # --------------------------------------------------------------------------- #

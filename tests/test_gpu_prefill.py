@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from gva_inputs import make_case, make_prefill_chunk, workload
-from helpers import assert_close, dims_of, gva, oracle_rows, rope_tab
+from helpers import assert_close, dims_of, gva, oracle_rows, oracle_table, rope_tab
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,7 @@ class Run:
         R = oracle_rows(c)
         for i in range(n):
             oracle.append(ch.v_new[:, i], ch.k_new[:, i], ch.L0.to(torch.int64) + i, R, Vh, Kh,
-                          self.tab_h.numpy())
+                          oracle_table(c, int(self.tab_h.shape[0])))
         return Vh, Kh
 
     def oracle_out(self, Vh, Kh, q_nope=None, n=None):
@@ -163,7 +163,7 @@ def test_prefill_past_capacity_is_reported():
     seq1 = oracle.Rows("ragged", offsets=np.array([c.T_cap, 2 * c.T_cap]))
     for i in range(4, 8):
         oracle.append(r.ch.v_new[1:, i], r.ch.k_new[1:, i], [22 + i], seq1, Vh, Kh,
-                      r.tab_h.numpy())
+                      oracle_table(c, int(r.tab_h.shape[0])))
     _check_cache(r, Vh, Kh)
     out, lse = r.got()
     ref, ref_lse = r.oracle_out(Vh, Kh, n=4)

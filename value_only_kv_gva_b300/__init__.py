@@ -139,6 +139,55 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+_ELEM_DT = {GVA_F32: torch.float32, GVA_BF16: torch.bfloat16}
+
+
+def _need(t, n: int, what: str, dtype=None) -> None:
+    """The C call reads or writes n elements of `t`: refuse a smaller tensor (or one of
+    another dtype than the dims declare) before any device memory is touched."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise GvaError(GVA_ERR_ARG, f"{what}: dtype {t.dtype}, the dims declare {dtype}")
+    if t.numel() < n:
+        raise GvaError(GVA_ERR_ARG, f"{what}: {t.numel()} elements, the call touches {n}")
+
+
+def _check_rows(rows, B: int) -> None:
+    if rows.offsets is not None:
+        _need(rows.offsets, B + 1, "offsets")
+    if rows.block_table is not None and rows.block_table.shape[0] < B:
+        raise GvaError(GVA_ERR_ARG, f"block_table: {rows.block_table.shape[0]} rows < B = {B}")
+
+
+def _check_cache(dims, cache) -> None:
+    """V [num_rows, G, d_h] and K_rope [num_rows, d_r] in the cache dtype."""
+    n = int(cache.rows.num_rows)
+    _need(cache.V, n * dims.G * dims.d_h, "V", _ELEM_DT.get(dims.cache_dtype))
+    if dims.d_r:
+        _need(cache.K_rope, n * dims.d_r, "K_rope", _ELEM_DT.get(dims.cache_dtype))
+    _check_rows(cache.rows, dims.B)
+
+
+def _check_tab(rope_tab, d_r: int) -> None:
+    if d_r and rope_tab is not None:
+        _need(rope_tab, int(rope_tab.shape[0]) * d_r, "rope_tab")
+
+
+def _check_decode(dims, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse, per=1) -> None:
+    """Sizes a GVA decode (per = 1) or a prefill of `per` queries per sequence touches."""
+    B, H, qd = dims.B, dims.H, _ELEM_DT.get(dims.q_dtype)
+    _need(q_nope, B * per * H * dims.d_n, "q_nope", qd)
+    if dims.d_r:
+        _need(q_rope, B * per * H * dims.d_r, "q_rope", qd)
+    _need(M, H * dims.d_h * dims.d_n, "M")
+    _need(seq_len, B, "seq_len")
+    _check_cache(dims, cache)
+    _check_tab(rope_tab, dims.d_r)
+    _need(out, B * per * H * dims.d_h, "out")
+    _need(lse, B * per * H, "lse")
+
+
 # --------------------------------------------------------------------------- #
 # argument holders
 # --------------------------------------------------------------------------- #
@@ -255,6 +304,15 @@ def gva_absorb_query(dims: Dims, q_nope, q_rope, M, seq_len, rope_tab, scale: fl
     """gva_absorb_query / gva_absorb_query_ex (q_norm as in _opts)."""
     d = dims.c()
     o = _opts("auto", 0, q_norm)
+    B, H, qd = dims.B, dims.H, _ELEM_DT.get(dims.q_dtype)
+    _need(q_nope, B * H * dims.d_n, "q_nope", qd)
+    if dims.d_r:
+        _need(q_rope, B * H * dims.d_r, "q_rope", qd)
+        _need(q_rope_rot, B * H * dims.d_r, "q_rope_rot")
+    _need(M, H * dims.d_h * dims.d_n, "M")
+    _need(seq_len, B, "seq_len")
+    _check_tab(rope_tab, dims.d_r)
+    _need(q_tilde, B * H * dims.d_h, "q_tilde")
     _check(_lib.gva_absorb_query_ex(
         _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
         _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
@@ -266,10 +324,22 @@ def gva_absorb_query(dims: Dims, q_nope, q_rope, M, seq_len, rope_tab, scale: fl
         ctypes.byref(o)), "gva_absorb_query")
 
 
+def _check_append(dims, v_new, k_rope_new, pos, seq_len_out, cache, rope_tab) -> None:
+    B = dims.B
+    _need(v_new, B * dims.G * dims.d_h, "v_new")
+    if dims.d_r:
+        _need(k_rope_new, B * dims.d_r, "k_rope_new")
+    _need(pos, B, "pos")
+    _need(seq_len_out, B, "seq_len_out")
+    _check_cache(dims, cache)
+    _check_tab(rope_tab, dims.d_r)
+
+
 def gva_append_cache(dims: Dims, v_new, k_rope_new, pos, seq_len_out, cache: Cache,
                      rope_tab, stream=None) -> None:
     d = dims.c()
     cc = cache.c()
+    _check_append(dims, v_new, k_rope_new, pos, seq_len_out, cache, rope_tab)
     _check(_lib.gva_append_cache(
         _stream(stream), ctypes.byref(d), _ptr(v_new, torch.float32, "v_new"),
         _ptr(k_rope_new, torch.float32, "k_rope_new") if dims.d_r else None,
@@ -290,6 +360,7 @@ def gva_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, r
     d = dims.c()
     cc = cache.c()
     o = _opts(path, num_ctas, q_norm)
+    _check_decode(dims, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse)
     _check(_lib.gva_decode_attention_ex(
         _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
         _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
@@ -319,6 +390,10 @@ def gva_prefill_attention(dims: Dims, q_nope, q_rope, M, L0, v_new, k_rope_new, 
     cc = cache.c()
     o = _opts(path, num_ctas, q_norm)
     n = int(q_nope.shape[1])
+    _check_decode(dims, q_nope, q_rope, M, L0, cache, rope_tab, out, lse, per=n)
+    _need(v_new, dims.B * n * dims.G * dims.d_h, "v_new")
+    if dims.d_r:
+        _need(k_rope_new, dims.B * n * dims.d_r, "k_rope_new")
     _check(_lib.gva_prefill_attention(
         _stream(stream), ctypes.byref(d), n, _ptr(q_nope, None, "q_nope"),
         _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
@@ -348,6 +423,7 @@ def prepare_append_cache(dims: Dims, v_new, k_rope_new, pos, seq_len_out, cache:
                          rope_tab, stream=None) -> PreparedCall:
     """gva_append_cache with fixed arguments (see PreparedCall)."""
     d, cc = dims.c(), cache.c()
+    _check_append(dims, v_new, k_rope_new, pos, seq_len_out, cache, rope_tab)
     args = (_stream(stream), ctypes.byref(d), _ptr(v_new, torch.float32, "v_new"),
             _ptr(k_rope_new, torch.float32, "k_rope_new") if dims.d_r else None,
             _ptr(pos, torch.int32, "pos"), _ptr(seq_len_out, torch.int32, "seq_len_out"),
@@ -362,6 +438,7 @@ def prepare_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cach
                              num_ctas: int = 0, stream=None, q_norm=None) -> PreparedCall:
     """gva_decode_attention(_ex) with fixed arguments (see PreparedCall)."""
     d, cc, o = dims.c(), cache.c(), _opts(path, num_ctas, q_norm)
+    _check_decode(dims, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse)
     args = (_stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
             _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),
             _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc),
@@ -381,6 +458,14 @@ def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: floa
     d = dims.c()
     cc = cache.c()
     o = _opts(path, num_ctas)
+    B, H, n = dims.B, dims.H, int(cache.rows.num_rows)
+    _need(q, B * H * dims.d_h, "q", _ELEM_DT.get(dims.q_dtype))
+    _need(seq_len, B, "seq_len")
+    _need(cache.K, n * dims.G * dims.d_h, "K", _ELEM_DT.get(dims.cache_dtype))
+    _need(cache.V, n * dims.G * dims.d_h, "V", _ELEM_DT.get(dims.cache_dtype))
+    _check_rows(cache.rows, B)
+    _need(out, B * H * dims.d_h, "out")
+    _need(lse, B * H, "lse")
     _check(_lib.gva_gqa_decode_attention(
         _stream(stream), ctypes.byref(d), _ptr(q, None, "q"),
         _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc), float(scale),
@@ -395,6 +480,7 @@ def gva_decode_attention_static(dims: Dims, q_nope, q_rope, M, seq_len, cache: C
     library's fixed device scratch array stands in for the workspace (see gva.h)."""
     d = dims.c()
     cc = cache.c()
+    _check_decode(dims, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse)
     _check(_lib.gva_decode_attention_static(
         _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
         _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(M, torch.float32, "M"),

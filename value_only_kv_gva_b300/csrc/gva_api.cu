@@ -804,11 +804,11 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
 // Decode without a caller-provided workspace.
 //
 // For callers that cannot allocate device memory at the point where they decode:
-// code running while a stream is being captured into a CUDA graph (allocation calls
-// are refused there), plugins and embedded runtimes that are handed no allocator or
-// scratch buffer, and latency-critical loops that forbid allocator calls because they
-// can block or synchronise the device.  The scratch lives in one fixed-size array in
-// device memory that every GPU loading this library holds until the process exits.
+// plugins and embedded runtimes that are handed no allocator and no scratch buffer,
+// engines whose device memory is planned once at start-up and may not grow, and
+// latency-critical loops that forbid allocator calls because those can block or
+// synchronise the device.  The scratch lives in one fixed-size array in device memory
+// that every GPU loading this library holds until the process exits.
 // ---------------------------------------------------------------------------- //
 static __device__ __align__(256) unsigned char g_static_scratch[GVA_STATIC_SCRATCH_BYTES];
 
@@ -818,12 +818,8 @@ static std::mutex g_static_scratch_mu;
 // Resolve the array's device address once per device, with that device current.
 // Host code must not hand `g_static_scratch` itself to a kernel: on the host the name
 // is a stand-in, not a device address.
-static void *static_scratch_for_current_device() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
-        cudaGetLastError();
-        return nullptr;
-    }
+static void *static_scratch_for_device(int dev) {
+    if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
     std::lock_guard<std::mutex> lk(g_static_scratch_mu);
     if (!g_static_scratch_ptr[dev]) {
         void *ptr = nullptr;
@@ -844,11 +840,27 @@ int gva_decode_attention_static(void *stream, const gva_dims *d, const void *q_n
                                 float scale, float *out, float *lse) {
     if (!dims_ok(d, true)) return GVA_ERR_ARG;
     if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && stream != nullptr) {
+        // the scratch handed to the kernels must be the stream's device's own copy
+        int sdev = -1;
+        e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+        if (e == cudaSuccess && sdev != dev) e = cudaErrorInvalidDevice;
+    }
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        cudaGetLastError();
+        return GVA_ERR_CUDA;
+    }
     const size_t need = gva_decode_workspace_size(d);
     if (need == 0) return GVA_ERR_CUDA;
     if (need > (size_t)GVA_STATIC_SCRATCH_BYTES) return GVA_ERR_WORKSPACE;  // beyond the fixed maximum
-    void *ws = static_scratch_for_current_device();
+    void *ws = static_scratch_for_device(dev);
     if (!ws) return GVA_ERR_CUDA;
+    // opts = NULL: the automatic path, which takes the separate-kernel decode; it
+    // writes every scratch value before reading it, so nothing in the shared array
+    // has to start at zero (the fused path's tickets would, and it is never taken here)
     return gva_decode_attention_ex(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab,
                                    rope_max_pos, scale, out, lse, ws,
                                    (size_t)GVA_STATIC_SCRATCH_BYTES, nullptr);
