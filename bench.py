@@ -170,8 +170,168 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
+def default_layers(w) -> int:
+    """Layers per step: a layer smaller than L2 (126 MB) gets at least 32 distinct layer
+    caches and four times L2 in all; a larger layer is streamed from HBM on every call."""
+    c_bytes = (w.B * (w.T or sum(w.len_range) // 2)) * (w.G * w.d_h + w.d_r) * 2
+    n = max(1, min(64, math.ceil(4 * 126e6 / c_bytes)))
+    return max(32, n) if c_bytes < 126e6 else n
+
+
+def timed_graph(torch, dist, stream, graph, K, W, sampler=None):
+    """W untimed replays, then K timed replays of `graph` on `stream` (CUDA events at every
+    step boundary), barrier + synchronize on both sides.  Returns (seconds, per-step ms)."""
+    for _ in range(W):
+        graph.replay()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    if sampler:
+        sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for k in range(K):
+            graph.replay()
+            ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    dist.barrier()
+    steps = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+    return ev[0].elapsed_time(ev[K]) / 1e3, steps
+
+
+class LayerStack:
+    """`nl` layers of one workload on the device, each with its own cache, queries, maps
+    and new-token inputs (the seeded case, copied per layer)."""
+
+    def __init__(self, gva, torch, gva_inputs, name, nl, dev):
+        w = gva_inputs.workload(name)
+        c = gva_inputs.make_case(w)
+        self.w, self.c, self.nl, self.dev = w, c, nl, dev
+        self.lengths = c.seq_len.tolist()
+        self.dims = gva.Dims(w.B, w.H, w.G, w.d_h, w.d_n, w.d_r,
+                             gva.GVA_F32 if w.cache_dtype == "f32" else gva.GVA_BF16,
+                             gva.GVA_F32 if w.q_dtype == "f32" else gva.GVA_BF16)
+        V0, K0 = c.V.to(dev), c.Kr.to(dev)
+        self.V0 = V0
+        self.layers = []
+        for li in range(nl):
+            V = V0.clone() if li else V0
+            K = K0.clone() if li else K0
+            self.layers.append(dict(
+                cache=gva.Cache(self.rows(gva, V), V, K),
+                q_nope=c.q_nope.to(dev).clone(), q_rope=c.q_rope.to(dev).clone(),
+                M=c.M.to(dev).clone(), v_new=c.v_new.to(dev).clone(),
+                k_new=c.k_new.to(dev).clone(),
+                out=torch.empty((w.B, w.H, w.d_h), device=dev),
+                lse=torch.empty((w.B, w.H), device=dev)))
+        self.seq = c.seq_len.to(dev)
+        self.pos = (c.seq_len - 1).to(torch.int32).to(dev)
+        self.tab = gva.gva_rope_table_fill(int(max(self.lengths)) + 1, w.d_r, w.base).to(dev)
+        self.ws = gva.workspace(self.dims, dev)
+        self.bytes_layer = algorithmic_bytes(w, self.lengths)
+
+    def rows(self, gva, V):
+        c, w, dev = self.c, self.w, self.dev
+        offs = c.offsets.to(dev) if c.offsets is not None else None
+        bt = c.block_table.to(dev) if c.block_table is not None else None
+        return gva.Rows(w.layout, c.num_rows, T_cap=c.T_cap, offsets=offs, block_table=bt,
+                        page_size=w.page_size)
+
+
+def measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path, with_gqa):
+    """Layer step (append + decode) and decode op of every layer of stack S, each as one
+    CUDA graph, timed on `stream`; the matched GQA comparator when asked.  Returns the
+    workload's figures (microseconds per layer, GB/s, fraction of the measured copy peak)."""
+    w, nl = S.w, S.nl
+
+    def layer_step(L):
+        gva.gva_append_cache(S.dims, L["v_new"], L["k_new"], S.pos, None, L["cache"], S.tab)
+        gva.gva_decode_attention(S.dims, L["q_nope"], L["q_rope"], L["M"], S.seq, L["cache"],
+                                 S.tab, w.scale, L["out"], L["lse"], S.ws, path=path)
+
+    def decode_only(L):
+        gva.gva_decode_attention(S.dims, L["q_nope"], L["q_rope"], L["M"], S.seq, L["cache"],
+                                 S.tab, w.scale, L["out"], L["lse"], S.ws, path=path)
+
+    g_step = capture_list(torch, stream, S.layers, layer_step)
+    g_dec = capture_list(torch, stream, S.layers, decode_only)
+    assert gva.gva_get_device_status() == 0
+    soak_t = time.time()
+    while time.time() - soak_t < args.soak:
+        for _ in range(max(1, 64 // nl)):
+            g_step.replay()
+        torch.cuda.synchronize()
+    secs, step_ms = timed_graph(torch, dist, stream, g_step, args.steps, args.warmup, sampler)
+    max_secs = dist.max(secs, S.dev)
+    dsecs, dec_ms = timed_graph(torch, dist, stream, g_dec, args.steps, max(3, args.warmup))
+    dsecs = dist.max(dsecs, S.dev)
+    us_layer = max_secs / (args.steps * nl) * 1e6
+    us_decode = dsecs / (args.steps * nl) * 1e6
+    achieved = S.bytes_layer / (us_decode * 1e-6) / 1e9
+    peaks = measured_peaks()
+    hbm_peak = peaks["hbm_gbs"] if peaks else FALLBACK_HBM_GBS
+    out = {"layers": nl, "tokens_per_layer": int(sum(S.lengths)), "bytes_per_layer": S.bytes_layer,
+           "us_per_layer_step": round(us_layer, 3), "us_per_decode": round(us_decode, 3),
+           "median_of_steps": {"us_per_layer_step": round(statistics.median(step_ms) * 1e3 / nl, 3),
+                               "us_per_decode": round(statistics.median(dec_ms) * 1e3 / nl, 3),
+                               "reps": args.steps},
+           "layer_step_gbs": round(aggregate(S.bytes_layer * nl * args.steps * dist.world,
+                                             max_secs) / 1e9, 2),
+           "decode_gbs": round(achieved, 1), "decode_frac_of_measured_copy": round(achieved / hbm_peak, 4),
+           "seconds": max_secs}
+    del g_step, g_dec
+    if not with_gqa:
+        return out
+    if w.layout == "ragged":
+        # the graph replay of this comparator on the full ragged batch ended in a launch
+        # failure twice while the library was built (cause not found): it is not run
+        out["gqa_comparator"] = {"not_run": "ragged-layout comparator replay kept off the GPU "
+                                            "(unresolved launch failure)"}
+        return out
+    Kq0 = gva_inputs.make_gqa_keys(S.c).to(S.dev)
+    qq = gva_inputs.make_gqa_query(S.c).to(S.dev)
+    glayers = []
+    for li in range(nl):
+        glayers.append(dict(kv=gva.KVCache(S.rows(gva, S.V0), Kq0.clone() if li else Kq0,
+                                           S.layers[li]["cache"].V), q=qq.clone(),
+                            out=torch.empty((w.B, w.H, w.d_h), device=S.dev),
+                            lse=torch.empty((w.B, w.H), device=S.dev)))
+
+    def gqa_call(L):
+        gva.gva_gqa_decode_attention(S.dims, L["q"], S.seq, L["kv"], 1.0 / math.sqrt(w.d_h),
+                                     L["out"], L["lse"], S.ws, path=path)
+    gg = capture_list(torch, stream, glayers, gqa_call)
+    gsecs, _ = timed_graph(torch, dist, stream, gg, args.steps, max(3, args.warmup))
+    us_gqa = dist.max(gsecs, S.dev) / (args.steps * nl) * 1e6
+    gb = gqa_bytes(w, S.lengths)
+    out["gqa_comparator"] = {"us_per_layer": round(us_gqa, 3), "bytes_per_layer": gb,
+                             "gbs": round(gb / (us_gqa * 1e-6) / 1e9, 1),
+                             "gva_bytes_saved_pct": round(100 * (1 - S.bytes_layer / gb), 3),
+                             "gva_time_saved_pct": round(100 * (1 - us_decode / us_gqa), 1)}
+    del glayers, gg, Kq0
+    return out
+
+
+def single_pass_floor(gva, torch, dist, stream, dev, nbytes, nl, K, W):
+    """The fastest single pass over `nbytes` this GPU gives one kernel in the same launch
+    configuration as the decode op: `nl` distinct buffers of `nbytes` (more than L2 in
+    all), one read-probe launch each, captured in one CUDA graph.  Microseconds per pass
+    and GB/s."""
+    n16 = nbytes // 16 * 16
+    bufs = [torch.ones(n16 // 4, dtype=torch.int32, device=dev) for _ in range(nl)]
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    g = capture_list(torch, stream, bufs, lambda b: gva.gva_read_probe(b, sink, stream=stream))
+    secs, _ = timed_graph(torch, dist, stream, g, K, W)
+    us = dist.max(secs, dev) / (K * nl) * 1e6
+    del bufs, g
+    return {"us_per_pass": round(us, 3), "gbs": round(n16 / (us * 1e-6) / 1e9, 1),
+            "bytes": n16, "buffers": nl}
+
+
 def run_ours(args, dist: Dist):
-    import numpy as np
     import torch
 
     import gva_inputs
@@ -180,161 +340,69 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     dist.init("nccl")
-    w = gva_inputs.workload(args.workload)
-    c = gva_inputs.make_case(w)
-    lengths = c.seq_len.tolist()
-    nl = args.layers
-    dims = gva.Dims(w.B, w.H, w.G, w.d_h, w.d_n, w.d_r,
-                    gva.GVA_F32 if w.cache_dtype == "f32" else gva.GVA_BF16,
-                    gva.GVA_F32 if w.q_dtype == "f32" else gva.GVA_BF16)
-    log(f"[bench] workload {w.name}: B={w.B} H={w.H} G={w.G} d_h={w.d_h} d_r={w.d_r} "
-        f"tokens={sum(lengths)} layers={nl}")
-
-    # per-layer device state: every layer owns its cache and its new-token inputs
-    def dev_rows(V):
-        offs = c.offsets.to(dev) if c.offsets is not None else None
-        bt = c.block_table.to(dev) if c.block_table is not None else None
-        return gva.Rows(w.layout, c.num_rows, T_cap=c.T_cap, offsets=offs, block_table=bt,
-                        page_size=w.page_size)
-
-    V0, K0 = c.V.to(dev), c.Kr.to(dev)
-    layers = []
-    for li in range(nl):
-        V = V0.clone() if li else V0
-        K = K0.clone() if li else K0
-        layers.append(dict(
-            cache=gva.Cache(dev_rows(V), V, K),
-            q_nope=c.q_nope.to(dev).clone(), q_rope=c.q_rope.to(dev).clone(),
-            M=c.M.to(dev).clone(), v_new=c.v_new.to(dev).clone(), k_new=c.k_new.to(dev).clone(),
-            out=torch.empty((w.B, w.H, w.d_h), device=dev),
-            lse=torch.empty((w.B, w.H), device=dev)))
-    seq = c.seq_len.to(dev)
-    pos = (c.seq_len - 1).to(torch.int32).to(dev)
-    tab = gva.gva_rope_table_fill(int(max(lengths)) + 1, w.d_r, w.base).to(dev)
-    ws = gva.workspace(dims, dev)
-    path = args.path
-
-    def layer_step(L):
-        gva.gva_append_cache(dims, L["v_new"], L["k_new"], pos, None, L["cache"], tab)
-        gva.gva_decode_attention(dims, L["q_nope"], L["q_rope"], L["M"], seq, L["cache"], tab,
-                                 w.scale, L["out"], L["lse"], ws, path=path)
-
-    def decode_only(L):
-        gva.gva_decode_attention(dims, L["q_nope"], L["q_rope"], L["M"], seq, L["cache"], tab,
-                                 w.scale, L["out"], L["lse"], ws, path=path)
-
     stream = torch.cuda.Stream(device=dev)
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            for L in layers:        # eager once (sets kernel attributes), then capture
-                fn(L)
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for L in layers:
-                    fn(L)
-        torch.cuda.synchronize()
-        return g
-
-    g_step = capture(layer_step)
-    g_dec = capture(decode_only)
-    assert gva.gva_get_device_status() == 0
-
-    step_ms = []   # per-step durations of the last timed region (events between steps)
-
-    def timed(graph, K, W, sampler=None):
-        for _ in range(W):
-            graph.replay()
-        torch.cuda.synchronize()
-        dist.barrier()
-        torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-        if sampler:
-            sampler.mark("t0")
-        with torch.cuda.stream(stream):
-            ev[0].record(stream)
-            for k in range(K):
-                graph.replay()
-                ev[k + 1].record(stream)
-        torch.cuda.synchronize()
-        if sampler:
-            sampler.mark("t1")
-        dist.barrier()
-        step_ms[:] = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
-        return ev[0].elapsed_time(ev[K]) / 1e3
+    path = args.path
+    S = LayerStack(gva, torch, gva_inputs, args.workload, args.layers, dev)
+    w, nl = S.w, S.nl
+    log(f"[bench] workload {w.name}: B={w.B} H={w.H} G={w.G} d_h={w.d_h} d_r={w.d_r} "
+        f"tokens={sum(S.lengths)} layers={nl}")
+    peaks = measured_peaks()
+    hbm_peak = peaks["hbm_gbs"] if peaks else FALLBACK_HBM_GBS
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     time.sleep(0.3)
-    # soak so the clocks under load are what the samples see (not timed)
-    soak_t = time.time()
-    while time.time() - soak_t < args.soak:
-        for _ in range(20):
-            g_step.replay()
-        torch.cuda.synchronize()
-    secs = timed(g_step, args.steps, args.warmup, sampler)
-    clocks = sampler.summary(sampler.t_marks.get("t0", soak_t) - args.soak,
+    t_soak = time.time()
+    m = measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path,
+                      not args.no_gqa)
+    clocks = sampler.summary(sampler.t_marks.get("t0", t_soak) - args.soak,
                              sampler.t_marks.get("t1", time.time()))
-    sampler.stop()
-    max_secs = dist.max(secs, dev)
-    bytes_layer = algorithmic_bytes(w, lengths)
-    step_bytes = bytes_layer * nl
-    value = aggregate(step_bytes * args.steps * dist.world, max_secs) / 1e9   # GB/s, all ranks
-    ms_per_step = max_secs / args.steps * 1e3
-    us_layer = ms_per_step * 1e3 / nl
-    us_layer_median = statistics.median(step_ms) * 1e3 / nl   # this rank's per-step median
-
-    # the decode op alone (absorb + split-K partial + combine), same stream, live
-    dsecs = dist.max(timed(g_dec, args.steps, max(3, args.warmup)), dev)
-    us_decode = dsecs / (args.steps * nl) * 1e6
-    us_decode_median = statistics.median(step_ms) * 1e3 / nl
-    achieved = bytes_layer / (us_decode * 1e-6) / 1e9
-
-    peaks = measured_peaks()
-    hbm_peak = peaks["hbm_gbs"] if peaks else FALLBACK_HBM_GBS
+    value = m["layer_step_gbs"]                       # GB/s, all ranks
+    ms_per_step = m["seconds"] / args.steps * 1e3
+    achieved = m["decode_gbs"]
     read_probe = read_probe_gbs(gva, torch, stream, dev)
-
-    # GQA comparator of matched H, G, d_h reading explicit K and V
-    gqa = None
-    if w.layout == "ragged" and not args.no_gqa:
-        # the graph replay of this comparator on the full ragged batch ended in a launch
-        # failure twice while the library was built (cause not found); it is not run
-        gqa = {"not_run": "ragged-layout comparator replay kept off the GPU (unresolved "
-                          "launch failure; see the design notes)"}
-    elif not args.no_gqa:
-        Kq0 = gva_inputs.make_gqa_keys(c).to(dev)
-        qq = gva_inputs.make_gqa_query(c).to(dev)
-        glayers = []
-        for li in range(nl):
-            glayers.append(dict(kv=gva.KVCache(dev_rows(V0), Kq0.clone() if li else Kq0,
-                                               layers[li]["cache"].V), q=qq.clone(),
-                                out=torch.empty((w.B, w.H, w.d_h), device=dev),
-                                lse=torch.empty((w.B, w.H), device=dev)))
-
-        def gqa_call(L):
-            gva.gva_gqa_decode_attention(dims, L["q"], seq, L["kv"], 1.0 / math.sqrt(w.d_h),
-                                         L["out"], L["lse"], ws, path=path)
-        gg = capture_list(torch, stream, glayers, gqa_call)
-        gsecs = dist.max(timed(gg, args.steps, max(3, args.warmup)), dev)
-        us_gqa = gsecs / (args.steps * nl) * 1e6
-        gb = gqa_bytes(w, lengths)
-        gqa = {"us_per_layer": round(us_gqa, 3), "bytes_per_layer": gb,
-               "gbs": round(gb / (us_gqa * 1e-6) / 1e9, 1),
-               "gva_bytes_saved_pct": round(100 * (1 - bytes_layer / gb), 3),
-               "gva_time_saved_pct": round(100 * (1 - us_decode / us_gqa), 1)}
-        del glayers, gg, Kq0
+    floor = single_pass_floor(gva, torch, dist, stream, dev, S.bytes_layer, nl, args.steps,
+                              max(3, args.warmup))
 
     # end to end through the public API with host buffers (eager calls, pinned copies)
-    e2e = run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path,
-                  bytes_layer, dist)
+    e2e = run_e2e(args, w, S.c, S.dims, gva, torch, dev, S.layers, S.seq, S.pos, S.tab, S.ws,
+                  path, S.bytes_layer, dist)
+    c_case = S.c
+    del S
+    torch.cuda.empty_cache()
+
+    # the other workloads the target names, measured in this process with the same clock
+    # sampling: the long-context layer and the paged serving batch
+    others = {}
+    if not args.no_others:
+        for name in args.others:
+            if name == w.name:
+                continue
+            S2 = LayerStack(gva, torch, gva_inputs, name, default_layers(gva_inputs.workload(name)), dev)
+            m2 = measure_stack(args, dist, torch, gva, gva_inputs, S2, stream, sampler, path, True)
+            ck = sampler.summary(sampler.t_marks["t0"], sampler.t_marks["t1"])
+            w2 = S2.w
+            others[name] = {
+                "workload": f"{name}: GVA decode layer B={w2.B} H={w2.H} G={w2.G} d_h={w2.d_h} "
+                            f"d_n={w2.d_n} d_r={w2.d_r} "
+                            + (f"T={w2.T}" if w2.layout == "contiguous" else f"{w2.layout} lengths")
+                            + f" {w2.cache_dtype} cache",
+                **{k: v for k, v in m2.items() if k != "seconds"},
+                "roofline": {"bound": "hbm", "achieved": m2["decode_gbs"], "peak": hbm_peak,
+                             "unit": "GB/s", "frac": m2["decode_frac_of_measured_copy"],
+                             "peak_source": "measured" if peaks else "fallback",
+                             "traffic": profiled_traffic(name) if path in ("auto", "mma") else None},
+                "clocks": ck}
+            del S2
+            torch.cuda.empty_cache()
+    sampler.stop()
 
     # the CPU oracle on a bounded sample (rank 0 only)
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
-        cpu = oracle_baseline(w, c, budget_s=args.cpu_seconds)
+        cpu = oracle_baseline(w, c_case, budget_s=args.cpu_seconds)
 
-    launches_per_step = nl * (3 if path == "fused" else 4)
+    launches_per_step = nl * (2 if path == "fused" else 4)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -345,26 +413,28 @@ def run_ours(args, dist: Dist):
                         f"d_n={w.d_n} d_r={w.d_r} "
                         + (f"T={w.T}" if w.layout == "contiguous" else f"{w.layout} lengths")
                         + f" {w.cache_dtype} cache; step = append + decode through {nl} layers",
-            "layers": nl, "tokens_per_layer": int(sum(lengths)),
-            "bytes_per_layer": bytes_layer, "us_per_layer_step": round(us_layer, 3),
-            "us_per_decode": round(us_decode, 3),
-            "median_of_steps": {"us_per_layer_step": round(us_layer_median, 3),
-                                "us_per_decode": round(us_decode_median, 3),
-                                "reps": args.steps},
+            **{k: v for k, v in m.items() if k not in ("seconds", "layer_step_gbs",
+                                                       "decode_gbs",
+                                                       "decode_frac_of_measured_copy",
+                                                       "gqa_comparator")},
             "pct_of_8tbs_spec": round(100 * value / dist.world / SPEC_HBM_GBS, 2),
             "pct_of_measured_copy": round(100 * value / dist.world / hbm_peak, 2),
             "read_probe_gbs": read_probe,
             "decode_pct_of_read_probe": round(100 * achieved / read_probe, 2) if read_probe else None,
+            "single_pass_floor": {**floor,
+                                  "decode_frac_of_floor": round(floor["us_per_pass"] /
+                                                                m["us_per_decode"], 4)},
             "seqs_steps_per_s": round(w.B * dist.world / (ms_per_step * 1e-3), 1),
             "l2": f"inputs larger than L2: {nl} distinct layer caches, "
-                  f"{bytes_layer * nl / 1e6:.0f} MB",
+                  f"{S_bytes_mb(m)} MB",
             "path": path, "accumulate": "fp32", "parallelism": f"replicas x{dist.world}",
-            "gqa_comparator": gqa,
+            "gqa_comparator": m.get("gqa_comparator"),
+            "other_workloads": others or None,
         },
         "roofline": {"bound": "hbm", "kernel": "gva_decode_attention (absorb + split-K "
                      "partial + combine), per call", "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4),
+                     "frac": m["decode_frac_of_measured_copy"],
                      "peak_source": "measured" if peaks else "fallback",
                      "traffic": profiled_traffic(w.name) if path in ("auto", "mma") else None,
                      "traffic_kernel": "decode_mma_kernel, DRAM bytes per launch (ncu)"},
@@ -376,6 +446,10 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+def S_bytes_mb(m) -> int:
+    return int(round(m["bytes_per_layer"] * m["layers"] / 1e6))
 
 
 def prefill_work(w, L0, n: int):
@@ -789,6 +863,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-gqa", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--others", nargs="*", default=["long", "paged"],
+                    help="further workloads measured in the same run (config.other_workloads)")
+    ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time the causal chunked prefill of this many new tokens per "
                          "sequence instead of the decode step")
@@ -797,13 +874,7 @@ def main():
         args.warmup = 3
     if args.layers == 0:
         import gva_inputs
-        w = gva_inputs.workload(args.workload)
-        c_bytes = (w.B * (w.T or sum(w.len_range) // 2)) * (w.G * w.d_h + w.d_r) * 2
-        # a layer smaller than L2 (126 MB): at least 32 distinct layer caches, and four
-        # times L2 in all; a larger layer is already streamed from HBM on every call
-        args.layers = max(1, min(64, math.ceil(4 * 126e6 / c_bytes)))
-        if c_bytes < 126e6:
-            args.layers = max(32, args.layers)
+        args.layers = default_layers(gva_inputs.workload(args.workload))
     dist = Dist()
     if args.impl == "reference":
         run_reference(args, dist)

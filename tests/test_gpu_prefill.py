@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 def _supported(c, path):
     w = c.w
     if path in ("mma", "fused"):
-        return w.cache_dtype == "bf16" and w.d_h in (64, 128) and (path == "fused" or w.G <= 8)
+        return w.cache_dtype == "bf16" and w.d_h in (64, 128) and w.G <= 8
     return True
 
 

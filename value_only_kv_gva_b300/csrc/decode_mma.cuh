@@ -43,8 +43,12 @@ namespace gva {
 #ifndef GVA_MMA_CONSUMERS
 #define GVA_MMA_CONSUMERS 8
 #endif
-constexpr int MMA_CONSUMERS = GVA_MMA_CONSUMERS;   // at most 15 (launch bound)
-constexpr int MMA_THREADS = 16 * 32;                  // launch bound (-> <= 128 registers)
+#ifndef GVA_MMA_THREADS
+#define GVA_MMA_THREADS 512
+#endif
+constexpr int MMA_CONSUMERS = GVA_MMA_CONSUMERS;      // at most GVA_MMA_THREADS / 32 - 1
+constexpr int MMA_THREADS = GVA_MMA_THREADS;          // launch bound (512 -> <= 128 registers)
+static_assert((MMA_CONSUMERS + 1) * 32 <= MMA_THREADS, "consumer warps exceed the launch bound");
 constexpr float MMA_RESCALE_TH = 8.f;                 // log2 units
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MMA_MAX_STAGES = 24;
@@ -282,6 +286,306 @@ __device__ __forceinline__ uint32_t vtile_addr(uint32_t base, int g, int t, int 
 }
 
 // ---------------------------------------------------------------------------- //
+// consumer building blocks (shared by the tensor-core decode kernels)
+// ---------------------------------------------------------------------------- //
+// Products with a slab's 16 tokens on the MMA rows and the group's heads on the
+// columns, two columns per head (the bf16 "hi" part of the query or probability and
+// its "lo" remainder), so r <= 4 heads fill one 8-column tile with no padding:
+//   S[16 tok x 8]    = V_g[16 tok x d_h] . Q^T[d_h x 8]  (+ K_rope . Q_r^T)
+//   O^T[d_h x 8]    += V_g^T[d_h x 16 tok] . P^T[16 tok x 8]
+// Lane (gid, tig) holds the scores of head 4nt + tig for tokens gid and gid + 8, and
+// the output of the same head for dimensions 16mt + gid (+ 8).
+template <int DH, int DR, int NT>
+struct QFrags {
+    static constexpr int KD = DH / 16;       // k16 steps over d_h
+    static constexpr int DRK16 = DR / 16;    // full k16 steps over the positional slice
+    uint32_t bq[KD][NT][2];
+    uint32_t bqr[DRK16 > 0 ? DRK16 : 1][NT][2];
+    uint32_t bqr8[NT];                       // the trailing k8 step when DR % 16 == 8
+};
+
+// Q^T fragments of value group g for sequence b: column gid of tile nt is head
+// 4nt + gid/2 of the group, its hi part (gid even) or lo remainder (gid odd).  The
+// content query comes from p.qc (fp32 or bf16, times p.qc_scale; read through L2 only
+// when `cg`, for queries written by other CTAs of the same grid); the positional query
+// is p.qr when given (already rotated and scaled), else q_rope rotated here by
+// Rot(L_b - 1) and scaled by p.qr_scale.
+template <int DH, int DR, int NT, bool CG>
+__device__ __forceinline__ void load_q_frags(const DecodeParams &p, int b, int g, int Lb, int lane,
+                                             QFrags<DH, DR, NT> &q) {
+    constexpr int KD = DH / 16, DRK16 = DR / 16;
+    constexpr bool DR_K8 = (DR % 16) == 8;
+    const int gid = lane >> 2, tig = lane & 3;
+    const bool lo_col = (gid & 1) != 0;
+    const int r = p.r, H = p.H;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hl = 4 * nt + (gid >> 1);
+        const bool real = hl < r;
+        const long long qoff = ((long long)b * H + g * r + hl) * DH;
+        float x[KD][4];
+#pragma unroll
+        for (int kk = 0; kk < KD; ++kk) {
+            x[kk][0] = x[kk][1] = x[kk][2] = x[kk][3] = 0.f;
+            if (real) {
+                const int d0 = kk * 16 + tig * 2;
+                if (p.qc_f32) {
+                    const float *qf = reinterpret_cast<const float *>(p.qc) + qoff;
+                    const float2 u = CG ? __ldcg(reinterpret_cast<const float2 *>(qf + d0))
+                                        : *reinterpret_cast<const float2 *>(qf + d0);
+                    const float2 v = CG ? __ldcg(reinterpret_cast<const float2 *>(qf + d0 + 8))
+                                        : *reinterpret_cast<const float2 *>(qf + d0 + 8);
+                    x[kk][0] = u.x; x[kk][1] = u.y; x[kk][2] = v.x; x[kk][3] = v.y;
+                } else {
+                    const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(p.qc) + qoff;
+                    const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qb + d0));
+                    const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qb + d0 + 8));
+                    x[kk][0] = u.x; x[kk][1] = u.y; x[kk][2] = v.x; x[kk][3] = v.y;
+                }
+            }
+        }
+        float xr[DRK16 > 0 ? DRK16 : 1][4], xr8[2] = {0.f, 0.f};
+        if (DR > 0) {
+            // this lane's positional query pairs (d0, d0+1), (d0+8, d0+9) are RoPE
+            // pairs d0/2 and d0/2 + 4: either rotated by the absorption kernel
+            // (p.qr), or rotated here by Rot(L_b - 1) from the raw q_rope
+            const long long qo = ((long long)b * H + g * r + hl) * DR;
+            int t = Lb - 1;
+            if (t < 0) t = 0;
+            if (t >= p.rope_max_pos) {
+                if (p.qr == nullptr && real && tig == 0 && (gid & 1) == 0)
+                    dev_report(GVA_DEV_BAD_POSITION);
+                t = 0;
+            }
+            const float2 *cs = reinterpret_cast<const float2 *>(p.rope_tab) + (long long)t * (DR / 2);
+            auto pair = [&](int d) -> float2 {   // rotated, scaled pair (d, d + 1)
+                if (p.qr != nullptr) return *reinterpret_cast<const float2 *>(p.qr + qo + d);
+                float2 x;
+                if (p.qr_f32) {
+                    x = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(p.q_rope) + qo + d);
+                } else {
+                    x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
+                        reinterpret_cast<const __nv_bfloat16 *>(p.q_rope) + qo + d));
+                }
+                const float2 c = cs[d / 2];
+                return make_float2(p.qr_scale * (x.x * c.x - x.y * c.y),
+                                   p.qr_scale * (x.x * c.y + x.y * c.x));
+            };
+#pragma unroll
+            for (int kk = 0; kk < DRK16; ++kk) {
+                xr[kk][0] = xr[kk][1] = xr[kk][2] = xr[kk][3] = 0.f;
+                if (real) {
+                    const int d0 = kk * 16 + tig * 2;
+                    const float2 u = pair(d0);
+                    const float2 v = pair(d0 + 8);
+                    xr[kk][0] = u.x; xr[kk][1] = u.y; xr[kk][2] = v.x; xr[kk][3] = v.y;
+                }
+            }
+            if (DR_K8 && real) {
+                const float2 u = pair(DRK16 * 16 + tig * 2);
+                xr8[0] = u.x; xr8[1] = u.y;
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KD; ++kk) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[kk][e] *= p.qc_scale;
+            q.bq[kk][nt][0] = part_bf16x2(x[kk][0], x[kk][1], lo_col);
+            q.bq[kk][nt][1] = part_bf16x2(x[kk][2], x[kk][3], lo_col);
+        }
+        if (DR > 0) {
+#pragma unroll
+            for (int kk = 0; kk < DRK16; ++kk) {
+                q.bqr[kk][nt][0] = part_bf16x2(xr[kk][0], xr[kk][1], lo_col);
+                q.bqr[kk][nt][1] = part_bf16x2(xr[kk][2], xr[kk][3], lo_col);
+            }
+            if (DR_K8) q.bqr8[nt] = part_bf16x2(xr8[0], xr8[1], lo_col);
+        }
+    }
+}
+
+// Scores of one staged slab for value group g: sc[nt][a] accumulates the k16 steps of
+// parity a (two independent chains), hi and lo columns still separate.  kst: the tile
+// scored against the content query (the value tile, or the GQA key tile); rst: the
+// positional keys (DR > 0).
+template <int DH, int DR, int NT>
+__device__ __forceinline__ void slab_scores(uint32_t kst, uint32_t rst, int g, int lane,
+                                            const QFrags<DH, DR, NT> &q, float (&sc)[NT][2][4]) {
+    constexpr int KD = DH / 16, DRK16 = DR / 16;
+    constexpr bool DR_K8 = (DR % 16) == 8;
+    const int lm_mat = lane >> 3, lm_row = lane & 7;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int a2 = 0; a2 < 2; ++a2)
+            sc[nt][a2][0] = sc[nt][a2][1] = sc[nt][a2][2] = sc[nt][a2][3] = 0.f;
+    uint32_t av[KD][4];
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk)
+        ldsm_x4(vtile_addr<DH>(kst, g, lm_row + 8 * (lm_mat & 1), 2 * kk + (lm_mat >> 1)),
+                av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
+    uint32_t ar[DRK16 > 0 ? DRK16 : 1][4], ar8[2];
+    if (DR > 0) {
+#pragma unroll
+        for (int kk = 0; kk < DRK16; ++kk)
+            ldsm_x4(rst + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + (2 * kk + (lm_mat >> 1)) * 16,
+                    ar[kk][0], ar[kk][1], ar[kk][2], ar[kk][3]);
+        if (DR_K8)
+            ldsm_x2(rst + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + DRK16 * 32, ar8[0], ar8[1]);
+    }
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            mma16816(sc[nt][kk & 1], av[kk], q.bq[kk][nt][0], q.bq[kk][nt][1]);
+    if (DR > 0) {
+#pragma unroll
+        for (int kk = 0; kk < DRK16; ++kk)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma16816(sc[nt][(KD + kk) & 1], ar[kk], q.bqr[kk][nt][0], q.bqr[kk][nt][1]);
+        if (DR_K8) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma1688(sc[nt][(KD + DRK16) & 1], ar8[0], ar8[1], q.bqr8[nt]);
+        }
+    }
+}
+
+// Value tiles of group g as the A operand of O^T += V^T P^T (ldmatrix.trans).
+template <int DH>
+__device__ __forceinline__ void slab_value_tiles(uint32_t st, int g, int lane,
+                                                 uint32_t (&apv)[DH / 16][4]) {
+    const int lm_mat = lane >> 3, lm_row = lane & 7;
+#pragma unroll
+    for (int mt = 0; mt < DH / 16; ++mt)
+        ldsm_x4_t(vtile_addr<DH>(st, g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
+                  apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
+}
+
+// Zero the value tiles of tokens at or past nv (a slot past a sequence's end may hold
+// anything, including NaN, and 0 * NaN would poison the sum).
+template <int DH>
+__device__ __forceinline__ void mask_value_tiles(uint32_t (&apv)[DH / 16][4], int nv, int lane) {
+    const int tig = lane & 3;
+    const int ta = 2 * tig, tb = 8 + 2 * tig;
+    const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
+    const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
+#pragma unroll
+    for (int mt = 0; mt < DH / 16; ++mt) {
+        apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
+    }
+}
+
+// ---------------------------------------------------------------------------- //
+// producer warp (shared by the tensor-core decode kernels)
+// ---------------------------------------------------------------------------- //
+// One step issues up to il = min(NS, 32) consecutive slabs, one per lane: lane j finds
+// its slab's storage row (for a paged cache the block-table reads of the step are in
+// flight together), waits until its ring stage is free, and issues the copies.  The
+// stages of one step are distinct, so no lane waits on another lane's copy.  A short
+// cache (the whole share fits in the ring) is issued in a single step.  Slab s0 + i of
+// the share goes to stage i mod NS in round i / NS.
+template <int DH, int DR, bool GQA>
+__device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUtensorMap *tm_k,
+                                             const MmaParams &mp, const int *F, long long s0,
+                                             long long s1, uint32_t base_u32, uint32_t bar_full,
+                                             uint32_t bar_empty, volatile int *abort,
+                                             int *stage_bad, uint64_t pol) {
+    const DecodeParams &p = mp.d;
+    const int NS = mp.nstages, G = p.G, B = p.B;
+    const int lane = threadIdx.x & 31;
+    const int il = NS < 32 ? NS : 32;
+    int stage = 0;                      // stage of the step's first slab
+    uint32_t round = 0;                 // ring wraps before the step's first slab
+    bool dead = false;
+    long long n_tried = 0;              // slabs of the steps attempted
+    int b = seq_of_slab(F, B, s0);      // sequence of the step's first slab
+    if (lane == 0) GVA_TRACE_AT(6);
+    if (lane == 0) GVA_TRACE_AT(200);
+    for (long long sb = s0; sb < s1; sb += il) {
+        const long long s = sb + lane;
+        const bool act = lane < il && s < s1;
+        int st = stage + lane;
+        uint32_t rd = round;
+        if (st >= NS) { st -= NS; ++rd; }
+        bool ok = true;
+        if (act) {
+            int bl = b;
+            while (F[bl + 1] <= s) ++bl;
+            const long long row = row_of(p.R, bl, (s - F[bl]) * SLAB);
+            const int yk = row < 0 ? 0 : (int)row;
+            if (s == s0) GVA_TRACE_AT(201);
+            if (rd > 0 && !mbar_wait(bar_empty + 8 * st, (rd - 1) & 1u, abort)) {
+                ok = false;
+            } else {
+                const uint32_t stb = base_u32 + st * mp.stage_bytes;
+                const uint32_t fb = bar_full + 8 * st;
+                stage_bad[st] = row < 0;   // published by the arrive below
+                // the positional keys of the slab are one contiguous run of rows;
+                // rows past the end of the cache storage are not copied (their
+                // tokens are past every sequence's end, and masked)
+                int rrows = SLAB;
+                if ((long long)yk + SLAB > p.R.num_rows) {
+                    const long long left = p.R.num_rows - (long long)yk;
+                    rrows = left < 0 ? 0 : (int)left;
+                }
+                const uint32_t rbytes = (uint32_t)rrows * (DR * 2);
+                mbar_expect_tx(fb, (uint32_t)mp.off_r + rbytes);
+                if (s == s0) GVA_TRACE_AT(202);
+                if (mp.v3d) {
+                    tma_load_3d(stb, tm_v, 0, yk, 0, fb, pol);
+                    if (s == s0) GVA_TRACE_AT(203);
+                    if (GQA) tma_load_3d(stb + mp.off_k, tm_k, 0, yk, 0, fb, pol);
+                } else {
+                    for (int bx = 0; bx < G * (DH / 64); ++bx) {
+                        tma_load_2d(stb + bx * 2048, tm_v, bx * 64, yk, fb, pol);
+                        if (GQA) tma_load_2d(stb + mp.off_k + bx * 2048, tm_k, bx * 64, yk, fb, pol);
+                    }
+                }
+                if (DR > 0 && rbytes > 0)
+                    bulk_load(stb + mp.off_r,
+                              reinterpret_cast<const unsigned char *>(p.Krope) + (size_t)yk * (DR * 2),
+                              rbytes, fb, pol);
+                const int ti = (int)(s - s0);
+                if (ti == 0) GVA_TRACE_AT(2);
+                if (ti < 64) GVA_TRACE_AT(300 + ti);
+            }
+        }
+        n_tried += min((long long)il, s1 - sb);
+        dead = __any_sync(0xffffffffu, act && !ok);
+        if (dead) break;
+        {   // sequence of the next step's first slab
+            const long long sn = sb + il;
+            while (b < B - 1 && F[b + 1] <= sn) ++b;
+        }
+        stage += il;
+        if (stage >= NS) { stage -= NS; ++round; }
+    }
+    if (lane == 0) {
+        GVA_TRACE_AT(3);
+        GVA_TRACE_FLUSH(2, 4);
+        GVA_TRACE_FLUSH(6, 8);
+        GVA_TRACE_FLUSH(300, 364);
+        GVA_TRACE_FLUSH(200, 204);
+        // Never leave with copies in flight: wait (bounded) for the last copy of each
+        // stage used.  Slab i used stage i % NS in round i / NS.  After an abort a
+        // stage's last slab may not have been issued: those waits are kept short.
+        const unsigned long long limit = dead ? 1000000ull : WAIT_LIMIT_NS;
+        for (int st = 0; st < NS && st < n_tried; ++st) {
+            const uint32_t par = (uint32_t)((n_tried - 1 - st) / NS) & 1u;
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try_wait(bar_full + 8 * st, par)) {
+                if (global_ns() - t0 > limit) {
+                    if (!dead) dev_report(GVA_DEV_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------- //
 // the kernel
 // ---------------------------------------------------------------------------- //
 template <int DH, int DR, bool GQA, int NT>
@@ -320,7 +624,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         prefetch_tmap(&tm_v);
         if (GQA) prefetch_tmap(&tm_k);
     }
+    // the cache loads' L2 policy, made while the lengths load (it takes a while)
+    const uint64_t pol = warp == 0 ? l2_evict_first_policy() : 0ull;
     if (threadIdx.x == 0) GVA_TRACE_AT(0);
+    if (threadIdx.x == 0) GVA_REC(3, 0);
     if (threadIdx.x == 0) GVA_KT(5);
     if (threadIdx.x == 0) GVA_CTA_T(0);
     // Lengths, row maps and the cache are final before the preceding grid (the query
@@ -338,107 +645,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     if (s0 >= s1) return;
 
     // ============================= producer warp ============================= //
-    // One step issues up to il = min(NS, 32) consecutive slabs, one per lane: lane j
-    // finds its slab's storage row (for a paged cache the block-table reads of the step
-    // are in flight together), waits until its ring stage is free, and issues the copies.
-    // The stages of one step are distinct, so no lane waits on another lane's copy.  A
-    // short cache (the whole share fits in the ring) is issued in a single step.
     if (warp == 0) {
-        const int il = NS < 32 ? NS : 32;
-        const uint64_t pol = l2_evict_first_policy();
-        int stage = 0;                      // stage of the step's first slab
-        uint32_t round = 0;                 // ring wraps before the step's first slab
-        bool dead = false;
-        long long n_tried = 0;              // slabs of the steps attempted
-        int b = seq_of_slab(F, B, s0);      // sequence of the step's first slab
-        if (lane == 0) GVA_TRACE_AT(6);
-        for (long long sb = s0; sb < s1; sb += il) {
-            const long long s = sb + lane;
-            const bool act = lane < il && s < s1;
-            int st = stage + lane;
-            uint32_t rd = round;
-            if (st >= NS) { st -= NS; ++rd; }
-            bool ok = true;
-            if (act) {
-                int bl = b;
-                while (F[bl + 1] <= s) ++bl;
-                const long long row = row_of(p.R, bl, (s - F[bl]) * SLAB);
-                const int yk = row < 0 ? 0 : (int)row;
-                if (rd > 0 && !mbar_wait(bar_empty + 8 * st, (rd - 1) & 1u, abort)) {
-                    ok = false;
-                } else {
-                    const uint32_t stb = base_u32 + st * mp.stage_bytes;
-                    const uint32_t fb = bar_full + 8 * st;
-                    stage_bad[st] = row < 0;   // published by the arrive below
-                    // the positional keys of the slab are one contiguous run of rows;
-                    // rows past the end of the cache storage are not copied (their
-                    // tokens are past every sequence's end, and masked)
-                    int rrows = SLAB;
-                    if ((long long)yk + SLAB > p.R.num_rows) {
-                        const long long left = p.R.num_rows - (long long)yk;
-                        rrows = left < 0 ? 0 : (int)left;
-                    }
-                    const uint32_t rbytes = (uint32_t)rrows * (DR * 2);
-                    mbar_expect_tx(fb, (uint32_t)mp.off_r + rbytes);
-                    if (mp.v3d) {
-                        tma_load_3d(stb, &tm_v, 0, yk, 0, fb, pol);
-                        if (GQA) tma_load_3d(stb + mp.off_k, &tm_k, 0, yk, 0, fb, pol);
-                    } else {
-                        for (int bx = 0; bx < G * (DH / 64); ++bx) {
-                            tma_load_2d(stb + bx * 2048, &tm_v, bx * 64, yk, fb, pol);
-                            if (GQA) tma_load_2d(stb + mp.off_k + bx * 2048, &tm_k, bx * 64, yk, fb, pol);
-                        }
-                    }
-                    if (DR > 0 && rbytes > 0)
-                        bulk_load(stb + mp.off_r,
-                                  reinterpret_cast<const unsigned char *>(p.Krope) + (size_t)yk * (DR * 2),
-                                  rbytes, fb, pol);
-                    const int ti = (int)(s - s0);
-                    if (ti == 0) GVA_TRACE_AT(2);
-                    if (ti < 64) GVA_TRACE_AT(300 + ti);
-                }
-            }
-            n_tried += min((long long)il, s1 - sb);
-            dead = __any_sync(0xffffffffu, act && !ok);
-            if (dead) break;
-            {   // sequence of the next step's first slab
-                const long long sn = sb + il;
-                while (b < B - 1 && F[b + 1] <= sn) ++b;
-            }
-            stage += il;
-            if (stage >= NS) { stage -= NS; ++round; }
-        }
-        if (lane == 0) {
-            GVA_TRACE_AT(3);
-            GVA_TRACE_FLUSH(2, 4);
-            GVA_TRACE_FLUSH(6, 8);
-            GVA_TRACE_FLUSH(300, 364);
-            // Never leave with copies in flight: wait (bounded) for the last copy of each
-            // stage used.  Slab i used stage i % NS in round i / NS.  After an abort a
-            // stage's last slab may not have been issued: those waits are kept short.
-            const unsigned long long limit = dead ? 1000000ull : WAIT_LIMIT_NS;
-            for (int st = 0; st < NS && st < n_tried; ++st) {
-                const uint32_t par = (uint32_t)((n_tried - 1 - st) / NS) & 1u;
-                const unsigned long long t0 = global_ns();
-                while (!mbar_try_wait(bar_full + 8 * st, par)) {
-                    if (global_ns() - t0 > limit) {
-                        if (!dead) dev_report(GVA_DEV_TIMEOUT);
-                        break;
-                    }
-                }
-            }
-        }
+        mma_producer<DH, DR, GQA>(&tm_v, &tm_k, mp, F, s0, s1, base_u32, bar_full, bar_empty,
+                                  abort, stage_bad, pol);
         return;
     }
 
     // ============================= consumer warps ============================ //
-    // Products with the slab's 16 tokens on the MMA rows and the group's heads on the
-    // columns, two columns per head (the bf16 "hi" part of the query or probability and
-    // its "lo" remainder), so r <= 4 heads fill one 8-column tile with no padding:
-    //   S[16 tok x 8]    = V_g[16 tok x d_h] . Q^T[d_h x 8]  (+ K_rope . Q_r^T)
-    //   O^T[d_h x 8]    += V_g^T[d_h x 16 tok] . P^T[16 tok x 8]
-    // Lane (gid, tig) holds the scores of head 4nt + tig for tokens gid and gid + 8, and
-    // the output of the same head for dimensions 16mt + gid (+ 8).
     const int ci = warp - 1;          // consumer index
     if (ci >= mp.ncons) return;       // spare warps
     const int g = ci % G;             // value group of this warp
@@ -446,16 +659,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     const int wpg = mp.wpg;
     const int gid = lane >> 2, tig = lane & 3;
     constexpr int KD = DH / 16;       // k16 steps over d_h (and 16-row tiles of O^T)
-    constexpr int DRK16 = DR / 16;    // full k16 steps over the positional slice
-    constexpr bool DR_K8 = (DR % 16) == 8;  // one trailing k8 step
-    // ldmatrix lane roles
-    const int lm_mat = lane >> 3, lm_row = lane & 7;
     // P^T exchange: the lanes holding tokens 2tig and 2tig+1 of this lane's column head
     const int srcA = (2 * tig) * 4 + (gid >> 1), srcB = (2 * tig + 1) * 4 + (gid >> 1);
     const bool lo_col = (gid & 1) != 0;
 
     if (mp.early) pdl_wait();         // the absorbed queries come from the preceding grid
     if (w == 0 && g == 0 && lane == 0) GVA_KT(6);
+    if (w == 0 && g == 0 && lane == 0) GVA_REC(3, 1);
     if (w == 0 && g == 0 && lane == 0) GVA_CTA_T(1);
     // The slabs of the share go round-robin to the group's warps: this warp takes
     // s0 + w, s0 + w + wpg, ...; slab s0 + i sits in ring stage i mod NS, phase (i / NS) & 1.
@@ -472,92 +682,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         const int Lb = Ls[b];
         const int Fb = F[b];
 
-        // ---- Q^T fragments: column gid = head 4nt + gid/2, hi (gid even) or lo part ----
-        uint32_t bq[KD][NT][2];
-        uint32_t bqr[DRK16 > 0 ? DRK16 : 1][NT][2];
-        uint32_t bqr8[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int hl = 4 * nt + (gid >> 1);
-            const bool real = hl < r;
-            const long long qoff = ((long long)b * H + g * r + hl) * DH;
-            float x[KD][4];
-#pragma unroll
-            for (int kk = 0; kk < KD; ++kk) {
-                x[kk][0] = x[kk][1] = x[kk][2] = x[kk][3] = 0.f;
-                if (real) {
-                    const int d0 = kk * 16 + tig * 2;
-                    if (p.qc_f32) {
-                        const float *qf = reinterpret_cast<const float *>(p.qc) + qoff;
-                        const float2 u = *reinterpret_cast<const float2 *>(qf + d0);
-                        const float2 v = *reinterpret_cast<const float2 *>(qf + d0 + 8);
-                        x[kk][0] = u.x; x[kk][1] = u.y; x[kk][2] = v.x; x[kk][3] = v.y;
-                    } else {
-                        const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(p.qc) + qoff;
-                        const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qb + d0));
-                        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qb + d0 + 8));
-                        x[kk][0] = u.x; x[kk][1] = u.y; x[kk][2] = v.x; x[kk][3] = v.y;
-                    }
-                }
-            }
-            float xr[DRK16 > 0 ? DRK16 : 1][4], xr8[2] = {0.f, 0.f};
-            if (DR > 0) {
-                // this lane's positional query pairs (d0, d0+1), (d0+8, d0+9) are RoPE
-                // pairs d0/2 and d0/2 + 4: either rotated by the absorption kernel
-                // (p.qr), or rotated here by Rot(L_b - 1) from the raw q_rope
-                const long long qo = ((long long)b * H + g * r + hl) * DR;
-                int t = Lb - 1;
-                if (t < 0) t = 0;
-                if (t >= p.rope_max_pos) {
-                    if (p.qr == nullptr && real && tig == 0 && (gid & 1) == 0)
-                        dev_report(GVA_DEV_BAD_POSITION);
-                    t = 0;
-                }
-                const float2 *cs = reinterpret_cast<const float2 *>(p.rope_tab) + (long long)t * (DR / 2);
-                auto pair = [&](int d) -> float2 {   // rotated, scaled pair (d, d + 1)
-                    if (p.qr != nullptr) return *reinterpret_cast<const float2 *>(p.qr + qo + d);
-                    float2 x;
-                    if (p.qr_f32) {
-                        x = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(p.q_rope) + qo + d);
-                    } else {
-                        x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
-                            reinterpret_cast<const __nv_bfloat16 *>(p.q_rope) + qo + d));
-                    }
-                    const float2 c = cs[d / 2];
-                    return make_float2(p.qr_scale * (x.x * c.x - x.y * c.y),
-                                       p.qr_scale * (x.x * c.y + x.y * c.x));
-                };
-#pragma unroll
-                for (int kk = 0; kk < DRK16; ++kk) {
-                    xr[kk][0] = xr[kk][1] = xr[kk][2] = xr[kk][3] = 0.f;
-                    if (real) {
-                        const int d0 = kk * 16 + tig * 2;
-                        const float2 u = pair(d0);
-                        const float2 v = pair(d0 + 8);
-                        xr[kk][0] = u.x; xr[kk][1] = u.y; xr[kk][2] = v.x; xr[kk][3] = v.y;
-                    }
-                }
-                if (DR_K8 && real) {
-                    const float2 u = pair(DRK16 * 16 + tig * 2);
-                    xr8[0] = u.x; xr8[1] = u.y;
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < KD; ++kk) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x[kk][e] *= p.qc_scale;
-                bq[kk][nt][0] = part_bf16x2(x[kk][0], x[kk][1], lo_col);
-                bq[kk][nt][1] = part_bf16x2(x[kk][2], x[kk][3], lo_col);
-            }
-            if (DR > 0) {
-#pragma unroll
-                for (int kk = 0; kk < DRK16; ++kk) {
-                    bqr[kk][nt][0] = part_bf16x2(xr[kk][0], xr[kk][1], lo_col);
-                    bqr[kk][nt][1] = part_bf16x2(xr[kk][2], xr[kk][3], lo_col);
-                }
-                if (DR_K8) bqr8[nt] = part_bf16x2(xr8[0], xr8[1], lo_col);
-            }
-        }
+        QFrags<DH, DR, NT> qf;
+        load_q_frags<DH, DR, NT, false>(p, b, g, Lb, lane, qf);
 
         float oacc[KD][NT][4];
 #pragma unroll
@@ -588,53 +714,12 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
             // ---- scores: A = the key tile (tokens x d), B = Q^T ----
             float sc[NT][2][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int a2 = 0; a2 < 2; ++a2)
-                    sc[nt][a2][0] = sc[nt][a2][1] = sc[nt][a2][2] = sc[nt][a2][3] = 0.f;
-            {
-                const uint32_t kst = GQA ? st + mp.off_k : st;
-                uint32_t av[KD][4];
-#pragma unroll
-                for (int kk = 0; kk < KD; ++kk)
-                    ldsm_x4(vtile_addr<DH>(kst, g, lm_row + 8 * (lm_mat & 1), 2 * kk + (lm_mat >> 1)),
-                            av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
-                uint32_t ar[DRK16 > 0 ? DRK16 : 1][4], ar8[2];
-                if (DR > 0) {
-                    const uint32_t rbase = st + mp.off_r;
-#pragma unroll
-                    for (int kk = 0; kk < DRK16; ++kk)
-                        ldsm_x4(rbase + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + (2 * kk + (lm_mat >> 1)) * 16,
-                                ar[kk][0], ar[kk][1], ar[kk][2], ar[kk][3]);
-                    if (DR_K8)
-                        ldsm_x2(rbase + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + DRK16 * 32, ar8[0], ar8[1]);
-                }
-#pragma unroll
-                for (int kk = 0; kk < KD; ++kk)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma16816(sc[nt][kk & 1], av[kk], bq[kk][nt][0], bq[kk][nt][1]);
-                if (DR > 0) {
-#pragma unroll
-                    for (int kk = 0; kk < DRK16; ++kk)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma16816(sc[nt][(KD + kk) & 1], ar[kk], bqr[kk][nt][0], bqr[kk][nt][1]);
-                    if (DR_K8) {
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma1688(sc[nt][(KD + DRK16) & 1], ar8[0], ar8[1], bqr8[nt]);
-                    }
-                }
-            }
+            slab_scores<DH, DR, NT>(GQA ? st + mp.off_k : st, st + mp.off_r, g, lane, qf, sc);
+            if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(100 + 10 * tslab);
             // value tiles for the weighted sum (V^T as the A operand), read while the
             // softmax below runs
             uint32_t apv[KD][4];
-#pragma unroll
-            for (int mt = 0; mt < KD; ++mt)
-                ldsm_x4_t(vtile_addr<DH>(st, g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
-                          apv[mt][0], apv[mt][1], apv[mt][2], apv[mt][3]);
+            slab_value_tiles<DH>(st, g, lane, apv);
 
             // ---- per head: hi + lo columns -> score of tokens gid, gid + 8 ----
             float z[NT][2];
@@ -651,6 +736,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             // more than the threshold (always on a head's first valid token); otherwise
             // the probabilities are taken against the stale maximum (at most 2^threshold)
             // and the max reduction over the token lanes is skipped.
+            if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(101 + 10 * tslab);
             if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -684,16 +770,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 bp[nt][1] = part_bf16x2(a1, b1, lo_col);
             }
             // ---- O^T += V^T . P^T ----
-            if (nv < SLAB) {
-                // zero the values of tokens past the end (they may hold NaN)
-                const int ta = 2 * tig, tb = 8 + 2 * tig;
-                const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
-                const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
-#pragma unroll
-                for (int mt = 0; mt < KD; ++mt) {
-                    apv[mt][0] &= ma; apv[mt][1] &= ma; apv[mt][2] &= mb; apv[mt][3] &= mb;
-                }
-            }
+            if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(102 + 10 * tslab);
+            if (nv < SLAB) mask_value_tiles<DH>(apv, nv, lane);
 #pragma unroll
             for (int mt = 0; mt < KD; ++mt)
 #pragma unroll
@@ -701,6 +779,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
             // the products above consumed every tile register, so all of the warp's
             // shared-memory reads of the stage are complete: release it to the producer
+            if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(103 + 10 * tslab);
             __syncwarp();
             if (lane == 0) mbar_arrive_relaxed(bar_empty + 8 * my_stage);
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(9 + 2 * tslab);
@@ -800,11 +879,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         }
     }
     if (w == 0 && g == 0 && lane == 0) {
+        GVA_REC(3, 2);
         GVA_KT(7);
         GVA_CTA_T(2);
         GVA_TRACE_FLUSH(0, 2);
         GVA_TRACE_FLUSH(4, 6);
         GVA_TRACE_FLUSH(8, 8 + 2 * tslab);
+        GVA_TRACE_FLUSH(100, 180);
     }
 }
 

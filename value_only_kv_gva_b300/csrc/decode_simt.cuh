@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     __shared__ float red_f[COMBINE_THREADS / 32];
     __shared__ float acc_s[4][32];
     if (threadIdx.x == 0) GVA_KT(8);
+    if (threadIdx.x == 0 && blockIdx.y == 0) GVA_REC(4, 0);
     pdl_launch_dependents();
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
         c_hi = nb > 0 ? P.cta_of(Fb + nb - 1) : 0;
     }
     if (threadIdx.x == 0) GVA_KT(9);
+    if (threadIdx.x == 0 && blockIdx.y == 0) GVA_REC(4, 1);
     if (nb == 0) {
         if (tid < 32 && d0 + tid < p.d_h) out[d0 + tid] = 0.f;
         if (tid == 0 && blockIdx.y == 0 && p.lse) p.lse[(long long)b * p.H + h] = -INFINITY;
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     if (tid == 0 && blockIdx.y == 0 && p.lse)
         p.lse[(long long)b * p.H + h] = den > 0.f ? (mstar + log2f(den)) * LN2 : -INFINITY;
     if (tid == 0) GVA_KT(10);
+    if (tid == 0 && blockIdx.y == 0) GVA_REC(4, 2);
 }
 
 }  // namespace gva

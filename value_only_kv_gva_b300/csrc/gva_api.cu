@@ -13,7 +13,7 @@
 #include "prep_kernels.cuh"
 #include "decode_simt.cuh"
 #include "decode_mma.cuh"
-#include "decode_fused.cuh"
+#include "decode_one.cuh"
 #include "prefill_mma.cuh"
 
 using namespace gva;
@@ -71,6 +71,17 @@ cudaError_t opt_in_smem(Kern k) {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_LIMIT);
 }
 
+// The small kernels chained with the decode (append, absorption, combine, prefill view
+// and merge) prefer the largest shared-memory carveout, the one the decode kernels need:
+// an SM holds CTAs of one L1 / shared-memory split at a time, so a small kernel running
+// under a small carveout would keep the next decode grid off that SM until it drains,
+// instead of the decode's CTAs starting (and streaming the cache) beside it.
+template <typename Kern>
+cudaError_t max_carveout(Kern k) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
+}
+
 template <typename Kern>
 int kernel_regs(Kern k) {
     cudaFuncAttributes a;
@@ -97,8 +108,21 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, true>);
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, true>);
     if (e == cudaSuccess) e = mma_opt_in_all();
-    if (e == cudaSuccess) e = fused_opt_in_all();
+    if (e == cudaSuccess) e = one_opt_in_all();
     if (e == cudaSuccess) e = prefill_opt_in_all();
+    if (e == cudaSuccess) e = max_carveout(append_kernel<float>);
+    if (e == cudaSuccess) e = max_carveout(append_kernel<__nv_bfloat16>);
+    if (e == cudaSuccess) e = max_carveout(combine_kernel);
+    if (e == cudaSuccess) e = max_carveout(prefill_view_kernel);
+    if (e == cudaSuccess) e = max_carveout(prefill_combine_kernel<64>);
+    if (e == cudaSuccess) e = max_carveout(prefill_combine_kernel<128>);
+    for (int q = 0; q < 2 && e == cudaSuccess; ++q) {
+        const bool f = q == 0;
+        if (e == cudaSuccess) e = f ? max_carveout(absorb_kernel<float, 0>) : max_carveout(absorb_kernel<__nv_bfloat16, 0>);
+        if (e == cudaSuccess) e = f ? max_carveout(absorb_kernel<float, 8>) : max_carveout(absorb_kernel<__nv_bfloat16, 8>);
+        if (e == cudaSuccess) e = f ? max_carveout(absorb_kernel<float, 16>) : max_carveout(absorb_kernel<__nv_bfloat16, 16>);
+        if (e == cudaSuccess) e = f ? max_carveout(absorb_kernel<float, 32>) : max_carveout(absorb_kernel<__nv_bfloat16, 32>);
+    }
     if (e == cudaSuccess && !encode_fn()) e = cudaErrorSymbolNotFound;
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
@@ -177,9 +201,9 @@ WsPlan plan_ws(const gva_dims *d, int sms) {
     w.qh = o; o = align_up(o + sizeof(float) * d->B * d->H * (d->d_r > 0 ? d->d_r : 1), 256);
     w.po = o; o = align_up(o + sizeof(float) * w.slots * d->H * d->d_h, 256);
     w.pm = o; o = align_up(o + sizeof(float) * w.slots * d->H * 2, 256);
-    // fused path: one ticket per (group, sequence); its partial slots (CTA c + pair
-    // index, r heads each) fit in po / pm
-    w.tk = o; o = align_up(o + sizeof(int) * (size_t)d->G * d->B, 256);
+    // one-kernel path: per sequence an absorbed-heads count and a parts ticket, both
+    // zero between calls
+    w.tk = o; o = align_up(o + sizeof(int) * 2 * (size_t)d->B, 256);
     w.pf = o; o = align_up(o + sizeof(int) * ((size_t)d->B + 1), 256);   // slab offsets
     w.total = o;
     return w;
@@ -359,6 +383,19 @@ bool prefill_layout_ok(const gva_rows &R) {
 
 const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0, 0.f, nullptr};
 
+// The one-kernel decode's arguments beyond the separate-kernel ones.
+void one_extras(OneParams &op, const gva_dims *d, const void *q_nope, const float *M,
+                float prescale, char *w, const WsPlan &plan) {
+    op.q_nope = q_nope;
+    op.M = M;
+    op.d_n = d->d_n;
+    op.q_f32 = d->q_dtype == GVA_F32;
+    op.prescale = prescale;
+    op.qt = reinterpret_cast<float *>(w + plan.qt);
+    op.ready = reinterpret_cast<int *>(w + plan.tk);
+    op.ticket = op.ready + d->B;
+}
+
 // Option flags: only the query RMSNorm, with a finite eps >= 0.
 bool flags_ok(const gva_decode_opts *o) {
     if ((o->flags & ~GVA_FLAG_QUERY_RMSNORM) != 0) return false;
@@ -387,9 +424,20 @@ __global__ void __launch_bounds__(PROBE_THREADS) read_probe_kernel(const uint4 *
 #pragma unroll
         for (int u = 0; u < PROBE_UNROLL; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
     }
-    for (; i < n16; i += stride) {
-        const uint4 v = p[i];
-        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    // the rest (a buffer smaller than one full trip of the grid, or the last part of a
+    // larger one): up to PROBE_UNROLL predicated loads per thread, all in flight together
+    if (i < n16) {
+        uint4 v[PROBE_UNROLL];
+#pragma unroll
+        for (int u = 0; u < PROBE_UNROLL; ++u) {
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i + u * stride < n16)
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                             : "l"(p + i + u * stride));
+        }
+#pragma unroll
+        for (int u = 0; u < PROBE_UNROLL; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
@@ -537,43 +585,17 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
                        !aligned16(q_rope) || !aligned16(cache->K_rope) || !aligned16(rope_tab)))
         return GVA_ERR_ARG;
     const bool mma_ok = mma_supported(d);
-    const bool fused_ok = fused_supported(d, cache->rows);
+    const bool one_ok = one_supported(d);
     if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
-    if (o->path == GVA_PATH_FUSED && !fused_ok) return GVA_ERR_UNSUPPORTED;
+    if (o->path == GVA_PATH_FUSED && !one_ok) return GVA_ERR_UNSUPPORTED;
     WsPlan plan;
     int sms = 0;
     st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
     if (st != GVA_OK) return st;
     char *w = static_cast<char *>(ws);
-    // AUTO takes the separate-kernel tensor-core path: on every measured workload it is
-    // faster than the fused kernel (whose per-group tiles read each cache row in
-    // d_h-wide pieces and whose in-kernel merge lengthens the tail)
-    if (o->path == GVA_PATH_FUSED) {
-        float *qt = reinterpret_cast<float *>(w + plan.qt);
-        float *qh = reinterpret_cast<float *>(w + plan.qh);
-        st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                           scale * LOG2E, qt, qh, sms, &cache->rows, false, o);
-        if (st != GVA_OK) return st;
-        FusedParams fp;
-        memset(&fp, 0, sizeof(fp));
-        fp.B = d->B;
-        fp.H = d->H;
-        fp.G = d->G;
-        fp.r = d->H / d->G;
-        fp.d_r = d->d_r;
-        fp.seq_len = seq_len;
-        fp.R = to_dev(cache->rows);
-        fp.Krope = cache->K_rope;
-        fp.qt = qt;
-        fp.qh = qh;
-        fp.out = out;
-        fp.lse = lse;
-        fp.part_o = reinterpret_cast<float *>(w + plan.po);
-        fp.part_ml = reinterpret_cast<float *>(w + plan.pm);
-        fp.ticket = reinterpret_cast<int *>(w + plan.tk);
-        fp.early = 1;
-        return run_fused(stream, fp, cache->V, cache->rows, d->d_h, sms, o->num_ctas);
-    }
+    // the automatic path takes the separate kernels: on every measured workload they are
+    // faster than the one-kernel decode
+    const bool use_one = o->path == GVA_PATH_FUSED;
     const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
 
     float *qt = reinterpret_cast<float *>(w + plan.qt);
@@ -581,9 +603,12 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     // the tensor-core decode rotates the positional query itself (its inputs are final
     // before the call, so it overlaps the absorption), leaving the absorption a single
     // memory round trip
-    st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o);
-    if (st != GVA_OK) return st;
+    // (the one-kernel decode absorbs inside its own grid)
+    if (!use_one) {
+        st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                           scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o);
+        if (st != GVA_OK) return st;
+    }
 
     DecodeParams dp;
     dp.B = d->B;
@@ -612,6 +637,17 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
     dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
+    if (use_one) {
+        OneParams op;
+        memset(&op, 0, sizeof(op));
+        dp.qr = nullptr;   // the kernel rotates the positional query itself
+        op.m.d = dp;
+        one_extras(op, d, q_nope, M, scale * LOG2E, w, plan);
+        op.qnorm = (o->flags & GVA_FLAG_QUERY_RMSNORM) ? 1 : 0;
+        op.qn_gain = op.qnorm ? o->q_norm_gain : nullptr;
+        op.qn_eps = op.qnorm ? o->q_norm_eps : 0.f;
+        return run_one(stream, op, cache->rows, sms, o->num_ctas, false);
+    }
     if (use_mma) {
         st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, true);
     } else if (d->cache_dtype == GVA_F32) {
@@ -691,7 +727,7 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     }
     // a path that cannot run the chunk is refused before anything is appended
     if (o->path == GVA_PATH_MMA && !mma_supported(d)) return GVA_ERR_UNSUPPORTED;
-    if (o->path == GVA_PATH_FUSED && !fused_supported(&pp.dv, vr)) return GVA_ERR_UNSUPPORTED;
+    if (o->path == GVA_PATH_FUSED && !one_supported(&pp.dv)) return GVA_ERR_UNSUPPORTED;
     int st = cuda_status(launch(prefill_view_kernel, dim3(d->B, (n + PV_ROWS - 1) / PV_ROWS),
                                 dim3(128), 0, stream, vp));
     if (st != GVA_OK) return st;
@@ -750,16 +786,19 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     if (!q || !seq_len || !cache->K || !cache->V || !aligned16(q) || !aligned16(cache->K) ||
         !aligned16(cache->V))
         return GVA_ERR_ARG;
-    if (o->path == GVA_PATH_FUSED || (o->flags & GVA_FLAG_QUERY_RMSNORM))
-        return GVA_ERR_UNSUPPORTED;   // GVA decode only
+    if (o->flags & GVA_FLAG_QUERY_RMSNORM) return GVA_ERR_UNSUPPORTED;   // GVA decode only
     gva_dims dg = *d;
     dg.d_r = 0;
     const bool mma_ok = mma_supported(&dg);
+    const bool one_ok = one_supported(&dg);
     if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
+    if (o->path == GVA_PATH_FUSED && !one_ok) return GVA_ERR_UNSUPPORTED;
     WsPlan plan;
     int sms = 0;
     st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
     if (st != GVA_OK) return st;
+    // the same choice as the GVA decode, so that the comparator runs the same design
+    const bool use_one = o->path == GVA_PATH_FUSED;
     const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
     char *w = static_cast<char *>(ws);
     DecodeParams dp;
@@ -789,6 +828,13 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
     dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
+    if (use_one) {
+        OneParams op;
+        memset(&op, 0, sizeof(op));
+        op.m.d = dp;
+        op.ticket = reinterpret_cast<int *>(w + plan.tk) + d->B;
+        return run_one(stream, op, cache->rows, sms, o->num_ctas, true);
+    }
     if (use_mma) {
         st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, true, false);
     } else if (d->cache_dtype == GVA_F32) {
@@ -858,9 +904,19 @@ int gva_decode_attention_static(void *stream, const gva_dims *d, const void *q_n
     if (need > (size_t)GVA_STATIC_SCRATCH_BYTES) return GVA_ERR_WORKSPACE;  // beyond the fixed maximum
     void *ws = static_scratch_for_device(dev);
     if (!ws) return GVA_ERR_CUDA;
-    // opts = NULL: the automatic path, which takes the separate-kernel decode; it
-    // writes every scratch value before reading it, so nothing in the shared array
-    // has to start at zero (the fused path's tickets would, and it is never taken here)
+    // The automatic path may take the one-kernel decode, which counts absorbed heads and
+    // finished parts per sequence in the scratch and relies on them starting at zero.  A
+    // completed call leaves them zero, but one that gave up (GVA_DEV_TIMEOUT) may not, so
+    // every call clears them first: a memset on the stream, no allocation.  Everything
+    // else in the array is written before it is read.
+    const WsPlan plan = plan_ws(d, num_sms_current());
+    e = cudaMemsetAsync(static_cast<char *>(ws) + plan.tk, 0, sizeof(int) * 2 * (size_t)d->B,
+                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        cudaGetLastError();
+        return GVA_ERR_CUDA;
+    }
     return gva_decode_attention_ex(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab,
                                    rope_max_pos, scale, out, lse, ws,
                                    (size_t)GVA_STATIC_SCRATCH_BYTES, nullptr);
@@ -885,6 +941,26 @@ int gva_debug_trace_clear(void) {
 int gva_debug_cta_read(unsigned long long *host, int n) {
     if (n > 4096) n = 4096;
     return cudaMemcpyFromSymbol(host, g_cta_t, sizeof(unsigned long long) * 4 * n) == cudaSuccess
+               ? GVA_OK : GVA_ERR_CUDA;
+}
+// kernel event log: n records of (tag, time); returns the count written (capped)
+int gva_debug_rec_read(unsigned long long *host, int n) {
+    unsigned cnt = 0;
+    if (cudaMemcpyFromSymbol(&cnt, g_rec_n, sizeof(cnt)) != cudaSuccess) return -1;
+    if (cnt > (1u << 16)) cnt = 1u << 16;
+    if ((int)cnt < n) n = (int)cnt;
+    if (n > 0 && cudaMemcpyFromSymbol(host, g_rec, sizeof(unsigned long long) * 2 * n) != cudaSuccess)
+        return -1;
+    return n;
+}
+int gva_debug_rec_clear(void) {
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_rec_n, &zero, sizeof(zero)) == cudaSuccess ? GVA_OK : GVA_ERR_CUDA;
+}
+// one-kernel decode phases: [cta][8] global-timer readings
+int gva_debug_one_read(unsigned long long *host, int n) {
+    if (n > 1024) n = 1024;
+    return cudaMemcpyFromSymbol(host, g_one_t, sizeof(unsigned long long) * 8 * n) == cudaSuccess
                ? GVA_OK : GVA_ERR_CUDA;
 }
 // [0..16) earliest, [16..32) latest global-timer reading per timeline slot

@@ -29,7 +29,9 @@ struct AppendParams {
 template <typename CT>
 __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     if (threadIdx.x == 0) GVA_KT(0);
+    if (threadIdx.x == 0) GVA_REC(1, 0);
     pdl_wait();
+    if (threadIdx.x == 0) GVA_REC(1, 1);
     pdl_launch_dependents();
     const int b = blockIdx.x;
     const int W = p.G * p.d_h;
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     __syncthreads();
     if (threadIdx.x == 0 && p.seq_len_out) p.seq_len_out[b] = pos + 1;
     if (threadIdx.x == 0) GVA_KT(1);
+    if (threadIdx.x == 0) GVA_REC(1, 2);
 }
 
 // --------------------------------------------------------------------------- //
@@ -200,8 +203,10 @@ template <typename QT, int CSF>
 __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbParams p) {
     extern __shared__ __align__(16) float sm_abs[];
     if (threadIdx.x == 0) GVA_KT(2);
+    if (threadIdx.x == 0) GVA_REC(2, 0);
     pdl_wait();
     if (threadIdx.x == 0) GVA_KT(3);
+    if (threadIdx.x == 0) GVA_REC(2, 1);
     pdl_launch_dependents();
     const int h = blockIdx.x;
     const int b0 = blockIdx.y * p.bpb;
@@ -385,6 +390,7 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
         }
     }
     if (threadIdx.x == 0) GVA_KT(4);
+    if (threadIdx.x == 0) GVA_REC(2, 2);
 }
 
 }  // namespace gva
