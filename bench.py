@@ -312,6 +312,32 @@ def measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path, 
                              "gva_bytes_saved_pct": round(100 * (1 - S.bytes_layer / gb), 3),
                              "gva_time_saved_pct": round(100 * (1 - us_decode / us_gqa), 1)}
     del glayers, gg, Kq0
+    # the MLA-shaped comparator at matched cache bytes (latent width d_c = G d_h)
+    mw = gva.MlaDims(w.B, w.H, w.G * w.d_h, w.d_n, w.d_r, w.d_h)
+    if w.cache_dtype == "bf16" and gva.gva_mla_workspace_size(mw) > 0:
+        mc = gva_inputs.make_mla_case(S.c)
+        C0 = mc.C.to(S.dev)
+        mws = gva.mla_workspace(mw, S.dev)
+        mlayers = []
+        for li in range(nl):
+            mlayers.append(dict(cache=gva.Cache(S.rows(gva, C0), C0.clone() if li else C0,
+                                                S.layers[li]["cache"].K_rope),
+                                Wuk=mc.W_uk.to(S.dev), Wuv=mc.W_uv.to(S.dev),
+                                out=torch.empty((w.B, w.H, w.d_h), device=S.dev),
+                                lse=torch.empty((w.B, w.H), device=S.dev)))
+
+        def mla_call(L):
+            gva.gva_mla_decode_attention(mw, S.layers[0]["q_nope"], S.layers[0]["q_rope"],
+                                         L["Wuk"], L["Wuv"], S.seq, L["cache"], S.tab, w.scale,
+                                         L["out"], L["lse"], mws)
+        gm = capture_list(torch, stream, mlayers, mla_call)
+        msecs, _ = timed_graph(torch, dist, stream, gm, args.steps, max(3, args.warmup))
+        us_mla = dist.max(msecs, S.dev) / (args.steps * nl) * 1e6
+        out["mla_comparator"] = {"us_per_layer": round(us_mla, 3), "latent_width": mw.d_c,
+                                 "bytes_per_layer": S.bytes_layer,
+                                 "gbs": round(S.bytes_layer / (us_mla * 1e-6) / 1e9, 1),
+                                 "gva_time_saved_pct": round(100 * (1 - us_decode / us_mla), 1)}
+        del mlayers, gm, C0, mws
     return out
 
 
@@ -416,7 +442,7 @@ def run_ours(args, dist: Dist):
             **{k: v for k, v in m.items() if k not in ("seconds", "layer_step_gbs",
                                                        "decode_gbs",
                                                        "decode_frac_of_measured_copy",
-                                                       "gqa_comparator")},
+                                                       "gqa_comparator", "mla_comparator")},
             "pct_of_8tbs_spec": round(100 * value / dist.world / SPEC_HBM_GBS, 2),
             "pct_of_measured_copy": round(100 * value / dist.world / hbm_peak, 2),
             "read_probe_gbs": read_probe,
@@ -429,6 +455,7 @@ def run_ours(args, dist: Dist):
                   f"{S_bytes_mb(m)} MB",
             "path": path, "accumulate": "fp32", "parallelism": f"replicas x{dist.world}",
             "gqa_comparator": m.get("gqa_comparator"),
+            "mla_comparator": m.get("mla_comparator"),
             "other_workloads": others or None,
         },
         "roofline": {"bound": "hbm", "kernel": "gva_decode_attention (absorb + split-K "

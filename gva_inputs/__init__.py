@@ -202,6 +202,30 @@ def make_gqa_query(case: Case) -> torch.Tensor:
 
 
 @dataclass
+class MlaCase:
+    """Inputs of the MLA-shaped comparator at matched cache bytes (latent width
+    d_c = G d_h, so a latent row plus the positional key has the size of a GVA row):
+    latent rows C [rows, d_c] N(0, 1) in the cache dtype (the case's row layout), up-
+    projections W_uk [H, d_c, d_n] and W_uv [H, d_c, d_h] N(0, 1/d_c) fp32.  The queries,
+    positional keys and lengths are the case's own."""
+    d_c: int
+    C: torch.Tensor
+    W_uk: torch.Tensor
+    W_uv: torch.Tensor
+
+
+def make_mla_case(case: Case) -> MlaCase:
+    """Drawn from a fourth generator (seed + 4000) in the order C, W_uk, W_uv."""
+    w = case.w
+    d_c = w.G * w.d_h
+    g = torch.Generator().manual_seed(w.seed + 4000)
+    C = torch.randn((case.num_rows, d_c), generator=g, dtype=torch.float32)
+    Wuk = torch.randn((w.H, d_c, w.d_n), generator=g, dtype=torch.float32) / math.sqrt(d_c)
+    Wuv = torch.randn((w.H, d_c, w.d_h), generator=g, dtype=torch.float32) / math.sqrt(d_c)
+    return MlaCase(d_c=d_c, C=C.to(case.V.dtype), W_uk=Wuk, W_uv=Wuv)
+
+
+@dataclass
 class Chunk:
     """A prefill chunk of n new tokens per sequence, all on the CPU: the history L0
     [B] int32, queries q_nope [B,n,H,d_n] and q_rope [B,n,H,d_r] (query dtype), new

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define GVA_ABI_VERSION 3
+#define GVA_ABI_VERSION 4
 
 typedef enum {
     GVA_OK = 0,
@@ -269,6 +269,46 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *dims, const void *q,
                              const int *seq_len, const gva_kv_cache *cache, float scale,
                              float *out, float *lse, void *workspace, size_t ws_bytes,
                              const gva_decode_opts *opts);
+
+/* MLA-shaped decode: the second reference point at matched cache bytes ([A] 问题 and
+ * 对 MLA 的优势: a latent cache of T (d_c + d_r) scalars against GVA's T (G d_h + d_r); the
+ * KV-cache compression survey's MLA sections: per-head up-projections of one latent).
+ * Cache rows hold a latent c_j [d_c] and one shared, already-rotated positional key [d_r]
+ * (gva_cache with V -> the latent rows).  Head h's key is [c_j W_uk_h ; k_rope_j] with
+ * W_uk_h in R^{d_c x d_n}, its value c_j W_uv_h with W_uv_h in R^{d_c x d_h}; the query is
+ * [q_nope ; Rot(t) q_rope], t = L_b - 1:
+ *   z_j = scale (q_nope . c_j W_uk_h + Rot(t) q_rope . k_rope_j)
+ *   out[b,h,:] = sum_j softmax(z)_j c_j W_uv_h,   lse[b,h] = ln sum_j exp(z_j)
+ * computed as the absorbed decode over the latent rows followed by the up-projection:
+ * q~_h = q_nope W_uk_h^T, o~ = sum_j softmax(z)_j c_j, out = o~ W_uv_h.
+ * Supported: bf16 cache; d_c in {128, 256}; H a multiple of 4 with H / 4 <= 8; d_n in
+ * 8..256 (multiple of 8); d_r in {0, 8, 16, 24, 32}; d_h in {32, 64, 128, 256}. */
+typedef struct {
+    int B;            /* sequences */
+    int H;            /* query heads */
+    int d_c;          /* latent width of a cache row */
+    int d_n;          /* content-query width */
+    int d_r;          /* positional width */
+    int d_h;          /* output (value) width per head */
+    int cache_dtype;  /* gva_dtype of the cache rows (GVA_BF16 runs; GVA_F32: UNSUPPORTED) */
+    int q_dtype;      /* gva_dtype of the queries */
+} gva_mla_dims;
+
+/* Bytes of device workspace gva_mla_decode_attention needs on the current device (0 on
+ * invalid dims). */
+size_t gva_mla_workspace_size(const gva_mla_dims *dims);
+
+/* MLA-shaped decode (see gva_mla_dims).  q_nope device [B][H][d_n], q_rope [B][H][d_r]
+ * (q_dtype); W_uk device fp32 [H][d_c][d_n]; W_uv device fp32 [H][d_c][d_h]; seq_len device
+ * int [B]; cache: latent rows [d_c] in cache->V, positional keys [d_r] in cache->K_rope,
+ * laid out by cache->rows; rope_tab as in gva_absorb_query; out device fp32 [B][H][d_h];
+ * lse device fp32 [B][H] or NULL; workspace device, 256-byte aligned, >=
+ * gva_mla_workspace_size(dims) (scratch only).  Errors as gva_decode_attention. */
+int gva_mla_decode_attention(void *stream, const gva_mla_dims *dims, const void *q_nope,
+                             const void *q_rope, const float *W_uk, const float *W_uv,
+                             const int *seq_len, const gva_cache *cache, const float *rope_tab,
+                             int rope_max_pos, float scale, float *out, float *lse,
+                             void *workspace, size_t ws_bytes);
 
 /* Size of the fixed device array behind gva_decode_attention_static (24 MiB). */
 #define GVA_STATIC_SCRATCH_BYTES (24u << 20)

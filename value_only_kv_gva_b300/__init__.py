@@ -57,6 +57,12 @@ class gva_kv_cache(ctypes.Structure):
     _fields_ = [("rows", gva_rows), ("K", ctypes.c_void_p), ("V", ctypes.c_void_p)]
 
 
+class gva_mla_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("d_c", ctypes.c_int),
+                ("d_n", ctypes.c_int), ("d_r", ctypes.c_int), ("d_h", ctypes.c_int),
+                ("cache_dtype", ctypes.c_int), ("q_dtype", ctypes.c_int)]
+
+
 class gva_decode_opts(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("flags", ctypes.c_int),
                 ("q_norm_eps", ctypes.c_float), ("q_norm_gain", ctypes.c_void_p)]
@@ -88,6 +94,10 @@ _lib.gva_decode_attention_static.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _
 _lib.gva_read_probe.argtypes = [_P, _P, _Z, _P]
 _lib.gva_prefill_workspace_size.restype = _Z
 _lib.gva_prefill_workspace_size.argtypes = [_PD, _I, ctypes.POINTER(gva_rows)]
+_lib.gva_mla_workspace_size.restype = _Z
+_lib.gva_mla_workspace_size.argtypes = [ctypes.POINTER(gva_mla_dims)]
+_lib.gva_mla_decode_attention.argtypes = [_P, ctypes.POINTER(gva_mla_dims), _P, _P, _P, _P, _P,
+                                          _PC, _P, _I, _F, _P, _P, _P, _Z]
 _lib.gva_prefill_attention.argtypes = [_P, _PD, _I, _P, _P, _P, _P, _P, _P, _PC, _P, _I, _F,
                                        _P, _P, _P, _Z, _PO]
 
@@ -96,7 +106,7 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
            "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static",
            "gva_read_probe", "gva_absorb_query_ex", "gva_prefill_workspace_size",
-           "gva_prefill_attention"]
+           "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention"]
 
 
 class GvaError(RuntimeError):
@@ -472,6 +482,66 @@ def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: floa
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
         ctypes.byref(o)), "gva_gqa_decode_attention")
+
+
+@dataclass
+class MlaDims:
+    """gva_mla_dims: the MLA-shaped comparator (latent width d_c, output width d_h)."""
+    B: int
+    H: int
+    d_c: int
+    d_n: int
+    d_r: int
+    d_h: int
+    cache_dtype: int = GVA_BF16
+    q_dtype: int = GVA_BF16
+
+    def c(self) -> gva_mla_dims:
+        return gva_mla_dims(self.B, self.H, self.d_c, self.d_n, self.d_r, self.d_h,
+                            self.cache_dtype, self.q_dtype)
+
+
+def gva_mla_workspace_size(dims: MlaDims) -> int:
+    d = dims.c()
+    return int(_lib.gva_mla_workspace_size(ctypes.byref(d)))
+
+
+def gva_mla_decode_attention(dims: MlaDims, q_nope, q_rope, W_uk, W_uv, seq_len, cache: Cache,
+                             rope_tab, scale: float, out, lse, workspace, stream=None) -> None:
+    """gva_mla_decode_attention: cache.V holds the latent rows [rows, d_c], cache.K_rope the
+    shared positional keys; W_uk [H, d_c, d_n], W_uv [H, d_c, d_h] fp32; out [B, H, d_h]."""
+    d = dims.c()
+    cc = cache.c()
+    B, H, qd = dims.B, dims.H, _ELEM_DT.get(dims.q_dtype)
+    _need(q_nope, B * H * dims.d_n, "q_nope", qd)
+    if dims.d_r:
+        _need(q_rope, B * H * dims.d_r, "q_rope", qd)
+        _need(cache.K_rope, int(cache.rows.num_rows) * dims.d_r, "K_rope",
+              _ELEM_DT.get(dims.cache_dtype))
+    _need(cache.V, int(cache.rows.num_rows) * dims.d_c, "latent rows", _ELEM_DT.get(dims.cache_dtype))
+    _check_rows(cache.rows, B)
+    _need(W_uk, H * dims.d_c * dims.d_n, "W_uk")
+    _need(W_uv, H * dims.d_c * dims.d_h, "W_uv")
+    _need(seq_len, B, "seq_len")
+    _check_tab(rope_tab, dims.d_r)
+    _need(out, B * H * dims.d_h, "out")
+    _need(lse, B * H, "lse")
+    _check(_lib.gva_mla_decode_attention(
+        _stream(stream), ctypes.byref(d), _ptr(q_nope, None, "q_nope"),
+        _ptr(q_rope, None, "q_rope") if dims.d_r else None, _ptr(W_uk, torch.float32, "W_uk"),
+        _ptr(W_uv, torch.float32, "W_uv"), _ptr(seq_len, torch.int32, "seq_len"),
+        ctypes.byref(cc), _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size())),
+        "gva_mla_decode_attention")
+
+
+def mla_workspace(dims: MlaDims, device=None) -> torch.Tensor:
+    n = gva_mla_workspace_size(dims)
+    if n == 0:
+        raise GvaError(GVA_ERR_ARG, "gva_mla_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def gva_decode_attention_static(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cache, rope_tab,

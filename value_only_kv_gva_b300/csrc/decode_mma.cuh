@@ -66,6 +66,8 @@ struct MmaParams {
     int off_f;         // Ls[B], F[B+1]
     int off_merge;     // group-merge buffer
     int v3d;           // 1: one 3D TMA box per slab covers every value column
+    int vg;            // value groups stored per row: G, or 1 when every group of heads
+                       //    reads the same row (the latent rows of the MLA-shaped decode)
     int early;         // 1: the preceding kernel only writes the queries, so the cache
                        //    may be streamed before the grid dependency resolves
 };
@@ -419,11 +421,15 @@ __device__ __forceinline__ void slab_scores(uint32_t kst, uint32_t rst, int g, i
 #pragma unroll
         for (int a2 = 0; a2 < 2; ++a2)
             sc[nt][a2][0] = sc[nt][a2][1] = sc[nt][a2][2] = sc[nt][a2][3] = 0.f;
-    uint32_t av[KD][4];
+    // wide rows (d > 128) read each k-step's tile just before its products (registers)
+    constexpr bool STAGED = KD > 8;
+    uint32_t av[STAGED ? 1 : KD][4];
+    if constexpr (!STAGED) {
 #pragma unroll
-    for (int kk = 0; kk < KD; ++kk)
-        ldsm_x4(vtile_addr<DH>(kst, g, lm_row + 8 * (lm_mat & 1), 2 * kk + (lm_mat >> 1)),
-                av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
+        for (int kk = 0; kk < KD; ++kk)
+            ldsm_x4(vtile_addr<DH>(kst, g, lm_row + 8 * (lm_mat & 1), 2 * kk + (lm_mat >> 1)),
+                    av[kk][0], av[kk][1], av[kk][2], av[kk][3]);
+    }
     uint32_t ar[DRK16 > 0 ? DRK16 : 1][4], ar8[2];
     if (DR > 0) {
 #pragma unroll
@@ -433,11 +439,22 @@ __device__ __forceinline__ void slab_scores(uint32_t kst, uint32_t rst, int g, i
         if (DR_K8)
             ldsm_x2(rst + (lm_row + 8 * (lm_mat & 1)) * (DR * 2) + DRK16 * 32, ar8[0], ar8[1]);
     }
+    if constexpr (!STAGED) {
 #pragma unroll
-    for (int kk = 0; kk < KD; ++kk)
+        for (int kk = 0; kk < KD; ++kk)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            mma16816(sc[nt][kk & 1], av[kk], q.bq[kk][nt][0], q.bq[kk][nt][1]);
+            for (int nt = 0; nt < NT; ++nt)
+                mma16816(sc[nt][kk & 1], av[kk], q.bq[kk][nt][0], q.bq[kk][nt][1]);
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < KD; ++kk) {
+            ldsm_x4(vtile_addr<DH>(kst, g, lm_row + 8 * (lm_mat & 1), 2 * kk + (lm_mat >> 1)),
+                    av[0][0], av[0][1], av[0][2], av[0][3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma16816(sc[nt][kk & 1], av[0], q.bq[kk][nt][0], q.bq[kk][nt][1]);
+        }
+    }
     if (DR > 0) {
 #pragma unroll
         for (int kk = 0; kk < DRK16; ++kk)
@@ -493,7 +510,7 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
                                              uint32_t bar_empty, volatile int *abort,
                                              int *stage_bad, uint64_t pol) {
     const DecodeParams &p = mp.d;
-    const int NS = mp.nstages, G = p.G, B = p.B;
+    const int NS = mp.nstages, B = p.B;
     const int lane = threadIdx.x & 31;
     const int il = NS < 32 ? NS : 32;
     int stage = 0;                      // stage of the step's first slab
@@ -538,7 +555,7 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
                     if (s == s0) GVA_TRACE_AT(203);
                     if (GQA) tma_load_3d(stb + mp.off_k, tm_k, 0, yk, 0, fb, pol);
                 } else {
-                    for (int bx = 0; bx < G * (DH / 64); ++bx) {
+                    for (int bx = 0; bx < mp.vg * (DH / 64); ++bx) {
                         tma_load_2d(stb + bx * 2048, tm_v, bx * 64, yk, fb, pol);
                         if (GQA) tma_load_2d(stb + mp.off_k + bx * 2048, tm_k, bx * 64, yk, fb, pol);
                     }
@@ -588,7 +605,7 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
 // ---------------------------------------------------------------------------- //
 // the kernel
 // ---------------------------------------------------------------------------- //
-template <int DH, int DR, bool GQA, int NT>
+template <int DH, int DR, bool GQA, int NT, bool SV = false>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_k, const MmaParams mp) {
@@ -714,12 +731,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
             // ---- scores: A = the key tile (tokens x d), B = Q^T ----
             float sc[NT][2][4];
-            slab_scores<DH, DR, NT>(GQA ? st + mp.off_k : st, st + mp.off_r, g, lane, qf, sc);
+            slab_scores<DH, DR, NT>(GQA ? st + mp.off_k : st, st + mp.off_r, SV ? 0 : g, lane,
+                                    qf, sc);
             if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(100 + 10 * tslab);
             // value tiles for the weighted sum (V^T as the A operand), read while the
             // softmax below runs
-            uint32_t apv[KD][4];
-            slab_value_tiles<DH>(st, g, lane, apv);
+            // (wide value rows: the value tiles are read per output tile below instead)
+            constexpr bool STAGED = KD > 8;
+            uint32_t apv[STAGED ? 1 : KD][4];
+            if constexpr (!STAGED) slab_value_tiles<DH>(st, SV ? 0 : g, lane, apv);
 
             // ---- per head: hi + lo columns -> score of tokens gid, gid + 8 ----
             float z[NT][2];
@@ -771,12 +791,28 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             }
             // ---- O^T += V^T . P^T ----
             if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(102 + 10 * tslab);
-            if (nv < SLAB) mask_value_tiles<DH>(apv, nv, lane);
+            if constexpr (!STAGED) {
+                if (nv < SLAB) mask_value_tiles<DH>(apv, nv, lane);
 #pragma unroll
-            for (int mt = 0; mt < KD; ++mt)
+                for (int mt = 0; mt < KD; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816(oacc[mt][nt], apv[mt], bp[nt][0], bp[nt][1]);
+            } else {
+                const int lm_mat = lane >> 3, lm_row = lane & 7;
+                const int ta = 2 * tig, tb = 8 + 2 * tig;
+                const uint32_t ma = (ta >= nv ? 0u : 0xffffu) | (ta + 1 >= nv ? 0u : 0xffff0000u);
+                const uint32_t mb = (tb >= nv ? 0u : 0xffffu) | (tb + 1 >= nv ? 0u : 0xffff0000u);
+#pragma unroll
+                for (int mt = 0; mt < KD; ++mt) {
+                    uint32_t a[4];
+                    ldsm_x4_t(vtile_addr<DH>(st, SV ? 0 : g, lm_row + 8 * (lm_mat >> 1), 2 * mt + (lm_mat & 1)),
+                              a[0], a[1], a[2], a[3]);
+                    if (nv < SLAB) { a[0] &= ma; a[1] &= ma; a[2] &= mb; a[3] &= mb; }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816(oacc[mt][nt], a, bp[nt][0], bp[nt][1]);
+                }
+            }
             // the products above consumed every tile register, so all of the warp's
             // shared-memory reads of the stage are complete: release it to the producer
             if (w == 0 && g == 0 && lane == 0 && tslab < 8) GVA_TRACE_AT(103 + 10 * tslab);
@@ -967,7 +1003,7 @@ inline int merge_bytes_of(int wpg, int G, int DH, int NT) {
 
 inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
     const DecodeParams &d = mp.d;
-    const int vbytes = d.G * DH * SLAB * 2;
+    const int vbytes = mp.vg * DH * SLAB * 2;
     mp.off_k = vbytes;
     mp.off_r = vbytes * (gqa ? 2 : 1);
     const int rbytes = DR * SLAB * 2;
@@ -994,10 +1030,10 @@ inline size_t mma_smem_bytes(const MmaParams &mp, int DH, int NT) {
     return 1024 + (size_t)mp.off_merge + merge_bytes_of(mp.wpg, mp.d.G, DH, NT);
 }
 
-template <int DH, int DR, bool GQA, int NT>
+template <int DH, int DR, bool GQA, int NT, bool SV = false>
 inline int launch_mma_t(void *stream, MmaParams &mp, const CUtensorMap &tv, const CUtensorMap &tk,
                         int grid) {
-    auto kern = decode_mma_kernel<DH, DR, GQA, NT>;
+    auto kern = decode_mma_kernel<DH, DR, GQA, NT, SV>;
     const size_t smem = mma_smem_bytes(mp, DH, NT);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -1031,8 +1067,24 @@ inline cudaError_t mma_opt_in_dh() {
     }
     return cudaSuccess;
 }
+template <int DH>
+inline cudaError_t mma_opt_in_sv() {
+    const void *ks[] = {(const void *)decode_mma_kernel<DH, 0, false, 1, true>,
+                        (const void *)decode_mma_kernel<DH, 8, false, 1, true>,
+                        (const void *)decode_mma_kernel<DH, 16, false, 1, true>,
+                        (const void *)decode_mma_kernel<DH, 24, false, 1, true>,
+                        (const void *)decode_mma_kernel<DH, 32, false, 1, true>};
+    for (const void *k : ks) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_LIMIT);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 inline cudaError_t mma_opt_in_all() {
-    cudaError_t e = mma_opt_in_dh<64, 1>();
+    cudaError_t e = mma_opt_in_sv<128>();
+    if (e == cudaSuccess) e = mma_opt_in_sv<256>();
+    if (e == cudaSuccess) e = mma_opt_in_dh<64, 1>();
     if (e == cudaSuccess) e = mma_opt_in_dh<64, 2>();
     if (e == cudaSuccess) e = mma_opt_in_dh<128, 1>();
     if (e == cudaSuccess) e = mma_opt_in_dh<128, 2>();
@@ -1053,29 +1105,48 @@ inline int launch_mma_dr(void *stream, MmaParams &mp, const CUtensorMap &tv, con
     }
 }
 
-// Sets dp.n_ctas and launches the tensor-core decode (one CTA per SM by default).
+template <int DH>
+inline int launch_mma_sv(void *stream, MmaParams &mp, const CUtensorMap &tv, int grid, int DR) {
+    switch (DR) {
+    case 0: return launch_mma_t<DH, 0, false, 1, true>(stream, mp, tv, tv, grid);
+    case 8: return launch_mma_t<DH, 8, false, 1, true>(stream, mp, tv, tv, grid);
+    case 16: return launch_mma_t<DH, 16, false, 1, true>(stream, mp, tv, tv, grid);
+    case 24: return launch_mma_t<DH, 24, false, 1, true>(stream, mp, tv, tv, grid);
+    case 32: return launch_mma_t<DH, 32, false, 1, true>(stream, mp, tv, tv, grid);
+    default: return GVA_ERR_UNSUPPORTED;
+    }
+}
+
+// Sets dp.n_ctas and launches the tensor-core decode (one CTA per SM by default).  With
+// `shared_v` every one of the dp.G groups of dp.r <= 4 heads reads the same value row of
+// width dp.d_h in {128, 256} (the latent rows of the MLA-shaped decode).
 inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms, int req_ctas,
-                   bool gqa, bool early) {
+                   bool gqa, bool early, bool shared_v = false) {
     if (rows.num_rows > 0x7fffffffLL) return GVA_ERR_UNSUPPORTED;   // TMA row coordinate is int32
     MmaParams mp;
     mp.d = dp;
     const int DH = dp.d_h, DR = gqa ? 0 : dp.d_r;
     const int NT = dp.r <= 4 ? 1 : 2;   // 8-column tiles holding the group's heads (hi, lo)
+    if (shared_v && (gqa || NT != 1 || (DH != 128 && DH != 256))) return GVA_ERR_UNSUPPORTED;
+    mp.vg = shared_v ? 1 : dp.G;
     if (!plan_mma(mp, DH, DR, gqa, NT)) return GVA_ERR_UNSUPPORTED;
     const long long nrows = rows.num_rows > 0 ? rows.num_rows : 1;
     CUtensorMap tv, tk;
     mp.early = early ? 1 : 0;
-    mp.v3d = make_map3(&tv, dp.Vc, nrows, dp.G * DH) &&
-             (!gqa || make_map3(&tk, dp.Kc, nrows, dp.G * DH));
+    mp.v3d = make_map3(&tv, dp.Vc, nrows, mp.vg * DH) &&
+             (!gqa || make_map3(&tk, dp.Kc, nrows, mp.vg * DH));
     if (!mp.v3d) {
-        if (!make_map(&tv, dp.Vc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
-        if (gqa && !make_map(&tk, dp.Kc, nrows, dp.G * DH, 64, true)) return GVA_ERR_CUDA;
+        if (!make_map(&tv, dp.Vc, nrows, mp.vg * DH, 64, true)) return GVA_ERR_CUDA;
+        if (gqa && !make_map(&tk, dp.Kc, nrows, mp.vg * DH, 64, true)) return GVA_ERR_CUDA;
     }
     if (!gqa) tk = tv;
     int grid = req_ctas > 0 ? req_ctas : sms;
     if (grid > sms * 8) grid = sms * 8;
     dp.n_ctas = grid;
     mp.d.n_ctas = grid;
+    if (shared_v)
+        return DH == 128 ? launch_mma_sv<128>(stream, mp, tv, grid, DR)
+                         : launch_mma_sv<256>(stream, mp, tv, grid, DR);
     if (DH == 64)
         return NT == 1 ? launch_mma_dr<64, 1>(stream, mp, tv, tk, grid, DR, gqa)
                        : launch_mma_dr<64, 2>(stream, mp, tv, tk, grid, DR, gqa);

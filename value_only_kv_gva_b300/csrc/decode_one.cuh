@@ -670,6 +670,7 @@ inline bool one_supported(const gva_dims *d) { return mma_supported(d); }
 inline bool plan_one(OneParams &op, int DH, int DR, bool gqa, int NT) {
     MmaParams &mp = op.m;
     const DecodeParams &d = mp.d;
+    mp.vg = d.G;
     const int vbytes = d.G * DH * SLAB * 2;
     mp.off_k = vbytes;
     mp.off_r = vbytes * (gqa ? 2 : 1);

@@ -113,6 +113,7 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = max_carveout(append_kernel<float>);
     if (e == cudaSuccess) e = max_carveout(append_kernel<__nv_bfloat16>);
     if (e == cudaSuccess) e = max_carveout(combine_kernel);
+    if (e == cudaSuccess) e = max_carveout(mla_up_kernel);
     if (e == cudaSuccess) e = max_carveout(prefill_view_kernel);
     if (e == cudaSuccess) e = max_carveout(prefill_combine_kernel<64>);
     if (e == cudaSuccess) e = max_carveout(prefill_combine_kernel<128>);
@@ -439,12 +440,63 @@ __global__ void __launch_bounds__(PROBE_THREADS) read_probe_kernel(const uint4 *
 #pragma unroll
         for (int u = 0; u < PROBE_UNROLL; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
     }
+    // one atomic per CTA (same-address atomics serialise: one per warp would dominate a
+    // small buffer's time)
+    __shared__ unsigned warp_x[PROBE_THREADS / 32];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
-    if ((threadIdx.x & 31) == 0) atomicXor(sink, acc);
+    if ((threadIdx.x & 31) == 0) warp_x[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned x = 0;
+#pragma unroll
+        for (int k = 0; k < PROBE_THREADS / 32; ++k) x ^= warp_x[k];
+        atomicXor(sink, x);
+    }
 }
 
 // =========================================================================== //
+// MLA-shaped decode helpers (the entry points are below).
+namespace {
+
+bool mla_dims_ok(const gva_mla_dims *d) {
+    if (!d) return false;
+    if (d->B < 1 || d->B > MAX_B || d->H < 4 || d->H % 4 != 0 || d->H / 4 > MMA_CONSUMERS)
+        return false;
+    if (d->d_c != 128 && d->d_c != 256) return false;
+    if (d->d_n < 8 || d->d_n > 256 || d->d_n % 8 != 0) return false;
+    if (d->d_r < 0 || d->d_r > 32 || d->d_r % 8 != 0) return false;
+    if (d->d_h != 32 && d->d_h != 64 && d->d_h != 128 && d->d_h != 256) return false;
+    if (d->q_dtype != GVA_F32 && d->q_dtype != GVA_BF16) return false;
+    return d->cache_dtype == GVA_F32 || d->cache_dtype == GVA_BF16;
+}
+
+// The latent decode viewed as this library's decode: H/4 groups of 4 heads, every group
+// reading the whole latent row of width d_c.
+gva_dims mla_as_gva(const gva_mla_dims *d) {
+    gva_dims g;
+    g.B = d->B;
+    g.H = d->H;
+    g.G = d->H / 4;
+    g.d_h = d->d_c;
+    g.d_n = d->d_n;
+    g.d_r = d->d_r;
+    g.cache_dtype = d->cache_dtype;
+    g.q_dtype = d->q_dtype;
+    return g;
+}
+
+// Workspace: the decode's (queries, partials, slab offsets) for the latent width, then
+// the latent outputs [B][H][d_c].
+size_t mla_ws_bytes(const gva_mla_dims *d, int sms, size_t *off_lat) {
+    const gva_dims g = mla_as_gva(d);
+    const WsPlan w = plan_ws(&g, sms);
+    *off_lat = w.total;
+    return w.total + align_up(sizeof(float) * (size_t)d->B * d->H * d->d_c, 256);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char *gva_status_string(int s) {
@@ -844,6 +896,93 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     }
     if (st != GVA_OK) return st;
     return launch_combine(stream, dp, cache->rows);
+}
+
+// ---------------------------------------------------------------------------- //
+// MLA-shaped decode (the comparator with a latent cache)
+// ---------------------------------------------------------------------------- //
+size_t gva_mla_workspace_size(const gva_mla_dims *d) {
+    if (!mla_dims_ok(d)) return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    size_t off = 0;
+    return mla_ws_bytes(d, sms, &off);
+}
+
+int gva_mla_decode_attention(void *stream, const gva_mla_dims *d, const void *q_nope,
+                             const void *q_rope, const float *W_uk, const float *W_uv,
+                             const int *seq_len, const gva_cache *cache, const float *rope_tab,
+                             int rope_max_pos, float scale, float *out, float *lse, void *ws,
+                             size_t ws_bytes) {
+    if (!mla_dims_ok(d) || !cache || !rows_ok(&cache->rows, d->B)) return GVA_ERR_ARG;
+    if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
+    if (!q_nope || !W_uk || !W_uv || !seq_len || !cache->V || !aligned16(q_nope) ||
+        !aligned16(W_uk) || !aligned16(W_uv) || !aligned16(cache->V))
+        return GVA_ERR_ARG;
+    if (d->d_r > 0 && (!q_rope || !cache->K_rope || !rope_tab || rope_max_pos < 1 ||
+                       !aligned16(q_rope) || !aligned16(cache->K_rope) || !aligned16(rope_tab)))
+        return GVA_ERR_ARG;
+    if (d->cache_dtype != GVA_BF16) return GVA_ERR_UNSUPPORTED;   // tensor-core kernel only
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    const int sms = num_sms_current();
+    if (sms <= 0) return GVA_ERR_CUDA;
+    size_t off_lat = 0;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
+        ws_bytes < mla_ws_bytes(d, sms, &off_lat))
+        return GVA_ERR_WORKSPACE;
+    const gva_dims g = mla_as_gva(d);
+    const WsPlan plan = plan_ws(&g, sms);
+    char *w = static_cast<char *>(ws);
+    float *qt = reinterpret_cast<float *>(w + plan.qt);
+    float *qh = reinterpret_cast<float *>(w + plan.qh);
+    float *o_lat = reinterpret_cast<float *>(w + off_lat);
+    // 1. q~_h = scale log2(e) q_nope W_uk_h^T (width d_c); the decode rotates q_rope itself
+    int st = absorb_launch(stream, &g, q_nope, q_rope, W_uk, seq_len, rope_tab, rope_max_pos,
+                           scale * LOG2E, qt, qh, sms, &cache->rows, true, nullptr);
+    if (st != GVA_OK) return st;
+    // 2. split-K attention over the latent rows, 3. log-sum-exp merge into o_lat
+    DecodeParams dp;
+    memset(&dp, 0, sizeof(dp));
+    dp.B = d->B;
+    dp.H = d->H;
+    dp.G = d->H / 4;
+    dp.r = 4;
+    dp.d_h = d->d_c;
+    dp.d_r = d->d_r;
+    dp.seq_len = seq_len;
+    dp.R = to_dev(cache->rows);
+    dp.Kc = cache->V;
+    dp.Vc = cache->V;
+    dp.Krope = cache->K_rope;
+    dp.qc = qt;
+    dp.qc_f32 = 1;
+    dp.qc_scale = 1.f;
+    dp.qr = nullptr;
+    dp.q_rope = q_rope;
+    dp.qr_f32 = d->q_dtype == GVA_F32;
+    dp.rope_tab = rope_tab;
+    dp.rope_max_pos = rope_max_pos;
+    dp.qr_scale = scale * LOG2E;
+    dp.out = o_lat;
+    dp.lse = lse;
+    dp.part_o = reinterpret_cast<float *>(w + plan.po);
+    dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
+    dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
+    st = run_mma(stream, dp, cache->rows, sms, 0, false, true, true);
+    if (st != GVA_OK) return st;
+    st = launch_combine(stream, dp, cache->rows);
+    if (st != GVA_OK) return st;
+    // 4. out[b,h] = o_lat[b,h] W_uv_h
+    UpProjParams up;
+    up.B = d->B;
+    up.H = d->H;
+    up.d_c = d->d_c;
+    up.d_h = d->d_h;
+    up.o_lat = o_lat;
+    up.Wuv = W_uv;
+    up.out = out;
+    return cuda_status(launch(mla_up_kernel, dim3(d->H, (d->B + UP_SEQ - 1) / UP_SEQ),
+                              dim3(UP_THREADS), mla_up_smem_bytes(d->d_c), stream, up));
 }
 
 // ---------------------------------------------------------------------------- //

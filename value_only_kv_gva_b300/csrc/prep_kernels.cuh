@@ -393,4 +393,67 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
     if (threadIdx.x == 0) GVA_REC(2, 2);
 }
 
+// --------------------------------------------------------------------------- //
+// MLA-shaped decode: per-head up-projection of the latent attention output
+// (KV-cache compression survey, MLA sections: the value of head h is c_j W^UV_h, so
+// sum_j p_j (c_j W^UV_h) = (sum_j p_j c_j) W^UV_h)
+// --------------------------------------------------------------------------- //
+struct UpProjParams {
+    int B, H, d_c, d_h;
+    const float *o_lat;     // [B][H][d_c]  softmax-weighted latent rows
+    const float *Wuv;       // [H][d_c][d_h]
+    float *out;             // [B][H][d_h]
+};
+constexpr int UP_THREADS = 256;
+constexpr int UP_SEQ = 8;      // sequences per CTA (one map read serves all of them)
+constexpr int UP_UNROLL = 16;  // map loads in flight per thread
+
+// Grid (H, ceil(B / UP_SEQ)).  The CTA's threads are (c-quarter, output column d) pairs:
+// each sums UP_SEQ dot products over its quarter of the latent width with UP_UNROLL map
+// loads in flight, then the quarters are added through shared memory.
+__global__ void __launch_bounds__(UP_THREADS) mla_up_kernel(const UpProjParams p) {
+    extern __shared__ float s_up[];           // o rows [UP_SEQ][d_c], then partial sums
+    pdl_wait();
+    pdl_launch_dependents();
+    const int h = blockIdx.x, b0 = blockIdx.y * UP_SEQ;
+    const int nb = min(UP_SEQ, p.B - b0);
+    float *so = s_up;
+    float *sp = s_up + UP_SEQ * p.d_c;        // [UP_THREADS][UP_SEQ]
+    for (int e = threadIdx.x; e < UP_SEQ * p.d_c; e += UP_THREADS) {
+        const int bi = e / p.d_c, c = e % p.d_c;
+        so[e] = bi < nb ? p.o_lat[((long long)(b0 + bi) * p.H + h) * p.d_c + c] : 0.f;
+    }
+    __syncthreads();
+    const int splits = UP_THREADS / p.d_h;    // d_h divides UP_THREADS
+    const int d = threadIdx.x % p.d_h, part = threadIdx.x / p.d_h;
+    const int c_per = p.d_c / splits, c0 = part * c_per;
+    const float *w = p.Wuv + ((long long)h * p.d_c + c0) * p.d_h + d;
+    float acc[UP_SEQ];
+#pragma unroll
+    for (int bi = 0; bi < UP_SEQ; ++bi) acc[bi] = 0.f;
+    for (int cc = 0; cc < c_per; cc += UP_UNROLL) {   // c_per is a multiple of UP_UNROLL
+        float wv[UP_UNROLL];
+#pragma unroll
+        for (int u = 0; u < UP_UNROLL; ++u) wv[u] = __ldg(w + (long long)(cc + u) * p.d_h);
+#pragma unroll
+        for (int u = 0; u < UP_UNROLL; ++u)
+#pragma unroll
+            for (int bi = 0; bi < UP_SEQ; ++bi)
+                acc[bi] = fmaf(so[bi * p.d_c + c0 + cc + u], wv[u], acc[bi]);
+    }
+#pragma unroll
+    for (int bi = 0; bi < UP_SEQ; ++bi) sp[threadIdx.x * UP_SEQ + bi] = acc[bi];
+    __syncthreads();
+    if (threadIdx.x < p.d_h) {
+        for (int bi = 0; bi < nb; ++bi) {
+            float v = 0.f;
+            for (int k = 0; k < splits; ++k) v += sp[(k * p.d_h + d) * UP_SEQ + bi];
+            p.out[((long long)(b0 + bi) * p.H + h) * p.d_h + d] = v;
+        }
+    }
+}
+inline size_t mla_up_smem_bytes(int d_c) {
+    return sizeof(float) * ((size_t)UP_SEQ * d_c + (size_t)UP_THREADS * UP_SEQ);
+}
+
 }  // namespace gva
