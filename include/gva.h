@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define GVA_ABI_VERSION 4
+#define GVA_ABI_VERSION 5
 
 typedef enum {
     GVA_OK = 0,
@@ -309,6 +309,44 @@ int gva_mla_decode_attention(void *stream, const gva_mla_dims *dims, const void 
                              const int *seq_len, const gva_cache *cache, const float *rope_tab,
                              int rope_max_pos, float scale, float *out, float *lse,
                              void *workspace, size_t ws_bytes);
+
+/* ------------------------------------------------------------------------- */
+/* Decode of the variant with ordinary RoPE on the reconstructed key.           */
+/* The agihunt summary (results discussion) describes a scale-matched GVA row   */
+/* that rotates the rebuilt key K_h = V_g M_h itself with plain RoPE, so that   */
+/* M_h can no longer be folded into the query; the analysis page (关键技巧二)   */
+/* explains why: the relative rotation would sit between q and M_h^T.  The     */
+/* pages give no formula; this library reads it as                              */
+/*   z_j = scale * (Rot(t) q_h) . (Rot(j) v_{j,g} M_h),  t = L_b - 1,             */
+/*   out[b,h] = sum_j softmax(z)_j v_{j,g},  lse[b,h] = logsumexp_j z_j,          */
+/* with Rot over d_n dimensions in interleaved pairs (theta_i over d_n) and no  */
+/* separate positional key.  Each token costs d_h * d_n multiply-adds per head  */
+/* on the tensor cores.                                                          */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of device workspace gva_rope_keys_decode_attention needs for `dims` on the
+ * current device (0 on invalid dims).  dims->d_r must be 0. */
+size_t gva_rope_keys_workspace_size(const gva_dims *dims);
+
+/* Decode of the variant above, one new query per sequence.
+ *   q        device [B][H][d_n] (dims->q_dtype), the whole query of each head
+ *   M        device fp32 [H][d_h][d_n]
+ *   seq_len  device int [B]; L_b = 0 gives out = 0, lse = -inf
+ *   cache    value rows [G][d_h] in cache->V (bf16 runs; fp32 returns
+ *            GVA_ERR_UNSUPPORTED), laid out by cache->rows; cache->K_rope is not read
+ *   rope_tab device fp32 [rope_max_pos][d_n/2][2] (cos, sin)(p theta_i), theta_i =
+ *            base^(-2i/d_n) (gva_rope_table_fill with d_r = d_n); rope_max_pos >= 128
+ *            and >= every L_b (a longer sequence counts as empty and sets
+ *            GVA_DEV_BAD_POSITION)
+ *   out      device fp32 [B][H][d_h]; lse device fp32 [B][H] or NULL
+ *   workspace device, 256-byte aligned, >= gva_rope_keys_workspace_size(dims); scratch only
+ * Runs for d_h and d_n in {64, 128} (else GVA_ERR_UNSUPPORTED).  All device buffers are
+ * caller-owned and 16-byte aligned; asynchronous on `stream`.  Errors as
+ * gva_decode_attention. */
+int gva_rope_keys_decode_attention(void *stream, const gva_dims *dims, const void *q,
+                                   const float *M, const int *seq_len, const gva_cache *cache,
+                                   const float *rope_tab, int rope_max_pos, float scale,
+                                   float *out, float *lse, void *workspace, size_t ws_bytes);
 
 /* Size of the fixed device array behind gva_decode_attention_static (24 MiB). */
 #define GVA_STATIC_SCRATCH_BYTES (24u << 20)

@@ -49,7 +49,7 @@ def test_every_declared_symbol_is_exported(gva):
 
 
 def test_abi_version_and_status_strings(gva):
-    assert gva.gva_abi_version() == 4
+    assert gva.gva_abi_version() == 5
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 3, 4):
         s = gva.gva_status_string(code)
         assert s and "unknown" not in s

@@ -98,6 +98,10 @@ _lib.gva_mla_workspace_size.restype = _Z
 _lib.gva_mla_workspace_size.argtypes = [ctypes.POINTER(gva_mla_dims)]
 _lib.gva_mla_decode_attention.argtypes = [_P, ctypes.POINTER(gva_mla_dims), _P, _P, _P, _P, _P,
                                           _PC, _P, _I, _F, _P, _P, _P, _Z]
+_lib.gva_rope_keys_workspace_size.restype = _Z
+_lib.gva_rope_keys_workspace_size.argtypes = [_PD]
+_lib.gva_rope_keys_decode_attention.argtypes = [_P, _PD, _P, _P, _P, _PC, _P, _I, _F, _P, _P,
+                                                _P, _Z]
 _lib.gva_prefill_attention.argtypes = [_P, _PD, _I, _P, _P, _P, _P, _P, _P, _PC, _P, _I, _F,
                                        _P, _P, _P, _Z, _PO]
 
@@ -106,7 +110,8 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_decode_attention", "gva_decode_attention_ex", "gva_gqa_decode_attention",
            "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static",
            "gva_read_probe", "gva_absorb_query_ex", "gva_prefill_workspace_size",
-           "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention"]
+           "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention",
+           "gva_rope_keys_workspace_size", "gva_rope_keys_decode_attention"]
 
 
 class GvaError(RuntimeError):
@@ -541,6 +546,46 @@ def mla_workspace(dims: MlaDims, device=None) -> torch.Tensor:
     n = gva_mla_workspace_size(dims)
     if n == 0:
         raise GvaError(GVA_ERR_ARG, "gva_mla_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gva_rope_keys_workspace_size(dims: Dims) -> int:
+    d = dims.c()
+    return int(_lib.gva_rope_keys_workspace_size(ctypes.byref(d)))
+
+
+def gva_rope_keys_decode_attention(dims: Dims, q, M, seq_len, cache: Cache, rope_tab,
+                                   scale: float, out, lse, workspace, stream=None) -> None:
+    """gva_rope_keys_decode_attention: the variant with ordinary RoPE on the reconstructed
+    key.  q [B, H, d_n] (the whole query), M [H, d_h, d_n] fp32, cache.V the value rows
+    [rows, G, d_h] (cache.K_rope unused), rope_tab [max_pos, d_n/2, 2] over d_n (max_pos
+    >= 128 and >= every length), dims.d_r = 0; out [B, H, d_h], lse [B, H] or None."""
+    d = dims.c()
+    cc = cache.c()
+    B, H, qd = dims.B, dims.H, _ELEM_DT.get(dims.q_dtype)
+    _need(q, B * H * dims.d_n, "q", qd)
+    _need(M, H * dims.d_h * dims.d_n, "M")
+    _need(seq_len, B, "seq_len")
+    _check_rows(cache.rows, B)
+    _need(cache.V, int(cache.rows.num_rows) * dims.G * dims.d_h, "V",
+          _ELEM_DT.get(dims.cache_dtype))
+    _check_tab(rope_tab, dims.d_n)
+    _need(out, B * H * dims.d_h, "out")
+    if lse is not None:
+        _need(lse, B * H, "lse")
+    _check(_lib.gva_rope_keys_decode_attention(
+        _stream(stream), ctypes.byref(d), _ptr(q, None, "q"), _ptr(M, torch.float32, "M"),
+        _ptr(seq_len, torch.int32, "seq_len"), ctypes.byref(cc),
+        _ptr(rope_tab, torch.float32, "rope_tab"), int(rope_tab.shape[0]), float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size())),
+        "gva_rope_keys_decode_attention")
+
+
+def rope_keys_workspace(dims: Dims, device=None) -> torch.Tensor:
+    n = gva_rope_keys_workspace_size(dims)
+    if n == 0:
+        raise GvaError(GVA_ERR_ARG, "gva_rope_keys_workspace_size")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 

@@ -15,6 +15,7 @@
 #include "decode_mma.cuh"
 #include "decode_one.cuh"
 #include "prefill_mma.cuh"
+#include "decode_rope_keys.cuh"
 
 using namespace gva;
 
@@ -110,6 +111,7 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = mma_opt_in_all();
     if (e == cudaSuccess) e = one_opt_in_all();
     if (e == cudaSuccess) e = prefill_opt_in_all();
+    if (e == cudaSuccess) e = rk_opt_in_all();
     if (e == cudaSuccess) e = max_carveout(append_kernel<float>);
     if (e == cudaSuccess) e = max_carveout(append_kernel<__nv_bfloat16>);
     if (e == cudaSuccess) e = max_carveout(combine_kernel);
@@ -494,6 +496,56 @@ size_t mla_ws_bytes(const gva_mla_dims *d, int sms, size_t *off_lat) {
     *off_lat = w.total;
     return w.total + align_up(sizeof(float) * (size_t)d->B * d->H * d->d_c, 256);
 }
+
+}  // namespace
+
+// =========================================================================== //
+// Helpers of the decode with RoPE on the reconstructed key (entry points below).
+namespace {
+
+bool rk_dims_ok(const gva_dims *d) {
+    if (!d) return false;
+    if (d->B < 1 || d->B > MAX_B || d->H < 1 || d->G < 1 || d->H % d->G != 0) return false;
+    if (d->d_r != 0) return false;                     // the query is d_n wide, no extra slice
+    if (d->d_h < 8 || d->d_h > 256 || d->d_h % 8 != 0) return false;
+    if (d->d_n < 2 || d->d_n > 256 || d->d_n % 2 != 0) return false;
+    if (d->q_dtype != GVA_F32 && d->q_dtype != GVA_BF16) return false;
+    return d->cache_dtype == GVA_F32 || d->cache_dtype == GVA_BF16;
+}
+
+// Workspace: [Ls B][pre B+1] | images [streams][hi, lo] | part_o [slots][hc][d_h] |
+// part_ml [slots][hc][2]; streams = B G nhs, slots = streams + CTAs.
+struct RkWs {
+    size_t ls, pre, img, po, pm, total;
+    int hc, nhs;
+};
+
+RkWs rk_plan(const gva_dims *d, int sms) {
+    RkWs w;
+    const int r = d->H / d->G;
+    w.hc = rk_hc(r, d->d_n);
+    w.nhs = r / w.hc;
+    const long long streams = (long long)d->B * d->G * w.nhs;
+    const long long slots = streams + sms;
+    size_t o = 0;
+    w.ls = o;
+    o += sizeof(int) * d->B;
+    w.pre = o;
+    o += sizeof(int) * (d->B + 1);
+    o = align_up(o, 256);
+    w.img = o;
+    o += (size_t)streams * rk_img_bytes(d->d_h, w.hc * d->d_n);
+    o = align_up(o, 256);
+    w.po = o;
+    o += sizeof(float) * (size_t)slots * w.hc * d->d_h;
+    o = align_up(o, 256);
+    w.pm = o;
+    o += sizeof(float) * (size_t)slots * w.hc * 2;
+    w.total = align_up(o, 256);
+    return w;
+}
+
+int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 
 }  // namespace
 
@@ -983,6 +1035,72 @@ int gva_mla_decode_attention(void *stream, const gva_mla_dims *d, const void *q_
     up.out = out;
     return cuda_status(launch(mla_up_kernel, dim3(d->H, (d->B + UP_SEQ - 1) / UP_SEQ),
                               dim3(UP_THREADS), mla_up_smem_bytes(d->d_c), stream, up));
+}
+
+// ---------------------------------------------------------------------------- //
+// Decode with ordinary RoPE on the reconstructed key (M_h not absorbable)
+// ---------------------------------------------------------------------------- //
+size_t gva_rope_keys_workspace_size(const gva_dims *d) {
+    if (!rk_dims_ok(d)) return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    return rk_plan(d, sms).total;
+}
+
+int gva_rope_keys_decode_attention(void *stream, const gva_dims *d, const void *q, const float *M,
+                                   const int *seq_len, const gva_cache *cache,
+                                   const float *rope_tab, int rope_max_pos, float scale,
+                                   float *out, float *lse, void *ws, size_t ws_bytes) {
+    if (!rk_dims_ok(d) || !cache || !rows_ok(&cache->rows, d->B)) return GVA_ERR_ARG;
+    if (!q || !M || !seq_len || !cache->V || !rope_tab || !out) return GVA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(M) || !aligned16(cache->V) || !aligned16(rope_tab) ||
+        !aligned16(out) || (lse && !aligned16(lse)))
+        return GVA_ERR_ARG;
+    if (rope_max_pos < RK_TILE || !std::isfinite(scale)) return GVA_ERR_ARG;
+    if (!rk_supported(d)) return GVA_ERR_UNSUPPORTED;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    const int sms = num_sms_current();
+    if (sms <= 0) return GVA_ERR_CUDA;
+    const RkWs w = rk_plan(d, sms);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w.total)
+        return GVA_ERR_WORKSPACE;
+    char *wb = static_cast<char *>(ws);
+    RkParams p;
+    memset(&p, 0, sizeof(p));
+    p.B = d->B;
+    p.H = d->H;
+    p.G = d->G;
+    p.r = d->H / d->G;
+    p.d_h = d->d_h;
+    p.d_n = d->d_n;
+    p.hc = w.hc;
+    p.nhs = w.nhs;
+    p.seq_len = seq_len;
+    p.R = to_dev(cache->rows);
+    p.q = q;
+    p.q_f32 = d->q_dtype == GVA_F32;
+    p.M = M;
+    p.tab = rope_tab;
+    p.tab_rows = rope_max_pos;
+    p.scale_log2 = scale * LOG2E;
+    p.img = reinterpret_cast<unsigned char *>(wb + w.img);
+    p.Ls = reinterpret_cast<int *>(wb + w.ls);
+    p.pre = reinterpret_cast<int *>(wb + w.pre);
+    p.part_o = reinterpret_cast<float *>(wb + w.po);
+    p.part_ml = reinterpret_cast<float *>(wb + w.pm);
+    p.out = out;
+    p.lse = lse;
+    p.n_ctas = sms;
+    p.ch = cache->rows.layout == GVA_LAYOUT_PAGED ? gcd_int(cache->rows.page_size, 64) : 64;
+    CUtensorMap tv;
+    if (!rk_make_map(&tv, cache->V, cache->rows.num_rows, d->G * d->d_h, p.ch)) return GVA_ERR_CUDA;
+    int st = cuda_status(launch(rk_prep_kernel, dim3(d->B * d->H + 1), dim3(RK_PREP_THREADS), 0,
+                                stream, p));
+    if (st != GVA_OK) return st;
+    st = rk_launch_decode(stream, p, tv);
+    if (st != GVA_OK) return st;
+    return cuda_status(launch(rk_merge_kernel, dim3(d->B * d->H), dim3(RK_MERGE_THREADS), 0,
+                              stream, p));
 }
 
 // ---------------------------------------------------------------------------- //

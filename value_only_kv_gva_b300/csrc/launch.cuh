@@ -34,9 +34,9 @@ inline bool pdl_allowed(cudaStream_t s) {
     return true;
 }
 
-template <typename Kern, typename Params>
+template <typename Kern, typename... Params>
 cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, void *stream,
-                   const Params &params) {
+                   const Params &...params) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = grid;
@@ -48,7 +48,7 @@ cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, void *stream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_allowed(cfg.stream) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, params);
+    return cudaLaunchKernelEx(&cfg, kernel, params...);
 }
 
 inline int cuda_status(cudaError_t e) {
