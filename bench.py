@@ -31,6 +31,7 @@ if ROOT not in sys.path:
 METRIC = "GVA decode cache-read HBM GB/s (% of B300 peak) and μs/step, B=8 T=4096"
 SPEC_HBM_GBS = 8000.0          # the "~8 TB/s" B300 HBM figure the target is stated against
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_SUSTAINED = 1400.0
 
 
 def log(*a):
@@ -341,6 +342,77 @@ def measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path, 
     return out
 
 
+def measure_rope_keys(args, dist, torch, gva, gva_inputs, name, stream, dev, sampler):
+    """The variant with ordinary RoPE on the reconstructed key (gva_rope_keys_decode_attention)
+    on workload `name`'s shape with the query d_n wide and no positional slice: nl decode
+    calls on distinct layer caches (more than L2 in all), one CUDA graph, timed on
+    `stream`.  It is a dense contraction (2 d_h d_n flops per token and head, the
+    algorithmic count), run as two bf16 products per weight (high and low parts)."""
+    w = gva_inputs.workload(name)
+    nl = default_layers(w)
+    c = gva_inputs.make_case(w)
+    lengths = c.seq_len.tolist()
+    dims = gva.Dims(w.B, w.H, w.G, w.d_h, w.d_n, 0, gva.GVA_BF16,
+                    gva.GVA_F32 if w.q_dtype == "f32" else gva.GVA_BF16)
+    if gva.gva_rope_keys_workspace_size(dims) == 0:
+        return None
+    V0 = c.V.to(dev)
+    offs = c.offsets.to(dev) if c.offsets is not None else None
+    bt = c.block_table.to(dev) if c.block_table is not None else None
+    rows = gva.Rows(w.layout, c.num_rows, T_cap=c.T_cap, offsets=offs, block_table=bt,
+                    page_size=w.page_size)
+    tab = torch.from_numpy(_rope_keys_table(max(128, int(max(lengths)) + 1), w.d_n, w.base)).to(dev)
+    seq = c.seq_len.to(dev)
+    ws = gva.rope_keys_workspace(dims, dev)
+    layers = []
+    for li in range(nl):
+        layers.append(dict(cache=gva.Cache(rows, V0.clone() if li else V0, None),
+                           q=c.q_nope.to(dev).clone(), M=c.M.to(dev).clone(),
+                           out=torch.empty((w.B, w.H, w.d_h), device=dev),
+                           lse=torch.empty((w.B, w.H), device=dev)))
+
+    def call(L):
+        gva.gva_rope_keys_decode_attention(dims, L["q"], L["M"], seq, L["cache"], tab, w.scale,
+                                           L["out"], L["lse"], ws)
+    g = capture_list(torch, stream, layers, call)
+    assert gva.gva_get_device_status() == 0
+    secs, step_ms = timed_graph(torch, dist, stream, g, args.steps, max(3, args.warmup), sampler)
+    us = dist.max(secs, dev) / (args.steps * nl) * 1e6
+    ck = sampler.summary(sampler.t_marks["t0"], sampler.t_marks["t1"])
+    tokens = int(sum(int(L) for L in lengths))
+    flops = 2.0 * tokens * w.H * w.d_h * w.d_n
+    tflops = flops / (us * 1e-6) / 1e12
+    peaks = measured_peaks()
+    pk = (peaks["bf16_tflops_sustained"] if peaks else FALLBACK_BF16_SUSTAINED)
+    cache_bytes = tokens * w.G * w.d_h * 2
+    del g, layers, V0, ws
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"{name} shape, RoPE on the reconstructed key: B={w.B} H={w.H} G={w.G} "
+                    f"d_h={w.d_h} d_n={w.d_n} (query d_n wide) "
+                    + (f"T={w.T}" if w.layout == "contiguous" else f"{w.layout} lengths")
+                    + f" bf16 cache; {nl} layer(s) per graph",
+        "us_per_decode": round(us, 3),
+        "median_us_per_decode": round(statistics.median(step_ms) * 1e3 / nl, 3),
+        "flops_per_decode": flops, "cache_bytes_per_decode": cache_bytes,
+        "cache_gbs": round(cache_bytes / (us * 1e-6) / 1e9, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
+                     "peak": pk, "unit": "TFLOP/s", "frac": round(tflops / pk, 4),
+                     "peak_source": ("measured bf16, sustained" if peaks else "fallback"),
+                     "mma_flops_issued_frac": round(2 * tflops / pk, 4),
+                     "note": "algorithmic flops (2 d_h d_n per token and head); the kernel "
+                             "issues two bf16 products per weight (high and low parts)"},
+        "launches_per_decode": 3,
+        "clocks": ck,
+    }
+
+
+def _rope_keys_table(rows: int, d_n: int, base: float):
+    """(cos, sin)(p theta_i) over d_n, fp32 from fp64 (the library's host routine)."""
+    import value_only_kv_gva_b300 as gva
+    return gva.gva_rope_table_fill(rows, d_n, base).numpy()
+
+
 def single_pass_floor(gva, torch, dist, stream, dev, nbytes, nl, K, W):
     """The fastest single pass over `nbytes` this GPU gives one kernel in the same launch
     configuration as the decode op: `nl` distinct buffers of `nbytes` (more than L2 in
@@ -368,6 +440,18 @@ def run_ours(args, dist: Dist):
     dist.init("nccl")
     stream = torch.cuda.Stream(device=dev)
     path = args.path
+    if args.rope_keys_only:
+        sampler = ClockSampler(dev.index if dev.index is not None else 0)
+        sampler.start()
+        time.sleep(0.3)
+        res = {n: measure_rope_keys(args, dist, torch, gva, gva_inputs, n, stream, dev, sampler)
+               for n in args.rope_keys}
+        sampler.stop()
+        if dist.rank == 0:
+            print(json.dumps({"rope_keys_variant": res, "steps": args.steps,
+                              "warmup": args.warmup}), flush=True)
+        dist.close()
+        return
     S = LayerStack(gva, torch, gva_inputs, args.workload, args.layers, dev)
     w, nl = S.w, S.nl
     log(f"[bench] workload {w.name}: B={w.B} H={w.H} G={w.G} d_h={w.d_h} d_r={w.d_r} "
@@ -421,6 +505,12 @@ def run_ours(args, dist: Dist):
                 "clocks": ck}
             del S2
             torch.cuda.empty_cache()
+    rope_keys = {}
+    if not args.no_rope_keys:
+        for name in args.rope_keys:
+            rk = measure_rope_keys(args, dist, torch, gva, gva_inputs, name, stream, dev, sampler)
+            if rk:
+                rope_keys[name] = rk
     sampler.stop()
 
     # the CPU oracle on a bounded sample (rank 0 only)
@@ -457,6 +547,7 @@ def run_ours(args, dist: Dist):
             "gqa_comparator": m.get("gqa_comparator"),
             "mla_comparator": m.get("mla_comparator"),
             "other_workloads": others or None,
+            "rope_keys_variant": rope_keys or None,
         },
         "roofline": {"bound": "hbm", "kernel": "gva_decode_attention (absorb + split-K "
                      "partial + combine), per call", "achieved": round(achieved, 1),
@@ -893,6 +984,14 @@ def main():
     ap.add_argument("--others", nargs="*", default=["long", "paged"],
                     help="further workloads measured in the same run (config.other_workloads)")
     ap.add_argument("--no-others", action="store_true")
+    ap.add_argument("--no-rope-keys", action="store_true",
+                    help="skip the variant with RoPE on the reconstructed key "
+                         "(config.rope_keys_variant)")
+    ap.add_argument("--rope-keys", nargs="*", default=["350m", "long"],
+                    help="workload shapes of config.rope_keys_variant")
+    ap.add_argument("--rope-keys-only", action="store_true",
+                    help="measure only the variant with RoPE on the reconstructed key and "
+                         "print its figures (a profiling aid; not the bench line)")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time the causal chunked prefill of this many new tokens per "
                          "sequence instead of the decode step")

@@ -44,8 +44,9 @@ namespace gva {
 
 constexpr int RK_TILE = 128;          // tokens per work unit (the MMA's M)
 constexpr int RK_EPI_WARPS = 8;       // two per tensor-memory lane quarter
+constexpr int RK_EPI_T = RK_EPI_WARPS * 32;
 constexpr int RK_THREADS = (RK_EPI_WARPS + 2) * 32;
-constexpr int RK_PREP_THREADS = 256;
+constexpr int RK_PREP_THREADS = 128;   // >= d_n
 constexpr int RK_MERGE_THREADS = 128;
 constexpr int RK_MAX_STAGES = 6;
 constexpr float RK_RESCALE_TH = 8.f;  // log2 units
@@ -88,13 +89,16 @@ __device__ __forceinline__ bool rk_len_ok(const RkParams &p, int b, int L) {
     return length_ok(p.R, b, L) && L <= p.tab_rows;
 }
 
-// Blocks [0, B H): the image rows of head h for sequence b.  Block B H: lengths and the
-// unit prefix (units of sequence b: ceil(L_b / 128) tiles x G x nhs streams).
+// Blocks [0, B H d_h / 8): for (sequence b, head h, value rows 8 ic .. 8 ic + 7), thread k
+// writes image row hh d_n + k of those rows (one 16-byte chunk of the high and of the low
+// image).  The last block: lengths and the unit prefix (units of sequence b:
+// ceil(L_b / 128) tiles x G x nhs streams).
 __global__ void __launch_bounds__(RK_PREP_THREADS) rk_prep_kernel(const RkParams p) {
     pdl_wait();
     pdl_launch_dependents();
+    const int dn = p.d_n, dh = p.d_h, nic = dh / 8;
     const int blk = blockIdx.x;
-    if (blk == p.B * p.H) {
+    if (blk == p.B * p.H * nic) {
         for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
             int L = p.seq_len[b];
             if (!rk_len_ok(p, b, L)) {
@@ -125,52 +129,43 @@ __global__ void __launch_bounds__(RK_PREP_THREADS) rk_prep_kernel(const RkParams
         }
         return;
     }
-    __shared__ float Qs[256];
-    const int b = blk / p.H, h = blk % p.H;
-    const int dn = p.d_n, dh = p.d_h;
+    const int k = threadIdx.x;
+    if (k >= dn) return;
+    const int ic = blk % nic, bh = blk / nic, b = bh / p.H, h = bh % p.H;
     const int L = p.seq_len[b];
     const int t = (rk_len_ok(p, b, L) && L > 0) ? L - 1 : 0;
-    const long long qb = ((long long)b * p.H + h) * dn;
-    for (int i = threadIdx.x; i < dn / 2; i += blockDim.x) {
-        const float q0 = rk_ld_q(p.q, p.q_f32, qb + 2 * i);
-        const float q1 = rk_ld_q(p.q, p.q_f32, qb + 2 * i + 1);
-        const float c = p.tab[((long long)t * (dn / 2) + i) * 2];
-        const float s = p.tab[((long long)t * (dn / 2) + i) * 2 + 1];
-        Qs[2 * i] = (q0 * c - q1 * s) * p.scale_log2;
-        Qs[2 * i + 1] = (q0 * s + q1 * c) * p.scale_log2;
-    }
-    __syncthreads();
+    // this thread's rotation pair of Q = scale log2(e) Rot(t) q_bh
+    const int pp = k >> 1;
+    const long long qb = (long long)bh * dn;
+    const float q0 = rk_ld_q(p.q, p.q_f32, qb + 2 * pp);
+    const float q1 = rk_ld_q(p.q, p.q_f32, qb + 2 * pp + 1);
+    const float2 cs = reinterpret_cast<const float2 *>(p.tab)[(long long)t * (dn / 2) + pp];
+    const float Q0 = (q0 * cs.x - q1 * cs.y) * p.scale_log2;
+    const float Q1 = (q0 * cs.y + q1 * cs.x) * p.scale_log2;
     const int g = h / p.r, hl = h % p.r, hs = hl / p.hc, hh = hl % p.hc;
     const int N = p.hc * dn;
     const long long stream = ((long long)b * p.G + g) * p.nhs + hs;
     unsigned char *img = p.img + stream * rk_img_bytes(dh, N);
-    const size_t lo_off = (size_t)dh * N * 2;
-    const float *Mh = p.M + (long long)h * dh * dn;
-    // item (k, ic): output column k, value columns 8 ic .. 8 ic + 7 (one 16-byte chunk)
-    for (int w = threadIdx.x; w < dn * (dh / 8); w += blockDim.x) {
-        const int k = w % dn, ic = w / dn, pp = k >> 1;
-        const float Q0 = Qs[2 * pp], Q1 = Qs[2 * pp + 1];
-        uint32_t hw[4], lw[4];
+    const float2 *Mp = reinterpret_cast<const float2 *>(p.M + (long long)h * dh * dn) + pp;
+    float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            float x[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int i = ic * 8 + e + u;
-                const float m0 = Mh[(long long)i * dn + 2 * pp], m1 = Mh[(long long)i * dn + 2 * pp + 1];
-                x[u] = (k & 1) ? (m0 * Q1 - m1 * Q0) : (m0 * Q0 + m1 * Q1);
-            }
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(x[0]), h1 = __float2bfloat16_rn(x[1]);
-            const __nv_bfloat16 l0 = __float2bfloat16_rn(x[0] - __bfloat162float(h0));
-            const __nv_bfloat16 l1 = __float2bfloat16_rn(x[1] - __bfloat162float(h1));
-            hw[e / 2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-            lw[e / 2] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-        }
-        const int n = hh * dn + k;
-        const size_t off = (size_t)(ic >> 3) * N * 128 + (size_t)n * 128 + (size_t)(((ic & 7) ^ (n & 7)) << 4);
-        *reinterpret_cast<uint4 *>(img + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(img + lo_off + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    for (int e = 0; e < 8; ++e) {
+        const float2 m = Mp[(long long)(ic * 8 + e) * (dn / 2)];
+        x[e] = (k & 1) ? (m.x * Q1 - m.y * Q0) : (m.x * Q0 + m.y * Q1);
     }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(x[e]), h1 = __float2bfloat16_rn(x[e + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(x[e] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(x[e + 1] - __bfloat162float(h1));
+        hw[e / 2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lw[e / 2] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const int n = hh * dn + k;
+    const size_t off = (size_t)(ic >> 3) * N * 128 + (size_t)n * 128 + (size_t)(((ic & 7) ^ (n & 7)) << 4);
+    *reinterpret_cast<uint4 *>(img + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4 *>(img + (size_t)dh * N * 2 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
 // ---------------------------------------------------------------------------------- //
@@ -262,23 +257,24 @@ struct RkIter {
 // ---------------------------------------------------------------------------------- //
 // Decode
 // ---------------------------------------------------------------------------------- //
-template <int HC>
+template <int DH, int DN, int HC>
 struct RkSmem {   // the small buffers after the weight images and the value ring
-    static constexpr int ZP = 2 * 2 * HC * RK_TILE * 4;    // z halves [buf][half][hc][128]; the
-                                                            // segment reduction reuses it
-    static constexpr int P = 2 * RK_TILE * HC * 4;         // probabilities [buf][128][hc]
-    static constexpr int WM = 2 * 4 * HC * 4;              // warp maxima [buf][4][hc]
-    static constexpr int LS = 4 * HC * 4;                  // warp sums [4][hc]
-    static constexpr int total = ZP + P + WM + LS;
+    static constexpr int ZX = 2 * 4 * 2 * HC * 32 * 4;  // z halves [buf][quarter][half][hc][32]
+    static constexpr int RED = 4 * HC * DH * 4;         // segment value sums [quarter][hc][d_h]
+    static constexpr int ML = 4 * HC * 2 * 4;           // segment (max, sum) [quarter][hc]
+    static constexpr int TR = RK_MAX_STAGES * DN * 4;   // table row of each stage's tile
+    static constexpr int total = ZX + RED + ML + TR;
 };
 
 __host__ __device__ inline int rk_bar_bytes(int ns, int nbuf) {
     return (2 * ns + 2 * nbuf + 5) * 8 + 16;
 }
 
-template <int DH, int DN, int HC>
-__host__ __device__ constexpr int rk_fixed_bytes() { return RkSmem<HC>::total; }
-
+// Epilogue layout: warp w < 8 reads tensor-memory lane quarter q = w & 3 (tokens 32 q ..
+// 32 q + 31 of the tile) and handles half hf = w >> 2 of the rotation pairs and of the value
+// columns.  The two warps of a quarter exchange their partial scores through shared memory
+// (a 64-thread barrier); each quarter keeps its own running maximum, so the quarters run
+// unsynchronised and are merged at the end of each segment.
 template <int DH, int DN, int HC>
 __global__ void __launch_bounds__(RK_THREADS, 1)
     rk_decode_kernel(const __grid_constant__ CUtensorMap tm_v, const RkParams p) {
@@ -290,12 +286,13 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     constexpr int IMG = 2 * DH * N * 2;
     constexpr int IMG_LO = DH * N * 2;
     constexpr int PH = DN / 4;                  // rotation pairs per epilogue thread
-    constexpr int DP = DH / 2;                  // value-column pairs
-    constexpr int NSUB = 256 / DP;              // token subsets of the value sum
-    constexpr int TPS = RK_TILE / NSUB;         // tokens per subset
+    constexpr int DGW = DH / 16;                // 8-column groups per warp (half the row)
+    constexpr int NS = 32 / DGW;                // token subsets per warp
+    constexpr int TS = 32 / NS;                 // tokens per subset
+    static_assert(RK_EPI_WARPS == 8, "two epilogue warps per lane quarter");
     static_assert(N >= 64 && N <= 256 && (N % NCH) == 0, "accumulator width");
     static_assert(PH % 8 == 0, "pairs per thread");
-    using SM = RkSmem<HC>;
+    using SM = RkSmem<DH, DN, HC>;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -305,10 +302,10 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     const uint32_t img_s = base;
     const uint32_t stage_s = img_s + (uint32_t)(nbuf * IMG);
     unsigned char *small = sm + nbuf * IMG + ns * STAGE;
-    float *zp = reinterpret_cast<float *>(small);
-    float *Ps = reinterpret_cast<float *>(small + SM::ZP);
-    float *wmax = reinterpret_cast<float *>(small + SM::ZP + SM::P);
-    float *lsum = reinterpret_cast<float *>(small + SM::ZP + SM::P + SM::WM);
+    float *zx = reinterpret_cast<float *>(small);
+    float *red = reinterpret_cast<float *>(small + SM::ZX);
+    float *mls = reinterpret_cast<float *>(small + SM::ZX + SM::RED);
+    float *trow_s = reinterpret_cast<float *>(small + SM::ZX + SM::RED + SM::ML);
     const uint32_t bars = smem_u32(small + SM::total);
     const uint32_t bar_full = bars, bar_empty = bars + 8 * ns;
     const uint32_t bar_bfull = bar_empty + 8 * ns, bar_bempty = bar_bfull + 8 * nbuf;
@@ -340,15 +337,15 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
 
     // the epilogue thread's in-tile rotations (cos, sin)(tau th_p) for its pairs: the
     // table's rows 0..127 (an input, readable before the preceding grid completes)
-    const int eq = warp & 3, half = (warp >> 2) & 1, tau = 32 * eq + lane;
+    const int q = warp & 3, hf = (warp >> 2) & 1, tau = 32 * q + lane;
     float ct[PH], st[PH];
     if (warp < RK_EPI_WARPS) {
-        const float2 *row = reinterpret_cast<const float2 *>(p.tab) + (long long)tau * (DN / 2) + half * PH;
+        const float2 *row = reinterpret_cast<const float2 *>(p.tab) + (long long)tau * (DN / 2) + hf * PH;
 #pragma unroll
-        for (int q = 0; q < PH; ++q) {
-            const float2 cs = __ldg(row + q);
-            ct[q] = cs.x;
-            st[q] = cs.y;
+        for (int i = 0; i < PH; ++i) {
+            const float2 cs = __ldg(row + i);
+            ct[i] = cs.x;
+            st[i] = cs.y;
         }
     }
     pdl_wait();
@@ -412,7 +409,9 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
                     }
                 }
                 const uint32_t fb = bar_full + 8 * sl;
-                mbar_expect_tx(fb, (uint32_t)(nl * p.ch * 128 * KB));
+                mbar_expect_tx(fb, (uint32_t)(nl * p.ch * 128 * KB + DN * 4));
+                // (cos, sin)(j0 th_p) of the tile start, for the epilogue's rotations
+                bulk_load(smem_u32(trow_s + sl * DN), p.tab + (long long)j0 * DN, DN * 4, fb, pol);
                 const uint32_t dst = stage_s + sl * STAGE;
                 for (int c = 0; c < nbox; ++c) {
                     if (rows[c] < 0) continue;
@@ -478,15 +477,20 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
         }
     } else {
         // ------------------------------ epilogue ------------------------------ //
-        float m[HC], lrun[HC], acc[HC][2];
+        // paired fp32 arithmetic (two lanes per instruction) for the dot products and the
+        // value sum: acc[hh][e] holds value columns d0 + 2 e, d0 + 2 e + 1
+        float m[HC], lrun[HC];
+        float2 acc[HC][4];
 #pragma unroll
         for (int hh = 0; hh < HC; ++hh) {
             m[hh] = -INFINITY;
             lrun[hh] = 0.f;
-            acc[hh][0] = acc[hh][1] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[hh][e] = make_float2(0.f, 0.f);
         }
-        const int dp = tid % DP, sub = tid / DP;
-        const int d = 2 * dp, vkb = d >> 6, vkk = d & 63;
+        const int lg = lane % DGW, ls = lane / DGW;
+        const int d0 = hf * (DH / 2) + 8 * lg, vkb = d0 >> 6, vch = (d0 & 63) >> 3;
+        const uint32_t tbase0 = tmem + ((uint32_t)(32 * q) << 16) + hf * (2 * PH);
         RkIter it{p.pre, p.B, Gn};
         it.begin(u0);
         bool ok = true;
@@ -496,141 +500,169 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
             const int j0 = it.tile * RK_TILE, nv = min(RK_TILE, L - j0);
             const int tb = (int)(k & 1), buf = tb, sl = (int)(k % ns);
             ok = ok && mbar_wait(bar_tfull + 8 * tb, (uint32_t)(k >> 1) & 1u, abort);
-            // the staged value tile (read below) is published by its own barrier
+            // the staged value tile and table row are published by the stage's own barrier
             ok = ok && mbar_wait(bar_full + 8 * sl, (uint32_t)(k / ns) & 1u, abort);
             ok = __all_sync(0xffffffffu, ok);
             float z[HC];
+            float2 zz[HC][2];
 #pragma unroll
-            for (int hh = 0; hh < HC; ++hh) z[hh] = 0.f;
+            for (int hh = 0; hh < HC; ++hh) zz[hh][0] = zz[hh][1] = make_float2(0.f, 0.f);
             if (ok) {
                 tc_fence_after();
-                const float4 *trow = reinterpret_cast<const float4 *>(
-                    p.tab + ((long long)j0 * (DN / 2) + half * PH) * 2);
-                const uint32_t tbase = tmem + ((uint32_t)(32 * eq) << 16) + tb * N + half * (DN / 2);
+                const float4 *trow = reinterpret_cast<const float4 *>(trow_s + sl * DN + hf * PH * 2);
+                const uint32_t tbase = tbase0 + tb * N;
 #pragma unroll
                 for (int c = 0; c < PH / 8; ++c) {
-                    float cc[8], ss[8];
+                    float2 cs[8];   // (cos, sin)(j th_p), j = j0 + tau, of the chunk's pairs
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const float4 x = __ldg(trow + c * 4 + q4);   // (c0, s0) of two pairs
-                        const int q = 2 * q4, a = c * 8 + q;
-                        cc[q] = x.x * ct[a] - x.y * st[a];
-                        ss[q] = x.y * ct[a] + x.x * st[a];
-                        cc[q + 1] = x.z * ct[a + 1] - x.w * st[a + 1];
-                        ss[q + 1] = x.w * ct[a + 1] + x.z * st[a + 1];
+                        const float4 x = trow[c * 4 + q4];   // (c0, s0) of two pairs
+                        const int i = 2 * q4, a = c * 8 + i;
+                        cs[i] = make_float2(x.x * ct[a] - x.y * st[a], x.y * ct[a] + x.x * st[a]);
+                        cs[i + 1] = make_float2(x.z * ct[a + 1] - x.w * st[a + 1],
+                                                x.w * ct[a + 1] + x.z * st[a + 1]);
                     }
-                    uint32_t v[HC][16];
+                    // at most two heads' columns in flight (register budget)
 #pragma unroll
-                    for (int hh = 0; hh < HC; ++hh) tc_ld16(tbase + hh * DN + c * 16, v[hh]);
-                    tc_wait_ld();
+                    for (int h0 = 0; h0 < HC; h0 += 2) {
+                        constexpr int NH = HC < 2 ? HC : 2;
+                        uint32_t v[NH][16];
 #pragma unroll
-                    for (int hh = 0; hh < HC; ++hh)
+                        for (int w = 0; w < NH; ++w) tc_ld16(tbase + (h0 + w) * DN + c * 16, v[w]);
+                        tc_wait_ld();
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            z[hh] += __uint_as_float(v[hh][2 * q]) * cc[q] +
-                                     __uint_as_float(v[hh][2 * q + 1]) * ss[q];
+                        for (int w = 0; w < NH; ++w)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                zz[h0 + w][i & 1] = __ffma2_rn(
+                                    make_float2(__uint_as_float(v[w][2 * i]), __uint_as_float(v[w][2 * i + 1])),
+                                    cs[i], zz[h0 + w][i & 1]);
+                    }
                 }
                 tc_fence_before();
             }
+#pragma unroll
+            for (int hh = 0; hh < HC; ++hh) z[hh] = (zz[hh][0].x + zz[hh][1].x) + (zz[hh][0].y + zz[hh][1].y);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + 8 * tb);
+            // the partner warp's half of the pairs
+            float *zmine = zx + (((buf * 4 + q) * 2 + hf) * HC) * 32;
+            const float *zother = zx + (((buf * 4 + q) * 2 + (hf ^ 1)) * HC) * 32;
 #pragma unroll
-            for (int hh = 0; hh < HC; ++hh) zp[((buf * 2 + half) * HC + hh) * RK_TILE + tau] = z[hh];
-            named_sync(1, 256);
-            float zt[HC];
-            if (half == 0) {
-#pragma unroll
-                for (int hh = 0; hh < HC; ++hh) {
-                    zt[hh] = tau < nv ? zp[((buf * 2) * HC + hh) * RK_TILE + tau] +
-                                            zp[((buf * 2 + 1) * HC + hh) * RK_TILE + tau]
-                                      : -INFINITY;
-                    float mx = zt[hh];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                    if (lane == 0) wmax[(buf * 4 + eq) * HC + hh] = mx;
-                }
-            }
-            named_sync(1, 256);
-            float alpha[HC];
+            for (int hh = 0; hh < HC; ++hh) zmine[hh * 32 + lane] = z[hh];
+            named_sync(2 + q, 64);
+            const bool valid = tau < nv;
+            float pz[HC], alpha[HC];
 #pragma unroll
             for (int hh = 0; hh < HC; ++hh) {
-                float tmax = wmax[(buf * 4) * HC + hh];
+                const float zt = valid ? z[hh] + zother[hh * 32 + lane] : -INFINITY;
+                float mx = zt;
 #pragma unroll
-                for (int w = 1; w < 4; ++w) tmax = fmaxf(tmax, wmax[(buf * 4 + w) * HC + hh]);
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 alpha[hh] = 1.f;
-                if (tmax > m[hh] + RK_RESCALE_TH) {
-                    alpha[hh] = exp2f(m[hh] - tmax);
-                    m[hh] = tmax;
+                if (mx > m[hh] + RK_RESCALE_TH) {
+                    alpha[hh] = exp2f(m[hh] - mx);
+                    m[hh] = mx;
                 }
+                pz[hh] = valid ? exp2f(zt - m[hh]) : 0.f;
+                lrun[hh] = lrun[hh] * alpha[hh] + pz[hh];
             }
-            if (half == 0) {
+            // value sum over this warp's columns d0 .. d0 + 7 (lane group lg) and tokens
+            // ls * TS .. ls * TS + TS - 1 of the quarter; probabilities from their lanes
 #pragma unroll
-                for (int hh = 0; hh < HC; ++hh) {
-                    const float pz = exp2f(zt[hh] - m[hh]);
-                    lrun[hh] = lrun[hh] * alpha[hh] + pz;
-                    Ps[(buf * RK_TILE + tau) * HC + hh] = pz;
+            for (int hh = 0; hh < HC; ++hh)
+                if (alpha[hh] != 1.f) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[hh][e] = __fmul2_rn(acc[hh][e], make_float2(alpha[hh], alpha[hh]));
                 }
-            }
-            named_sync(1, 256);
-            // value sum over this thread's tokens for value columns d, d + 1
-#pragma unroll
-            for (int hh = 0; hh < HC; ++hh) {
-                acc[hh][0] *= alpha[hh];
-                acc[hh][1] *= alpha[hh];
-            }
             const unsigned char *vt = sm + nbuf * IMG + sl * STAGE + vkb * (RK_TILE * 128);
-            const int tend = min(TPS, nv - sub * TPS);
-            for (int i = 0; i < tend; ++i) {
-                const int tk = sub * TPS + i;
-                const uint32_t vv = *reinterpret_cast<const uint32_t *>(
-                    vt + tk * 128 + ((((vkk >> 3) ^ (tk & 7))) << 4) + (vkk & 7) * 2);
-                const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xffff0000u);
-                const float *pr = Ps + (buf * RK_TILE + tk) * HC;
 #pragma unroll
-                for (int hh = 0; hh < HC; ++hh) {
-                    acc[hh][0] += pr[hh] * v0;
-                    acc[hh][1] += pr[hh] * v1;
+            for (int i = 0; i < TS; ++i) {
+                const int tl = ls * TS + i, tk = 32 * q + tl;
+                float ph[HC];
+#pragma unroll
+                for (int hh = 0; hh < HC; ++hh) ph[hh] = __shfl_sync(0xffffffffu, pz[hh], tl);
+                if (tk < nv) {
+                    const uint4 vv = *reinterpret_cast<const uint4 *>(vt + tk * 128 + ((vch ^ (tk & 7)) << 4));
+                    float2 v[4];
+                    v[0] = make_float2(__uint_as_float(vv.x << 16), __uint_as_float(vv.x & 0xffff0000u));
+                    v[1] = make_float2(__uint_as_float(vv.y << 16), __uint_as_float(vv.y & 0xffff0000u));
+                    v[2] = make_float2(__uint_as_float(vv.z << 16), __uint_as_float(vv.z & 0xffff0000u));
+                    v[3] = make_float2(__uint_as_float(vv.w << 16), __uint_as_float(vv.w & 0xffff0000u));
+#pragma unroll
+                    for (int hh = 0; hh < HC; ++hh) {
+                        const float2 p2 = make_float2(ph[hh], ph[hh]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[hh][e] = __ffma2_rn(p2, v[e], acc[hh][e]);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * sl);
             if (it.tile == it.nt - 1 || u + 1 == u1) {
-                // end of this CTA's segment of the stream: write its partial
+                // end of this CTA's segment of the stream: merge the quarters, write the partial
                 const long long slot = (long long)it.stream() + cta;
-                if (half == 0) {
+#pragma unroll
+                for (int o = DGW; o < 32; o <<= 1)
+#pragma unroll
+                    for (int hh = 0; hh < HC; ++hh)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[hh][e].x += __shfl_xor_sync(0xffffffffu, acc[hh][e].x, o);
+                            acc[hh][e].y += __shfl_xor_sync(0xffffffffu, acc[hh][e].y, o);
+                        }
+                if (lane < DGW) {
 #pragma unroll
                     for (int hh = 0; hh < HC; ++hh) {
-                        float lw = lrun[hh];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-                        if (lane == 0) lsum[eq * HC + hh] = lw;
+                        float4 *dst = reinterpret_cast<float4 *>(red + (q * HC + hh) * DH + d0);
+                        dst[0] = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
+                        dst[1] = make_float4(acc[hh][2].x, acc[hh][2].y, acc[hh][3].x, acc[hh][3].y);
                     }
                 }
-                float *red = zp;   // [NSUB][HC][DH]; the z halves are consumed
 #pragma unroll
                 for (int hh = 0; hh < HC; ++hh) {
-                    red[(sub * HC + hh) * DH + d] = acc[hh][0];
-                    red[(sub * HC + hh) * DH + d + 1] = acc[hh][1];
+                    float lw = lrun[hh];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+                    if (hf == 0 && lane == 0) {
+                        mls[(q * HC + hh) * 2] = m[hh];
+                        mls[(q * HC + hh) * 2 + 1] = lw;
+                    }
                 }
-                named_sync(1, 256);
-                for (int o = tid; o < HC * DH; o += 256) {
-                    const int hh = o / DH, dd = o - hh * DH;
+                named_sync(1, RK_EPI_T);
+                for (int o = tid; o < HC * DH; o += RK_EPI_T) {
+                    const int hh = o / DH;
+                    float M = mls[hh * 2];
+#pragma unroll
+                    for (int w = 1; w < 4; ++w) M = fmaxf(M, mls[(w * HC + hh) * 2]);
                     float sum = 0.f;
 #pragma unroll
-                    for (int s2 = 0; s2 < NSUB; ++s2) sum += red[(s2 * HC + hh) * DH + dd];
-                    p.part_o[(slot * HC + hh) * DH + dd] = sum;
+                    for (int w = 0; w < 4; ++w) {
+                        const float mw = mls[(w * HC + hh) * 2];
+                        if (mw != -INFINITY) sum += red[w * HC * DH + o] * exp2f(mw - M);
+                    }
+                    p.part_o[slot * HC * DH + o] = sum;
                 }
                 if (tid < HC) {
-                    p.part_ml[(slot * HC + tid) * 2] = m[tid];
-                    p.part_ml[(slot * HC + tid) * 2 + 1] =
-                        lsum[tid] + lsum[HC + tid] + lsum[2 * HC + tid] + lsum[3 * HC + tid];
+                    float M = mls[tid * 2];
+#pragma unroll
+                    for (int w = 1; w < 4; ++w) M = fmaxf(M, mls[(w * HC + tid) * 2]);
+                    float l = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float mw = mls[(w * HC + tid) * 2];
+                        if (mw != -INFINITY) l += mls[(w * HC + tid) * 2 + 1] * exp2f(mw - M);
+                    }
+                    p.part_ml[(slot * HC + tid) * 2] = M;
+                    p.part_ml[(slot * HC + tid) * 2 + 1] = l;
                 }
-                named_sync(1, 256);
+                named_sync(1, RK_EPI_T);
 #pragma unroll
                 for (int hh = 0; hh < HC; ++hh) {
                     m[hh] = -INFINITY;
                     lrun[hh] = 0.f;
-                    acc[hh][0] = acc[hh][1] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[hh][e] = make_float2(0.f, 0.f);
                 }
             }
         }
@@ -648,40 +680,67 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
 // ---------------------------------------------------------------------------------- //
 // Merge
 // ---------------------------------------------------------------------------------- //
+constexpr int RK_MAX_PARTS = 1024;   // partials of one (sequence, head): at most the grid + 1
+
+// One block per (sequence b, head h): weights of the parts (one thread each), then every
+// output column sums its parts' values with all loads independent.
 __global__ void __launch_bounds__(RK_MERGE_THREADS) rk_merge_kernel(const RkParams p) {
+    __shared__ float wts[RK_MAX_PARTS];
+    __shared__ float red[RK_MERGE_THREADS / 32];
     pdl_wait();
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int g = h / p.r, hl = h % p.r, hs = hl / p.hc, hh = hl % p.hc;
     const int Gn = p.G * p.nhs, sidx = g * p.nhs + hs;
     const long long s = (long long)b * Gn + sidx;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *o = p.out + (long long)bh * p.d_h;
     const long long U = p.pre[p.B];
     const int nt = (p.pre[b + 1] - p.pre[b]) / Gn;
     if (U == 0 || nt == 0) {
-        for (int dd = threadIdx.x; dd < p.d_h; dd += blockDim.x) o[dd] = 0.f;
-        if (p.lse && threadIdx.x == 0) p.lse[bh] = -INFINITY;
+        for (int dd = tid; dd < p.d_h; dd += blockDim.x) o[dd] = 0.f;
+        if (p.lse && tid == 0) p.lse[bh] = -INFINITY;
         return;
     }
     const long long uf = p.pre[b] + (long long)sidx * nt, ul = uf + nt - 1;
     const Part part{U, p.n_ctas};
-    const int c0 = part.cta_of(uf), c1 = part.cta_of(ul);
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.part_ml[((s + c) * p.hc + hh) * 2]);
+    const int c0 = part.cta_of(uf), np = part.cta_of(ul) - c0 + 1;
+    // slot of part i: s + c0 + i
+    const float *ml = p.part_ml + ((s + c0) * p.hc + hh) * 2;
+    float mx = -INFINITY;
+    for (int i = tid; i < np; i += blockDim.x) mx = fmaxf(mx, ml[(long long)i * p.hc * 2]);
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float M = red[0];
+    for (int w = 1; w < RK_MERGE_THREADS / 32; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
     float den = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-        const float *ml = p.part_ml + ((s + c) * p.hc + hh) * 2;
-        den += ml[1] * exp2f(ml[0] - M);
+    for (int i = tid; i < np; i += blockDim.x) {
+        const float w = exp2f(ml[(long long)i * p.hc * 2] - M);
+        wts[i] = w;
+        den += w * ml[(long long)i * p.hc * 2 + 1];
     }
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) den += __shfl_xor_sync(0xffffffffu, den, k);
+    if (lane == 0) red[warp] = den;
+    __syncthreads();
+    den = 0.f;
+    for (int w = 0; w < RK_MERGE_THREADS / 32; ++w) den += red[w];
     const float inv = 1.f / den;
-    for (int dd = threadIdx.x; dd < p.d_h; dd += blockDim.x) {
-        float num = 0.f;
-        for (int c = c0; c <= c1; ++c) {
-            const float w = exp2f(p.part_ml[((s + c) * p.hc + hh) * 2] - M);
-            num += w * p.part_o[((s + c) * p.hc + hh) * p.d_h + dd];
+    const float *po = p.part_o + ((s + c0) * p.hc + hh) * p.d_h;
+    const long long pstride = (long long)p.hc * p.d_h;
+    for (int dd = tid; dd < p.d_h; dd += blockDim.x) {
+        float num0 = 0.f, num1 = 0.f;
+        int i = 0;
+        for (; i + 1 < np; i += 2) {
+            num0 += wts[i] * po[i * pstride + dd];
+            num1 += wts[i + 1] * po[(i + 1) * pstride + dd];
         }
-        o[dd] = num * inv;
+        if (i < np) num0 += wts[i] * po[i * pstride + dd];
+        o[dd] = (num0 + num1) * inv;
     }
-    if (p.lse && threadIdx.x == 0) p.lse[bh] = (M + log2f(den)) * 0.69314718055994531f;
+    if (p.lse && tid == 0) p.lse[bh] = (M + log2f(den)) * 0.69314718055994531f;
 }
 
 // ---------------------------------------------------------------------------------- //
@@ -704,7 +763,7 @@ template <int DH, int DN, int HC>
 inline int rk_smem_plan(RkParams &p, int limit) {
     constexpr int N = HC * DN;
     constexpr int IMG = 2 * DH * N * 2, STAGE = RK_TILE * DH * 2;
-    const int fixed = 1024 + RkSmem<HC>::total;
+    const int fixed = 1024 + RkSmem<DH, DN, HC>::total;
     for (int nbuf = 2; nbuf >= 1; --nbuf) {
         int ns = RK_MAX_STAGES;
         while (ns >= 2 && fixed + nbuf * IMG + ns * STAGE + rk_bar_bytes(ns, nbuf) > limit) --ns;

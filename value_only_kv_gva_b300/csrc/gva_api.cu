@@ -526,7 +526,7 @@ RkWs rk_plan(const gva_dims *d, int sms) {
     w.hc = rk_hc(r, d->d_n);
     w.nhs = r / w.hc;
     const long long streams = (long long)d->B * d->G * w.nhs;
-    const long long slots = streams + sms;
+    const long long slots = streams + (sms < RK_MAX_PARTS ? sms : RK_MAX_PARTS);
     size_t o = 0;
     w.ls = o;
     o += sizeof(int) * d->B;
@@ -1090,11 +1090,12 @@ int gva_rope_keys_decode_attention(void *stream, const gva_dims *d, const void *
     p.part_ml = reinterpret_cast<float *>(wb + w.pm);
     p.out = out;
     p.lse = lse;
-    p.n_ctas = sms;
+    p.n_ctas = sms < RK_MAX_PARTS ? sms : RK_MAX_PARTS;
     p.ch = cache->rows.layout == GVA_LAYOUT_PAGED ? gcd_int(cache->rows.page_size, 64) : 64;
     CUtensorMap tv;
     if (!rk_make_map(&tv, cache->V, cache->rows.num_rows, d->G * d->d_h, p.ch)) return GVA_ERR_CUDA;
-    int st = cuda_status(launch(rk_prep_kernel, dim3(d->B * d->H + 1), dim3(RK_PREP_THREADS), 0,
+    int st = cuda_status(launch(rk_prep_kernel, dim3(d->B * d->H * (d->d_h / 8) + 1),
+                                dim3(RK_PREP_THREADS), 0,
                                 stream, p));
     if (st != GVA_OK) return st;
     st = rk_launch_decode(stream, p, tv);
