@@ -229,17 +229,20 @@ __device__ __forceinline__ void rk_drain(uint32_t bar, uint32_t parity) {
         if (global_ns() - t0 > WAIT_LIMIT_NS) return;
 }
 
-// Walk over work units u = (sequence b, stream-in-sequence sidx, tile), b-major.
+// Walk over work units u = (sequence b, stream-in-sequence sidx, tile), b-major, over the
+// unit prefix and validated lengths the prep kernel wrote.
 struct RkIter {
     const int *pre;
+    const int *Ls;
     int B, Gn;
-    int b, nt, sidx, tile;
+    int b, nt, sidx, tile, L;
     __device__ __forceinline__ void begin(long long u) {
         b = seq_of_slab(pre, B, u);
         const int w = (int)(u - pre[b]);
         nt = (pre[b + 1] - pre[b]) / Gn;
         sidx = w / nt;
         tile = w - sidx * nt;
+        L = Ls[b];
     }
     __device__ __forceinline__ void next() {
         if (++tile < nt) return;
@@ -249,7 +252,10 @@ struct RkIter {
         do {
             ++b;
         } while (b < B && pre[b + 1] == pre[b]);
-        if (b < B) nt = (pre[b + 1] - pre[b]) / Gn;
+        if (b < B) {
+            nt = (pre[b + 1] - pre[b]) / Gn;
+            L = Ls[b];
+        }
     }
     __device__ __forceinline__ int stream() const { return b * Gn + sidx; }
 };
@@ -263,9 +269,11 @@ struct RkSmem {   // the small buffers after the weight images and the value rin
     static constexpr int RED = 4 * HC * DH * 4;         // segment value sums [quarter][hc][d_h]
     static constexpr int ML = 4 * HC * 2 * 4;           // segment (max, sum) [quarter][hc]
     static constexpr int TR = RK_MAX_STAGES * DN * 4;   // table row of each stage's tile
-    static constexpr int total = ZX + RED + ML + TR;
+    static constexpr int PW = RK_EPI_WARPS * 32 * HC * 4;  // per-warp probabilities [warp][32][hc]
+    static constexpr int total = ZX + RED + ML + TR + PW;
 };
 
+// barriers, then the tensor-memory address and the abort flag
 __host__ __device__ inline int rk_bar_bytes(int ns, int nbuf) {
     return (2 * ns + 2 * nbuf + 5) * 8 + 16;
 }
@@ -279,7 +287,10 @@ template <int DH, int DN, int HC>
 __global__ void __launch_bounds__(RK_THREADS, 1)
     rk_decode_kernel(const __grid_constant__ CUtensorMap tm_v, const RkParams p) {
     constexpr int N = HC * DN;                  // accumulator columns per tile
-    constexpr int NCH = N < 128 ? N : 128;      // columns per MMA instruction
+    // columns per MMA instruction: all of them (M = 128 takes N up to 256), so that each
+    // 16-column slice of the value tile is read from shared memory once per k-step; at
+    // N = 128 the two operands' reads alone would fill the shared-memory bandwidth
+    constexpr int NCH = N;
     constexpr int TCOLS = 2 * N;                // two accumulators (64 <= N <= 256)
     constexpr int KB = DH / 64;                 // 64-column blocks of a value row
     constexpr int STAGE = RK_TILE * DH * 2;
@@ -306,6 +317,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     float *red = reinterpret_cast<float *>(small + SM::ZX);
     float *mls = reinterpret_cast<float *>(small + SM::ZX + SM::RED);
     float *trow_s = reinterpret_cast<float *>(small + SM::ZX + SM::RED + SM::ML);
+    float *pws = reinterpret_cast<float *>(small + SM::ZX + SM::RED + SM::ML + SM::TR);
     const uint32_t bars = smem_u32(small + SM::total);
     const uint32_t bar_full = bars, bar_empty = bars + 8 * ns;
     const uint32_t bar_bfull = bar_empty + 8 * ns, bar_bempty = bar_bfull + 8 * nbuf;
@@ -316,6 +328,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     volatile int *abort = reinterpret_cast<volatile int *>(tail + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) GVA_TRACE_AT(0);
     if (tid == 0) {
         for (int s = 0; s < ns; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -350,6 +363,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (tid == 0) GVA_TRACE_AT(1);
     const long long U = p.pre[p.B];
     const Part part{U, p.n_ctas};
     const int cta = blockIdx.x;
@@ -368,17 +382,50 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int Gn = p.G * p.nhs;
+    if (tid == 0) GVA_TRACE_AT(2);
 
     if (warp == RK_EPI_WARPS) {
         // ------------------------------ producer ------------------------------ //
         if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            RkIter it{p.pre, p.B, Gn};
+            const uint64_t pol = l2_evict_first_policy();   // the cache and the images
+            uint64_t pol_keep;                              // the table rows, reused by all CTAs
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+            const int nbox = RK_TILE / p.ch;
+            // value tile and table row of unit k (stage k % ns, which is free)
+            auto issue_v = [&](const RkIter &it, long long k) {
+                const int sl = (int)(k % ns);
+                const int L = it.L;
+                const int j0 = it.tile * RK_TILE, nv = min(RK_TILE, L - j0);
+                const int g = it.sidx / p.nhs;
+                long long rows[RK_TILE / 16];
+                int nl = 0;
+                for (int c = 0; c < nbox; ++c) {
+                    rows[c] = -2;
+                    if (c * p.ch < nv) {
+                        rows[c] = row_of(p.R, it.b, j0 + c * p.ch);
+                        if (rows[c] == -1) dev_report(GVA_DEV_BAD_PAGE);
+                        if (rows[c] >= 0) ++nl;
+                    }
+                }
+                const uint32_t fb = bar_full + 8 * sl;
+                mbar_expect_tx(fb, (uint32_t)(nl * p.ch * 128 * KB + DN * 4));
+                // (cos, sin)(j0 th_p) of the tile start, for the epilogue's rotations
+                bulk_load(smem_u32(trow_s + sl * DN), p.tab + (long long)j0 * DN, DN * 4, fb, pol_keep);
+                const uint32_t dst = stage_s + sl * STAGE;
+                for (int c = 0; c < nbox; ++c) {
+                    if (rows[c] < 0) continue;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_2d(dst + kb * (RK_TILE * 128) + c * p.ch * 128, &tm_v,
+                                    g * DH + kb * 64, (int)rows[c], fb, pol);
+                }
+                GVA_TRACE_AT(200 + (int)k);
+            };
+            RkIter it{p.pre, p.Ls, p.B, Gn};
             it.begin(u0);
             int cur = -1, nimg = 0;
             long long k = 0;
-            const int nbox = RK_TILE / p.ch;
-            for (long long u = u0; u < u1; ++u, it.next()) {
+            for (long long u = u0; u < u1; ++u, it.next(), ++k) {
                 const int s = it.stream();
                 if (s != cur) {
                     const int bb = nimg % nbuf;
@@ -395,32 +442,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
                 const int sl = (int)(k % ns);
                 if (k >= ns && !mbar_wait(bar_empty + 8 * sl, (uint32_t)((k / ns) - 1) & 1u, abort))
                     break;
-                const int L = p.Ls[it.b];
-                const int j0 = it.tile * RK_TILE, nv = min(RK_TILE, L - j0);
-                const int g = it.sidx / p.nhs;
-                long long rows[RK_TILE / 16];
-                int nl = 0;
-                for (int c = 0; c < nbox; ++c) {
-                    rows[c] = -2;
-                    if (c * p.ch < nv) {
-                        rows[c] = row_of(p.R, it.b, j0 + c * p.ch);
-                        if (rows[c] == -1) dev_report(GVA_DEV_BAD_PAGE);
-                        if (rows[c] >= 0) ++nl;
-                    }
-                }
-                const uint32_t fb = bar_full + 8 * sl;
-                mbar_expect_tx(fb, (uint32_t)(nl * p.ch * 128 * KB + DN * 4));
-                // (cos, sin)(j0 th_p) of the tile start, for the epilogue's rotations
-                bulk_load(smem_u32(trow_s + sl * DN), p.tab + (long long)j0 * DN, DN * 4, fb, pol);
-                const uint32_t dst = stage_s + sl * STAGE;
-                for (int c = 0; c < nbox; ++c) {
-                    if (rows[c] < 0) continue;
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tma_load_2d(dst + kb * (RK_TILE * 128) + c * p.ch * 128, &tm_v,
-                                    g * DH + kb * 64, (int)rows[c], fb, pol);
-                }
-                ++k;
+                issue_v(it, k);
             }
             // let the copies in flight land before the CTA can leave
             for (long long i = (k > ns ? k - ns : 0); i < k; ++i)
@@ -434,7 +456,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
         // ------------------------------ MMA issuer ------------------------------ //
         if (lane == 0) {
             constexpr uint32_t idesc = rk_idesc(128, NCH);
-            RkIter it{p.pre, p.B, Gn};
+            RkIter it{p.pre, p.Ls, p.B, Gn};
             it.begin(u0);
             int cur = -1, nimg = 0, bb = 0;
             long long k = 0;
@@ -447,11 +469,13 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
                     cur = s;
                 }
                 const int sl = (int)(k % ns);
+                GVA_TRACE_AT(10 + 3 * (int)k);
                 if (!mbar_wait(bar_full + 8 * sl, (uint32_t)(k / ns) & 1u, abort)) break;
                 const int tb = (int)(k & 1);
                 if (k >= 2 && !mbar_wait(bar_tempty + 8 * tb, (uint32_t)((k >> 1) - 1) & 1u, abort))
                     break;
                 tc_fence_after();
+                GVA_TRACE_AT(11 + 3 * (int)k);
                 const uint32_t a0 = stage_s + sl * STAGE, b0 = img_s + bb * IMG;
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb)
@@ -468,6 +492,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
                                        (kb | kk | part_) != 0 ? 1u : 0u);
                             }
                 tc_commit(bar_tfull + 8 * tb);
+                GVA_TRACE_AT(12 + 3 * (int)k);
                 if (it.tile == it.nt - 1 || u + 1 == u1) tc_commit(bar_bempty + 8 * bb);
                 ++k;
             }
@@ -491,18 +516,19 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
         const int lg = lane % DGW, ls = lane / DGW;
         const int d0 = hf * (DH / 2) + 8 * lg, vkb = d0 >> 6, vch = (d0 & 63) >> 3;
         const uint32_t tbase0 = tmem + ((uint32_t)(32 * q) << 16) + hf * (2 * PH);
-        RkIter it{p.pre, p.B, Gn};
+        RkIter it{p.pre, p.Ls, p.B, Gn};
         it.begin(u0);
         bool ok = true;
         long long k = 0;
         for (long long u = u0; u < u1; ++u, it.next(), ++k) {
-            const int L = p.Ls[it.b];
+            const int L = it.L;
             const int j0 = it.tile * RK_TILE, nv = min(RK_TILE, L - j0);
             const int tb = (int)(k & 1), buf = tb, sl = (int)(k % ns);
             ok = ok && mbar_wait(bar_tfull + 8 * tb, (uint32_t)(k >> 1) & 1u, abort);
             // the staged value tile and table row are published by the stage's own barrier
             ok = ok && mbar_wait(bar_full + 8 * sl, (uint32_t)(k / ns) & 1u, abort);
             ok = __all_sync(0xffffffffu, ok);
+            if (tid == 0) GVA_TRACE_AT(100 + 3 * (int)k);
             float z[HC];
             float2 zz[HC][2];
 #pragma unroll
@@ -513,6 +539,12 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
                 const uint32_t tbase = tbase0 + tb * N;
 #pragma unroll
                 for (int c = 0; c < PH / 8; ++c) {
+                    // at most two heads' columns in flight (register budget); the first
+                    // group's loads are issued before the rotations, which hide their latency
+                    constexpr int NH = HC < 2 ? HC : 2;
+                    uint32_t v[NH][16];
+#pragma unroll
+                    for (int w = 0; w < NH; ++w) tc_ld16(tbase + w * DN + c * 16, v[w]);
                     float2 cs[8];   // (cos, sin)(j th_p), j = j0 + tau, of the chunk's pairs
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
@@ -522,13 +554,12 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
                         cs[i + 1] = make_float2(x.z * ct[a + 1] - x.w * st[a + 1],
                                                 x.w * ct[a + 1] + x.z * st[a + 1]);
                     }
-                    // at most two heads' columns in flight (register budget)
 #pragma unroll
                     for (int h0 = 0; h0 < HC; h0 += 2) {
-                        constexpr int NH = HC < 2 ? HC : 2;
-                        uint32_t v[NH][16];
+                        if (h0 > 0) {
 #pragma unroll
-                        for (int w = 0; w < NH; ++w) tc_ld16(tbase + (h0 + w) * DN + c * 16, v[w]);
+                            for (int w = 0; w < NH; ++w) tc_ld16(tbase + (h0 + w) * DN + c * 16, v[w]);
+                        }
                         tc_wait_ld();
 #pragma unroll
                         for (int w = 0; w < NH; ++w)
@@ -551,22 +582,31 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
 #pragma unroll
             for (int hh = 0; hh < HC; ++hh) zmine[hh * 32 + lane] = z[hh];
             named_sync(2 + q, 64);
+            if (tid == 0) GVA_TRACE_AT(101 + 3 * (int)k);
             const bool valid = tau < nv;
             float pz[HC], alpha[HC];
 #pragma unroll
             for (int hh = 0; hh < HC; ++hh) {
                 const float zt = valid ? z[hh] + zother[hh * 32 + lane] : -INFINITY;
-                float mx = zt;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 alpha[hh] = 1.f;
-                if (mx > m[hh] + RK_RESCALE_TH) {
+                // the exact maximum is needed only when a score passes the running one by
+                // more than the rescale threshold (first tile of a segment, rare later)
+                if (__any_sync(0xffffffffu, zt > m[hh] + RK_RESCALE_TH)) {
+                    float mx = zt;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                     alpha[hh] = exp2f(m[hh] - mx);
                     m[hh] = mx;
                 }
                 pz[hh] = valid ? exp2f(zt - m[hh]) : 0.f;
                 lrun[hh] = lrun[hh] * alpha[hh] + pz[hh];
             }
+            // this warp's copy of the probabilities [token][hc], read back per token below
+            float *pw = pws + warp * (32 * HC);
+            __syncwarp();
+#pragma unroll
+            for (int hh = 0; hh < HC; ++hh) pw[lane * HC + hh] = pz[hh];
+            __syncwarp();
             // value sum over this warp's columns d0 .. d0 + 7 (lane group lg) and tokens
             // ls * TS .. ls * TS + TS - 1 of the quarter; probabilities from their lanes
 #pragma unroll
@@ -579,10 +619,10 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < TS; ++i) {
                 const int tl = ls * TS + i, tk = 32 * q + tl;
-                float ph[HC];
-#pragma unroll
-                for (int hh = 0; hh < HC; ++hh) ph[hh] = __shfl_sync(0xffffffffu, pz[hh], tl);
                 if (tk < nv) {
+                    float ph[HC];
+#pragma unroll
+                    for (int hh = 0; hh < HC; ++hh) ph[hh] = pw[tl * HC + hh];
                     const uint4 vv = *reinterpret_cast<const uint4 *>(vt + tk * 128 + ((vch ^ (tk & 7)) << 4));
                     float2 v[4];
                     v[0] = make_float2(__uint_as_float(vv.x << 16), __uint_as_float(vv.x & 0xffff0000u));
@@ -599,6 +639,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * sl);
+            if (tid == 0) GVA_TRACE_AT(102 + 3 * (int)k);
             if (it.tile == it.nt - 1 || u + 1 == u1) {
                 // end of this CTA's segment of the stream: merge the quarters, write the partial
                 const long long slot = (long long)it.stream() + cta;
@@ -669,6 +710,10 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+        GVA_TRACE_AT(300);
+        GVA_TRACE_FLUSH(0, 320);
+    }
     if (warp == RK_EPI_WARPS + 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
