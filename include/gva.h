@@ -390,6 +390,14 @@ int gva_get_device_status(int *code_out);
  * 16-byte aligned, `bytes` a positive multiple of 16; otherwise GVA_ERR_ARG. */
 int gva_read_probe(void *stream, const void *buf, size_t bytes, unsigned *sink);
 
+/* Self-test of the kernels' bounded waits (not on the decode path).  Every in-kernel wait
+ * on an mbarrier gives up after a limit, records GVA_DEV_TIMEOUT and lets its kernel
+ * return, so a lost producer never hangs the GPU.  This launches one warp that waits on
+ * an mbarrier nothing arrives on, with a limit of `limit_us` microseconds (1 .. 10^6):
+ * after it the device status (gva_get_device_status) reads GVA_DEV_TIMEOUT and the
+ * context stays usable.  Asynchronous on `stream`; GVA_ERR_ARG for a limit out of range. */
+int gva_selftest_bounded_wait(void *stream, unsigned limit_us);
+
 /* Streaming multiprocessors of the current device (the decode grid is sized from it). */
 int gva_num_sms(void);
 

@@ -74,6 +74,28 @@ def test_rope_table_rejects_bad_args(gva):
     assert lib.gva_rope_table_fill(buf, 4, 8, -1.0) == gva.GVA_ERR_ARG
 
 
+def test_wait_selftest_rejects_bad_limits(gva):
+    assert gva._lib.gva_selftest_bounded_wait(None, 0) == gva.GVA_ERR_ARG
+    assert gva._lib.gva_selftest_bounded_wait(None, 2000000) == gva.GVA_ERR_ARG
+
+
+@pytest.mark.parametrize("bad", [dict(d_r=16), dict(d_n=3), dict(B=0), dict(H=16, G=3),
+                                 dict(cache_dtype=7), dict(d_h=12)])
+def test_rope_keys_invalid_dims_rejected_before_cuda(gva, bad):
+    """The rotated-key decode checks its arguments before any CUDA call."""
+    lib = gva._lib
+    base = dict(d_r=0)
+    base.update(bad)
+    d = _dims(gva, **base)
+    fake = ctypes.c_void_p(0x10000)
+    cache = gva.gva_cache(gva.gva_rows(0, 1 << 20, 1024, None, None, 0, 0), fake, None)
+    assert lib.gva_rope_keys_workspace_size(ctypes.byref(d)) == 0
+    st = lib.gva_rope_keys_decode_attention(None, ctypes.byref(d), fake, fake, fake,
+                                            ctypes.byref(cache), fake, 4096, ctypes.c_float(0.1),
+                                            fake, None, fake, ctypes.c_size_t(1 << 30))
+    assert st == gva.GVA_ERR_ARG
+
+
 def _dims(gva, **kw):
     base = dict(B=2, H=16, G=4, d_h=64, d_n=64, d_r=16, cache_dtype=1, q_dtype=1)
     base.update(kw)

@@ -92,6 +92,7 @@ _lib.gva_get_device_status.argtypes = [ctypes.POINTER(_I)]
 _lib.gva_last_cuda_error.restype = _I
 _lib.gva_decode_attention_static.argtypes = [_P, _PD, _P, _P, _P, _P, _PC, _P, _I, _F, _P, _P]
 _lib.gva_read_probe.argtypes = [_P, _P, _Z, _P]
+_lib.gva_selftest_bounded_wait.argtypes = [_P, ctypes.c_uint]
 _lib.gva_prefill_workspace_size.restype = _Z
 _lib.gva_prefill_workspace_size.argtypes = [_PD, _I, ctypes.POINTER(gva_rows)]
 _lib.gva_mla_workspace_size.restype = _Z
@@ -111,7 +112,8 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_get_device_status", "gva_last_cuda_error", "gva_decode_attention_static",
            "gva_read_probe", "gva_absorb_query_ex", "gva_prefill_workspace_size",
            "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention",
-           "gva_rope_keys_workspace_size", "gva_rope_keys_decode_attention"]
+           "gva_rope_keys_workspace_size", "gva_rope_keys_decode_attention",
+           "gva_selftest_bounded_wait"]
 
 
 class GvaError(RuntimeError):
@@ -547,6 +549,13 @@ def mla_workspace(dims: MlaDims, device=None) -> torch.Tensor:
     if n == 0:
         raise GvaError(GVA_ERR_ARG, "gva_mla_workspace_size")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gva_selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """One warp waits on an mbarrier nothing arrives on; after `limit_us` the wait gives
+    up and the device status reads GVA_DEV_TIMEOUT (see gva.h)."""
+    _check(_lib.gva_selftest_bounded_wait(_stream(stream), int(limit_us)),
+           "gva_selftest_bounded_wait")
 
 
 def gva_rope_keys_workspace_size(dims: Dims) -> int:

@@ -167,19 +167,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t a, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  Gives up (returns false) when
-// another warp raised `abort` or after WAIT_LIMIT_NS, raising abort and the status.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int *abort) {
+// another warp raised `abort` or after `limit_ns`, raising abort and the status.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t a, uint32_t parity, volatile int *abort,
+                                              unsigned long long limit_ns) {
     if (mbar_test_wait(a, parity)) return true;
     const unsigned long long t0 = global_ns();
+    const uint32_t sleep = limit_ns < WAIT_SLEEP_NS ? (uint32_t)limit_ns : WAIT_SLEEP_NS;
     for (;;) {
-        if (mbar_try_wait_sleep(a, parity, WAIT_SLEEP_NS)) return true;
+        if (mbar_try_wait_sleep(a, parity, sleep)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_ns() - t0 > limit_ns) {
             *abort = 1;
             dev_report(GVA_DEV_TIMEOUT);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int *abort) {
+    return mbar_wait_for(a, parity, abort, WAIT_LIMIT_NS);
 }
 // The cache is streamed once per step: its loads carry an L2 evict-first policy, so
 // that they do not push out of L2 what is reused (the kernels' code, the maps M, the

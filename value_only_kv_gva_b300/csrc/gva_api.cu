@@ -457,6 +457,20 @@ __global__ void __launch_bounds__(PROBE_THREADS) read_probe_kernel(const uint4 *
     }
 }
 
+// Self-test of the bounded waits: one warp waits on an mbarrier that nothing arrives on;
+// the wait gives up after `limit_ns` and records GVA_DEV_TIMEOUT.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_for(smem_u32(&bar), 0, &abort, limit_ns);
+}
+
 // =========================================================================== //
 // MLA-shaped decode helpers (the entry points are below).
 namespace {
@@ -570,6 +584,14 @@ const char *gva_status_string(int s) {
 int gva_abi_version(void) { return GVA_ABI_VERSION; }
 
 int gva_num_sms(void) { return num_sms_current(); }
+
+int gva_selftest_bounded_wait(void *stream, unsigned limit_us) {
+    if (limit_us < 1 || limit_us > 1000000) return GVA_ERR_ARG;
+    if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (unsigned long long)limit_us * 1000ull);
+    return cuda_status(cudaGetLastError());
+}
 
 int gva_read_probe(void *stream, const void *buf, size_t bytes, unsigned *sink) {
     if (!buf || !sink || bytes == 0 || bytes % 16 != 0 || !aligned16(buf)) return GVA_ERR_ARG;
