@@ -518,7 +518,7 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = oracle_baseline(w, c_case, budget_s=args.cpu_seconds)
 
-    launches_per_step = nl * (2 if path == "fused" else 4)
+    launches_per_step = nl * 4
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -756,7 +756,7 @@ def run_prefill(args, dist: Dist):
                      "peak_source": "measured" if peaks else "fallback", "traffic": None},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": nl * (4 if path == "fused" else 5) * args.steps,
+        "gpu_launches": nl * 5 * args.steps,
         "clocks": clocks,
     }
     if dist.rank == 0:
@@ -975,7 +975,7 @@ def main():
                     choices=["tiny", "350m", "ragged", "long", "paged"])
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per step (0 = enough distinct caches to exceed L2)")
-    ap.add_argument("--path", default="auto", choices=["auto", "simt", "mma", "fused"])
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing (s)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--e2e-steps", type=int, default=20)

@@ -119,12 +119,8 @@ typedef struct {
 typedef enum {
     GVA_PATH_AUTO = 0,       /* tensor-core kernels where they apply, else CUDA cores */
     GVA_PATH_SIMT = 1,       /* CUDA-core kernel (fp32 FMA); every supported shape */
-    GVA_PATH_MMA = 2,        /* separate absorb, bf16 tensor-core split-K and combine
+    GVA_PATH_MMA = 2         /* separate absorb, bf16 tensor-core split-K and combine
                                 kernels (bf16 cache only) */
-    GVA_PATH_FUSED = 3       /* one kernel: the absorption spread over the decode grid,
-                                the tensor-core split-K and the merge of the splits
-                                (bf16 cache, d_h 64 or 128, at most 8 value groups and
-                                8 heads per group) */
 } gva_path;
 
 /* Query RMSNorm before absorption (the "scale-matched + query RMSNorm" variant named
@@ -204,15 +200,10 @@ size_t gva_decode_workspace_size(const gva_dims *dims);
  *   lse[b,h]   = ln sum_j exp(z_j)                 (device fp32 [B][H], or NULL)
  * L_b = 0 gives out = 0 and lse = -inf.  Split-K flash-decoding over 16-token slabs
  * spread evenly over the GPU, then a log-sum-exp merge of the splits: three kernels
- * (absorb, split-K partial, combine) on the automatic path, or on GVA_PATH_FUSED one
- * kernel that absorbs inside the decode grid and merges each sequence's splits in the
- * CTA that finishes it last.  The
- * workspace (device, >= gva_decode_workspace_size(dims), 256-byte aligned) is scratch,
- * except for a block of per-sequence counters that must be zero before the first call
- * and that every completed call leaves zero: zero-fill a new workspace once, and again
- * after a call that reported GVA_DEV_TIMEOUT.  The one-kernel decode needs every CTA
- * of its grid (one per SM) resident at once, i.e. the whole GPU for this context.
- * q_nope/q_rope/M/seq_len/rope_tab as in gva_absorb_query. */
+ * (absorb, split-K partial, combine).  The workspace (device,
+ * >= gva_decode_workspace_size(dims), 256-byte aligned) is scratch only: every value
+ * the call reads there it wrote first.  q_nope/q_rope/M/seq_len/rope_tab as in
+ * gva_absorb_query. */
 int gva_decode_attention(void *stream, const gva_dims *dims, const void *q_nope,
                          const void *q_rope, const float *M, const int *seq_len,
                          const gva_cache *cache, const float *rope_tab, int rope_max_pos,
@@ -246,12 +237,11 @@ size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *r
  * Paths: GVA_PATH_AUTO runs, for bf16 caches with d_h 64 or 128, a tensor-core prefill
  * kernel that loads each 16-token slab of a sequence's rows once and scores it against
  * all of the chunk's queries (split over the history, merged by log-sum-exp); every
- * other case, and GVA_PATH_SIMT / _MMA / _FUSED, runs each query as one entry of a
+ * other case, and GVA_PATH_SIMT / _MMA, runs each query as one entry of a
  * decode batch of B*n entries reading sequence b's rows (a paged view of the cache).
  * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged returns
  * GVA_ERR_UNSUPPORTED.  B*n <= 4096 (else GVA_ERR_ARG).  Workspace: device, 256-byte
- * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), zero-filled once as
- * for gva_decode_attention.  A chunk that does not fit the capacity or the RoPE table
+ * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), scratch only.  A chunk that does not fit the capacity or the RoPE table
  * sets GVA_DEV_BAD_POSITION / GVA_DEV_BAD_LENGTH for the queries concerned. */
 int gva_prefill_attention(void *stream, const gva_dims *dims, int n, const void *q_nope,
                           const void *q_rope, const float *M, const int *L0,
@@ -263,8 +253,7 @@ int gva_prefill_attention(void *stream, const gva_dims *dims, int n, const void 
 /* Matched GQA decode, the comparator ([K] §4): out[b,h] = softmax(scale q_h K_g^T) V_g
  * with explicit K and V rows [G][d_h] (cache_dtype).  q device [B][H][d_h] (q_dtype);
  * dims.d_n and dims.d_r are ignored.  Same split-K design, workspace and outputs as
- * gva_decode_attention (GVA_PATH_FUSED: the one-kernel decode without the absorption);
- * opts may be NULL (GVA_FLAG_QUERY_RMSNORM: GVA_ERR_UNSUPPORTED). */
+ * gva_decode_attention; opts may be NULL (GVA_FLAG_QUERY_RMSNORM: GVA_ERR_UNSUPPORTED). */
 int gva_gqa_decode_attention(void *stream, const gva_dims *dims, const void *q,
                              const int *seq_len, const gva_kv_cache *cache, float scale,
                              float *out, float *lse, void *workspace, size_t ws_bytes,
@@ -365,11 +354,10 @@ int gva_rope_keys_decode_attention(void *stream, const gva_dims *dims, const voi
  *     that first call before any stream capture.  `stream` must belong to the current
  *     device (else GVA_ERR_CUDA).
  *   - Every call on a device shares the one array, and its contents persist from the
- *     previous call.  The call takes the automatic path; the per-sequence counters that
- *     path relies on are cleared by the call itself (a memset on `stream`) and every
- *     other scratch value is written before it is read.  Calls that may overlap on the
- *     GPU (different streams, or work not ordered by the caller) race on the array;
- *     order them.
+ *     previous call.  The call takes the automatic path, which writes every scratch
+ *     value before it reads it, so nothing in the array has to start at any value.
+ *     Calls that may overlap on the GPU (different streams, or work not ordered by the
+ *     caller) race on the array; order them.
  * Arguments, outputs and errors otherwise as gva_decode_attention. */
 int gva_decode_attention_static(void *stream, const gva_dims *dims, const void *q_nope,
                                 const void *q_rope, const float *M, const int *seq_len,

@@ -74,6 +74,21 @@ def test_rope_table_rejects_bad_args(gva):
     assert lib.gva_rope_table_fill(buf, 4, 8, -1.0) == gva.GVA_ERR_ARG
 
 
+def test_path_values_beyond_mma_rejected(gva):
+    """Paths are AUTO, SIMT and MMA; any other value is an argument error."""
+    lib = gva._lib
+    d = _dims(gva)
+    fake = ctypes.c_void_p(0x10000)
+    cache = gva.gva_cache(gva.gva_rows(0, 1 << 20, 1024, None, None, 0, 0), fake, fake)
+    for path in (3, -1):
+        o = gva.gva_decode_opts(path, 0, 0, 0.0, None)
+        st = lib.gva_decode_attention_ex(None, ctypes.byref(d), fake, fake, fake, fake,
+                                         ctypes.byref(cache), fake, 100, ctypes.c_float(0.1),
+                                         fake, None, fake, ctypes.c_size_t(1 << 30),
+                                         ctypes.byref(o))
+        assert st == gva.GVA_ERR_ARG
+
+
 def test_wait_selftest_rejects_bad_limits(gva):
     assert gva._lib.gva_selftest_bounded_wait(None, 0) == gva.GVA_ERR_ARG
     assert gva._lib.gva_selftest_bounded_wait(None, 2000000) == gva.GVA_ERR_ARG

@@ -21,15 +21,8 @@ def _mma_ok(c):
     return w.cache_dtype == "bf16" and w.d_h in (64, 128) and w.G <= 8
 
 
-def _fused_ok(c):
-    """The one-kernel path's support matrix (include/gva.h: bf16 cache, d_h 64 or 128, at
-    most 8 value groups)."""
-    w = c.w
-    return w.cache_dtype == "bf16" and w.d_h in (64, 128) and w.G <= 8
-
-
 def paths_for(c):
-    return (["simt"] + (["mma"] if _mma_ok(c) else []) + (["fused"] if _fused_ok(c) else []))
+    return ["simt"] + (["mma"] if _mma_ok(c) else [])
 
 
 # small variants of the five workloads: several slabs and CTAs, ragged tails
@@ -55,13 +48,11 @@ def _step(c, path, num_ctas=0):
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("path", ["simt", "mma", "fused", "auto"])
+@pytest.mark.parametrize("path", ["simt", "mma", "auto"])
 def test_step_small_workloads(name, path):
     c = make_case(workload(name, **SMALL[name]))
     if path == "mma" and not _mma_ok(c):
         pytest.skip("tensor-core path needs a bf16 cache")
-    if path == "fused" and not _fused_ok(c):
-        pytest.skip("fused path needs a bf16 cache")
     out, lse, ref, ref_lse, _ = _step(c, path)
     assert_close(out, ref, c.w.cache_dtype, f"{name}/{path} out")
     assert_close(lse, ref_lse, c.w.cache_dtype, f"{name}/{path} lse")
@@ -322,7 +313,7 @@ def test_gqa_comparator(name):
 # --------------------------------------------------------------------------- #
 # CUDA graphs: the calls can be captured (torch's default global capture mode)
 # --------------------------------------------------------------------------- #
-@pytest.mark.parametrize("path", ["simt", "mma", "fused"])
+@pytest.mark.parametrize("path", ["simt", "mma"])
 def test_graph_capture_and_replay(path):
     c = make_case(workload("350m", T=200, B=3))
     D = Dev(c)

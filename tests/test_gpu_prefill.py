@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 def _supported(c, path):
     w = c.w
-    if path in ("mma", "fused"):
+    if path == "mma":
         return w.cache_dtype == "bf16" and w.d_h in (64, 128) and w.G <= 8
     return True
 
@@ -91,7 +91,7 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("path", ["simt", "mma", "fused", "auto"])
+@pytest.mark.parametrize("path", ["simt", "mma", "auto"])
 def test_prefill_small_workloads(name, path):
     over, n = SMALL[name]
     c = make_case(workload(name, **over))
@@ -206,10 +206,10 @@ def test_prefill_shapes(H, G, d_h, d_n, d_r, n):
 
 def test_prefill_paths_agree_on_a_paged_batch():
     """Every path on the same paged chunk: the tensor-core prefill kernel (auto) and the
-    decode-entry compositions (simt, mma, fused), each against the oracle."""
+    decode-entry compositions (simt, mma), each against the oracle."""
     c = make_case(workload("paged", B=3, len_range=(100, 700)))
     refs = None
-    for path in ("auto", "simt", "mma", "fused"):
+    for path in ("auto", "simt", "mma"):
         r = Run(c, 12, path)
         assert r.status == 0
         if refs is None:

@@ -33,7 +33,7 @@ GVA_DEV_OK, GVA_DEV_BAD_LENGTH, GVA_DEV_BAD_PAGE, GVA_DEV_BAD_POSITION, \
     GVA_DEV_TIMEOUT = 0, 1, 2, 3, 4
 GVA_F32, GVA_BF16 = 0, 1
 LAYOUTS = {"contiguous": 0, "ragged": 1, "paged": 2}
-PATHS = {"auto": 0, "simt": 1, "mma": 2, "fused": 3}
+PATHS = {"auto": 0, "simt": 1, "mma": 2}
 
 
 class gva_dims(ctypes.Structure):
@@ -401,7 +401,7 @@ def gva_prefill_attention(dims: Dims, q_nope, q_rope, M, L0, v_new, k_rope_new, 
     after L0[b] cached ones, then causal attention of each new token (q_nope
     [B, n, H, d_n], v_new [B, n, G, d_h], k_rope_new [B, n, d_r], out [B, n, H, d_h],
     lse [B, n, H]; q_norm as in _opts).  path "auto" takes the tensor-core prefill
-    kernel where it applies; "simt", "mma" and "fused" run each query as a decode
+    kernel where it applies; "simt" and "mma" run each query as a decode
     entry."""
     d = dims.c()
     cc = cache.c()
@@ -625,9 +625,8 @@ def gva_get_device_status() -> int:
 
 
 def workspace(dims: Dims, device=None) -> torch.Tensor:
-    """Allocate a decode workspace (uint8, 256-byte aligned by the caching allocator),
-    zero-filled: its per-pair tickets must start at zero (each completed call leaves
-    them zero)."""
+    """Allocate a decode workspace (uint8, 256-byte aligned by the caching allocator;
+    scratch only, zero-filled for determinism of unused bytes)."""
     n = gva_decode_workspace_size(dims)
     if n == 0:
         raise GvaError(GVA_ERR_ARG, "gva_decode_workspace_size")

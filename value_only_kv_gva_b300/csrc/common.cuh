@@ -41,13 +41,6 @@ __device__ __forceinline__ unsigned smid() {
         if (blockIdx.x < 4096) g_cta_t[blockIdx.x][(k)] = kt_now();           \
         if ((k) == 2 && blockIdx.x < 4096) g_cta_t[blockIdx.x][3] = smid();  \
     } while (0)
-// one-kernel decode: per-CTA stamps of its phases (start, after the grid wait, prefix,
-// absorption published, first queries ready, slab loop done, tickets, end)
-__device__ unsigned long long g_one_t[1024][8];
-#define GVA_ONE_T(k)                                                          \
-    do {                                                                      \
-        if (blockIdx.x < 1024) g_one_t[blockIdx.x][(k)] = kt_now();           \
-    } while (0)
 // kernel event log: (kind << 56 | event << 48 | blockIdx.x, global time) per record
 __device__ unsigned long long g_rec[1 << 16][2];
 __device__ unsigned int g_rec_n;
@@ -71,9 +64,6 @@ __device__ unsigned int g_rec_n;
     do {             \
     } while (0)
 #define GVA_CTA_T(k) \
-    do {             \
-    } while (0)
-#define GVA_ONE_T(k) \
     do {             \
     } while (0)
 #define GVA_REC(kind, ev) \

@@ -13,7 +13,6 @@
 #include "prep_kernels.cuh"
 #include "decode_simt.cuh"
 #include "decode_mma.cuh"
-#include "decode_one.cuh"
 #include "prefill_mma.cuh"
 #include "decode_rope_keys.cuh"
 
@@ -109,7 +108,6 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<float, true>);
     if (e == cudaSuccess) e = opt_in_smem(decode_simt_kernel<__nv_bfloat16, true>);
     if (e == cudaSuccess) e = mma_opt_in_all();
-    if (e == cudaSuccess) e = one_opt_in_all();
     if (e == cudaSuccess) e = prefill_opt_in_all();
     if (e == cudaSuccess) e = rk_opt_in_all();
     if (e == cudaSuccess) e = max_carveout(append_kernel<float>);
@@ -192,7 +190,7 @@ RowsDev to_dev(const gva_rows &R) {
 
 // Workspace: [q_tilde B*H*d_h][q_hat B*H*d_r][part_o slots*H*d_h][part_ml slots*H*2]
 struct WsPlan {
-    size_t qt, qh, po, pm, tk, pf, total;
+    size_t qt, qh, po, pm, pf, total;
     long long slots;
 };
 
@@ -204,9 +202,6 @@ WsPlan plan_ws(const gva_dims *d, int sms) {
     w.qh = o; o = align_up(o + sizeof(float) * d->B * d->H * (d->d_r > 0 ? d->d_r : 1), 256);
     w.po = o; o = align_up(o + sizeof(float) * w.slots * d->H * d->d_h, 256);
     w.pm = o; o = align_up(o + sizeof(float) * w.slots * d->H * 2, 256);
-    // one-kernel path: per sequence an absorbed-heads count and a parts ticket, both
-    // zero between calls
-    w.tk = o; o = align_up(o + sizeof(int) * 2 * (size_t)d->B, 256);
     w.pf = o; o = align_up(o + sizeof(int) * ((size_t)d->B + 1), 256);   // slab offsets
     w.total = o;
     return w;
@@ -386,18 +381,6 @@ bool prefill_layout_ok(const gva_rows &R) {
 
 const gva_decode_opts kDefaultOpts = {GVA_PATH_AUTO, 0, 0, 0.f, nullptr};
 
-// The one-kernel decode's arguments beyond the separate-kernel ones.
-void one_extras(OneParams &op, const gva_dims *d, const void *q_nope, const float *M,
-                float prescale, char *w, const WsPlan &plan) {
-    op.q_nope = q_nope;
-    op.M = M;
-    op.d_n = d->d_n;
-    op.q_f32 = d->q_dtype == GVA_F32;
-    op.prescale = prescale;
-    op.qt = reinterpret_cast<float *>(w + plan.qt);
-    op.ready = reinterpret_cast<int *>(w + plan.tk);
-    op.ticket = op.ready + d->B;
-}
 
 // Option flags: only the query RMSNorm, with a finite eps >= 0.
 bool flags_ok(const gva_decode_opts *o) {
@@ -678,7 +661,7 @@ static int decode_arg_checks(const gva_dims *d, const gva_rows *rows, float *out
                              const gva_decode_opts *o, bool gva_shape) {
     if (!dims_ok(d, gva_shape) || !rows_ok(rows, d->B)) return GVA_ERR_ARG;
     if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
-    if (!flags_ok(o) || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_FUSED || o->num_ctas < 0)
+    if (!flags_ok(o) || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_MMA || o->num_ctas < 0)
         return GVA_ERR_ARG;
     return GVA_OK;
 }
@@ -711,17 +694,12 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
                        !aligned16(q_rope) || !aligned16(cache->K_rope) || !aligned16(rope_tab)))
         return GVA_ERR_ARG;
     const bool mma_ok = mma_supported(d);
-    const bool one_ok = one_supported(d);
     if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
-    if (o->path == GVA_PATH_FUSED && !one_ok) return GVA_ERR_UNSUPPORTED;
     WsPlan plan;
     int sms = 0;
     st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
     if (st != GVA_OK) return st;
     char *w = static_cast<char *>(ws);
-    // the automatic path takes the separate kernels: on every measured workload they are
-    // faster than the one-kernel decode
-    const bool use_one = o->path == GVA_PATH_FUSED;
     const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
 
     float *qt = reinterpret_cast<float *>(w + plan.qt);
@@ -729,12 +707,9 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     // the tensor-core decode rotates the positional query itself (its inputs are final
     // before the call, so it overlaps the absorption), leaving the absorption a single
     // memory round trip
-    // (the one-kernel decode absorbs inside its own grid)
-    if (!use_one) {
-        st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                           scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o);
-        if (st != GVA_OK) return st;
-    }
+    st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o);
+    if (st != GVA_OK) return st;
 
     DecodeParams dp;
     dp.B = d->B;
@@ -763,17 +738,6 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
     dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
-    if (use_one) {
-        OneParams op;
-        memset(&op, 0, sizeof(op));
-        dp.qr = nullptr;   // the kernel rotates the positional query itself
-        op.m.d = dp;
-        one_extras(op, d, q_nope, M, scale * LOG2E, w, plan);
-        op.qnorm = (o->flags & GVA_FLAG_QUERY_RMSNORM) ? 1 : 0;
-        op.qn_gain = op.qnorm ? o->q_norm_gain : nullptr;
-        op.qn_eps = op.qnorm ? o->q_norm_eps : 0.f;
-        return run_one(stream, op, cache->rows, sms, o->num_ctas, false);
-    }
     if (use_mma) {
         st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, true);
     } else if (d->cache_dtype == GVA_F32) {
@@ -811,7 +775,7 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     if (!cache || n < 1 || !dims_ok(d, true) || (long long)d->B * n > MAX_B) return GVA_ERR_ARG;
     if (!rows_ok(&cache->rows, d->B)) return GVA_ERR_ARG;
     if (!out || !aligned16(out) || (lse && !aligned16(lse))) return GVA_ERR_ARG;
-    if (!flags_ok(o) || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_FUSED || o->num_ctas < 0)
+    if (!flags_ok(o) || o->path < GVA_PATH_AUTO || o->path > GVA_PATH_MMA || o->num_ctas < 0)
         return GVA_ERR_ARG;
     if (!q_nope || !M || !L0 || !v_new || !cache->V || !aligned16(q_nope) || !aligned16(M) ||
         !aligned16(v_new) || !aligned16(cache->V))
@@ -853,7 +817,6 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     }
     // a path that cannot run the chunk is refused before anything is appended
     if (o->path == GVA_PATH_MMA && !mma_supported(d)) return GVA_ERR_UNSUPPORTED;
-    if (o->path == GVA_PATH_FUSED && !one_supported(&pp.dv)) return GVA_ERR_UNSUPPORTED;
     int st = cuda_status(launch(prefill_view_kernel, dim3(d->B, (n + PV_ROWS - 1) / PV_ROWS),
                                 dim3(128), 0, stream, vp));
     if (st != GVA_OK) return st;
@@ -916,15 +879,12 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     gva_dims dg = *d;
     dg.d_r = 0;
     const bool mma_ok = mma_supported(&dg);
-    const bool one_ok = one_supported(&dg);
     if (o->path == GVA_PATH_MMA && !mma_ok) return GVA_ERR_UNSUPPORTED;
-    if (o->path == GVA_PATH_FUSED && !one_ok) return GVA_ERR_UNSUPPORTED;
     WsPlan plan;
     int sms = 0;
     st = decode_device_checks(stream, d, ws, ws_bytes, &plan, &sms);
     if (st != GVA_OK) return st;
     // the same choice as the GVA decode, so that the comparator runs the same design
-    const bool use_one = o->path == GVA_PATH_FUSED;
     const bool use_mma = o->path == GVA_PATH_MMA || (o->path == GVA_PATH_AUTO && mma_ok);
     char *w = static_cast<char *>(ws);
     DecodeParams dp;
@@ -954,13 +914,6 @@ int gva_gqa_decode_attention(void *stream, const gva_dims *d, const void *q, con
     dp.part_ml = reinterpret_cast<float *>(w + plan.pm);
     dp.n_ctas = 0;
     dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
-    if (use_one) {
-        OneParams op;
-        memset(&op, 0, sizeof(op));
-        op.m.d = dp;
-        op.ticket = reinterpret_cast<int *>(w + plan.tk) + d->B;
-        return run_one(stream, op, cache->rows, sms, o->num_ctas, true);
-    }
     if (use_mma) {
         st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, true, false);
     } else if (d->cache_dtype == GVA_F32) {
@@ -1184,19 +1137,8 @@ int gva_decode_attention_static(void *stream, const gva_dims *d, const void *q_n
     if (need > (size_t)GVA_STATIC_SCRATCH_BYTES) return GVA_ERR_WORKSPACE;  // beyond the fixed maximum
     void *ws = static_scratch_for_device(dev);
     if (!ws) return GVA_ERR_CUDA;
-    // The automatic path may take the one-kernel decode, which counts absorbed heads and
-    // finished parts per sequence in the scratch and relies on them starting at zero.  A
-    // completed call leaves them zero, but one that gave up (GVA_DEV_TIMEOUT) may not, so
-    // every call clears them first: a memset on the stream, no allocation.  Everything
-    // else in the array is written before it is read.
-    const WsPlan plan = plan_ws(d, num_sms_current());
-    e = cudaMemsetAsync(static_cast<char *>(ws) + plan.tk, 0, sizeof(int) * 2 * (size_t)d->B,
-                        static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        g_last_cuda_error = (int)e;
-        cudaGetLastError();
-        return GVA_ERR_CUDA;
-    }
+    // The automatic path writes every scratch value it reads within the call, so nothing
+    // in the array has to start at any particular value.
     return gva_decode_attention_ex(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab,
                                    rope_max_pos, scale, out, lse, ws,
                                    (size_t)GVA_STATIC_SCRATCH_BYTES, nullptr);
@@ -1236,12 +1178,6 @@ int gva_debug_rec_read(unsigned long long *host, int n) {
 int gva_debug_rec_clear(void) {
     const unsigned zero = 0;
     return cudaMemcpyToSymbol(g_rec_n, &zero, sizeof(zero)) == cudaSuccess ? GVA_OK : GVA_ERR_CUDA;
-}
-// one-kernel decode phases: [cta][8] global-timer readings
-int gva_debug_one_read(unsigned long long *host, int n) {
-    if (n > 1024) n = 1024;
-    return cudaMemcpyFromSymbol(host, g_one_t, sizeof(unsigned long long) * 8 * n) == cudaSuccess
-               ? GVA_OK : GVA_ERR_CUDA;
 }
 // [0..16) earliest, [16..32) latest global-timer reading per timeline slot
 int gva_debug_kt_read(unsigned long long *host) {
