@@ -235,8 +235,10 @@ size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *r
  * q_nope [B][n][H][d_n], q_rope [B][n][H][d_r] (q_dtype); M, rope_tab, scale and opts
  * as in gva_decode_attention_ex.  L0 is not updated (the caller adds n).
  * Paths: GVA_PATH_AUTO runs, for bf16 caches with d_h 64 or 128, a tensor-core prefill
- * kernel that loads each 16-token slab of a sequence's rows once and scores it against
- * all of the chunk's queries (split over the history, merged by log-sum-exp); every
+ * kernel that loads each tile of a sequence's rows once and scores it against all of the
+ * chunk's queries (split over the history, merged by log-sum-exp): the tcgen05 kernel
+ * when a value group's chunk rows n * H / G fit one product (<= 64, or <= 128 at
+ * d_h = 64), else an mma.sync kernel; every
  * other case, and GVA_PATH_SIMT / _MMA, runs each query as one entry of a
  * decode batch of B*n entries reading sequence b's rows (a paged view of the cache).
  * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged returns

@@ -122,6 +122,24 @@ def test_prefill_chunk_lengths(n):
     assert_close(lse, ref_lse, "bf16", f"n={n} lse")
 
 
+@pytest.mark.parametrize("n", [20, 32])
+def test_prefill_128_row_groups(n):
+    """Chunks whose group rows (n r = 80 and 128) fill the tensor-core prefill kernel's
+    128-row products (d_h = 64), over histories that end mid-tile and in permuted pages."""
+    for name, over, lengths in (("350m", dict(T=400, B=3), [400, 231, n]),
+                                ("paged", dict(B=3, len_range=(64, 600), H=16, G=4, d_h=64, d_n=64),
+                                 None)):
+        c = make_case(workload(name, **over), lengths=lengths)
+        r = Run(c, n)
+        assert r.status == 0
+        Vh, Kh = r.oracle_cache()
+        _check_cache(r, Vh, Kh)
+        ref, ref_lse = r.oracle_out(Vh, Kh)
+        out, lse = r.got()
+        assert_close(out, ref, "bf16", f"{name} n={n}")
+        assert_close(lse, ref_lse, "bf16", f"{name} n={n} lse")
+
+
 def test_prefill_largest_batch():
     """B * n = 4096 decode entries, the largest the library takes."""
     c = make_case(workload("350m", T=160, B=64))

@@ -1,6 +1,7 @@
 // gva_api.cu -- the C ABI of libgva.so (declared in include/gva.h): host-side
 // validation, workspace planning and kernel launches.  One translation unit holds
 // every kernel so that they share the device status word.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -15,6 +16,7 @@
 #include "decode_mma.cuh"
 #include "prefill_mma.cuh"
 #include "decode_rope_keys.cuh"
+#include "prefill_tc.cuh"
 
 using namespace gva;
 
@@ -110,6 +112,7 @@ const DevState *device_state() {
     if (e == cudaSuccess) e = mma_opt_in_all();
     if (e == cudaSuccess) e = prefill_opt_in_all();
     if (e == cudaSuccess) e = rk_opt_in_all();
+    if (e == cudaSuccess) e = prefill_tc_opt_in_all();
     if (e == cudaSuccess) e = max_carveout(append_kernel<float>);
     if (e == cudaSuccess) e = max_carveout(append_kernel<__nv_bfloat16>);
     if (e == cudaSuccess) e = max_carveout(combine_kernel);
@@ -348,7 +351,9 @@ struct PrefillPlan {
     int max_pages;
     gva_dims dv;        // the decode batch: B*n entries
     WsPlan dws;         // its workspace plan (offsets relative to dec)
-    bool mq;            // the tensor-core prefill kernel takes this shape
+    bool mq;            // the mma.sync prefill kernel takes this shape
+    int tcm;            // rows per product of the tcgen05 prefill kernel (64 or 128), or 0
+    int tc_splits;      // its history ranges per sequence
     PrefillMmaPlan mp;
 };
 
@@ -365,8 +370,18 @@ bool plan_prefill(const gva_dims *d, int n, const gva_rows &R, int sms, PrefillP
     p->dws = plan_ws(&p->dv, sms);
     p->dec = o; o += p->dws.total;
     p->mq = prefill_mma_plan(d, n, sms, &p->mp);
-    p->po = o;  o += p->mq ? p->mp.part_o_bytes : 0;
-    p->pml = o; o += p->mq ? p->mp.part_ml_bytes : 0;
+    // the tcgen05 kernel: one CTA per (history range, value group, sequence), one wave
+    p->tcm = p->mq ? prefill_tc_m(d, n) : 0;
+    const long long gb = (long long)d->G * d->B;
+    p->tc_splits = p->tcm ? (int)(gb >= sms ? 1 : sms / gb) : 0;
+    size_t po_bytes = p->mq ? p->mp.part_o_bytes : 0, pml_bytes = p->mq ? p->mp.part_ml_bytes : 0;
+    if (p->tcm) {
+        const size_t rows = (size_t)d->B * p->tc_splits * p->mp.rows_pad;
+        po_bytes = std::max(po_bytes, align_up(rows * d->d_h * sizeof(float), 256));
+        pml_bytes = std::max(pml_bytes, align_up(rows * 2 * sizeof(float), 256));
+    }
+    p->po = o;  o += po_bytes;
+    p->pml = o; o += pml_bytes;
     p->total = o;
     return true;
 }
@@ -852,6 +867,19 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
         mp.rows_pad = pp.mp.rows_pad;
         mp.vpitch = pp.mp.vpitch;
         mp.stage_bytes = pp.mp.stage_bytes;
+        if (pp.tcm) {
+            // tcgen05 kernel: 128-token tiles of each sequence's rows through TMA
+            PrefillTcParams tp;
+            memset(&tp, 0, sizeof(tp));
+            tp.p = mp;
+            tp.p.splits = pp.tc_splits;
+            tp.ch = R.layout == GVA_LAYOUT_PAGED ? gcd_int(R.page_size, 64) : 64;
+            CUtensorMap tv, tk;
+            if (!prefill_tc_maps(&tv, &tk, cache->V, cache->K_rope, R.num_rows, d->G * d->d_h,
+                                 d->d_r, tp.ch))
+                return GVA_ERR_CUDA;
+            return cuda_status(prefill_tc_launch(stream, d->d_h, d->d_r, pp.tcm, tp, tv, tk));
+        }
         const cudaError_t e = d->d_h == 64 ? prefill_launch_dh<64>(stream, d->d_r, pp.mp, mp)
                                            : prefill_launch_dh<128>(stream, d->d_r, pp.mp, mp);
         return cuda_status(e);
