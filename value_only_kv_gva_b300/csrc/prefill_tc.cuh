@@ -14,7 +14,8 @@
 // and low parts accumulated into the same tensor-memory columns (about 16 bits kept).
 // The value tile is the B operand of both products: K-major (tokens x d_h) for the
 // scores, MN-major for P V.  The positional keys come in as a 64-wide box of which the
-// columns past d_r are zero (out of the tensor's bounds), matching zero columns of Q^.
+// columns past d_r are zero (out of the tensor's bounds), matching zero columns of Q^;
+// it is 16 (32-byte swizzle) or 32 (64-byte swizzle) columns wide.
 // Warps: 0-15 softmax (four per tensor-memory lane quadrant, a quarter of the columns
 // each), 16 the TMA producer, 17 the MMA issuer.  The ranges' partials use the layout of the mma.sync prefill kernel and its
 // log-sum-exp merge (prefill_mma.cuh).
@@ -33,7 +34,7 @@ namespace gva {
 constexpr int PT_TILE = 128;
 constexpr int PT_SWARPS = 16;   // softmax warps: four per tensor-memory lane quadrant
 constexpr int PT_THREADS = (PT_SWARPS + 2) * 32;
-constexpr int PT_MAX_STAGES = 4;
+constexpr int PT_MAX_STAGES = 8;
 
 struct PrefillTcParams {
     PrefillMmaParams p;   // shapes, inputs, partial layout (splits, wpg, rows_pad)
@@ -42,12 +43,16 @@ struct PrefillTcParams {
     int smem_bytes;
 };
 
-__device__ __forceinline__ uint64_t pt_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor: layout 2 = 128-byte swizzle (rows of 128 B), 4 = 64-byte,
+// 6 = 32-byte; sbo = bytes between groups of 8 rows, lbo = bytes between 64-element blocks
+// along the contiguous dimension of an MN-major operand.
+__device__ __forceinline__ uint64_t pt_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                             uint32_t layout = 2) {
     uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)layout << 61;
     return d;
 }
 // bf16 A and B, fp32 D; b_mn: B is MN-major (N contiguous)
@@ -87,6 +92,29 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t *v) {
         "r"(v[15])
         : "memory");
 }
+// 16 lanes x 256 bits per repeat: thread t gets lanes t/4 and 8 + t/4, columns 2 (t % 4)
+// and 2 (t % 4) + 1 of each 8-column block (registers 4 j + 0, 1 and 4 j + 2, 3).
+__device__ __forceinline__ void tc_ld16x256_x4(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_ld16x256_x2(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tc_st16x256_x2(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -109,7 +137,9 @@ struct PtSmem {
     static constexpr int QPART = KQ * M * 128;               // one of the two query parts
     static constexpr int PPART = 2 * M * 128;                // P part: 128 tokens
     static constexpr int VT = RK_TILE * DH * 2;              // value tile
-    static constexpr int KT = DR > 0 ? RK_TILE * 128 : 0;    // positional tile (64 wide)
+    // positional tile: 16 columns in 32-byte rows (d_r <= 16) or 32 in 64-byte rows
+    static constexpr int KRW = DR <= 16 ? 16 : 32;
+    static constexpr int KT = DR > 0 ? RK_TILE * KRW * 2 : 0;
     static constexpr int STAGE = VT + KT;
     static constexpr int XM = 2 * 4 * 4 * 32 * 4;            // row max parts [buf][quad][part][32]
     static constexpr int LS = 4 * 4 * 32 * 4;                // row sum parts [quad][part][32]
@@ -261,7 +291,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                     }
                 }
                 const uint32_t fb = bar_full + 8 * sl;
-                mbar_expect_tx(fb, (uint32_t)(nl * tp.ch * 128 * (KB + (DR > 0 ? 1 : 0))));
+                mbar_expect_tx(fb, (uint32_t)(nl * tp.ch * (128 * KB + (DR > 0 ? SM::KRW * 2 : 0))));
                 const uint32_t dst = st_s + sl * SM::STAGE;
                 for (int c = 0; c < nbox; ++c) {
                     if (rows[c] < 0) continue;
@@ -270,7 +300,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                         tma_load_2d(dst + kb * (PT_TILE * 128) + c * tp.ch * 128, &tm_v,
                                     g * DH + kb * 64, (int)rows[c], fb, pol);
                     if (DR > 0)
-                        tma_load_2d(dst + SM::VT + c * tp.ch * 128, &tm_k, 0, (int)rows[c], fb, pol);
+                        tma_load_2d(dst + SM::VT + c * tp.ch * (SM::KRW * 2), &tm_k, 0, (int)rows[c], fb, pol);
                 }
                 GVA_TRACE_AT(200 + k);
             }
@@ -282,19 +312,22 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t id_s = pt_idesc(M, PT_TILE, 0);
             constexpr uint32_t id_o = pt_idesc(M, DH, 1);
+            const uint64_t qd = pt_sdesc(q_s, 16, 1024);
+            // descriptors are built once per buffer; an operand offset within a buffer is
+            // added to the descriptor's address field (bytes / 16; addresses stay < 256 KB)
             auto pv = [&](int k) -> bool {   // O += P V of tile k (P hi and lo)
                 if (!mbar_wait(bar_pfull + 8 * (k & 1), (uint32_t)(k >> 1) & 1u, abort)) return false;
                 tc_fence_after();
-                const uint32_t vt = st_s + (k % ns) * SM::STAGE;
-                const uint32_t pbase = p_s + (k % PB) * 2 * SM::PPART;
+                const uint64_t pd = pt_sdesc(p_s + (k % PB) * 2 * SM::PPART, 16, 1024);
+                const uint64_t vd = pt_sdesc(st_s + (k % ns) * SM::STAGE, PT_TILE * 128, 1024);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int kk = 0; kk < PT_TILE / 16; ++kk) {
-                        const uint64_t ad = pt_sdesc(pbase + part * SM::PPART + (kk >> 2) * (M * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = pt_sdesc(vt + kk * 2048, PT_TILE * 128, 1024);
-                        tc_mma(tmem + O_COL, ad, bd, id_o, (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < PT_TILE / 16; ++kk)
+                        tc_mma(tmem + O_COL,
+                               pd + (uint64_t)((part * SM::PPART + (kk >> 2) * (M * 128) + (kk & 3) * 32) >> 4),
+                               vd + (uint64_t)((kk * 2048) >> 4), id_o,
+                               (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(bar_pvdone + 8 * (k & 1));
                 tc_commit(bar_empty + 8 * (k % ns));
                 return true;
@@ -309,21 +342,19 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                 tc_fence_after();
                 const uint32_t vt = st_s + sl * SM::STAGE;
                 const uint32_t d = tmem + sb * PT_TILE;
+                const uint64_t vd = pt_sdesc(vt, 16, 1024);
+                const uint64_t kd = pt_sdesc(vt + SM::VT, 16, 8 * SM::KRW * 2, SM::KRW == 16 ? 6u : 4u);
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
-                    const uint32_t qa = q_s + part * SM::QPART;
 #pragma unroll
-                    for (int kk = 0; kk < DH / 16; ++kk) {
-                        const uint64_t ad = pt_sdesc(qa + (kk >> 2) * (M * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = pt_sdesc(vt + (kk >> 2) * (PT_TILE * 128) + (kk & 3) * 32, 16, 1024);
-                        tc_mma(d, ad, bd, id_s, (part > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        tc_mma(d, qd + (uint64_t)((part * SM::QPART + (kk >> 2) * (M * 128) + (kk & 3) * 32) >> 4),
+                               vd + (uint64_t)(((kk >> 2) * (PT_TILE * 128) + (kk & 3) * 32) >> 4), id_s,
+                               (part > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < KR; ++kk) {
-                        const uint64_t ad = pt_sdesc(qa + KB * (M * 128) + kk * 32, 16, 1024);
-                        const uint64_t bd = pt_sdesc(vt + SM::VT + kk * 32, 16, 1024);
-                        tc_mma(d, ad, bd, id_s, 1u);
-                    }
+                    for (int kk = 0; kk < KR; ++kk)
+                        tc_mma(d, qd + (uint64_t)((part * SM::QPART + KB * (M * 128) + kk * 32) >> 4),
+                               kd + (uint64_t)((kk * 32) >> 4), id_s, 1u);
                 }
                 tc_commit(bar_sfull + 8 * sb);
                 GVA_TRACE_AT(10 + 3 * k);
@@ -337,6 +368,189 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         }
     } else {
         // ------------------------------ softmax ------------------------------ //
+        if constexpr (M == 64) {
+        // M = 64: rows 16 q .. 16 q + 15 sit in lanes 0-15 of quadrant q; the 16x256b loads
+        // spread them over all 32 threads: thread t holds rows A = 16 q + t/4 and
+        // B = A + 8, column pairs 2 (t % 4) + {0, 1} of each 8-column block of the warp's
+        // quarter (32 columns) of the tile
+        const int q = warp & 3, pt = warp >> 2;
+        const int tq = lane >> 2, tc = lane & 3;
+        const int rA = 16 * q + tq, rB = rA + 8;
+        const bool hA = rA < nrows, hB = rB < nrows;
+        const long long limA = (hA && l0 + rA / p.r < Lt) ? l0 + rA / p.r : -1;
+        const long long limB = (hB && l0 + rB / p.r < Lt) ? l0 + rB / p.r : -1;
+        const uint32_t tq0 = tmem + ((uint32_t)(32 * q) << 16);
+        const int cb = 32 * pt + 2 * tc;   // tile column of register 0
+        float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+        bool ok = true;
+        for (int k = 0; k < ntile; ++k) {
+            const int sb = k & 1, sl = k % ns, pbuf = k % PB;
+            const long long j0 = (long long)(k0 + k) * PT_TILE;
+            const int nv = (int)min((long long)PT_TILE, Lt - j0);
+            ok = ok && mbar_wait(bar_sfull + 8 * sb, (uint32_t)(k >> 1) & 1u, abort);
+            ok = __all_sync(0xffffffffu, ok);
+            if (tid == 0) GVA_TRACE_AT(100 + 3 * k);
+            uint32_t v[16];
+            if (ok) {
+                tc_fence_after();
+                tc_ld16x256_x4(tq0 + sb * PT_TILE + 32 * pt, v);
+                tc_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_sfree + 8 * sb);
+            const long long vA = limA - j0, vB = limB - j0;   // last visible tile column
+            float xA = -INFINITY, xB = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = cb + 8 * j + e;
+                    if (col <= vA) xA = fmaxf(xA, __uint_as_float(v[4 * j + e]));
+                    if (col <= vB) xB = fmaxf(xB, __uint_as_float(v[4 * j + 2 + e]));
+                }
+            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 1));
+            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 1));
+            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 2));
+            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 2));
+            float *xw = xm + (sb * 4 + q) * 64;   // [part][16 rows]
+            if (tc == 0) {
+                xw[pt * 16 + tq] = xA;
+                xw[pt * 16 + 8 + tq] = xB;
+            }
+            named_sync(1 + q, 128);
+            if (tid == 0) GVA_TRACE_AT(101 + 3 * k);
+            const float tA = fmaxf(fmaxf(xw[tq], xw[16 + tq]), fmaxf(xw[32 + tq], xw[48 + tq]));
+            const float tB = fmaxf(fmaxf(xw[8 + tq], xw[24 + tq]), fmaxf(xw[40 + tq], xw[56 + tq]));
+            float aA = 1.f, aB = 1.f;
+            if (tA > mA + RK_RESCALE_TH) {
+                aA = exp2f(mA - tA);
+                mA = tA;
+            }
+            if (tB > mB + RK_RESCALE_TH) {
+                aB = exp2f(mB - tB);
+                mB = tB;
+            }
+            float sA = 0.f, sB = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = cb + 8 * j + e;
+                    const float pa = col <= vA ? ex2_approx(__uint_as_float(v[4 * j + e]) - mA) : 0.f;
+                    const float pb = col <= vB ? ex2_approx(__uint_as_float(v[4 * j + 2 + e]) - mB) : 0.f;
+                    v[4 * j + e] = __float_as_uint(pa);
+                    v[4 * j + 2 + e] = __float_as_uint(pb);
+                    sA += pa;
+                    sB += pb;
+                }
+            lA = lA * aA + sA;
+            lB = lB * aB + sB;
+            // O is rescaled after the previous tile's products and before this one's; P's
+            // buffer is rewritten after the products that last read it
+            const bool rescale = __any_sync(0xffffffffu, aA != 1.f || aB != 1.f) && k >= 1;
+            if (rescale)
+                ok = ok && mbar_wait(bar_pvdone + 8 * ((k - 1) & 1), (uint32_t)((k - 1) >> 1) & 1u, abort);
+            if (k >= PB)
+                ok = ok && mbar_wait(bar_pvdone + 8 * ((k - PB) & 1), (uint32_t)((k - PB) >> 1) & 1u, abort);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok && rescale) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < DH / 64; ++c) {
+                    uint32_t o[8];
+                    const uint32_t oa = tq0 + O_COL + pt * (DH / 4) + 16 * c;
+                    tc_ld16x256_x2(oa, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * aA);
+                        o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * aA);
+                        o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * aB);
+                        o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * aB);
+                    }
+                    tc_st16x256_x2(oa, o);
+                }
+                tc_wait_st();
+                tc_fence_before();
+            }
+            // P (bf16 high and low parts): this thread's column pairs of rows A and B
+            {
+                unsigned char *pb = p8 + pbuf * 2 * SM::PPART;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int chunk = 4 * pt + j;
+                    uint32_t h0, l0w, h1, l1w;
+                    split_bf16(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), h0, l0w);
+                    split_bf16(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), h1, l1w);
+                    const uint32_t oA = pt_chunk(rA, chunk, 64) + 4 * tc, oB = pt_chunk(rB, chunk, 64) + 4 * tc;
+                    *reinterpret_cast<uint32_t *>(pb + oA) = h0;
+                    *reinterpret_cast<uint32_t *>(pb + SM::PPART + oA) = l0w;
+                    *reinterpret_cast<uint32_t *>(pb + oB) = h1;
+                    *reinterpret_cast<uint32_t *>(pb + SM::PPART + oB) = l1w;
+                }
+            }
+            // value rows past the sequence's end hold whatever the staged boxes brought
+            // (or nothing): zero them, so that P = 0 multiplies zeros
+            if (nv < PT_TILE) {
+                unsigned char *vt = sm + (st_s - base) + sl * SM::STAGE;
+                for (int e = tid; e < (PT_TILE - nv) * (DH / 8); e += PT_SWARPS * 32) {
+                    const int t = nv + e / (DH / 8), c = e % (DH / 8);
+                    *reinterpret_cast<uint4 *>(vt + (c >> 3) * (PT_TILE * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_pfull + 8 * sb);
+            if (tid == 0) GVA_TRACE_AT(102 + 3 * k);
+        }
+        // this range's partial of rows A and B: unnormalised O, running max, sum
+        if (ntile > 0)
+            ok = ok && mbar_wait(bar_pvdone + 8 * ((ntile - 1) & 1), (uint32_t)((ntile - 1) >> 1) & 1u, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        const long long prow0 = ((long long)b * p.splits + split) * p.rows_pad + (long long)g * p.wpg * 16;
+        if (ntile > 0 && ok) tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DH / 64; ++c) {
+            uint32_t o[8];
+            if (ntile > 0 && ok) {
+                tc_ld16x256_x2(tq0 + O_COL + pt * (DH / 4) + 16 * c, o);
+                tc_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = pt * (DH / 4) + 16 * c + 8 * j + 2 * tc;
+                if (hA)
+                    *reinterpret_cast<float2 *>(p.part_o + (prow0 + rA) * DH + col) =
+                        make_float2(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]));
+                if (hB)
+                    *reinterpret_cast<float2 *>(p.part_o + (prow0 + rB) * DH + col) =
+                        make_float2(__uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+            }
+        }
+        lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+        lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+        float *lw = lsh + q * 64;   // [part][16 rows]
+        if (tc == 0) {
+            lw[pt * 16 + tq] = lA;
+            lw[pt * 16 + 8 + tq] = lB;
+        }
+        named_sync(1 + q, 128);
+        if (pt == 0 && tc == 0) {
+            if (hA)
+                *reinterpret_cast<float2 *>(p.part_ml + (prow0 + rA) * 2) =
+                    make_float2(mA, (lw[tq] + lw[16 + tq]) + (lw[32 + tq] + lw[48 + tq]));
+            if (hB)
+                *reinterpret_cast<float2 *>(p.part_ml + (prow0 + rB) * 2) =
+                    make_float2(mB, (lw[8 + tq] + lw[24 + tq]) + (lw[40 + tq] + lw[56 + tq]));
+        }
+        } else {
         // the thread's query row: M = 128 lanes = rows; M = 64 puts rows 16 q .. 16 q + 15
         // in lanes 0-15 of quadrant q
         const int q = warp & 3, pt = warp >> 2;   // quadrant, column quarter
@@ -484,6 +698,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
             *reinterpret_cast<float2 *>(p.part_ml + prow * 2) =
                 make_float2(m, (lsh[(q * 4) * 32 + lane] + lsh[(q * 4 + 1) * 32 + lane]) +
                                    (lsh[(q * 4 + 2) * 32 + lane] + lsh[(q * 4 + 3) * 32 + lane]));
+            }
     }
     tc_fence_before();
     __syncthreads();
@@ -526,8 +741,9 @@ inline int prefill_tc_stages() {
     return ns;
 }
 
-// 2D maps: value rows [rows][G d_h] box {64, ch}; positional rows [rows][d_r] box {64, ch}
-// (the columns past d_r are outside the tensor and arrive as zeros).  Both 128-byte swizzled.
+// 2D maps: value rows [rows][G d_h] box {64, ch}, 128-byte swizzle; positional rows
+// [rows][d_r] box {16, ch} with the 32-byte swizzle (d_r <= 16) or {32, ch} with the 64-byte
+// one (the columns past d_r are outside the tensor and arrive as zeros).
 inline bool prefill_tc_maps(CUtensorMap *tv, CUtensorMap *tk, const void *V, const void *Kr,
                             long long rows, int width, int d_r, int ch) {
     if (!rk_make_map(tv, V, rows, width, ch)) return false;
@@ -539,10 +755,12 @@ inline bool prefill_tc_maps(CUtensorMap *tv, CUtensorMap *tk, const void *V, con
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)d_r, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[1] = {(cuuint64_t)d_r * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)ch};
+    const bool narrow = d_r <= 16;
+    cuuint32_t box[2] = {narrow ? 16u : 32u, (cuuint32_t)ch};
     cuuint32_t estr[2] = {1, 1};
     return enc(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(Kr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               narrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
