@@ -581,6 +581,22 @@ def prefill_work(w, L0, n: int):
     return nbytes, 2 * w.H * (2 * w.d_h + w.d_r) * pairs
 
 
+def _prefill_design(w, n: int, path: str) -> str:
+    """Which prefill kernel the library's automatic path takes for this shape."""
+    if path != "auto" or w.cache_dtype != "bf16" or w.d_h not in (64, 128):
+        return ("each new token run as one entry of a decode batch of B*n entries over a "
+                "paged view of the cache")
+    rows = n * (w.H // w.G)
+    if rows <= 64 or (rows <= 128 and w.d_h == 64):
+        return ("tcgen05 prefill kernel: one CTA per (history range, value group, sequence) "
+                "holds the group's chunk rows, streams 128-token tiles of its rows once "
+                "(TMA), S = Q V^T and O += P V accumulate in tensor memory, online softmax "
+                "in 16 warps; ranges merged by log-sum-exp")
+    return ("mma.sync prefill kernel: each 16-token slab of a sequence's rows loaded once "
+            "per CTA and scored against all the chunk's (query, head) rows, split over the "
+            "history and merged by log-sum-exp")
+
+
 def run_prefill(args, dist: Dist):
     """Causal chunked prefill: one step = gva_prefill_attention (append of n tokens per
     sequence, then the attention of each new token over the history and the chunk up to
@@ -744,12 +760,7 @@ def run_prefill(args, dist: Dist):
             "achieved_tflops": round(tflops, 3),
             "tensor_frac_of_bf16_peak": round(tflops / tc_peak, 5) if tc_peak else None,
             "l2": f"inputs larger than L2: {nl} distinct layer caches", "path": path,
-            "design": ("tensor-core prefill kernel: each 16-token slab of a sequence's rows "
-                       "loaded once per CTA and scored against all the chunk's (query, head) "
-                       "rows, split over the history and merged by log-sum-exp"
-                       if path == "auto" and w.cache_dtype == "bf16" and w.d_h in (64, 128)
-                       else "each new token run as one entry of a decode batch of B*n entries "
-                            "over a paged view of the cache")},
+            "design": _prefill_design(w, n, path)},
         "roofline": {"bound": "hbm", "kernel": "gva_prefill_attention (view + append + absorb + "
                      "prefill partial + combine), per call", "achieved": round(gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
