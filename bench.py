@@ -286,12 +286,6 @@ def measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path, 
     del g_step, g_dec
     if not with_gqa:
         return out
-    if w.layout == "ragged":
-        # the graph replay of this comparator on the full ragged batch ended in a launch
-        # failure twice while the library was built (cause not found): it is not run
-        out["gqa_comparator"] = {"not_run": "ragged-layout comparator replay kept off the GPU "
-                                            "(unresolved launch failure)"}
-        return out
     Kq0 = gva_inputs.make_gqa_keys(S.c).to(S.dev)
     qq = gva_inputs.make_gqa_query(S.c).to(S.dev)
     glayers = []

@@ -10,8 +10,9 @@ import numpy as np
 import pytest
 import torch
 
-from gva_inputs import make_case, workload
-from helpers import Dev, assert_close, gva, oracle_append, oracle_decode
+import oracle
+from gva_inputs import make_case, make_gqa_keys, make_gqa_query, workload
+from helpers import Dev, assert_close, gva, oracle_append, oracle_decode, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -65,3 +66,29 @@ def test_full_size_350m_share_boundaries(num_ctas):
     ref, ref_lse = oracle_decode(c)
     assert_close(out, ref, "bf16", f"350m n_ctas={num_ctas} out")
     assert_close(lse, ref_lse, "bf16", f"350m n_ctas={num_ctas} lse")
+
+
+@pytest.mark.parametrize("name", ["ragged", "350m"])
+def test_full_size_gqa_comparator_repeated(name):
+    """The GQA comparator at full size in the bench's launch configuration, five calls in a
+    row, every sequence and head against the oracle each time.  Both batches give each CTA
+    more slabs than its ring has stages (the ragged batch about five rounds), so the
+    consumer warps wait on stages whose previous round another warp of the group took."""
+    c = make_case(workload(name))
+    D = Dev(c)
+    g = gva()
+    K = make_gqa_keys(c)
+    q = make_gqa_query(c)
+    kv = g.KVCache(D.rows, K.cuda(), D.V)
+    w = c.w
+    scale = 1.0 / np.sqrt(w.d_h)
+    ref, ref_lse = oracle.gqa_decode(q, c.seq_len, oracle_rows(c), K, c.V, scale, w.G)
+    qd = q.cuda()
+    for it in range(5):
+        out = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+        lse = torch.full((w.B, w.H), float("nan"), device="cuda")
+        g.gva_gqa_decode_attention(D.dims, qd, D.seq_len, kv, scale, out, lse, D.ws, path="auto")
+        torch.cuda.synchronize()
+        assert g.gva_get_device_status() == 0
+        assert_close(out.cpu().numpy(), ref, "bf16", f"gqa {name} call {it} out")
+        assert_close(lse.cpu().numpy(), ref_lse, "bf16", f"gqa {name} call {it} lse")

@@ -1023,6 +1023,16 @@ inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
     int ns = (MMA_SMEM_TARGET - fixed) / mp.stage_bytes;
     if (ns < 4) ns = (MMA_SMEM_LIMIT - fixed) / mp.stage_bytes;
     if (ns > MMA_MAX_STAGES) ns = MMA_MAX_STAGES;
+    // Warp w of a group takes the share's slabs w, w + wpg, ... and slab i sits in stage
+    // i mod ns, so with ns a multiple of wpg every round of a stage goes to the same
+    // warp of each group: a warp waits for round R of a stage only after it consumed
+    // round R - 1 of that stage itself, so the stage's full barrier is then in phase R
+    // or past it, and the parity wait is exact.  With any other ns, a warp can reach
+    // round R while another warp's round R - 1 copy into that stage is still in flight;
+    // the barrier's current phase (R - 1) then has the other parity, the parity test
+    // passes at once, and the warp reads a half-written stage and gives back a stage
+    // whose round has not begun (the empty barrier's phases then drift from the rounds).
+    ns -= ns % mp.wpg;
     if (ns < 2) return false;
     mp.nstages = ns;
     mp.off_bar = ns * mp.stage_bytes;
