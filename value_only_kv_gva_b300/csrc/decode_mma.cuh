@@ -571,6 +571,7 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
                               rbytes, fb, pol);
                 const int ti = (int)(s - s0);
                 if (ti == 0) GVA_TRACE_AT(2);
+                if (ti == 0) GVA_REC(3, 3);
                 if (ti < 64) GVA_TRACE_AT(300 + ti);
             }
         }
@@ -660,6 +661,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0,   // includes __syncthreads
                  blockIdx.x == 0 ? p.prefix_ws : nullptr);
     if (threadIdx.x == 0) GVA_TRACE_AT(1);
+    if (threadIdx.x == 0) GVA_REC(3, 5);
     const Part P{F[B], p.n_ctas};
     const int c = blockIdx.x;
     if (P.S == 0) return;
@@ -726,6 +728,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 break;
             }
             if (w == 0 && g == 0 && lane == 0) GVA_TRACE_AT(8 + 2 * tslab);
+            if (w == 0 && g == 0 && lane == 0 && tslab == 0) GVA_REC(3, 4);
             const int j0 = (int)(my_s - Fb) * SLAB;
             int nv = min(SLAB, Lb - j0);
             if (stage_bad[my_stage]) {

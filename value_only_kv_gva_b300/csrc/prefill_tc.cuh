@@ -11,7 +11,11 @@
 //   O[M x d_h] += P V_g                          tcgen05.mma, O resident in tensor memory
 //
 // M = 64 (n r <= 64) or 128 rows.  The fp32 queries and probabilities enter as bf16 high
-// and low parts accumulated into the same tensor-memory columns (about 16 bits kept).
+// and low parts (about 16 bits kept).  The query parts accumulate into the same S columns.
+// With M = 64 the probability parts are stacked into one 128-row operand, so O += P V is
+// one 128-row product per k-step: the high part of row r lands in tensor-memory lane
+// 32 (r / 16) + r % 16 and the low part 16 lanes further, in the lane quadrant of the
+// warps that own score row r, and the two are summed once at the end.
 // The value tile is the B operand of both products: K-major (tokens x d_h) for the
 // scores, MN-major for P V.  The positional keys come in as a 64-wide box of which the
 // columns past d_r are zero (out of the tensor's bounds), matching zero columns of Q^;
@@ -102,19 +106,6 @@ __device__ __forceinline__ void tc_ld16x256_x4(uint32_t taddr, uint32_t (&v)[16]
           "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
 }
-__device__ __forceinline__ void tc_ld16x256_x2(uint32_t taddr, uint32_t (&v)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                   "=r"(v[6]), "=r"(v[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tc_st16x256_x2(uint32_t taddr, const uint32_t (&v)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
-                     taddr),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                 "r"(v[7])
-                 : "memory");
-}
 __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -124,6 +115,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+// Probability pair (x0, x1) >= 0 as bf16 high parts taken by truncation (the upper halves
+// of the fp32 words: one byte permute) and the remainders x - hi (exact in fp32) rounded
+// to bf16: hi + lo keeps about 16 bits, with one conversion per pair instead of two.
+__device__ __forceinline__ void split_bf16_trunc(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+    hi = __byte_perm(u0, u1, 0x7632);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(u0 & 0xffff0000u),
+                                                   x1 - __uint_as_float(u1 & 0xffff0000u));
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 // Byte offset of the 16-byte chunk holding elements 8 c .. 8 c + 7 of row r of a K-major
 // tile with `rows` rows, in 64-element (128-byte) swizzled blocks.
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         // ------------------------------ MMA issuer ------------------------------ //
         if (lane == 0) {
             constexpr uint32_t id_s = pt_idesc(M, PT_TILE, 0);
-            constexpr uint32_t id_o = pt_idesc(M, DH, 1);
+            constexpr uint32_t id_o = pt_idesc(M == 64 ? 128 : M, DH, 1);
             const uint64_t qd = pt_sdesc(q_s, 16, 1024);
             // descriptors are built once per buffer; an operand offset within a buffer is
             // added to the descriptor's address field (bytes / 16; addresses stay < 256 KB)
@@ -320,14 +321,22 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                 tc_fence_after();
                 const uint64_t pd = pt_sdesc(p_s + (k % PB) * 2 * SM::PPART, 16, 1024);
                 const uint64_t vd = pt_sdesc(st_s + (k % ns) * SM::STAGE, PT_TILE * 128, 1024);
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
+                if constexpr (M == 64) {
+                    // the stacked parts: 128 rows per 64-token K-block
 #pragma unroll
                     for (int kk = 0; kk < PT_TILE / 16; ++kk)
-                        tc_mma(tmem + O_COL,
-                               pd + (uint64_t)((part * SM::PPART + (kk >> 2) * (M * 128) + (kk & 3) * 32) >> 4),
-                               vd + (uint64_t)((kk * 2048) >> 4), id_o,
-                               (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma(tmem + O_COL, pd + (uint64_t)(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4),
+                               vd + (uint64_t)((kk * 2048) >> 4), id_o, (k > 0 || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < PT_TILE / 16; ++kk)
+                            tc_mma(tmem + O_COL,
+                                   pd + (uint64_t)((part * SM::PPART + (kk >> 2) * (M * 128) + (kk & 3) * 32) >> 4),
+                                   vd + (uint64_t)((kk * 2048) >> 4), id_o,
+                                   (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                }
                 tc_commit(bar_pvdone + 8 * (k & 1));
                 tc_commit(bar_empty + 8 * (k % ns));
                 return true;
@@ -399,16 +408,30 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_sfree + 8 * sb);
-            const long long vA = limA - j0, vB = limB - j0;   // last visible tile column
+            // last visible tile column of rows A and B, clamped to [-1, 127]
+            const int vA = (int)max(-1LL, min((long long)PT_TILE - 1, limA - j0));
+            const int vB = (int)max(-1LL, min((long long)PT_TILE - 1, limB - j0));
+            // the warp's whole quarter visible to all its rows (every history tile)
+            const bool whole = __all_sync(0xffffffffu, vA >= cb + 31 - 2 * tc && vB >= cb + 31 - 2 * tc);
             float xA = -INFINITY, xB = -INFINITY;
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = cb + 8 * j + e;
-                    if (col <= vA) xA = fmaxf(xA, __uint_as_float(v[4 * j + e]));
-                    if (col <= vB) xB = fmaxf(xB, __uint_as_float(v[4 * j + 2 + e]));
-                }
+                    for (int e = 0; e < 2; ++e) {
+                        xA = fmaxf(xA, __uint_as_float(v[4 * j + e]));
+                        xB = fmaxf(xB, __uint_as_float(v[4 * j + 2 + e]));
+                    }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = cb + 8 * j + e;
+                        if (col <= vA) xA = fmaxf(xA, __uint_as_float(v[4 * j + e]));
+                        if (col <= vB) xB = fmaxf(xB, __uint_as_float(v[4 * j + 2 + e]));
+                    }
+            }
             xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 1));
             xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 1));
             xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 2));
@@ -432,18 +455,32 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                 mB = tB;
             }
             float sA = 0.f, sB = 0.f;
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = cb + 8 * j + e;
-                    const float pa = col <= vA ? ex2_approx(__uint_as_float(v[4 * j + e]) - mA) : 0.f;
-                    const float pb = col <= vB ? ex2_approx(__uint_as_float(v[4 * j + 2 + e]) - mB) : 0.f;
-                    v[4 * j + e] = __float_as_uint(pa);
-                    v[4 * j + 2 + e] = __float_as_uint(pb);
-                    sA += pa;
-                    sB += pb;
-                }
+                    for (int e = 0; e < 2; ++e) {
+                        const float pa = ex2_approx(__uint_as_float(v[4 * j + e]) - mA);
+                        const float pb = ex2_approx(__uint_as_float(v[4 * j + 2 + e]) - mB);
+                        v[4 * j + e] = __float_as_uint(pa);
+                        v[4 * j + 2 + e] = __float_as_uint(pb);
+                        sA += pa;
+                        sB += pb;
+                    }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = cb + 8 * j + e;
+                        const float pa = col <= vA ? ex2_approx(__uint_as_float(v[4 * j + e]) - mA) : 0.f;
+                        const float pb = col <= vB ? ex2_approx(__uint_as_float(v[4 * j + 2 + e]) - mB) : 0.f;
+                        v[4 * j + e] = __float_as_uint(pa);
+                        v[4 * j + 2 + e] = __float_as_uint(pb);
+                        sA += pa;
+                        sB += pb;
+                    }
+            }
             lA = lA * aA + sA;
             lB = lB * aB + sB;
             // O is rescaled after the previous tile's products and before this one's; P's
@@ -455,21 +492,22 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                 ok = ok && mbar_wait(bar_pvdone + 8 * ((k - PB) & 1), (uint32_t)((k - PB) >> 1) & 1u, abort);
             ok = __all_sync(0xffffffffu, ok);
             if (ok && rescale) {
+                // O lane 32 q + t holds the high (t < 16) or low part of row 16 q + t % 16,
+                // whose factor is aA (t % 16 < 8) or aB of the threads with tq = t % 8
+                const int i = lane & 15;
+                const float xa = __shfl_sync(0xffffffffu, aA, 4 * (i & 7));
+                const float xb = __shfl_sync(0xffffffffu, aB, 4 * (i & 7));
+                const float ar = i < 8 ? xa : xb;
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < DH / 64; ++c) {
-                    uint32_t o[8];
+                    uint32_t o[16];
                     const uint32_t oa = tq0 + O_COL + pt * (DH / 4) + 16 * c;
-                    tc_ld16x256_x2(oa, o);
+                    tc_ld16(oa, o);
                     tc_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * aA);
-                        o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * aA);
-                        o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * aB);
-                        o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * aB);
-                    }
-                    tc_st16x256_x2(oa, o);
+                    for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * ar);
+                    tc_st16(oa, o);
                 }
                 tc_wait_st();
                 tc_fence_before();
@@ -481,13 +519,14 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                 for (int j = 0; j < 4; ++j) {
                     const int chunk = 4 * pt + j;
                     uint32_t h0, l0w, h1, l1w;
-                    split_bf16(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), h0, l0w);
-                    split_bf16(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), h1, l1w);
-                    const uint32_t oA = pt_chunk(rA, chunk, 64) + 4 * tc, oB = pt_chunk(rB, chunk, 64) + 4 * tc;
-                    *reinterpret_cast<uint32_t *>(pb + oA) = h0;
-                    *reinterpret_cast<uint32_t *>(pb + SM::PPART + oA) = l0w;
-                    *reinterpret_cast<uint32_t *>(pb + oB) = h1;
-                    *reinterpret_cast<uint32_t *>(pb + SM::PPART + oB) = l1w;
+                    split_bf16_trunc(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), h0, l0w);
+                    split_bf16_trunc(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]), h1, l1w);
+                    // stacked operand rows: high part of row 16 q + i at 32 q + i, low at 32 q + 16 + i
+                    const int ah = 32 * q + tq, bh = ah + 8;
+                    *reinterpret_cast<uint32_t *>(pb + pt_chunk(ah, chunk, 128) + 4 * tc) = h0;
+                    *reinterpret_cast<uint32_t *>(pb + pt_chunk(ah + 16, chunk, 128) + 4 * tc) = l0w;
+                    *reinterpret_cast<uint32_t *>(pb + pt_chunk(bh, chunk, 128) + 4 * tc) = h1;
+                    *reinterpret_cast<uint32_t *>(pb + pt_chunk(bh + 16, chunk, 128) + 4 * tc) = l1w;
                 }
             }
             // value rows past the sequence's end hold whatever the staged boxes brought
@@ -511,25 +550,28 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         const long long prow0 = ((long long)b * p.splits + split) * p.rows_pad + (long long)g * p.wpg * 16;
         if (ntile > 0 && ok) tc_fence_after();
+        // O of row 16 q + t % 16: its high part in lane 32 q + t % 16, its low part 16 lanes on
+        const int ro = 16 * q + (lane & 15);
 #pragma unroll
         for (int c = 0; c < DH / 64; ++c) {
-            uint32_t o[8];
+            uint32_t o[16];
             if (ntile > 0 && ok) {
-                tc_ld16x256_x2(tq0 + O_COL + pt * (DH / 4) + 16 * c, o);
+                tc_ld16(tq0 + O_COL + pt * (DH / 4) + 16 * c, o);
                 tc_wait_ld();
             } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = 0u;
+                for (int j = 0; j < 16; ++j) o[j] = 0u;
             }
+            float f[16];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = pt * (DH / 4) + 16 * c + 8 * j + 2 * tc;
-                if (hA)
-                    *reinterpret_cast<float2 *>(p.part_o + (prow0 + rA) * DH + col) =
-                        make_float2(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]));
-                if (hB)
-                    *reinterpret_cast<float2 *>(p.part_o + (prow0 + rB) * DH + col) =
-                        make_float2(__uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+            for (int j = 0; j < 16; ++j) {
+                f[j] = __uint_as_float(o[j]);
+                f[j] += __shfl_down_sync(0xffffffffu, f[j], 16);
+            }
+            if (lane < 16 && ro < nrows) {
+                float4 *dst = reinterpret_cast<float4 *>(p.part_o + (prow0 + ro) * DH + pt * (DH / 4) + 16 * c);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
             }
         }
         lA += __shfl_xor_sync(0xffffffffu, lA, 1);
@@ -647,7 +689,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        split_bf16(__uint_as_float(s[8 * c + 2 * u]), __uint_as_float(s[8 * c + 2 * u + 1]), hw[u], lw[u]);
+                        split_bf16_trunc(__uint_as_float(s[8 * c + 2 * u]), __uint_as_float(s[8 * c + 2 * u + 1]), hw[u], lw[u]);
                     const uint32_t off = pt_chunk(r, 4 * pt + c, M);
                     *reinterpret_cast<uint4 *>(pb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4 *>(pb + SM::PPART + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
