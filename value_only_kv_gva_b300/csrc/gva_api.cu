@@ -257,9 +257,12 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
                   const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
                   float prescale, float *q_tilde, float *q_hat, int sms,
                   const gva_rows *rows = nullptr, bool skip_rope = false,
-                  const gva_decode_opts *qn = nullptr) {
+                  const gva_decode_opts *qn = nullptr, const int *L0 = nullptr,
+                  int chunk_n = 0) {
     AbsorbParams p;
     p.skip_rope = skip_rope ? 1 : 0;
+    p.L0 = L0;
+    p.chunk_n = chunk_n;
     p.qnorm = qn && (qn->flags & GVA_FLAG_QUERY_RMSNORM) ? 1 : 0;
     p.qn_gain = p.qnorm ? qn->q_norm_gain : nullptr;
     p.qn_eps = p.qnorm ? qn->q_norm_eps : 0.f;
@@ -321,8 +324,11 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
 // One CTA per entry of the batch d->B (arguments validated by the caller).
 int append_launch(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
                   const int *pos, int *seq_len_out, const gva_rows &rows, void *V, void *Kr,
-                  const float *rope_tab, int rope_max_pos) {
+                  const float *rope_tab, int rope_max_pos, const int *L0 = nullptr,
+                  int chunk_n = 0) {
     AppendParams p;
+    p.L0 = L0;
+    p.chunk_n = chunk_n;
     p.B = d->B;
     p.G = d->G;
     p.d_h = d->d_h;
@@ -832,19 +838,31 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     }
     // a path that cannot run the chunk is refused before anything is appended
     if (o->path == GVA_PATH_MMA && !mma_supported(d)) return GVA_ERR_UNSUPPORTED;
-    int st = cuda_status(launch(prefill_view_kernel, dim3(d->B, (n + PV_ROWS - 1) / PV_ROWS),
+    // The tcgen05 prefill kernel reads the caller's rows: the append and the absorption
+    // take each chunk entry's position from L0 themselves, and no view is built.  The
+    // other paths run on the view (a decode batch of B n entries).
+    const bool tc_path = o->path == GVA_PATH_AUTO && pp.mq && pp.tcm;
+    int st;
+    if (tc_path) {
+        st = append_launch(stream, &pp.dv, v_new, k_new, nullptr, nullptr, R, cache->V,
+                           cache->K_rope, rope_tab, rope_max_pos, L0, n);
+    } else {
+        st = cuda_status(launch(prefill_view_kernel, dim3(d->B, (n + PV_ROWS - 1) / PV_ROWS),
                                 dim3(128), 0, stream, vp));
-    if (st != GVA_OK) return st;
-    st = append_launch(stream, &pp.dv, v_new, k_new, vp.pos, nullptr, vr, cache->V,
-                       cache->K_rope, rope_tab, rope_max_pos);
+        if (st != GVA_OK) return st;
+        st = append_launch(stream, &pp.dv, v_new, k_new, vp.pos, nullptr, vr, cache->V,
+                           cache->K_rope, rope_tab, rope_max_pos);
+    }
     if (st != GVA_OK) return st;
     if (o->path == GVA_PATH_AUTO && pp.mq) {
         // tensor-core prefill: absorb every (query, head) of the chunk, then one pass
         // over each sequence's rows shared by all its queries, then the merge
         float *qt = reinterpret_cast<float *>(w + pp.dec + pp.dws.qt);
         float *qh = reinterpret_cast<float *>(w + pp.dec + pp.dws.qh);
-        st = absorb_launch(stream, &pp.dv, q_nope, q_rope, M, vp.len, rope_tab, rope_max_pos,
-                           scale * LOG2E, qt, qh, sms, &vr, false, o);
+        st = tc_path ? absorb_launch(stream, &pp.dv, q_nope, q_rope, M, nullptr, rope_tab,
+                                     rope_max_pos, scale * LOG2E, qt, qh, sms, &R, false, o, L0, n)
+                     : absorb_launch(stream, &pp.dv, q_nope, q_rope, M, vp.len, rope_tab,
+                                     rope_max_pos, scale * LOG2E, qt, qh, sms, &vr, false, o);
         if (st != GVA_OK) return st;
         PrefillMmaParams mp;
         mp.B = d->B;

@@ -15,6 +15,8 @@ struct AppendParams {
     const float *k_new;     // [B][d_r], unrotated
     const int *pos;         // [B]
     int *seq_len_out;       // [B] or null; may alias pos
+    const int *L0;          // chunk mode (chunk_n > 0): entry v is token v % chunk_n of a
+    int chunk_n;            //   chunk appended to sequence v / chunk_n after its L0 tokens
     RowsDev R;
     void *V;                // rows [G][d_h]
     void *Kr;               // rows [d_r]
@@ -22,7 +24,15 @@ struct AppendParams {
     int rope_max_pos;
 };
 
-// One CTA per sequence.  V gets the new value rounded once; K_rope gets
+// Position of chunk entry v (token v % n of sequence v / n): L0[b] + v % n, or -1 when the
+// history is negative or the position leaves the int range (reported as a bad position).
+__device__ __forceinline__ int chunk_pos(const int *L0, int n, int v) {
+    const long long l0 = L0[v / n];
+    const long long e = l0 + v % n;
+    return (l0 >= 0 && e < 0x7fffffffLL) ? (int)e : -1;
+}
+
+// One CTA per sequence (per chunk entry in chunk mode).  V gets the new value rounded once; K_rope gets
 // Rot(pos) k_new computed in fp32 in the fixed order y0 = (x0*c) - (x1*s),
 // y1 = (x0*s) + (x1*c) with every product and sum rounded separately (no FMA), then
 // rounded once to the cache dtype, so the stored bytes are reproducible.
@@ -33,7 +43,8 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     pdl_wait();
     if (threadIdx.x == 0) GVA_REC(1, 1);
     pdl_launch_dependents();
-    const int b = blockIdx.x;
+    const int b = blockIdx.x;                                // entry of the inputs
+    const int sb = p.chunk_n > 0 ? b / p.chunk_n : b;        // sequence of its rows
     const int W = p.G * p.d_h;
     // Loads that do not depend on the position are issued with it: the new value (up
     // to 8 elements per thread), the unrotated key pair, the position.  The table entry
@@ -54,16 +65,16 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
         x0 = kn[2 * threadIdx.x];
         x1 = kn[2 * threadIdx.x + 1];
     }
-    const int pos = p.pos[b];
+    const int pos = p.chunk_n > 0 ? chunk_pos(p.L0, p.chunk_n, b) : p.pos[b];
     __syncthreads();  // every thread has read pos[b] before seq_len_out (may alias) is written
-    bool ok = pos >= 0 && (long long)pos < seq_capacity(p.R, b) && (p.d_r == 0 || pos < p.rope_max_pos);
+    bool ok = pos >= 0 && (long long)pos < seq_capacity(p.R, sb) && (p.d_r == 0 || pos < p.rope_max_pos);
     float c = 0.f, sn = 0.f;
     if (ok && kthr) {
         const float *cs = p.rope_tab + (long long)pos * p.d_r;  // (d_r/2) (cos, sin) pairs
         c = cs[2 * threadIdx.x];
         sn = cs[2 * threadIdx.x + 1];
     }
-    long long row = ok ? row_of(p.R, b, pos) : -1;
+    long long row = ok ? row_of(p.R, sb, pos) : -1;
     if (p.R.layout == GVA_LAYOUT_RAGGED && row >= p.R.num_rows) row = -1;
     if (row < 0) {
         if (threadIdx.x == 0) dev_report(ok ? GVA_DEV_BAD_PAGE : GVA_DEV_BAD_POSITION);
@@ -143,7 +154,9 @@ struct AbsorbParams {
     const void *q_nope;            // [B][H][d_n]
     const void *q_rope;            // [B][H][d_r]
     const float *M;                // [H][d_h][d_n]
-    const int *seq_len;            // [B]
+    const int *seq_len;            // [B]; in chunk mode null, and the length of entry v
+    const int *L0;                 //   is L0[v / chunk_n] + v % chunk_n + 1 (-1 when out of
+    int chunk_n;                   //   range), its rows those of sequence v / chunk_n
     const float *rope_tab;
     int rope_max_pos;
     float prescale;                // multiplies both outputs
@@ -234,7 +247,12 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
         if (rope && e < nb * half) {
             const int rb = b0 + e / half, ri = e % half;
             const QT *qr = reinterpret_cast<const QT *>(p.q_rope) + ((long long)rb * p.H + h) * p.d_r;
-            rL[u] = p.seq_len[rb];
+            if (p.chunk_n > 0) {
+                const int cp = chunk_pos(p.L0, p.chunk_n, rb);
+                rL[u] = cp < 0 ? -1 : cp + 1;
+            } else {
+                rL[u] = p.seq_len[rb];
+            }
             rx0[u] = to_f<QT>(qr[2 * ri]);
             rx1[u] = to_f<QT>(qr[2 * ri + 1]);
         }
@@ -379,7 +397,8 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
             int t = rL[u] - 1;
             if (t < 0) t = 0;
             if (t >= p.rope_max_pos) {
-                if (!p.check_rows || length_ok(p.R, rb, rL[u])) dev_report(GVA_DEV_BAD_POSITION);
+                if (!p.check_rows || length_ok(p.R, p.chunk_n > 0 ? rb / p.chunk_n : rb, rL[u]))
+                    dev_report(GVA_DEV_BAD_POSITION);
                 t = 0;
             }
             const float rc = p.rope_tab[((long long)t * half + ri) * 2];
