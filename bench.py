@@ -475,8 +475,8 @@ def run_ours(args, dist: Dist):
     del S
     torch.cuda.empty_cache()
 
-    # the other workloads the target names, measured in this process with the same clock
-    # sampling: the long-context layer and the paged serving batch
+    # the other workloads, measured in this process with the same clock sampling: the
+    # long-context layer, the paged serving batch and the ragged batch
     others = {}
     if not args.no_others:
         for name in args.others:
@@ -986,7 +986,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-gqa", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--others", nargs="*", default=["long", "paged"],
+    ap.add_argument("--others", nargs="*", default=["long", "paged", "ragged"],
                     help="further workloads measured in the same run (config.other_workloads)")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-rope-keys", action="store_true",
