@@ -575,17 +575,31 @@ def prefill_work(w, L0, n: int):
     return nbytes, 2 * w.H * (2 * w.d_h + w.d_r) * pairs
 
 
+def _prefill_tc(w, n: int, path: str) -> bool:
+    """True when the library's automatic path takes the tcgen05 prefill kernel."""
+    rows = n * (w.H // w.G)
+    return (path == "auto" and w.cache_dtype == "bf16" and w.d_h in (64, 128)
+            and (rows <= 64 or (rows <= 128 and w.d_h == 64)))
+
+
+def _prefill_chain(w, n: int, path: str):
+    """The kernels one prefill call launches: (description, launches per call)."""
+    if _prefill_tc(w, n, path):
+        return "append + absorb + tcgen05 prefill partial + combine", 4
+    return "view + append + absorb + prefill partial + combine", 5
+
+
 def _prefill_design(w, n: int, path: str) -> str:
     """Which prefill kernel the library's automatic path takes for this shape."""
     if path != "auto" or w.cache_dtype != "bf16" or w.d_h not in (64, 128):
         return ("each new token run as one entry of a decode batch of B*n entries over a "
                 "paged view of the cache")
-    rows = n * (w.H // w.G)
-    if rows <= 64 or (rows <= 128 and w.d_h == 64):
+    if _prefill_tc(w, n, path):
         return ("tcgen05 prefill kernel: one CTA per (history range, value group, sequence) "
                 "holds the group's chunk rows, streams 128-token tiles of its rows once "
-                "(TMA), S = Q V^T and O += P V accumulate in tensor memory, online softmax "
-                "in 16 warps; ranges merged by log-sum-exp")
+                "(TMA), S = Q V^T and O += P V accumulate in tensor memory (P's bf16 high and "
+                "low parts stacked as one 128-row product), online softmax in 16 warps; "
+                "ranges merged by log-sum-exp")
     return ("mma.sync prefill kernel: each 16-token slab of a sequence's rows loaded once "
             "per CTA and scored against all the chunk's (query, head) rows, split over the "
             "history and merged by log-sum-exp")
@@ -736,6 +750,7 @@ def run_prefill(args, dist: Dist):
                          f"of one {w.name} layer, fp64 C oracle with OpenMP over (b, h), "
                          f"{cs:.1f} s"}
 
+    chain, per_call = _prefill_chain(w, n, path)
     line = {
         "metric": f"GVA causal chunked prefill, new tokens/s ({w.name} layer, n={n} per "
                   f"sequence)",
@@ -755,13 +770,13 @@ def run_prefill(args, dist: Dist):
             "tensor_frac_of_bf16_peak": round(tflops / tc_peak, 5) if tc_peak else None,
             "l2": f"inputs larger than L2: {nl} distinct layer caches", "path": path,
             "design": _prefill_design(w, n, path)},
-        "roofline": {"bound": "hbm", "kernel": "gva_prefill_attention (view + append + absorb + "
-                     "prefill partial + combine), per call", "achieved": round(gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": f"gva_prefill_attention ({chain}), per call",
+                     "achieved": round(gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                      "peak_source": "measured" if peaks else "fallback", "traffic": None},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": nl * 5 * args.steps,
+        "gpu_launches": nl * per_call * args.steps,
         "clocks": clocks,
     }
     if dist.rank == 0:
