@@ -582,11 +582,19 @@ def _prefill_tc(w, n: int, path: str) -> bool:
             and (rows <= 64 or (rows <= 128 and w.d_h == 64)))
 
 
-def _prefill_chain(w, n: int, path: str):
-    """The kernels one prefill call launches: (description, launches per call)."""
+def _prefill_chain(w, n: int, path: str, sms: int = 148):
+    """The kernels one prefill call launches: (description, launches per call).  The
+    tcgen05 kernel merges its history ranges in the last CTA of each (value group,
+    sequence) when the ranges' (max, sum) of the group's rows fit its P buffers (at least
+    512 M bytes for M query rows per product)."""
     if _prefill_tc(w, n, path):
-        return "append + absorb + tcgen05 prefill partial + combine", 4
-    return "view + append + absorb + prefill partial + combine", 5
+        rows = n * (w.H // w.G)
+        m = 64 if rows <= 64 else 128
+        splits = max(1, sms // (w.G * w.B))
+        if (2 * rows * splits + 2 * rows) * 4 <= 512 * m:
+            return "append + absorb + tcgen05 prefill with the ranges' merge in its last CTAs", 3
+        return "append + absorb + tcgen05 prefill partial + merge", 4
+    return "view + append + absorb + prefill partial + merge", 5
 
 
 def _prefill_design(w, n: int, path: str) -> str:
@@ -599,7 +607,7 @@ def _prefill_design(w, n: int, path: str) -> str:
                 "holds the group's chunk rows, streams 128-token tiles of its rows once "
                 "(TMA), S = Q V^T and O += P V accumulate in tensor memory (P's bf16 high and "
                 "low parts stacked as one 128-row product), online softmax in 16 warps; "
-                "ranges merged by log-sum-exp")
+                "ranges merged by log-sum-exp in the last CTA of each (group, sequence)")
     return ("mma.sync prefill kernel: each 16-token slab of a sequence's rows loaded once "
             "per CTA and scored against all the chunk's (query, head) rows, split over the "
             "history and merged by log-sum-exp")
@@ -750,7 +758,7 @@ def run_prefill(args, dist: Dist):
                          f"of one {w.name} layer, fp64 C oracle with OpenMP over (b, h), "
                          f"{cs:.1f} s"}
 
-    chain, per_call = _prefill_chain(w, n, path)
+    chain, per_call = _prefill_chain(w, n, path, gva.gva_num_sms())
     line = {
         "metric": f"GVA causal chunked prefill, new tokens/s ({w.name} layer, n={n} per "
                   f"sequence)",

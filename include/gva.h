@@ -243,7 +243,9 @@ size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *r
  * decode batch of B*n entries reading sequence b's rows (a paged view of the cache).
  * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged returns
  * GVA_ERR_UNSUPPORTED.  B*n <= 4096 (else GVA_ERR_ARG).  Workspace: device, 256-byte
- * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), scratch only.  A chunk that does not fit the capacity or the RoPE table
+ * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), scratch only, one call
+ * in flight per workspace (the tcgen05 kernel's merge counters live in it and are reset
+ * by the call itself).  A chunk that does not fit the capacity or the RoPE table
  * sets GVA_DEV_BAD_POSITION / GVA_DEV_BAD_LENGTH for the queries concerned. */
 int gva_prefill_attention(void *stream, const gva_dims *dims, int n, const void *q_nope,
                           const void *q_rope, const float *M, const int *L0,

@@ -325,10 +325,12 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
 int append_launch(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
                   const int *pos, int *seq_len_out, const gva_rows &rows, void *V, void *Kr,
                   const float *rope_tab, int rope_max_pos, const int *L0 = nullptr,
-                  int chunk_n = 0) {
+                  int chunk_n = 0, int *zero = nullptr, int nzero = 0) {
     AppendParams p;
     p.L0 = L0;
     p.chunk_n = chunk_n;
+    p.zero = zero;
+    p.nzero = nzero;
     p.B = d->B;
     p.G = d->G;
     p.d_h = d->d_h;
@@ -351,9 +353,9 @@ int append_launch(void *stream, const gva_dims *d, const float *v_new, const flo
 // Chunked prefill over n queries per sequence: the view's tables, the decode workspace
 // of the B*n-entry batch (its absorbed-query regions also feed the tensor-core prefill
 // kernel), then that kernel's split partials.
-// Workspace: [view block table][positions][lengths][decode][prefill partials o][m, l].
+// Workspace: [view block table][positions][lengths][merge tickets][decode][prefill partials o][m, l].
 struct PrefillPlan {
-    size_t bt, pos, len, dec, po, pml, total;
+    size_t bt, pos, len, tk, dec, po, pml, total;
     int max_pages;
     gva_dims dv;        // the decode batch: B*n entries
     WsPlan dws;         // its workspace plan (offsets relative to dec)
@@ -373,6 +375,7 @@ bool plan_prefill(const gva_dims *d, int n, const gva_rows &R, int sms, PrefillP
     p->bt = o;  o = align_up(o + sizeof(int) * (size_t)p->dv.B * p->max_pages, 256);
     p->pos = o; o = align_up(o + sizeof(int) * (size_t)p->dv.B, 256);
     p->len = o; o = align_up(o + sizeof(int) * (size_t)p->dv.B, 256);
+    p->tk = o;  o = align_up(o + sizeof(int) * (size_t)d->B * d->G, 256);   // merge tickets
     p->dws = plan_ws(&p->dv, sms);
     p->dec = o; o += p->dws.total;
     p->mq = prefill_mma_plan(d, n, sms, &p->mp);
@@ -844,8 +847,10 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     const bool tc_path = o->path == GVA_PATH_AUTO && pp.mq && pp.tcm;
     int st;
     if (tc_path) {
+        // it also zeroes the prefill kernel's merge tickets
         st = append_launch(stream, &pp.dv, v_new, k_new, nullptr, nullptr, R, cache->V,
-                           cache->K_rope, rope_tab, rope_max_pos, L0, n);
+                           cache->K_rope, rope_tab, rope_max_pos, L0, n,
+                           reinterpret_cast<int *>(w + pp.tk), d->B * d->G);
     } else {
         st = cuda_status(launch(prefill_view_kernel, dim3(d->B, (n + PV_ROWS - 1) / PV_ROWS),
                                 dim3(128), 0, stream, vp));
@@ -891,6 +896,7 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
             memset(&tp, 0, sizeof(tp));
             tp.p = mp;
             tp.p.splits = pp.tc_splits;
+            tp.tickets = reinterpret_cast<int *>(w + pp.tk);   // zeroed by the append
             tp.ch = R.layout == GVA_LAYOUT_PAGED ? gcd_int(R.page_size, 64) : 64;
             CUtensorMap tv, tk;
             if (!prefill_tc_maps(&tv, &tk, cache->V, cache->K_rope, R.num_rows, d->G * d->d_h,

@@ -45,6 +45,8 @@ struct PrefillTcParams {
     int ch;               // cache rows per TMA box
     int nstages;
     int smem_bytes;
+    int *tickets;         // [B][G], zero at launch: the last CTA of each (value group,
+                          //   sequence) merges its ranges; null: a merge kernel follows
 };
 
 // Shared-memory matrix descriptor: layout 2 = 128-byte swizzle (rows of 128 B), 4 = 64-byte,
@@ -742,6 +744,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
                                    (lsh[(q * 4 + 2) * 32 + lane] + lsh[(q * 4 + 3) * 32 + lane]));
             }
     }
+    // every thread's partial writes are visible device-wide before the CTA's ticket
+    if (tp.tickets != nullptr) __threadfence();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -752,6 +756,59 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCOLS)
                      : "memory");
+    }
+    if (tp.tickets == nullptr) return;
+
+    // ---- the ranges' log-sum-exp merge, by the last CTA of this (value group, sequence) ----
+    volatile int *last = reinterpret_cast<volatile int *>(tail + 8);
+    if (tid == 0) *last = atomicAdd(tp.tickets + b * p.G + g, 1) == p.splits - 1;
+    __syncthreads();
+    if (!*last) return;
+    __threadfence();
+    // The ranges' (max, sum) of every row of the group (row q = i r + hl: query i, head
+    // g r + hl) are staged in the P buffers, which no product reads any more; each row's
+    // maximum and weights follow, then one thread per 4 output columns of a row sums the
+    // ranges' parts with independent loads.
+    const int S = p.splits;
+    const long long at_b = (long long)b * S * p.rows_pad + (long long)g * p.wpg * 16;
+    float *mls = reinterpret_cast<float *>(p8);   // [nrows][S] (max, sum), then weights
+    float *dens = mls + 2 * nrows * S, *mxs = dens + nrows;
+    for (int e = tid; e < nrows * S; e += PT_THREADS) {
+        const int q = e / S, r = e - q * S;
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (at_b + q + (long long)r * p.rows_pad) * 2));
+        mls[2 * e] = ml.x;
+        mls[2 * e + 1] = ml.y;
+    }
+    __syncthreads();
+    for (int q = tid; q < nrows; q += PT_THREADS) {
+        float Mx = -INFINITY;
+        for (int r = 0; r < S; ++r) Mx = fmaxf(Mx, mls[2 * (q * S + r)]);
+        float den = 0.f;
+        for (int r = 0; r < S; ++r) {
+            const float m = mls[2 * (q * S + r)];
+            const float wgt = (Mx == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - Mx);
+            den += wgt * mls[2 * (q * S + r) + 1];
+            mls[2 * (q * S + r)] = wgt;
+        }
+        dens[q] = den;
+        mxs[q] = Mx;
+    }
+    __syncthreads();
+    for (int e = tid; e < nrows * (DH / 4); e += PT_THREADS) {
+        const int q = e / (DH / 4), c = e - q * (DH / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < S; ++r) {
+            // a range whose rows saw nothing wrote zeros: weight 0 adds 0
+            const float wgt = mls[2 * (q * S + r)];
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (at_b + q + (long long)r * p.rows_pad) * DH) + c);
+            acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
+        }
+        const float den = dens[q];
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const int i = q / p.r, h = g * p.r + (q - i * p.r);
+        const long long row = ((long long)b * p.n + i) * p.H + h;
+        reinterpret_cast<float4 *>(p.out + row * DH)[c] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (c == 0 && p.lse) p.lse[row] = den > 0.f ? (mxs[q] + log2f(den)) * LN2 : -INFINITY;
     }
 }
 
@@ -813,10 +870,16 @@ inline cudaError_t prefill_tc_launch_t(void *stream, PrefillTcParams &tp, const 
     tp.nstages = prefill_tc_stages<DH, DR, M>();
     if (tp.nstages < 2) return cudaErrorInvalidValue;
     tp.smem_bytes = prefill_tc_smem<DH, DR, M>(tp.nstages);
+    // the in-kernel merge stages every range's (max, sum) of the group's rows in the P
+    // buffers: beyond their size the merge kernel runs instead
+    using SM = PtSmem<DH, DR, M>;
+    const long long nrows = (long long)tp.p.n * tp.p.r;
+    if (tp.tickets && (2 * nrows * tp.p.splits + 2 * nrows) * 4 > (long long)SM::PB * 2 * SM::PPART)
+        tp.tickets = nullptr;
     const dim3 grid(tp.p.splits, tp.p.G, tp.p.B);
     cudaError_t e = launch(prefill_tc_kernel<DH, DR, M>, grid, dim3(PT_THREADS), (size_t)tp.smem_bytes,
                            stream, tv, tk, tp);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || tp.tickets != nullptr) return e;
     const long long rows = (long long)tp.p.B * tp.p.n * tp.p.H;
     const dim3 cg((unsigned)((rows + PF_COMBINE_WARPS - 1) / PF_COMBINE_WARPS));
     return launch(prefill_combine_kernel<DH>, cg, dim3(PF_COMBINE_WARPS * 32), 0, stream, tp.p);

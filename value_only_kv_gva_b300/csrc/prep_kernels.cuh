@@ -17,6 +17,8 @@ struct AppendParams {
     int *seq_len_out;       // [B] or null; may alias pos
     const int *L0;          // chunk mode (chunk_n > 0): entry v is token v % chunk_n of a
     int chunk_n;            //   chunk appended to sequence v / chunk_n after its L0 tokens
+    int *zero;              // nzero words set to 0 (the counters of the kernel that follows
+    int nzero;              //   in the same call), or null
     RowsDev R;
     void *V;                // rows [G][d_h]
     void *Kr;               // rows [d_r]
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     pdl_launch_dependents();
     const int b = blockIdx.x;                                // entry of the inputs
     const int sb = p.chunk_n > 0 ? b / p.chunk_n : b;        // sequence of its rows
+    for (int e = b * 128 + (int)threadIdx.x; e < p.nzero; e += gridDim.x * 128) p.zero[e] = 0;
     const int W = p.G * p.d_h;
     // Loads that do not depend on the position are issued with it: the new value (up
     // to 8 elements per thread), the unrotated key pair, the position.  The table entry
