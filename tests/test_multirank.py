@@ -85,3 +85,17 @@ def test_prefill_work_counts_by_brute_force():
     assert nbytes == sum(l0 + n for l0 in L0) * (w.G * w.d_h + w.d_r) * 2
     pairs = sum(1 for l0 in L0 for i in range(n) for j in range(l0 + n) if j <= l0 + i)
     assert flops == 2 * w.H * (2 * w.d_h + w.d_r) * pairs
+
+
+def test_prefill_launch_counts():
+    """Launches per prefill call the bench claims: three on the tcgen05 path when the
+    kernel merges its ranges itself (the 350M chunk), four when the ranges' (max, sum)
+    exceed its P buffers (a 148-range split of one group), five on the view paths."""
+    import bench
+    from gva_inputs import workload
+    w = workload("350m")
+    assert bench._prefill_chain(w, 16, "auto", 148)[1] == 3
+    assert bench._prefill_chain(w, 16, "mma", 148)[1] == 5
+    assert bench._prefill_chain(workload("350m", B=1, H=4, G=1), 16, "auto", 148)[1] == 4
+    assert bench._prefill_chain(workload("long"), 16, "auto", 148)[1] == 3    # 64 rows, d_h 128
+    assert bench._prefill_chain(workload("350m", H=64), 16, "auto", 148)[1] == 5   # 256 rows
