@@ -252,3 +252,22 @@ def test_prefill_full_size_350m():
     out, lse = r.got()
     assert_close(out, ref, "bf16", "350m full size")
     assert_close(lse, ref_lse, "bf16", "350m full size lse")
+
+
+@pytest.mark.parametrize("B,H,G,n", [(1, 4, 1, 16), (1, 8, 2, 8), (2, 8, 1, 4)])
+def test_prefill_range_merge_paths(B, H, G, n):
+    """The tcgen05 prefill splits each (value group, sequence) over 148 / (B G) history
+    ranges, most of them empty at this length.  Their log-sum-exp merge runs in the
+    kernel's last CTA per (group, sequence) when the ranges' (max, sum) of the group's rows
+    fit its P buffers (32 rows over 74 ranges), else in the merge kernel (64 rows over 148
+    ranges)."""
+    w = workload("350m", B=B, T=3008, H=H, G=G)
+    c = make_case(w, lengths=[3008, 1777][:B])
+    r = Run(c, n)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, "bf16", f"B={B} H={H} G={G} n={n} out")
+    assert_close(lse, ref_lse, "bf16", f"B={B} H={H} G={G} n={n} lse")
