@@ -284,6 +284,19 @@ def measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path, 
            "decode_gbs": round(achieved, 1), "decode_frac_of_measured_copy": round(achieved / hbm_peak, 4),
            "seconds": max_secs}
     del g_step, g_dec
+    # The absorption alone (the public gva_absorb_query, which also rotates the positional
+    # query), one call per layer in its own graph: what GVA's chain adds to GQA's, before
+    # the overlap that programmatic dependent launch gives it inside the decode op.
+    qt = torch.empty((w.B, w.H, w.d_h), device=S.dev)
+    qr = torch.empty((w.B, w.H, max(1, w.d_r)), device=S.dev)
+
+    def absorb_only(L):
+        gva.gva_absorb_query(S.dims, L["q_nope"], L["q_rope"], L["M"], S.seq, S.tab, w.scale,
+                             qt, qr)
+    g_abs = capture_list(torch, stream, S.layers, absorb_only)
+    asecs, _ = timed_graph(torch, dist, stream, g_abs, args.steps, max(3, args.warmup))
+    out["absorb_only_us_per_layer"] = round(dist.max(asecs, S.dev) / (args.steps * nl) * 1e6, 3)
+    del g_abs
     if not with_gqa:
         return out
     Kq0 = gva_inputs.make_gqa_keys(S.c).to(S.dev)
