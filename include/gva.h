@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define GVA_ABI_VERSION 5
+#define GVA_ABI_VERSION 6
 
 typedef enum {
     GVA_OK = 0,
@@ -367,6 +367,37 @@ int gva_decode_attention_static(void *stream, const gva_dims *dims, const void *
                                 const void *q_rope, const float *M, const int *seq_len,
                                 const gva_cache *cache, const float *rope_tab,
                                 int rope_max_pos, float scale, float *out, float *lse);
+
+/* One layer of a decode step (gva_decode_step): its new token's value and positional key
+ * (v_new device fp32 [B][G][d_h], k_rope_new device fp32 [B][d_r] unrotated; v_new NULL:
+ * no append for this layer), its queries and map as in gva_decode_attention, its cache,
+ * and its outputs out (device fp32 [B][H][d_h]) and lse (device fp32 [B][H] or NULL). */
+typedef struct {
+    const float *v_new;
+    const float *k_rope_new;
+    const void *q_nope;
+    const void *q_rope;
+    const float *M;
+    gva_cache cache;
+    float *out;
+    float *lse;
+} gva_layer_args;
+
+/* One decode step through n_layers layers of the same shape, issued from one host call
+ * (a native executor for the per-step loop of a model's layers).  For l = 0 .. n_layers-1
+ * in order on `stream`: gva_append_cache(v_new, k_rope_new, pos, NULL) when layers[l].v_new
+ * is not NULL, then gva_decode_attention_ex(q_nope, q_rope, M, seq_len, layers[l].cache,
+ * rope_tab, rope_max_pos, scale, out, lse, workspace, ws_bytes, opts).  The layers share
+ * the positions, lengths, table, scale, options and one workspace (>= 
+ * gva_decode_workspace_size(dims)): every kernel of a layer waits for the layer before it,
+ * so the scratch is reused in order.  The result is that of the per-layer calls, bit for
+ * bit.  Returns GVA_OK, GVA_ERR_ARG for n_layers < 0 or a NULL `layers` with
+ * n_layers > 0, or the first error of a layer's call (the layers before it are launched,
+ * the rest are not). */
+int gva_decode_step(void *stream, const gva_dims *dims, int n_layers,
+                    const gva_layer_args *layers, const int *pos, const int *seq_len,
+                    const float *rope_tab, int rope_max_pos, float scale, void *workspace,
+                    size_t ws_bytes, const gva_decode_opts *opts);
 
 /* Read and clear the current device's status word (synchronous: it waits for all
  * work on the device).  *code_out receives a gva_device_check value.  Returns

@@ -49,7 +49,7 @@ def test_every_declared_symbol_is_exported(gva):
 
 
 def test_abi_version_and_status_strings(gva):
-    assert gva.gva_abi_version() == 5
+    assert gva.gva_abi_version() == 6
     for code in (0, -1, -2, -3, -4, -5, 1, 2, 3, 4):
         s = gva.gva_status_string(code)
         assert s and "unknown" not in s
@@ -279,3 +279,17 @@ def test_dims_validation_follows_the_header(gva):
 
     check()
     assert seen[gva.GVA_ERR_UNSUPPORTED] >= 20 and seen[gva.GVA_ERR_ARG] >= 20, seen
+
+
+def test_decode_step_argument_checks(gva):
+    """gva_decode_step refuses a negative layer count or a missing layer array before any
+    CUDA call, and a step of no layers does nothing."""
+    lib = gva._lib
+    d = gva.Dims(2, 16, 4, 64, 64, 16).c()
+
+    def step(n):
+        return lib.gva_decode_step(None, ctypes.byref(d), n, None, None, None, None, 0, 1.0,
+                                   None, 0, None)
+    assert step(-1) == gva.GVA_ERR_ARG
+    assert step(3) == gva.GVA_ERR_ARG
+    assert step(0) == gva.GVA_OK

@@ -462,3 +462,38 @@ def test_largest_batch():
         assert gva().gva_get_device_status() == 0
         assert_close(out, ref, "bf16", f"B=4096 {path}")
         assert_close(lse, ref_lse, "bf16", f"B=4096 {path} lse")
+
+
+@pytest.mark.parametrize("name", ["350m", "paged"])
+def test_decode_step_matches_per_layer_calls(name):
+    """gva_decode_step over three layers (one C call: each layer's append, then its decode,
+    the layers sharing one workspace) equals the per-layer gva_append_cache and
+    gva_decode_attention calls bit for bit, outputs and appended rows, and the oracle."""
+    g = gva()
+    c = make_case(workload(name, **SMALL[name]))
+    pos = (c.seq_len - 1).to(torch.int32).cuda()
+    a = [Dev(c) for _ in range(3)]          # per-layer calls
+    s = [Dev(c) for _ in range(3)]          # one step call
+    w = c.w
+    outs_a, outs_s = [], []
+    for D in a:
+        D.append(pos)
+        outs_a.append(D.decode())
+    layers = []
+    for D in s:
+        out = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+        lse = torch.full((w.B, w.H), float("nan"), device="cuda")
+        layers.append(dict(v_new=D.v_new, k_rope_new=D.k_new, q_nope=D.q_nope, q_rope=D.q_rope,
+                           M=D.M, cache=D.cache, out=out, lse=lse))
+    g.gva_decode_step(s[0].dims, layers, pos, s[0].seq_len, s[0].tab, w.scale, s[0].ws)
+    torch.cuda.synchronize()
+    assert g.gva_get_device_status() == 0
+    for (oa, la), L, Da, Ds in zip(outs_a, layers, a, s):
+        assert np.array_equal(oa, L["out"].cpu().numpy().astype(np.float64))
+        assert np.array_equal(la, L["lse"].cpu().numpy().astype(np.float64))
+        assert torch.equal(Da.V.view(torch.int16), Ds.V.view(torch.int16))
+        assert torch.equal(Da.Kr.view(torch.int16), Ds.Kr.view(torch.int16))
+    V, K = oracle_append(c, pos.cpu(), s[0].tab_h)
+    ref, ref_lse = oracle_decode(c, V, K)
+    assert_close(outs_a[0][0], ref, "bf16", f"{name} step out")
+    assert_close(outs_a[0][1], ref_lse, "bf16", f"{name} step lse")

@@ -63,6 +63,12 @@ class gva_mla_dims(ctypes.Structure):
                 ("cache_dtype", ctypes.c_int), ("q_dtype", ctypes.c_int)]
 
 
+class gva_layer_args(ctypes.Structure):
+    _fields_ = [("v_new", ctypes.c_void_p), ("k_rope_new", ctypes.c_void_p),
+                ("q_nope", ctypes.c_void_p), ("q_rope", ctypes.c_void_p), ("M", ctypes.c_void_p),
+                ("cache", gva_cache), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
 class gva_decode_opts(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("flags", ctypes.c_int),
                 ("q_norm_eps", ctypes.c_float), ("q_norm_gain", ctypes.c_void_p)]
@@ -103,6 +109,8 @@ _lib.gva_rope_keys_workspace_size.restype = _Z
 _lib.gva_rope_keys_workspace_size.argtypes = [_PD]
 _lib.gva_rope_keys_decode_attention.argtypes = [_P, _PD, _P, _P, _P, _PC, _P, _I, _F, _P, _P,
                                                 _P, _Z]
+_lib.gva_decode_step.argtypes = [_P, _PD, _I, ctypes.POINTER(gva_layer_args), _P, _P, _P, _I,
+                                 _F, _P, _Z, _PO]
 _lib.gva_prefill_attention.argtypes = [_P, _PD, _I, _P, _P, _P, _P, _P, _P, _PC, _P, _I, _F,
                                        _P, _P, _P, _Z, _PO]
 
@@ -113,7 +121,7 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_read_probe", "gva_absorb_query_ex", "gva_prefill_workspace_size",
            "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention",
            "gva_rope_keys_workspace_size", "gva_rope_keys_decode_attention",
-           "gva_selftest_bounded_wait"]
+           "gva_selftest_bounded_wait", "gva_decode_step"]
 
 
 class GvaError(RuntimeError):
@@ -467,6 +475,55 @@ def prepare_decode_attention(dims: Dims, q_nope, q_rope, M, seq_len, cache: Cach
     return PreparedCall(_lib.gva_decode_attention_ex, args, "gva_decode_attention",
                         (d, cc, o, q_nope, q_rope, M, seq_len, cache, rope_tab, out, lse, workspace,
                          q_norm))
+
+
+def _addr(t, dtype=None, what="tensor"):
+    """Device address of a contiguous CUDA tensor as an int (None -> NULL), for a field
+    of a C structure."""
+    p = _ptr(t, dtype, what)
+    return None if p is None else p.value
+
+
+def prepare_decode_step(dims: Dims, layers, pos, seq_len, rope_tab, scale: float, workspace,
+                        path: str = "auto", num_ctas: int = 0, stream=None,
+                        q_norm=None) -> PreparedCall:
+    """gva_decode_step with fixed arguments (see PreparedCall): one C call per step runs
+    every layer's append (when the layer has "v_new") and decode.  `layers` is a list of
+    dicts with the keys v_new, k_rope_new (optional), q_nope, q_rope, M, cache (Cache),
+    out and lse (optional), as in gva_append_cache and gva_decode_attention."""
+    d, o = dims.c(), _opts(path, num_ctas, q_norm)
+    arr = (gva_layer_args * len(layers))()
+    for i, L in enumerate(layers):
+        cache = L["cache"]
+        _check_decode(dims, L["q_nope"], L.get("q_rope"), L["M"], seq_len, cache, rope_tab,
+                      L["out"], L.get("lse"))
+        if L.get("v_new") is not None:
+            _check_append(dims, L["v_new"], L.get("k_rope_new"), pos, None, cache, rope_tab)
+        a = arr[i]
+        a.v_new = _addr(L.get("v_new"), torch.float32, "v_new")
+        a.k_rope_new = _addr(L.get("k_rope_new"), torch.float32, "k_rope_new") if dims.d_r else None
+        a.q_nope = _addr(L["q_nope"], None, "q_nope")
+        a.q_rope = _addr(L.get("q_rope"), None, "q_rope") if dims.d_r else None
+        a.M = _addr(L["M"], torch.float32, "M")
+        a.cache = cache.c()
+        a.out = _addr(L["out"], torch.float32, "out")
+        a.lse = _addr(L.get("lse"), torch.float32, "lse")
+    args = (_stream(stream), ctypes.byref(d), len(layers), arr,
+            _ptr(pos, torch.int32, "pos"), _ptr(seq_len, torch.int32, "seq_len"),
+            _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+            int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+            _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+            ctypes.byref(o))
+    return PreparedCall(_lib.gva_decode_step, args, "gva_decode_step",
+                        (d, o, arr, list(layers), pos, seq_len, rope_tab, workspace, q_norm))
+
+
+def gva_decode_step(dims: Dims, layers, pos, seq_len, rope_tab, scale: float, workspace,
+                    path: str = "auto", num_ctas: int = 0, stream=None, q_norm=None) -> None:
+    """gva_decode_step: every layer's append and decode from one C call (see
+    prepare_decode_step for `layers`)."""
+    prepare_decode_step(dims, layers, pos, seq_len, rope_tab, scale, workspace, path,
+                        num_ctas, stream, q_norm)()
 
 
 def gva_gqa_decode_attention(dims: Dims, q, seq_len, cache: KVCache, scale: float, out, lse,

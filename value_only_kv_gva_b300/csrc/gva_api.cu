@@ -781,6 +781,26 @@ int gva_decode_attention(void *stream, const gva_dims *d, const void *q_nope, co
                                    rope_max_pos, scale, out, lse, ws, ws_bytes, nullptr);
 }
 
+int gva_decode_step(void *stream, const gva_dims *d, int n_layers, const gva_layer_args *layers,
+                    const int *pos, const int *seq_len, const float *rope_tab, int rope_max_pos,
+                    float scale, void *ws, size_t ws_bytes, const gva_decode_opts *opts) {
+    if (n_layers < 0 || (n_layers > 0 && !layers)) return GVA_ERR_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        const gva_layer_args &L = layers[l];
+        int st;
+        if (L.v_new) {
+            st = gva_append_cache(stream, d, L.v_new, L.k_rope_new, pos, nullptr, &L.cache,
+                                  rope_tab, rope_max_pos);
+            if (st != GVA_OK) return st;
+        }
+        st = gva_decode_attention_ex(stream, d, L.q_nope, L.q_rope, L.M, seq_len, &L.cache,
+                                     rope_tab, rope_max_pos, scale, L.out, L.lse, ws, ws_bytes,
+                                     opts);
+        if (st != GVA_OK) return st;
+    }
+    return GVA_OK;
+}
+
 size_t gva_prefill_workspace_size(const gva_dims *d, int n, const gva_rows *rows) {
     if (!dims_ok(d, true) || !rows || !rows_ok(rows, d->B) || !prefill_layout_ok(*rows))
         return 0;
