@@ -855,11 +855,11 @@ def capture_list(torch, stream, items, fn):
 
 def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, bytes_layer,
             dist):
-    """Same metric through the public API, eager: every step copies its inputs from pinned
-    host memory (one transfer per input kind for all layers), makes one gva_decode_step
-    call (every layer's append and decode issued by the library's native step loop;
-    arguments marshalled once), and reads every layer's output back (one transfer), all
-    inside the timed region."""
+    """Same metric through the public API: every step copies its inputs from pinned host
+    memory (one transfer per input kind for all layers), launches the step plan
+    (gva_step_plan_create recorded every layer's append and decode once;
+    gva_step_plan_launch replays them with one call), and reads every layer's output back
+    (one transfer), all inside the timed region."""
     nl = len(layers)
     stream = torch.cuda.current_stream()
     # device inputs of all layers in one buffer per kind; host copies pinned
@@ -875,8 +875,8 @@ def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, 
     step_layers = [dict(v_new=d_vn[li], k_rope_new=d_kn[li], q_nope=d_qn[li], q_rope=d_qr[li],
                         M=L["M"], cache=L["cache"], out=d_out[li], lse=d_lse[li])
                    for li, L in enumerate(layers)]
-    calls = [gva.prepare_decode_step(dims, step_layers, pos, seq, tab, w.scale, ws, path=path,
-                                     stream=stream)]
+    plan = gva.create_step_plan(dims, step_layers, pos, seq, tab, w.scale, ws, path=path)
+    calls = [lambda: plan.launch(stream)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = h_out.numel() * h_out.element_size()
     steps = max(3, min(args.steps, args.e2e_steps))
@@ -899,9 +899,10 @@ def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, 
     val = bytes_layer * nl * steps * dist.world / t / 1e9
     return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 4),
-            "how": "one gva_decode_step C-ABI call per step (append + decode of every layer, "
-                   "issued by the library; arguments marshalled once); pinned host->device "
-                   "inputs and device->host outputs of every layer inside the timed region"}
+            "how": "one gva_step_plan_launch C-ABI call per step (the step's append + decode "
+                   "of every layer, recorded once by gva_step_plan_create as a CUDA graph); "
+                   "pinned host->device inputs and device->host outputs of every layer "
+                   "inside the timed region"}
 
 
 def read_probe_gbs(gva, torch, stream, dev, gib: float = 4.0, reps: int = 10):

@@ -399,6 +399,29 @@ int gva_decode_step(void *stream, const gva_dims *dims, int n_layers,
                     const float *rope_tab, int rope_max_pos, float scale, void *workspace,
                     size_t ws_bytes, const gva_decode_opts *opts);
 
+/* A decode step recorded once and replayed: a native executor over CUDA graphs.
+ * gva_step_plan_create records one gva_decode_step with these arguments (on a private
+ * stream of the current device, in stream capture) into an instantiated CUDA graph;
+ * gva_step_plan_launch replays the whole step on `stream` with one launch.  The plan keeps
+ * the addresses, not the contents: the caller refreshes the inputs in place between
+ * launches (new tokens, queries, lengths, positions), keeps every buffer alive and in
+ * place while the plan exists, and orders launches that share buffers.  A replay computes
+ * what gva_decode_step computes on the buffers' current contents, bit for bit.
+ * Creating a plan performs the library's one-time device set-up first and allocates
+ * driver resources (a stream and an instantiated graph), no device buffers.
+ * create: GVA_ERR_ARG for plan_out NULL, n_layers < 1 or layers NULL; any error of the
+ * recorded calls (then *plan_out is NULL); GVA_ERR_CUDA when recording or instantiation
+ * fails.  launch: GVA_ERR_ARG for a NULL plan, GVA_ERR_CUDA when the stream belongs to
+ * another device than the plan's or the launch fails.  destroy: releases the plan (NULL
+ * is accepted); the caller orders it after the plan's last launch has completed. */
+typedef struct gva_step_plan gva_step_plan;
+int gva_step_plan_create(const gva_dims *dims, int n_layers, const gva_layer_args *layers,
+                         const int *pos, const int *seq_len, const float *rope_tab,
+                         int rope_max_pos, float scale, void *workspace, size_t ws_bytes,
+                         const gva_decode_opts *opts, gva_step_plan **plan_out);
+int gva_step_plan_launch(gva_step_plan *plan, void *stream);
+int gva_step_plan_destroy(gva_step_plan *plan);
+
 /* Read and clear the current device's status word (synchronous: it waits for all
  * work on the device).  *code_out receives a gva_device_check value.  Returns
  * GVA_OK when no check tripped, GVA_ERR_DEVICE_CHECK when one did, GVA_ERR_CUDA on

@@ -293,3 +293,20 @@ def test_decode_step_argument_checks(gva):
     assert step(-1) == gva.GVA_ERR_ARG
     assert step(3) == gva.GVA_ERR_ARG
     assert step(0) == gva.GVA_OK
+
+
+def test_step_plan_argument_checks(gva):
+    """gva_step_plan_create refuses a missing output handle, an empty step or a missing
+    layer array before any CUDA call; launch refuses a NULL plan; destroy accepts one."""
+    lib = gva._lib
+    d = gva.Dims(2, 16, 4, 64, 64, 16).c()
+    h = ctypes.c_void_p()
+
+    def create(n, out):
+        return lib.gva_step_plan_create(ctypes.byref(d), n, None, None, None, None, 0, 1.0,
+                                        None, 0, None, out)
+    assert create(1, None) == gva.GVA_ERR_ARG
+    assert create(0, ctypes.byref(h)) == gva.GVA_ERR_ARG and not h.value
+    assert create(2, ctypes.byref(h)) == gva.GVA_ERR_ARG and not h.value
+    assert lib.gva_step_plan_launch(None, None) == gva.GVA_ERR_ARG
+    assert lib.gva_step_plan_destroy(None) == gva.GVA_OK

@@ -497,3 +497,40 @@ def test_decode_step_matches_per_layer_calls(name):
     ref, ref_lse = oracle_decode(c, V, K)
     assert_close(outs_a[0][0], ref, "bf16", f"{name} step out")
     assert_close(outs_a[0][1], ref_lse, "bf16", f"{name} step lse")
+
+
+@pytest.mark.parametrize("name", ["350m", "paged"])
+def test_step_plan_replays_the_step(name):
+    """A step recorded by gva_step_plan_create and launched twice, with new queries written
+    in place between the launches, gives what the per-layer calls give on the same
+    contents, bit for bit: outputs and appended rows of three layers."""
+    g = gva()
+    c = make_case(workload(name, **SMALL[name]))
+    pos = (c.seq_len - 1).to(torch.int32).cuda()
+    a = [Dev(c) for _ in range(3)]          # per-layer calls
+    s = [Dev(c) for _ in range(3)]          # the recorded step
+    w = c.w
+    layers = []
+    for D in s:
+        out = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+        lse = torch.full((w.B, w.H), float("nan"), device="cuda")
+        layers.append(dict(v_new=D.v_new, k_rope_new=D.k_new, q_nope=D.q_nope, q_rope=D.q_rope,
+                           M=D.M, cache=D.cache, out=out, lse=lse))
+    plan = g.create_step_plan(s[0].dims, layers, pos, s[0].seq_len, s[0].tab, w.scale, s[0].ws)
+    for it in range(2):
+        if it == 1:
+            for D in a + s:
+                D.q_nope.mul_(-0.5)             # new contents, same storage
+        plan.launch()
+        refs = []
+        for D in a:
+            D.append(pos)
+            refs.append(D.decode())
+        torch.cuda.synchronize()
+        assert g.gva_get_device_status() == 0
+        for (oa, la), L, Da, Ds in zip(refs, layers, a, s):
+            assert np.array_equal(oa, L["out"].cpu().numpy().astype(np.float64)), f"launch {it}"
+            assert np.array_equal(la, L["lse"].cpu().numpy().astype(np.float64)), f"launch {it}"
+            assert torch.equal(Da.V.view(torch.int16), Ds.V.view(torch.int16))
+            assert torch.equal(Da.Kr.view(torch.int16), Ds.Kr.view(torch.int16))
+    plan.close()

@@ -111,6 +111,10 @@ _lib.gva_rope_keys_decode_attention.argtypes = [_P, _PD, _P, _P, _P, _PC, _P, _I
                                                 _P, _Z]
 _lib.gva_decode_step.argtypes = [_P, _PD, _I, ctypes.POINTER(gva_layer_args), _P, _P, _P, _I,
                                  _F, _P, _Z, _PO]
+_lib.gva_step_plan_create.argtypes = [_PD, _I, ctypes.POINTER(gva_layer_args), _P, _P, _P, _I,
+                                      _F, _P, _Z, _PO, ctypes.POINTER(ctypes.c_void_p)]
+_lib.gva_step_plan_launch.argtypes = [_P, _P]
+_lib.gva_step_plan_destroy.argtypes = [_P]
 _lib.gva_prefill_attention.argtypes = [_P, _PD, _I, _P, _P, _P, _P, _P, _P, _PC, _P, _I, _F,
                                        _P, _P, _P, _Z, _PO]
 
@@ -121,7 +125,8 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_read_probe", "gva_absorb_query_ex", "gva_prefill_workspace_size",
            "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention",
            "gva_rope_keys_workspace_size", "gva_rope_keys_decode_attention",
-           "gva_selftest_bounded_wait", "gva_decode_step"]
+           "gva_selftest_bounded_wait", "gva_decode_step", "gva_step_plan_create",
+           "gva_step_plan_launch", "gva_step_plan_destroy"]
 
 
 class GvaError(RuntimeError):
@@ -491,6 +496,19 @@ def prepare_decode_step(dims: Dims, layers, pos, seq_len, rope_tab, scale: float
     every layer's append (when the layer has "v_new") and decode.  `layers` is a list of
     dicts with the keys v_new, k_rope_new (optional), q_nope, q_rope, M, cache (Cache),
     out and lse (optional), as in gva_append_cache and gva_decode_attention."""
+    d, o, arr = _step_layers(dims, layers, pos, seq_len, rope_tab, path, num_ctas, q_norm)
+    args = (_stream(stream), ctypes.byref(d), len(layers), arr,
+            _ptr(pos, torch.int32, "pos"), _ptr(seq_len, torch.int32, "seq_len"),
+            _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+            int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+            _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+            ctypes.byref(o))
+    return PreparedCall(_lib.gva_decode_step, args, "gva_decode_step",
+                        (d, o, arr, list(layers), pos, seq_len, rope_tab, workspace, q_norm))
+
+
+def _step_layers(dims, layers, pos, seq_len, rope_tab, path, num_ctas, q_norm):
+    """Checked gva_dims, options and the gva_layer_args array of a decode step."""
     d, o = dims.c(), _opts(path, num_ctas, q_norm)
     arr = (gva_layer_args * len(layers))()
     for i, L in enumerate(layers):
@@ -508,14 +526,48 @@ def prepare_decode_step(dims: Dims, layers, pos, seq_len, rope_tab, scale: float
         a.cache = cache.c()
         a.out = _addr(L["out"], torch.float32, "out")
         a.lse = _addr(L.get("lse"), torch.float32, "lse")
-    args = (_stream(stream), ctypes.byref(d), len(layers), arr,
-            _ptr(pos, torch.int32, "pos"), _ptr(seq_len, torch.int32, "seq_len"),
-            _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
-            int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
-            _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
-            ctypes.byref(o))
-    return PreparedCall(_lib.gva_decode_step, args, "gva_decode_step",
-                        (d, o, arr, list(layers), pos, seq_len, rope_tab, workspace, q_norm))
+    return d, o, arr
+
+
+class StepPlan:
+    """A decode step recorded once by gva_step_plan_create and replayed by launch(): the
+    buffers given at creation stay in place (kept alive here); refresh their contents in
+    place between launches."""
+
+    def __init__(self, handle, keep):
+        self._h, self._keep = handle, keep
+
+    def launch(self, stream=None) -> None:
+        if self._h is None:
+            raise GvaError(GVA_ERR_ARG, "gva_step_plan_launch: the plan was closed")
+        _check(_lib.gva_step_plan_launch(self._h, _stream(stream)), "gva_step_plan_launch")
+
+    def close(self) -> None:
+        """Release the plan (after its last launch has completed)."""
+        if self._h is not None:
+            _lib.gva_step_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def create_step_plan(dims: Dims, layers, pos, seq_len, rope_tab, scale: float, workspace,
+                     path: str = "auto", num_ctas: int = 0, q_norm=None) -> StepPlan:
+    """gva_step_plan_create (layers as in prepare_decode_step)."""
+    d, o, arr = _step_layers(dims, layers, pos, seq_len, rope_tab, path, num_ctas, q_norm)
+    h = ctypes.c_void_p()
+    _check(_lib.gva_step_plan_create(
+        ctypes.byref(d), len(layers), arr, _ptr(pos, torch.int32, "pos"),
+        _ptr(seq_len, torch.int32, "seq_len"),
+        _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+        ctypes.byref(o), ctypes.byref(h)), "gva_step_plan_create")
+    return StepPlan(h, (list(layers), pos, seq_len, rope_tab, workspace, q_norm))
 
 
 def gva_decode_step(dims: Dims, layers, pos, seq_len, rope_tab, scale: float, workspace,

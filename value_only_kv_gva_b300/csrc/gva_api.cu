@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "gva.h"
 #include "common.cuh"
@@ -798,6 +799,79 @@ int gva_decode_step(void *stream, const gva_dims *d, int n_layers, const gva_lay
                                      opts);
         if (st != GVA_OK) return st;
     }
+    return GVA_OK;
+}
+
+struct gva_step_plan {
+    int device;
+    cudaStream_t stream;      // private stream the step was recorded on
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+namespace {
+void plan_release(gva_step_plan *p) {
+    if (!p) return;
+    if (p->exec) cudaGraphExecDestroy(p->exec);
+    if (p->graph) cudaGraphDestroy(p->graph);
+    if (p->stream) cudaStreamDestroy(p->stream);
+    delete p;
+}
+}  // namespace
+
+int gva_step_plan_create(const gva_dims *d, int n_layers, const gva_layer_args *layers,
+                         const int *pos, const int *seq_len, const float *rope_tab,
+                         int rope_max_pos, float scale, void *ws, size_t ws_bytes,
+                         const gva_decode_opts *opts, gva_step_plan **plan_out) {
+    if (!plan_out) return GVA_ERR_ARG;
+    *plan_out = nullptr;
+    if (n_layers < 1 || !layers) return GVA_ERR_ARG;
+    // the one-time set-up (kernel attributes, SM count) must not happen inside a capture
+    if (!device_state()) return GVA_ERR_CUDA;
+    gva_step_plan *p = new (std::nothrow) gva_step_plan{};
+    if (!p) return GVA_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(p->stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        plan_release(p);
+        return GVA_ERR_CUDA;
+    }
+    const int st = gva_decode_step(p->stream, d, n_layers, layers, pos, seq_len, rope_tab,
+                                   rope_max_pos, scale, ws, ws_bytes, opts);
+    e = cudaStreamEndCapture(p->stream, &p->graph);
+    if (st != GVA_OK || e != cudaSuccess) {
+        if (e != cudaSuccess) g_last_cuda_error = (int)e;
+        cudaGetLastError();
+        plan_release(p);
+        return st != GVA_OK ? st : GVA_ERR_CUDA;
+    }
+    e = cudaGraphInstantiate(&p->exec, p->graph, 0);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        plan_release(p);
+        return GVA_ERR_CUDA;
+    }
+    *plan_out = p;
+    return GVA_OK;
+}
+
+int gva_step_plan_launch(gva_step_plan *p, void *stream) {
+    if (!p) return GVA_ERR_ARG;
+    int dev = -1;
+    cudaError_t e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &dev);
+    if (e == cudaSuccess && dev != p->device) e = cudaErrorInvalidDevice;
+    if (e == cudaSuccess) e = cudaGraphLaunch(p->exec, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return GVA_ERR_CUDA;
+    }
+    return GVA_OK;
+}
+
+int gva_step_plan_destroy(gva_step_plan *p) {
+    plan_release(p);
     return GVA_OK;
 }
 
