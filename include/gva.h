@@ -420,6 +420,30 @@ int gva_step_plan_create(const gva_dims *dims, int n_layers, const gva_layer_arg
                          int rope_max_pos, float scale, void *workspace, size_t ws_bytes,
                          const gva_decode_opts *opts, gva_step_plan **plan_out);
 int gva_step_plan_launch(gva_step_plan *plan, void *stream);
+
+/* One layer of a recorded prefill: its chunk's queries, map, new values and positional
+ * keys, cache and outputs, as in gva_prefill_attention. */
+typedef struct {
+    const void *q_nope;
+    const void *q_rope;
+    const float *M;
+    const float *v_new;
+    const float *k_rope_new;
+    gva_cache cache;
+    float *out;
+    float *lse;
+} gva_prefill_layer_args;
+
+/* A chunked prefill through n_layers layers recorded as a plan: one gva_prefill_attention
+ * per layer, in order, sharing L0, the table, scale, options and one workspace
+ * (>= gva_prefill_workspace_size(dims, n, &layers[0].cache.rows); every layer's rows
+ * must have that layout and size).  Launched and destroyed like a step plan, with the
+ * same rules on buffers, and the same errors (GVA_ERR_ARG also for n < 1). */
+int gva_prefill_plan_create(const gva_dims *dims, int n, int n_layers,
+                            const gva_prefill_layer_args *layers, const int *L0,
+                            const float *rope_tab, int rope_max_pos, float scale,
+                            void *workspace, size_t ws_bytes, const gva_decode_opts *opts,
+                            gva_step_plan **plan_out);
 int gva_step_plan_destroy(gva_step_plan *plan);
 
 /* Read and clear the current device's status word (synchronous: it waits for all

@@ -310,3 +310,11 @@ def test_step_plan_argument_checks(gva):
     assert create(2, ctypes.byref(h)) == gva.GVA_ERR_ARG and not h.value
     assert lib.gva_step_plan_launch(None, None) == gva.GVA_ERR_ARG
     assert lib.gva_step_plan_destroy(None) == gva.GVA_OK
+
+    def create_prefill(n, layers_n, out):
+        return lib.gva_prefill_plan_create(ctypes.byref(d), n, layers_n, None, None, None, 0,
+                                           1.0, None, 0, None, out)
+    assert create_prefill(16, 1, None) == gva.GVA_ERR_ARG
+    assert create_prefill(0, 1, ctypes.byref(h)) == gva.GVA_ERR_ARG and not h.value
+    assert create_prefill(16, 0, ctypes.byref(h)) == gva.GVA_ERR_ARG and not h.value
+    assert create_prefill(16, 1, ctypes.byref(h)) == gva.GVA_ERR_ARG and not h.value

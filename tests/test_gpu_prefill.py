@@ -271,3 +271,47 @@ def test_prefill_range_merge_paths(B, H, G, n):
     out, lse = r.got()
     assert_close(out, ref, "bf16", f"B={B} H={H} G={G} n={n} out")
     assert_close(lse, ref_lse, "bf16", f"B={B} H={H} G={G} n={n} lse")
+
+
+def test_prefill_plan_replays_the_chunk():
+    """A chunk through two layers recorded by gva_prefill_plan_create and launched twice,
+    with new queries written in place between the launches, gives what the per-layer
+    gva_prefill_attention calls give on the same contents, bit for bit."""
+    g = gva()
+    c = make_case(workload("350m", **SMALL["350m"][0]))
+    n = 9
+    w = c.w
+    d = torch.device("cuda")
+    ch = make_prefill_chunk(c, n)
+    rows = g.Rows(w.layout, c.num_rows, T_cap=c.T_cap)
+    dims = dims_of(c)
+    tab = rope_tab(c).to(d)
+    L0 = ch.L0.to(d)
+
+    def layer():
+        return dict(q_nope=ch.q_nope.to(d), q_rope=ch.q_rope.to(d), M=c.M.to(d),
+                    v_new=ch.v_new.to(d), k_rope_new=ch.k_new.to(d),
+                    cache=g.Cache(rows, c.V.to(d), c.Kr.to(d)),
+                    out=torch.full((w.B, n, w.H, w.d_h), float("nan"), device=d),
+                    lse=torch.full((w.B, n, w.H), float("nan"), device=d))
+    ref_layers, plan_layers = [layer(), layer()], [layer(), layer()]
+    ws_ref = g.prefill_workspace(dims, n, rows, d)
+    ws = g.prefill_workspace(dims, n, rows, d)
+    plan = g.create_prefill_plan(dims, n, plan_layers, L0, tab, w.scale, ws)
+    for it in range(2):
+        if it == 1:
+            for L in ref_layers + plan_layers:
+                L["q_nope"].mul_(-0.5)
+        plan.launch()
+        for L in ref_layers:
+            g.gva_prefill_attention(dims, L["q_nope"], L["q_rope"], L["M"], L0, L["v_new"],
+                                    L["k_rope_new"], L["cache"], tab, w.scale, L["out"],
+                                    L["lse"], ws_ref)
+        torch.cuda.synchronize()
+        assert g.gva_get_device_status() == 0
+        for R, P in zip(ref_layers, plan_layers):
+            assert torch.equal(R["out"], P["out"]), f"launch {it} out"
+            assert torch.equal(R["lse"], P["lse"]), f"launch {it} lse"
+            assert torch.equal(R["cache"].V.view(torch.int16), P["cache"].V.view(torch.int16))
+            assert torch.equal(R["cache"].K_rope.view(torch.int16), P["cache"].K_rope.view(torch.int16))
+    plan.close()

@@ -69,6 +69,12 @@ class gva_layer_args(ctypes.Structure):
                 ("cache", gva_cache), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
 
 
+class gva_prefill_layer_args(ctypes.Structure):
+    _fields_ = [("q_nope", ctypes.c_void_p), ("q_rope", ctypes.c_void_p), ("M", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p), ("k_rope_new", ctypes.c_void_p),
+                ("cache", gva_cache), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
 class gva_decode_opts(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("flags", ctypes.c_int),
                 ("q_norm_eps", ctypes.c_float), ("q_norm_gain", ctypes.c_void_p)]
@@ -114,6 +120,8 @@ _lib.gva_decode_step.argtypes = [_P, _PD, _I, ctypes.POINTER(gva_layer_args), _P
 _lib.gva_step_plan_create.argtypes = [_PD, _I, ctypes.POINTER(gva_layer_args), _P, _P, _P, _I,
                                       _F, _P, _Z, _PO, ctypes.POINTER(ctypes.c_void_p)]
 _lib.gva_step_plan_launch.argtypes = [_P, _P]
+_lib.gva_prefill_plan_create.argtypes = [_PD, _I, _I, ctypes.POINTER(gva_prefill_layer_args), _P,
+                                         _P, _I, _F, _P, _Z, _PO, ctypes.POINTER(ctypes.c_void_p)]
 _lib.gva_step_plan_destroy.argtypes = [_P]
 _lib.gva_prefill_attention.argtypes = [_P, _PD, _I, _P, _P, _P, _P, _P, _P, _PC, _P, _I, _F,
                                        _P, _P, _P, _Z, _PO]
@@ -126,7 +134,7 @@ EXPORTS = ["gva_status_string", "gva_abi_version", "gva_num_sms", "gva_rope_tabl
            "gva_prefill_attention", "gva_mla_workspace_size", "gva_mla_decode_attention",
            "gva_rope_keys_workspace_size", "gva_rope_keys_decode_attention",
            "gva_selftest_bounded_wait", "gva_decode_step", "gva_step_plan_create",
-           "gva_step_plan_launch", "gva_step_plan_destroy"]
+           "gva_step_plan_launch", "gva_step_plan_destroy", "gva_prefill_plan_create"]
 
 
 class GvaError(RuntimeError):
@@ -553,6 +561,39 @@ class StepPlan:
             self.close()
         except Exception:
             pass
+
+
+def create_prefill_plan(dims: Dims, n: int, layers, L0, rope_tab, scale: float, workspace,
+                        path: str = "auto", num_ctas: int = 0, q_norm=None) -> StepPlan:
+    """gva_prefill_plan_create: a chunk of n tokens per sequence through every layer,
+    recorded once.  `layers` is a list of dicts with the keys q_nope, q_rope, M, v_new,
+    k_rope_new, cache (Cache), out and lse (optional), as in gva_prefill_attention."""
+    d, o = dims.c(), _opts(path, num_ctas, q_norm)
+    arr = (gva_prefill_layer_args * len(layers))()
+    for i, L in enumerate(layers):
+        cache = L["cache"]
+        _check_decode(dims, L["q_nope"], L.get("q_rope"), L["M"], L0, cache, rope_tab,
+                      L["out"], L.get("lse"), per=n)
+        _need(L["v_new"], dims.B * n * dims.G * dims.d_h, "v_new")
+        if dims.d_r:
+            _need(L.get("k_rope_new"), dims.B * n * dims.d_r, "k_rope_new")
+        a = arr[i]
+        a.q_nope = _addr(L["q_nope"], None, "q_nope")
+        a.q_rope = _addr(L.get("q_rope"), None, "q_rope") if dims.d_r else None
+        a.M = _addr(L["M"], torch.float32, "M")
+        a.v_new = _addr(L["v_new"], torch.float32, "v_new")
+        a.k_rope_new = _addr(L.get("k_rope_new"), torch.float32, "k_rope_new") if dims.d_r else None
+        a.cache = cache.c()
+        a.out = _addr(L["out"], torch.float32, "out")
+        a.lse = _addr(L.get("lse"), torch.float32, "lse")
+    h = ctypes.c_void_p()
+    _check(_lib.gva_prefill_plan_create(
+        ctypes.byref(d), int(n), len(layers), arr, _ptr(L0, torch.int32, "L0"),
+        _ptr(rope_tab, torch.float32, "rope_tab") if dims.d_r else None,
+        int(rope_tab.shape[0]) if rope_tab is not None else 0, float(scale),
+        _ptr(workspace, None, "workspace"), int(workspace.numel() * workspace.element_size()),
+        ctypes.byref(o), ctypes.byref(h)), "gva_prefill_plan_create")
+    return StepPlan(h, (list(layers), L0, rope_tab, workspace, q_norm))
 
 
 def create_step_plan(dims: Dims, layers, pos, seq_len, rope_tab, scale: float, workspace,

@@ -819,13 +819,10 @@ void plan_release(gva_step_plan *p) {
 }
 }  // namespace
 
-int gva_step_plan_create(const gva_dims *d, int n_layers, const gva_layer_args *layers,
-                         const int *pos, const int *seq_len, const float *rope_tab,
-                         int rope_max_pos, float scale, void *ws, size_t ws_bytes,
-                         const gva_decode_opts *opts, gva_step_plan **plan_out) {
-    if (!plan_out) return GVA_ERR_ARG;
-    *plan_out = nullptr;
-    if (n_layers < 1 || !layers) return GVA_ERR_ARG;
+extern "C++" {
+// Records the calls `issue` makes on a private stream into an instantiated graph.
+template <typename Issue>
+int plan_record(Issue &&issue, gva_step_plan **plan_out) {
     // the one-time set-up (kernel attributes, SM count) must not happen inside a capture
     if (!device_state()) return GVA_ERR_CUDA;
     gva_step_plan *p = new (std::nothrow) gva_step_plan{};
@@ -838,8 +835,7 @@ int gva_step_plan_create(const gva_dims *d, int n_layers, const gva_layer_args *
         plan_release(p);
         return GVA_ERR_CUDA;
     }
-    const int st = gva_decode_step(p->stream, d, n_layers, layers, pos, seq_len, rope_tab,
-                                   rope_max_pos, scale, ws, ws_bytes, opts);
+    const int st = issue(p->stream);
     e = cudaStreamEndCapture(p->stream, &p->graph);
     if (st != GVA_OK || e != cudaSuccess) {
         if (e != cudaSuccess) g_last_cuda_error = (int)e;
@@ -855,6 +851,45 @@ int gva_step_plan_create(const gva_dims *d, int n_layers, const gva_layer_args *
     }
     *plan_out = p;
     return GVA_OK;
+}
+}  // extern "C++"
+
+int gva_step_plan_create(const gva_dims *d, int n_layers, const gva_layer_args *layers,
+                         const int *pos, const int *seq_len, const float *rope_tab,
+                         int rope_max_pos, float scale, void *ws, size_t ws_bytes,
+                         const gva_decode_opts *opts, gva_step_plan **plan_out) {
+    if (!plan_out) return GVA_ERR_ARG;
+    *plan_out = nullptr;
+    if (n_layers < 1 || !layers) return GVA_ERR_ARG;
+    return plan_record(
+        [&](cudaStream_t s) {
+            return gva_decode_step(s, d, n_layers, layers, pos, seq_len, rope_tab, rope_max_pos,
+                                   scale, ws, ws_bytes, opts);
+        },
+        plan_out);
+}
+
+int gva_prefill_plan_create(const gva_dims *d, int n, int n_layers,
+                            const gva_prefill_layer_args *layers, const int *L0,
+                            const float *rope_tab, int rope_max_pos, float scale, void *ws,
+                            size_t ws_bytes, const gva_decode_opts *opts,
+                            gva_step_plan **plan_out) {
+    if (!plan_out) return GVA_ERR_ARG;
+    *plan_out = nullptr;
+    if (n < 1 || n_layers < 1 || !layers) return GVA_ERR_ARG;
+    return plan_record(
+        [&](cudaStream_t s) {
+            for (int l = 0; l < n_layers; ++l) {
+                const gva_prefill_layer_args &L = layers[l];
+                const int st = gva_prefill_attention(s, d, n, L.q_nope, L.q_rope, L.M, L0,
+                                                     L.v_new, L.k_rope_new, &L.cache, rope_tab,
+                                                     rope_max_pos, scale, L.out, L.lse, ws,
+                                                     ws_bytes, opts);
+                if (st != GVA_OK) return st;
+            }
+            return (int)GVA_OK;
+        },
+        plan_out);
 }
 
 int gva_step_plan_launch(gva_step_plan *p, void *stream) {
