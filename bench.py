@@ -641,9 +641,6 @@ def run_prefill(args, dist: Dist):
     torch.cuda.set_device(dev)
     dist.init("nccl")
     w = gva_inputs.workload(args.workload)
-    if w.layout == "ragged":
-        raise SystemExit("--prefill takes contiguous or paged caches (gva_prefill_attention "
-                         "refuses ragged layouts)")
     c = gva_inputs.make_case(w)
     n = args.prefill
     ch = gva_inputs.make_prefill_chunk(c, n)
@@ -763,6 +760,8 @@ def run_prefill(args, dist: Dist):
             b = done % w.B
             if w.layout == "contiguous":
                 Rb = oracle.Rows("ragged", offsets=np.array([b * c.T_cap, (b + 1) * c.T_cap]))
+            elif w.layout == "ragged":
+                Rb = oracle.Rows("ragged", offsets=c.offsets.numpy()[[b, b + 1]])
             else:
                 Rb = oracle.Rows("paged", block_table=c.block_table.numpy()[[b]],
                                  page_size=w.page_size)

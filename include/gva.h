@@ -220,7 +220,8 @@ int gva_decode_attention_ex(void *stream, const gva_dims *dims, const void *q_no
 
 /* Bytes of device workspace gva_prefill_attention needs for a chunk of n queries per
  * sequence over `rows` on the current device.  0 on invalid arguments or a layout the
- * prefill does not take. */
+ * prefill does not take (a ragged cache when the tcgen05 prefill kernel does not take
+ * the shape). */
 size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *rows);
 
 /* Causal chunked prefill ([K] §1: every new token attends to the cached history and to
@@ -241,8 +242,9 @@ size_t gva_prefill_workspace_size(const gva_dims *dims, int n, const gva_rows *r
  * d_h = 64), else an mma.sync kernel; every
  * other case, and GVA_PATH_SIMT / _MMA, runs each query as one entry of a
  * decode batch of B*n entries reading sequence b's rows (a paged view of the cache).
- * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged returns
- * GVA_ERR_UNSUPPORTED.  B*n <= 4096 (else GVA_ERR_ARG).  Workspace: device, 256-byte
+ * Layouts: paged, and contiguous with T_cap a positive multiple of 16; ragged only on
+ * GVA_PATH_AUTO when the tcgen05 kernel takes the shape (it reads the caller's rows; the
+ * other paths need page-aligned rows), else GVA_ERR_UNSUPPORTED.  B*n <= 4096 (else GVA_ERR_ARG).  Workspace: device, 256-byte
  * aligned, >= gva_prefill_workspace_size(dims, n, &cache->rows), scratch only, one call
  * in flight per workspace (the tcgen05 kernel's merge counters live in it and are reset
  * by the call itself).  A chunk that does not fit the capacity or the RoPE table

@@ -193,12 +193,25 @@ def test_prefill_past_capacity_is_reported():
     assert gva().gva_get_device_status() == 0
 
 
-def test_prefill_refuses_ragged_layout():
-    c = make_case(workload("ragged", B=3, len_range=(20, 60)))
+@pytest.mark.parametrize("B,lens,n", [(3, (20, 60), 4), (5, (30, 900), 16), (4, (129, 700), 20)])
+def test_prefill_ragged_layout(B, lens, n):
+    """Ragged rows (sequences packed at arbitrary offsets): the tcgen05 prefill reads the
+    caller's rows (64 query rows per group at n = 16, 128 at n = 20), appended rows
+    bit-exact and outputs against the oracle; the view paths refuse the layout."""
+    c = make_case(workload("ragged", B=B, len_range=lens))
+    r = Run(c, n)
+    assert r.status == 0
+    Vh, Kh = r.oracle_cache()
+    _check_cache(r, Vh, Kh)
+    ref, ref_lse = r.oracle_out(Vh, Kh)
+    out, lse = r.got()
+    assert_close(out, ref, "bf16", f"ragged B={B} n={n} out")
+    assert_close(lse, ref_lse, "bf16", f"ragged B={B} n={n} lse")
     g = gva()
-    with pytest.raises(g.GvaError) as e:
-        Run(c, 4)
-    assert e.value.status in (g.GVA_ERR_ARG, g.GVA_ERR_UNSUPPORTED)
+    for path in ("simt", "mma"):
+        with pytest.raises(g.GvaError) as e:
+            Run(c, n, path)
+        assert e.value.status == g.GVA_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("H,G,d_h,d_n,d_r", [

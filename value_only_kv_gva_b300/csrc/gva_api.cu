@@ -910,13 +910,21 @@ int gva_step_plan_destroy(gva_step_plan *p) {
     return GVA_OK;
 }
 
+// A ragged cache has no view (its rows are not page-aligned): only the tcgen05 prefill,
+// which reads the caller's rows, takes it.
+bool prefill_takes_ragged(const gva_dims *d, const PrefillPlan &pp) {
+    return d->cache_dtype == GVA_BF16 && pp.mq && pp.tcm > 0;
+}
+
 size_t gva_prefill_workspace_size(const gva_dims *d, int n, const gva_rows *rows) {
-    if (!dims_ok(d, true) || !rows || !rows_ok(rows, d->B) || !prefill_layout_ok(*rows))
-        return 0;
+    if (!dims_ok(d, true) || !rows || !rows_ok(rows, d->B)) return 0;
+    const bool ragged = rows->layout == GVA_LAYOUT_RAGGED;
+    if (!ragged && !prefill_layout_ok(*rows)) return 0;
     const int sms = num_sms_current();
     if (sms <= 0) return 0;
     PrefillPlan pp;
-    return plan_prefill(d, n, *rows, sms, &pp) ? pp.total : 0;
+    if (!plan_prefill(d, n, *rows, sms, &pp)) return 0;
+    return ragged && !prefill_takes_ragged(d, pp) ? 0 : pp.total;
 }
 
 int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_nope,
@@ -938,12 +946,15 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
                        !aligned16(rope_tab)))
         return GVA_ERR_ARG;
     const gva_rows &R = cache->rows;
-    if (!prefill_layout_ok(R)) return GVA_ERR_UNSUPPORTED;
+    const bool ragged = R.layout == GVA_LAYOUT_RAGGED;
+    if (!ragged && !prefill_layout_ok(R)) return GVA_ERR_UNSUPPORTED;
     if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
     const int sms = num_sms_current();
     if (sms <= 0) return GVA_ERR_CUDA;
     PrefillPlan pp;
     if (!plan_prefill(d, n, R, sms, &pp)) return GVA_ERR_ARG;
+    if (ragged && (o->path != GVA_PATH_AUTO || !prefill_takes_ragged(d, pp)))
+        return GVA_ERR_UNSUPPORTED;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < pp.total)
         return GVA_ERR_WORKSPACE;
     char *w = static_cast<char *>(ws);
