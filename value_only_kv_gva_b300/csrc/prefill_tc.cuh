@@ -146,9 +146,10 @@ struct PtSmem {
     static constexpr int STAGE = VT + KT;
     static constexpr int XM = 2 * 4 * 4 * 32 * 4;            // row max parts [buf][quad][part][32]
     static constexpr int LS = 4 * 4 * 32 * 4;                // row sum parts [quad][part][32]
-    // two P buffers when they fit beside two stages, so that the products of tile k - 1
-    // run while the softmax of tile k writes its P
-    static constexpr int PB = 1024 + 2 * QPART + 4 * PPART + 2 * STAGE + XM + LS + 256 <= MMA_SMEM_LIMIT ? 2 : 1;
+    // two P buffers (the products of tile k - 1 run while the softmax of tile k writes
+    // its P) when four stages still fit beside them; otherwise the stages come first:
+    // with two stages only one tile is in flight while the other is scored
+    static constexpr int PB = 1024 + 2 * QPART + 4 * PPART + 4 * STAGE + XM + LS + 256 <= MMA_SMEM_LIMIT ? 2 : 1;
     static constexpr int fixed = 2 * QPART + PB * 2 * PPART + XM + LS;
 };
 
