@@ -383,7 +383,9 @@ bool plan_prefill(const gva_dims *d, int n, const gva_rows &R, int sms, PrefillP
     // the tcgen05 kernel: one CTA per (history range, value group, sequence), one wave
     p->tcm = p->mq ? prefill_tc_m(d, n) : 0;
     const long long gb = (long long)d->G * d->B;
-    p->tc_splits = p->tcm ? (int)(gb >= sms ? 1 : sms / gb) : 0;
+    // one wave of CTAs, and at least two history ranges per (group, sequence), so that a
+    // long sequence among short ones does not run alone at the end
+    p->tc_splits = p->tcm ? (int)std::max<long long>(2, sms / gb) : 0;
     size_t po_bytes = p->mq ? p->mp.part_o_bytes : 0, pml_bytes = p->mq ? p->mp.part_ml_bytes : 0;
     if (p->tcm) {
         const size_t rows = (size_t)d->B * p->tc_splits * p->mp.rows_pad;
