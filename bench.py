@@ -603,7 +603,7 @@ def _prefill_chain(w, n: int, path: str, sms: int = 148):
     if _prefill_tc(w, n, path):
         rows = n * (w.H // w.G)
         m = 64 if rows <= 64 else 128
-        splits = max(1, sms // (w.G * w.B))
+        splits = max(2, sms // (w.G * w.B))
         if (2 * rows * splits + 2 * rows) * 4 <= 512 * m:
             return "append + absorb + tcgen05 prefill with the ranges' merge in its last CTAs", 3
         return "append + absorb + tcgen05 prefill partial + merge", 4
