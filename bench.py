@@ -297,6 +297,14 @@ def measure_stack(args, dist, torch, gva, gva_inputs, S, stream, sampler, path, 
     asecs, _ = timed_graph(torch, dist, stream, g_abs, args.steps, max(3, args.warmup))
     out["absorb_only_us_per_layer"] = round(dist.max(asecs, S.dev) / (args.steps * nl) * 1e6, 3)
     del g_abs
+
+    # the append alone (one new token per sequence and layer), in its own graph
+    def append_only(L):
+        gva.gva_append_cache(S.dims, L["v_new"], L["k_new"], S.pos, None, L["cache"], S.tab)
+    g_app = capture_list(torch, stream, S.layers, append_only)
+    psecs, _ = timed_graph(torch, dist, stream, g_app, args.steps, max(3, args.warmup))
+    out["append_only_us_per_layer"] = round(dist.max(psecs, S.dev) / (args.steps * nl) * 1e6, 3)
+    del g_app
     if not with_gqa:
         return out
     Kq0 = gva_inputs.make_gqa_keys(S.c).to(S.dev)
