@@ -59,12 +59,14 @@ int main(void) {
     gva_decode_opts o = {GVA_PATH_AUTO, 0, 2 /* unknown flag */, 0.f, NULL};
     CHECK(gva_decode_attention_ex(NULL, &d, fake, fake, ff, (const int *)fake, &cache, ff, 100,
                                   0.1f, ff, NULL, fake, (size_t)1 << 30, &o) == GVA_ERR_ARG);
-    /* prefill: ragged caches are not taken; an empty chunk is an argument error */
+    /* prefill: ragged caches are not taken by the view paths; an empty chunk is an
+       argument error */
     gva_cache rag = cache;
     rag.rows.layout = GVA_LAYOUT_RAGGED;
     rag.rows.offsets = (const int *)fake;
+    gva_decode_opts simt = {GVA_PATH_SIMT, 0, 0, 0.f, NULL};
     CHECK(gva_prefill_attention(NULL, &d, 4, fake, fake, ff, (const int *)fake, ff, ff, &rag, ff,
-                                100, 0.1f, ff, NULL, fake, (size_t)1 << 30, NULL) ==
+                                100, 0.1f, ff, NULL, fake, (size_t)1 << 30, &simt) ==
           GVA_ERR_UNSUPPORTED);
     CHECK(gva_prefill_attention(NULL, &d, 0, fake, fake, ff, (const int *)fake, ff, ff, &cache,
                                 ff, 100, 0.1f, ff, NULL, fake, (size_t)1 << 30, NULL) ==

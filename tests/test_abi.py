@@ -186,22 +186,26 @@ def test_bad_option_flags_rejected_before_cuda(gva, flags, eps):
 
 
 def test_prefill_arguments_rejected_before_cuda(gva):
-    """Ragged caches and contiguous capacities that are not a multiple of 16 are not
-    taken (GVA_ERR_UNSUPPORTED); an empty chunk or more than 4096 decode entries is an
-    argument error."""
+    """Contiguous capacities that are not a multiple of 16, and ragged caches on a path
+    other than the automatic one (the view paths), are not taken (GVA_ERR_UNSUPPORTED);
+    an empty chunk or more than 4096 decode entries is an argument error.  (Whether the
+    automatic path takes a ragged cache depends on the device's plan: GPU tests.)"""
     lib = gva._lib
     d = _dims(gva)
     fake = ctypes.c_void_p(0x10000)
 
-    def call(rows, n):
+    def call(rows, n, path=None):
         cache = gva.gva_cache(rows, fake, fake)
+        o = None if path is None else ctypes.byref(gva.gva_decode_opts(path, 0, 0, 0.0, None))
         return lib.gva_prefill_attention(None, ctypes.byref(d), n, fake, fake, fake, fake, fake,
                                          fake, ctypes.byref(cache), fake, 100,
                                          ctypes.c_float(0.1), fake, None, fake,
-                                         ctypes.c_size_t(1 << 30), None)
+                                         ctypes.c_size_t(1 << 30), o)
 
     contig = gva.gva_rows(0, 2 * 1024, 1024, None, None, 0, 0)
-    assert call(gva.gva_rows(1, 640, 0, fake, None, 0, 0), 4) == gva.GVA_ERR_UNSUPPORTED
+    ragged = gva.gva_rows(1, 640, 0, fake, None, 0, 0)
+    for path in (gva.PATHS["simt"], gva.PATHS["mma"]):
+        assert call(ragged, 4, path) == gva.GVA_ERR_UNSUPPORTED
     assert call(gva.gva_rows(0, 2 * 1000, 1000, None, None, 0, 0), 4) == gva.GVA_ERR_UNSUPPORTED
     assert call(contig, 0) == gva.GVA_ERR_ARG
     assert call(contig, 2049) == gva.GVA_ERR_ARG          # B = 2: 4098 entries
@@ -231,14 +235,15 @@ def _documented_valid(B, H, G, d_h, d_n, d_r, cd, qd):
 
 def test_dims_validation_follows_the_header(gva):
     """Random shapes: the library refuses exactly those the header's support matrix
-    excludes.  The probe is gva_prefill_attention on a ragged cache, which returns
-    before any CUDA call either way: GVA_ERR_ARG for unsupported dims,
-    GVA_ERR_UNSUPPORTED (ragged layouts are not taken) for supported ones."""
+    excludes.  The probe is gva_prefill_attention on a ragged cache with the SIMT path,
+    which returns before any CUDA call either way: GVA_ERR_ARG for unsupported dims,
+    GVA_ERR_UNSUPPORTED (the view paths do not take ragged layouts) for supported ones."""
     from hypothesis import given, settings, strategies as st
 
     lib = gva._lib
     fake = ctypes.c_void_p(0x10000)
     rag = gva.gva_cache(gva.gva_rows(1, 640, 0, fake, None, 0, 0), fake, fake)
+    simt = gva.gva_decode_opts(gva.PATHS["simt"], 0, 0, 0.0, None)
 
     seen = {gva.GVA_ERR_ARG: 0, gva.GVA_ERR_UNSUPPORTED: 0}
 
@@ -271,7 +276,8 @@ def test_dims_validation_follows_the_header(gva):
         d = gva.gva_dims(B, H, G, d_h, d_n, d_r, cd, qd)
         st_ = lib.gva_prefill_attention(None, ctypes.byref(d), 1, fake, fake, fake, fake, fake,
                                         fake, ctypes.byref(rag), fake, 100, ctypes.c_float(0.1),
-                                        fake, None, fake, ctypes.c_size_t(1 << 30), None)
+                                        fake, None, fake, ctypes.c_size_t(1 << 30),
+                                        ctypes.byref(simt))
         want = gva.GVA_ERR_UNSUPPORTED if _documented_valid(B, H, G, d_h, d_n, d_r, cd, qd) \
             else gva.GVA_ERR_ARG
         assert st_ == want, (B, H, G, d_h, d_n, d_r, cd, qd, st_)

@@ -950,6 +950,7 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
     const gva_rows &R = cache->rows;
     const bool ragged = R.layout == GVA_LAYOUT_RAGGED;
     if (!ragged && !prefill_layout_ok(R)) return GVA_ERR_UNSUPPORTED;
+    if (ragged && o->path != GVA_PATH_AUTO) return GVA_ERR_UNSUPPORTED;   // the view paths
     if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
     const int sms = num_sms_current();
     if (sms <= 0) return GVA_ERR_CUDA;
