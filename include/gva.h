@@ -393,9 +393,13 @@ typedef struct {
  * the positions, lengths, table, scale, options and one workspace (>= 
  * gva_decode_workspace_size(dims)): every kernel of a layer waits for the layer before it,
  * so the scratch is reused in order.  The result is that of the per-layer calls, bit for
- * bit.  Returns GVA_OK, GVA_ERR_ARG for n_layers < 0 or a NULL `layers` with
- * n_layers > 0, or the first error of a layer's call (the layers before it are launched,
- * the rest are not). */
+ * bit.  The append and the absorption read and write disjoint buffers, so on the
+ * tensor-core path with a bf16 cache and d_n = 64 or 128 they run as one grid (a layer is
+ * then three launches, and its decode reads the cache once that grid has completed); the
+ * layer's cache must not overlap its queries, map or lengths.  A layer's append and decode
+ * arguments are both checked before its first launch.  Returns GVA_OK, GVA_ERR_ARG for
+ * n_layers < 0 or a NULL `layers` with n_layers > 0, or the first error of a layer's call
+ * (the layers before it are launched, the rest are not). */
 int gva_decode_step(void *stream, const gva_dims *dims, int n_layers,
                     const gva_layer_args *layers, const int *pos, const int *seq_len,
                     const float *rope_tab, int rope_max_pos, float scale, void *workspace,

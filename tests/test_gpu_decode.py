@@ -464,13 +464,23 @@ def test_largest_batch():
         assert_close(lse, ref_lse, "bf16", f"B=4096 {path} lse")
 
 
-@pytest.mark.parametrize("name", ["350m", "paged", "tiny"])
-def test_decode_step_matches_per_layer_calls(name):
+STEP_CASES = {
+    "350m": ("350m", {}), "paged": ("paged", {}), "tiny": ("tiny", {}),
+    "ragged": ("ragged", {}), "long": ("long", {}),
+    "350m_f32_query": ("350m", dict(q_dtype="f32")),
+}
+
+
+@pytest.mark.parametrize("case", list(STEP_CASES))
+def test_decode_step_matches_per_layer_calls(case):
     """gva_decode_step over three layers (one C call: each layer's append, then its decode,
     the layers sharing one workspace) equals the per-layer gva_append_cache and
-    gva_decode_attention calls bit for bit, outputs and appended rows, and the oracle."""
+    gva_decode_attention calls bit for bit, outputs and appended rows, and the oracle.
+    On the tensor-core path with a bf16 cache the step runs each layer's append inside
+    the absorption's grid (bf16 and fp32 queries), on the others as its own kernel."""
     g = gva()
-    c = make_case(workload(name, **SMALL[name]))
+    name, extra = STEP_CASES[case]
+    c = make_case(workload(name, **SMALL[name], **extra))
     pos = (c.seq_len - 1).to(torch.int32).cuda()
     a = [Dev(c) for _ in range(3)]          # per-layer calls
     s = [Dev(c) for _ in range(3)]          # one step call
@@ -494,8 +504,8 @@ def test_decode_step_matches_per_layer_calls(name):
         assert torch.equal(Da.V, Ds.V) and torch.equal(Da.Kr, Ds.Kr)
     V, K = oracle_append(c, pos.cpu(), s[0].tab_h)
     ref, ref_lse = oracle_decode(c, V, K)
-    assert_close(outs_a[0][0], ref, w.cache_dtype, f"{name} step out")
-    assert_close(outs_a[0][1], ref_lse, w.cache_dtype, f"{name} step lse")
+    assert_close(outs_a[0][0], ref, w.cache_dtype, f"{case} step out")
+    assert_close(outs_a[0][1], ref_lse, w.cache_dtype, f"{case} step lse")
 
 
 @pytest.mark.parametrize("name", ["350m", "paged", "tiny"])

@@ -32,13 +32,27 @@ def _bits(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
 
 
+@pytest.mark.parametrize("via", ["calls", "step"])
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_parity(name):
+def test_full_size_parity(name, via):
+    """`calls`: gva_append_cache then gva_decode_attention.  `step`: one gva_decode_step
+    layer, the call the benchmark's step makes (the append inside the absorption's grid)."""
     c = make_case(workload(name))
     D = Dev(c)
     pos = (c.seq_len - 1).to(torch.int32)
-    D.append(pos)
-    out, lse = D.decode(path="auto")
+    if via == "calls":
+        D.append(pos)
+        out, lse = D.decode(path="auto")
+    else:
+        w = c.w
+        o = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+        l = torch.full((w.B, w.H), float("nan"), device="cuda")
+        layer = dict(v_new=D.v_new, k_rope_new=D.k_new, q_nope=D.q_nope, q_rope=D.q_rope,
+                     M=D.M, cache=D.cache, out=o, lse=l)
+        gva().gva_decode_step(D.dims, [layer], pos.cuda(), D.seq_len, D.tab, w.scale, D.ws)
+        torch.cuda.synchronize()
+        out = o.cpu().numpy().astype(np.float64)
+        lse = l.cpu().numpy().astype(np.float64)
     assert gva().gva_get_device_status() == 0
     V, K = oracle_append(c, pos, D.tab_h)
     ref, ref_lse = oracle_decode(c, V, K)           # every sequence, every head

@@ -254,13 +254,19 @@ int run_simt(void *stream, DecodeParams &dp, int sms, int req_ctas) {
     return cuda_status(launch(kern, dim3(dp.n_ctas), dim3(SIMT_THREADS), L.total, stream, dp));
 }
 
-int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
-                  const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
-                  float prescale, float *q_tilde, float *q_hat, int sms,
-                  const gva_rows *rows = nullptr, bool skip_rope = false,
-                  const gva_decode_opts *qn = nullptr, const int *L0 = nullptr,
-                  int chunk_n = 0) {
+// The absorption's parameters, grid and shared memory (arguments validated by the caller).
+struct AbsorbLaunch {
     AbsorbParams p;
+    dim3 grid;
+    size_t smem;
+};
+AbsorbLaunch absorb_plan(const gva_dims *d, const void *q_nope, const void *q_rope,
+                         const float *M, const int *seq_len, const float *rope_tab,
+                         int rope_max_pos, float prescale, float *q_tilde, float *q_hat, int sms,
+                         const gva_rows *rows, bool skip_rope, const gva_decode_opts *qn,
+                         const int *L0, int chunk_n) {
+    AbsorbLaunch A;
+    AbsorbParams &p = A.p;
     p.skip_rope = skip_rope ? 1 : 0;
     p.L0 = L0;
     p.chunk_n = chunk_n;
@@ -297,8 +303,29 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     p.prescale = prescale;
     p.q_tilde = q_tilde;
     p.q_hat = q_hat;
-    const size_t smem = (size_t)absorb_smem_bytes(d->d_n, bpb);
-    dim3 grid(d->H, (d->B + bpb - 1) / bpb, zs);
+    A.smem = (size_t)absorb_smem_bytes(d->d_n, bpb);
+    A.grid = dim3(d->H, (d->B + bpb - 1) / bpb, zs);
+    return A;
+}
+
+int absorb_run(void *stream, const gva_dims *d, const AbsorbLaunch &A);
+
+int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                  const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
+                  float prescale, float *q_tilde, float *q_hat, int sms,
+                  const gva_rows *rows = nullptr, bool skip_rope = false,
+                  const gva_decode_opts *qn = nullptr, const int *L0 = nullptr,
+                  int chunk_n = 0) {
+    return absorb_run(stream, d,
+                      absorb_plan(d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                                  prescale, q_tilde, q_hat, sms, rows, skip_rope, qn, L0,
+                                  chunk_n));
+}
+
+int absorb_run(void *stream, const gva_dims *d, const AbsorbLaunch &A) {
+    const AbsorbParams &p = A.p;
+    const dim3 grid = A.grid;
+    const size_t smem = A.smem;
     cudaError_t e;
     const dim3 blk(ABSORB_THREADS);
     const bool f32 = d->q_dtype == GVA_F32;
@@ -322,11 +349,11 @@ int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const voi
     return cuda_status(e);
 }
 
-// One CTA per entry of the batch d->B (arguments validated by the caller).
-int append_launch(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
-                  const int *pos, int *seq_len_out, const gva_rows &rows, void *V, void *Kr,
-                  const float *rope_tab, int rope_max_pos, const int *L0 = nullptr,
-                  int chunk_n = 0, int *zero = nullptr, int nzero = 0) {
+// The append's parameters (arguments validated by the caller).
+AppendParams append_params(const gva_dims *d, const float *v_new, const float *k_new,
+                           const int *pos, int *seq_len_out, const gva_rows &rows, void *V,
+                           void *Kr, const float *rope_tab, int rope_max_pos, const int *L0,
+                           int chunk_n, int *zero, int nzero) {
     AppendParams p;
     p.L0 = L0;
     p.chunk_n = chunk_n;
@@ -345,9 +372,44 @@ int append_launch(void *stream, const gva_dims *d, const float *v_new, const flo
     p.Kr = Kr;
     p.rope_tab = rope_tab;
     p.rope_max_pos = rope_max_pos;
+    return p;
+}
+
+// One CTA per entry of the batch d->B (arguments validated by the caller).
+int append_launch(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
+                  const int *pos, int *seq_len_out, const gva_rows &rows, void *V, void *Kr,
+                  const float *rope_tab, int rope_max_pos, const int *L0 = nullptr,
+                  int chunk_n = 0, int *zero = nullptr, int nzero = 0) {
+    const AppendParams p = append_params(d, v_new, k_new, pos, seq_len_out, rows, V, Kr,
+                                         rope_tab, rope_max_pos, L0, chunk_n, zero, nzero);
     cudaError_t e = d->cache_dtype == GVA_F32
                         ? launch(append_kernel<float>, dim3(d->B), dim3(128), 0, stream, p)
                         : launch(append_kernel<__nv_bfloat16>, dim3(d->B), dim3(128), 0, stream, p);
+    return cuda_status(e);
+}
+
+// The absorption and the append of one decode step as one grid: bf16 cache and a
+// content-query width of 64 or 128 (the other shapes launch the two kernels).
+bool prep_step_supported(const gva_dims *d) {
+    return d->cache_dtype == GVA_BF16 && (d->d_n == 64 || d->d_n == 128);
+}
+
+int prep_step_launch(void *stream, const gva_dims *d, const AbsorbLaunch &A,
+                     const AppendParams &ap) {
+    const int ny = (int)A.grid.y, nz = (int)A.grid.z;
+    const dim3 grid(A.grid.x * A.grid.y * A.grid.z + d->B), blk(ABSORB_THREADS);
+    const bool f32 = d->q_dtype == GVA_F32;
+    cudaError_t e;
+    if (d->d_n == 64)
+        e = f32 ? launch(prep_step_kernel<float, 8, __nv_bfloat16>, grid, blk, A.smem, stream,
+                         A.p, ap, ny, nz)
+                : launch(prep_step_kernel<__nv_bfloat16, 8, __nv_bfloat16>, grid, blk, A.smem,
+                         stream, A.p, ap, ny, nz);
+    else
+        e = f32 ? launch(prep_step_kernel<float, 16, __nv_bfloat16>, grid, blk, A.smem, stream,
+                         A.p, ap, ny, nz)
+                : launch(prep_step_kernel<__nv_bfloat16, 16, __nv_bfloat16>, grid, blk, A.smem,
+                         stream, A.p, ap, ny, nz);
     return cuda_status(e);
 }
 
@@ -662,14 +724,23 @@ int gva_absorb_query_ex(void *stream, const gva_dims *d, const void *q_nope, con
                          q_tilde, q_rope_rot, num_sms_current(), nullptr, false, o);
 }
 
-int gva_append_cache(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
-                     const int *pos, int *seq_len_out, const gva_cache *cache,
-                     const float *rope_tab, int rope_max_pos) {
+// Host-only checks of the append's arguments (no CUDA call).
+static int append_arg_checks(const gva_dims *d, const float *v_new, const float *k_new,
+                             const int *pos, const gva_cache *cache, const float *rope_tab,
+                             int rope_max_pos) {
     if (!dims_ok(d, true) || !cache || !rows_ok(&cache->rows, d->B)) return GVA_ERR_ARG;
     if (!v_new || !pos || !cache->V || !aligned16(v_new) || !aligned16(cache->V)) return GVA_ERR_ARG;
     if (d->d_r > 0 && (!k_new || !cache->K_rope || !rope_tab || rope_max_pos < 1 ||
                        !aligned16(k_new) || !aligned16(cache->K_rope)))
         return GVA_ERR_ARG;
+    return GVA_OK;
+}
+
+int gva_append_cache(void *stream, const gva_dims *d, const float *v_new, const float *k_new,
+                     const int *pos, int *seq_len_out, const gva_cache *cache,
+                     const float *rope_tab, int rope_max_pos) {
+    const int ck = append_arg_checks(d, v_new, k_new, pos, cache, rope_tab, rope_max_pos);
+    if (ck != GVA_OK) return ck;
     if (bind_or_fail(stream) != GVA_OK) return GVA_ERR_CUDA;
     if (!device_state()) return GVA_ERR_CUDA;
     return append_launch(stream, d, v_new, k_new, pos, seq_len_out, cache->rows, cache->V,
@@ -705,15 +776,30 @@ static int decode_device_checks(void *stream, const gva_dims *d, void *ws, size_
     return GVA_OK;
 }
 
-int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
-                            const void *q_rope, const float *M, const int *seq_len,
-                            const gva_cache *cache, const float *rope_tab, int rope_max_pos,
-                            float scale, float *out, float *lse, void *ws, size_t ws_bytes,
-                            const gva_decode_opts *opts) {
+// The new token of a decode step, appended by the same call (gva_decode_step).
+struct StepAppend {
+    const float *v_new, *k_new;
+    const int *pos;
+};
+
+// One layer's decode, after the append of `app` when it is given: with the tensor-core
+// decode and a shape the fused kernel takes, the append runs in the absorption's grid
+// and the decode reads the cache only after that grid has completed; otherwise the
+// append kernel runs first.
+static int decode_call(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                       const float *M, const int *seq_len, const gva_cache *cache,
+                       const float *rope_tab, int rope_max_pos, float scale, float *out,
+                       float *lse, void *ws, size_t ws_bytes, const gva_decode_opts *opts,
+                       const StepAppend *app) {
     const gva_decode_opts *o = opts ? opts : &kDefaultOpts;
     if (!cache) return GVA_ERR_ARG;
     int st = decode_arg_checks(d, &cache->rows, out, lse, o, true);
     if (st != GVA_OK) return st;
+    if (app) {
+        st = append_arg_checks(d, app->v_new, app->k_new, app->pos, cache, rope_tab,
+                               rope_max_pos);
+        if (st != GVA_OK) return st;
+    }
     if (!q_nope || !M || !seq_len || !cache->V || !aligned16(q_nope) || !aligned16(M) ||
         !aligned16(cache->V))
         return GVA_ERR_ARG;
@@ -734,8 +820,24 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     // the tensor-core decode rotates the positional query itself (its inputs are final
     // before the call, so it overlaps the absorption), leaving the absorption a single
     // memory round trip
-    st = absorb_launch(stream, d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o);
+    const AbsorbLaunch A = absorb_plan(d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                                       scale * LOG2E, qt, qh, sms, &cache->rows, use_mma, o,
+                                       nullptr, 0);
+    const bool fused = app && use_mma && prep_step_supported(d);
+    if (fused) {
+        st = prep_step_launch(stream, d, A,
+                              append_params(d, app->v_new, app->k_new, app->pos, nullptr,
+                                            cache->rows, cache->V, cache->K_rope, rope_tab,
+                                            rope_max_pos, nullptr, 0, nullptr, 0));
+    } else {
+        if (app) {
+            if (!device_state()) return GVA_ERR_CUDA;
+            st = append_launch(stream, d, app->v_new, app->k_new, app->pos, nullptr, cache->rows,
+                               cache->V, cache->K_rope, rope_tab, rope_max_pos);
+            if (st != GVA_OK) return st;
+        }
+        st = absorb_run(stream, d, A);
+    }
     if (st != GVA_OK) return st;
 
     DecodeParams dp;
@@ -766,7 +868,9 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     dp.n_ctas = 0;
     dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
     if (use_mma) {
-        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, true);
+        // `early` (stream the cache before the grid dependency resolves) only when the
+        // preceding grid does not write the cache
+        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, !fused);
     } else if (d->cache_dtype == GVA_F32) {
         st = run_simt<float, false>(stream, dp, sms, o->num_ctas);
     } else {
@@ -774,6 +878,15 @@ int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
     }
     if (st != GVA_OK) return st;
     return launch_combine(stream, dp, cache->rows);
+}
+
+int gva_decode_attention_ex(void *stream, const gva_dims *d, const void *q_nope,
+                            const void *q_rope, const float *M, const int *seq_len,
+                            const gva_cache *cache, const float *rope_tab, int rope_max_pos,
+                            float scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                            const gva_decode_opts *opts) {
+    return decode_call(stream, d, q_nope, q_rope, M, seq_len, cache, rope_tab, rope_max_pos,
+                       scale, out, lse, ws, ws_bytes, opts, nullptr);
 }
 
 int gva_decode_attention(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
@@ -790,15 +903,10 @@ int gva_decode_step(void *stream, const gva_dims *d, int n_layers, const gva_lay
     if (n_layers < 0 || (n_layers > 0 && !layers)) return GVA_ERR_ARG;
     for (int l = 0; l < n_layers; ++l) {
         const gva_layer_args &L = layers[l];
-        int st;
-        if (L.v_new) {
-            st = gva_append_cache(stream, d, L.v_new, L.k_rope_new, pos, nullptr, &L.cache,
-                                  rope_tab, rope_max_pos);
-            if (st != GVA_OK) return st;
-        }
-        st = gva_decode_attention_ex(stream, d, L.q_nope, L.q_rope, L.M, seq_len, &L.cache,
-                                     rope_tab, rope_max_pos, scale, L.out, L.lse, ws, ws_bytes,
-                                     opts);
+        const StepAppend app{L.v_new, L.k_rope_new, pos};
+        const int st = decode_call(stream, d, L.q_nope, L.q_rope, L.M, seq_len, &L.cache,
+                                   rope_tab, rope_max_pos, scale, L.out, L.lse, ws, ws_bytes,
+                                   opts, L.v_new ? &app : nullptr);
         if (st != GVA_OK) return st;
     }
     return GVA_OK;

@@ -38,26 +38,22 @@ __device__ __forceinline__ int chunk_pos(const int *L0, int n, int v) {
 // Rot(pos) k_new computed in fp32 in the fixed order y0 = (x0*c) - (x1*s),
 // y1 = (x0*s) + (x1*c) with every product and sum rounded separately (no FMA), then
 // rounded once to the cache dtype, so the stored bytes are reproducible.
-template <typename CT>
-__global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
-    if (threadIdx.x == 0) GVA_KT(0);
-    if (threadIdx.x == 0) GVA_REC(1, 0);
-    pdl_wait();
-    if (threadIdx.x == 0) GVA_REC(1, 1);
-    pdl_launch_dependents();
-    const int b = blockIdx.x;                                // entry of the inputs
+// The work of entry b, for a CTA of NTHR threads (the block's first NTHR threads; nblk
+// CTAs share the zeroing).
+template <typename CT, int NTHR>
+__device__ __forceinline__ void append_body(const AppendParams &p, int b, int nblk) {
     const int sb = p.chunk_n > 0 ? b / p.chunk_n : b;        // sequence of its rows
-    for (int e = b * 128 + (int)threadIdx.x; e < p.nzero; e += gridDim.x * 128) p.zero[e] = 0;
+    for (int e = b * NTHR + (int)threadIdx.x; e < p.nzero; e += nblk * NTHR) p.zero[e] = 0;
     const int W = p.G * p.d_h;
     // Loads that do not depend on the position are issued with it: the new value (up
-    // to 8 elements per thread), the unrotated key pair, the position.  The table entry
+    // to VPT elements per thread), the unrotated key pair, the position.  The table entry
     // and, for a paged cache, the block-table entry follow: two memory round trips.
-    constexpr int VPT = 8;
+    constexpr int VPT = 1024 / NTHR;
     const float *vn = p.v_new + (long long)b * W;
     float vv[VPT];
 #pragma unroll
     for (int u = 0; u < VPT; ++u) {
-        const int e = threadIdx.x + u * 128;
+        const int e = threadIdx.x + u * NTHR;
         vv[u] = e < W ? vn[e] : 0.f;
     }
     const int half = p.d_r / 2;
@@ -86,10 +82,10 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     CT *V = reinterpret_cast<CT *>(p.V) + row * W;
 #pragma unroll
     for (int u = 0; u < VPT; ++u) {
-        const int e = threadIdx.x + u * 128;
+        const int e = threadIdx.x + u * NTHR;
         if (e < W) V[e] = from_f<CT>(vv[u]);
     }
-    for (int e = threadIdx.x + VPT * 128; e < W; e += 128) V[e] = from_f<CT>(vn[e]);
+    for (int e = threadIdx.x + VPT * NTHR; e < W; e += NTHR) V[e] = from_f<CT>(vn[e]);
     if (kthr) {
         CT *K = reinterpret_cast<CT *>(p.Kr) + row * p.d_r;
         const float y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
@@ -99,6 +95,16 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     }
     __syncthreads();
     if (threadIdx.x == 0 && p.seq_len_out) p.seq_len_out[b] = pos + 1;
+}
+
+template <typename CT>
+__global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
+    if (threadIdx.x == 0) GVA_KT(0);
+    if (threadIdx.x == 0) GVA_REC(1, 0);
+    pdl_wait();
+    if (threadIdx.x == 0) GVA_REC(1, 1);
+    pdl_launch_dependents();
+    append_body<CT, 128>(p, blockIdx.x, gridDim.x);
     if (threadIdx.x == 0) GVA_KT(1);
     if (threadIdx.x == 0) GVA_REC(1, 2);
 }
@@ -215,19 +221,13 @@ template <> __device__ __forceinline__ float vec_elem<__nv_bfloat16>(const uint4
 }
 
 // CSF: the chunk size d_n / 8 when it is fixed at compile time (8, 16, 32), 0 otherwise.
+// The work of CTA (h, by, bz) of the grid above, staging in sm_abs.
 template <typename QT, int CSF>
-__global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbParams p) {
-    extern __shared__ __align__(16) float sm_abs[];
-    if (threadIdx.x == 0) GVA_KT(2);
-    if (threadIdx.x == 0) GVA_REC(2, 0);
-    pdl_wait();
-    if (threadIdx.x == 0) GVA_KT(3);
-    if (threadIdx.x == 0) GVA_REC(2, 1);
-    pdl_launch_dependents();
-    const int h = blockIdx.x;
-    const int b0 = blockIdx.y * p.bpb;
+__device__ __forceinline__ void absorb_body(const AbsorbParams &p, int h, int by, int bz,
+                                            float *sm_abs) {
+    const int b0 = by * p.bpb;
     const int nb = min(p.bpb, p.B - b0);
-    const int i0 = blockIdx.z * 32;
+    const int i0 = bz * 32;
     const int d_n = p.d_n, d_h = p.d_h;
     const int cs = CSF > 0 ? CSF : d_n / 8, cst = absorb_cst(8 * cs);
     constexpr int CSMAX = CSF > 0 ? CSF : ABSORB_CSMAX;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
     // (bpb * d_r / 2 <= 32 * 16).  Its inputs are loaded with the rest; the rotation
     // table entries, which depend on the lengths, right after.
     const int half = p.d_r / 2;
-    const bool rope = p.d_r > 0 && !p.skip_rope && blockIdx.z == 0;
+    const bool rope = p.d_r > 0 && !p.skip_rope && bz == 0;
     constexpr int RPT = 2;
     int rL[RPT];
     float rx0[RPT], rx1[RPT];
@@ -411,8 +411,42 @@ __global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbP
             qh[2 * ri + 1] = p.prescale * (rx0[u] * rs + rx1[u] * rc);
         }
     }
+}
+
+template <typename QT, int CSF>
+__global__ void __launch_bounds__(ABSORB_THREADS, 2) absorb_kernel(const AbsorbParams p) {
+    extern __shared__ __align__(16) float sm_abs[];
+    if (threadIdx.x == 0) GVA_KT(2);
+    if (threadIdx.x == 0) GVA_REC(2, 0);
+    pdl_wait();
+    if (threadIdx.x == 0) GVA_KT(3);
+    if (threadIdx.x == 0) GVA_REC(2, 1);
+    pdl_launch_dependents();
+    absorb_body<QT, CSF>(p, blockIdx.x, blockIdx.y, blockIdx.z, sm_abs);
     if (threadIdx.x == 0) GVA_KT(4);
     if (threadIdx.x == 0) GVA_REC(2, 2);
+}
+
+// --------------------------------------------------------------------------- //
+// Absorption and append of one decode step in one grid.  The two read disjoint inputs
+// and write disjoint outputs (the absorbed queries; the new cache rows), so they need
+// not be ordered: the first na CTAs (a linear form of the absorption's grid, H x ny x
+// nz) absorb, the next B append one entry each.  A decode grid that follows reads the
+// cache only after its grid dependency resolves.
+// --------------------------------------------------------------------------- //
+template <typename QT, int CSF, typename CT>
+__global__ void __launch_bounds__(ABSORB_THREADS, 2)
+    prep_step_kernel(const AbsorbParams a, const AppendParams ap, int ny, int nz) {
+    extern __shared__ __align__(16) float sm_abs[];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int na = a.H * ny * nz;
+    const int bid = blockIdx.x;
+    if (bid < na) {
+        absorb_body<QT, CSF>(a, bid % a.H, (bid / a.H) % ny, bid / (a.H * ny), sm_abs);
+    } else {
+        append_body<CT, ABSORB_THREADS>(ap, bid - na, gridDim.x - na);
+    }
 }
 
 // --------------------------------------------------------------------------- //
