@@ -395,8 +395,10 @@ typedef struct {
  * so the scratch is reused in order.  The result is that of the per-layer calls, bit for
  * bit.  The append and the absorption read and write disjoint buffers, so on the
  * tensor-core path with a bf16 cache and d_n = 64 or 128 they run as one grid (a layer is
- * then three launches, and its decode reads the cache once that grid has completed); the
- * layer's cache must not overlap its queries, map or lengths.  A layer's append and decode
+ * then three launches).  The decode streams the cache while that grid runs and copies the
+ * 16-row slab that holds sequence b's position pos[b] only once the grid has completed, so
+ * a new row must be read by its own sequence only (no other sequence's rows or pages may
+ * hold it), and the layer's cache must not overlap its queries, map, lengths or positions.  A layer's append and decode
  * arguments are both checked before its first launch.  Returns GVA_OK, GVA_ERR_ARG for
  * n_layers < 0 or a NULL `layers` with n_layers > 0, or the first error of a layer's call
  * (the layers before it are launched, the rest are not). */

@@ -508,6 +508,48 @@ def test_decode_step_matches_per_layer_calls(case):
     assert_close(outs_a[0][1], ref_lse, w.cache_dtype, f"{case} step lse")
 
 
+@pytest.mark.parametrize("name", ["350m", "ragged", "paged"])
+def test_decode_step_rows_inside_the_sequences(name):
+    """gva_decode_step whose appends overwrite rows inside the sequences (positions in the
+    first slab, in a middle slab, in the last slab, and past the length, which the decode
+    does not read): the decode holds back exactly the slab each new row falls in, so the
+    outputs and rows equal those of the per-layer calls bit for bit, and the oracle."""
+    g = gva()
+    c = make_case(workload(name, **SMALL[name], extra_slots=2))
+    w = c.w
+    L = c.seq_len.tolist()
+    pos_l = []
+    for b, Lb in enumerate(L):
+        choice = b % 4
+        if choice == 0:
+            p = min(3, Lb - 1)
+        elif choice == 1:
+            p = Lb // 2
+        elif choice == 2:
+            p = Lb - 1
+        else:
+            p = Lb if w.extra_slots > 0 else Lb - 1     # every capacity is L_b + extra_slots
+        pos_l.append(max(p, 0))
+    pos = torch.tensor(pos_l, dtype=torch.int32).cuda()
+    a, s = Dev(c), Dev(c)
+    a.append(pos)
+    oa, la = a.decode()
+    out = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+    lse = torch.full((w.B, w.H), float("nan"), device="cuda")
+    layer = dict(v_new=s.v_new, k_rope_new=s.k_new, q_nope=s.q_nope, q_rope=s.q_rope, M=s.M,
+                 cache=s.cache, out=out, lse=lse)
+    g.gva_decode_step(s.dims, [layer], pos, s.seq_len, s.tab, w.scale, s.ws)
+    torch.cuda.synchronize()
+    assert g.gva_get_device_status() == 0
+    assert np.array_equal(oa, out.cpu().numpy().astype(np.float64))
+    assert np.array_equal(la, lse.cpu().numpy().astype(np.float64))
+    assert torch.equal(a.V, s.V) and torch.equal(a.Kr, s.Kr)
+    V, K = oracle_append(c, pos.cpu(), s.tab_h)
+    ref, ref_lse = oracle_decode(c, V, K)
+    assert_close(oa, ref, w.cache_dtype, f"{name} overwrite step out")
+    assert_close(la, ref_lse, w.cache_dtype, f"{name} overwrite step lse")
+
+
 @pytest.mark.parametrize("name", ["350m", "paged", "tiny"])
 def test_step_plan_replays_the_step(name):
     """A step recorded by gva_step_plan_create and launched twice, with new queries written

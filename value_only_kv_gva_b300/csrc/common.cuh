@@ -166,15 +166,20 @@ struct Part {
 // Invalid lengths count as 0 and set GVA_DEV_BAD_LENGTH when `report` is set.
 // When `prefix_out` is given, the CTA also stores F[0..B] there (one CTA of the grid
 // does, for the combine kernel's large-batch path).
+// With `hold_pos` (and Hs[B]), Hs[b] is the slab of sequence b that holds position
+// hold_pos[b] when 0 <= hold_pos[b] < L_b, else -1 (loaded with the lengths).
 __device__ void build_prefix(const int *seq_len, const RowsDev &R, int B, int *Ls, int *F,
-                             bool report, int *prefix_out = nullptr) {
+                             bool report, int *prefix_out = nullptr,
+                             const int *hold_pos = nullptr, int *Hs = nullptr) {
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seq_len[b];
+        const int hp = hold_pos ? hold_pos[b] : -1;
         if (!length_ok(R, b, L)) {
             if (report) dev_report(GVA_DEV_BAD_LENGTH);
             L = 0;
         }
         Ls[b] = L;
+        if (hold_pos) Hs[b] = (hp >= 0 && hp < L) ? hp / SLAB : -1;
     }
     __syncthreads();
     if (threadIdx.x < 32) {

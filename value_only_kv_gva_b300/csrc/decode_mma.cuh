@@ -63,13 +63,16 @@ struct MmaParams {
     int wpg;           // consumer warps per value group
     int ncons;         // G * wpg consumer warps
     int off_bar;       // barriers, from the aligned dynamic smem base
-    int off_f;         // Ls[B], F[B+1]
+    int off_f;         // Ls[B], F[B+1] (and Hs[B] with hold_pos)
     int off_merge;     // group-merge buffer
     int v3d;           // 1: one 3D TMA box per slab covers every value column
     int vg;            // value groups stored per row: G, or 1 when every group of heads
                        //    reads the same row (the latent rows of the MLA-shaped decode)
     int early;         // 1: the preceding kernel only writes the queries, so the cache
                        //    may be streamed before the grid dependency resolves
+    const int *hold_pos;  // with early: the preceding kernel also writes row hold_pos[b] of
+                          //    each sequence b, so the producer waits on the grid dependency
+                          //    before it copies the slab holding that row (Hs after F)
 };
 
 // Optional timeline of a few CTAs (compiled in only with -DGVA_TRACE; a debugging aid
@@ -510,10 +513,10 @@ __device__ __forceinline__ void mask_value_tiles(uint32_t (&apv)[DH / 16][4], in
 // the share goes to stage i mod NS in round i / NS.
 template <int DH, int DR, bool GQA>
 __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUtensorMap *tm_k,
-                                             const MmaParams &mp, const int *F, long long s0,
-                                             long long s1, uint32_t base_u32, uint32_t bar_full,
-                                             uint32_t bar_empty, volatile int *abort,
-                                             int *stage_bad, uint64_t pol) {
+                                             const MmaParams &mp, const int *F, const int *Hs,
+                                             long long s0, long long s1, uint32_t base_u32,
+                                             uint32_t bar_full, uint32_t bar_empty,
+                                             volatile int *abort, int *stage_bad, uint64_t pol) {
     const DecodeParams &p = mp.d;
     const int NS = mp.nstages, B = p.B;
     const int lane = threadIdx.x & 31;
@@ -523,6 +526,7 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
     bool dead = false;
     long long n_tried = 0;              // slabs of the steps attempted
     int b = seq_of_slab(F, B, s0);      // sequence of the step's first slab
+    bool held = Hs == nullptr;          // the grid dependency has resolved (or need not)
     if (lane == 0) GVA_TRACE_AT(6);
     if (lane == 0) GVA_TRACE_AT(200);
     for (long long sb = s0; sb < s1; sb += il) {
@@ -532,9 +536,18 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
         uint32_t rd = round;
         if (st >= NS) { st -= NS; ++rd; }
         bool ok = true;
-        if (act) {
-            int bl = b;
+        int bl = b;
+        if (act)
             while (F[bl + 1] <= s) ++bl;
+        // a slab holding a row the preceding grid appends is copied only after that grid
+        // has completed (its writes are then visible); the whole warp waits once
+        if (!held) {
+            if (__any_sync(0xffffffffu, act && Hs[bl] == (int)(s - F[bl]))) {
+                pdl_wait();
+                held = true;
+            }
+        }
+        if (act) {
             const long long row = row_of(p.R, bl, (s - F[bl]) * SLAB);
             const int yk = row < 0 ? 0 : (int)row;
             if (s == s0) GVA_TRACE_AT(201);
@@ -658,8 +671,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     // cache streams while that grid still runs; the queries are read after the wait.
     if (!mp.early) pdl_wait();
     pdl_launch_dependents();
+    int *Hs = mp.hold_pos ? F + B + 1 : nullptr;
     build_prefix(p.seq_len, p.R, B, Ls, F, blockIdx.x == 0,   // includes __syncthreads
-                 blockIdx.x == 0 ? p.prefix_ws : nullptr);
+                 blockIdx.x == 0 ? p.prefix_ws : nullptr, mp.hold_pos, Hs);
     if (threadIdx.x == 0) GVA_TRACE_AT(1);
     if (threadIdx.x == 0) GVA_REC(3, 5);
     const Part P{F[B], p.n_ctas};
@@ -670,8 +684,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
     // ============================= producer warp ============================= //
     if (warp == 0) {
-        mma_producer<DH, DR, GQA>(&tm_v, &tm_k, mp, F, s0, s1, base_u32, bar_full, bar_empty,
-                                  abort, stage_bad, pol);
+        mma_producer<DH, DR, GQA>(&tm_v, &tm_k, mp, F, Hs, s0, s1, base_u32, bar_full,
+                                  bar_empty, abort, stage_bad, pol);
         return;
     }
 
@@ -1021,7 +1035,8 @@ inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
     if (mp.wpg < 1) mp.wpg = 1;
     mp.ncons = d.G * mp.wpg;
     const int merge_bytes = merge_bytes_of(mp.wpg, d.G, DH, NT);
-    const int fixed = 1024 /* alignment slack */ + (int)align_up(sizeof(int) * (2 * d.B + 1), 16) +
+    const int narr = (mp.hold_pos ? 3 : 2) * d.B + 1;   // Ls, F (and Hs) in shared memory
+    const int fixed = 1024 /* alignment slack */ + (int)align_up(sizeof(int) * narr, 16) +
                       merge_bytes + bar_region_bytes(MMA_MAX_STAGES);
     int ns = (MMA_SMEM_TARGET - fixed) / mp.stage_bytes;
     if (ns < 4) ns = (MMA_SMEM_LIMIT - fixed) / mp.stage_bytes;
@@ -1040,7 +1055,7 @@ inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
     mp.nstages = ns;
     mp.off_bar = ns * mp.stage_bytes;
     mp.off_f = mp.off_bar + bar_region_bytes(ns);
-    mp.off_merge = mp.off_f + (int)align_up(sizeof(int) * (2 * d.B + 1), 16);
+    mp.off_merge = mp.off_f + (int)align_up(sizeof(int) * narr, 16);
     return true;
 }
 
@@ -1138,11 +1153,14 @@ inline int launch_mma_sv(void *stream, MmaParams &mp, const CUtensorMap &tv, int
 // Sets dp.n_ctas and launches the tensor-core decode (one CTA per SM by default).  With
 // `shared_v` every one of the dp.G groups of dp.r <= 4 heads reads the same value row of
 // width dp.d_h in {128, 256} (the latent rows of the MLA-shaped decode).
+// With hold_pos (and early), the preceding grid also appends row hold_pos[b] of each
+// sequence b: the cache streams early except for the slabs holding those rows.
 inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms, int req_ctas,
-                   bool gqa, bool early, bool shared_v = false) {
+                   bool gqa, bool early, bool shared_v = false, const int *hold_pos = nullptr) {
     if (rows.num_rows > 0x7fffffffLL) return GVA_ERR_UNSUPPORTED;   // TMA row coordinate is int32
     MmaParams mp;
     mp.d = dp;
+    mp.hold_pos = early ? hold_pos : nullptr;
     const int DH = dp.d_h, DR = gqa ? 0 : dp.d_r;
     const int NT = dp.r <= 4 ? 1 : 2;   // 8-column tiles holding the group's heads (hi, lo)
     if (shared_v && (gqa || NT != 1 || (DH != 128 && DH != 256))) return GVA_ERR_UNSUPPORTED;

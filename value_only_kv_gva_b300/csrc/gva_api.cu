@@ -784,8 +784,9 @@ struct StepAppend {
 
 // One layer's decode, after the append of `app` when it is given: with the tensor-core
 // decode and a shape the fused kernel takes, the append runs in the absorption's grid
-// and the decode reads the cache only after that grid has completed; otherwise the
-// append kernel runs first.
+// and the decode streams the cache meanwhile, except for the slab that holds each
+// sequence's new row (copied once that grid has completed); otherwise the append kernel
+// runs first.
 static int decode_call(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
                        const float *M, const int *seq_len, const gva_cache *cache,
                        const float *rope_tab, int rope_max_pos, float scale, float *out,
@@ -868,9 +869,10 @@ static int decode_call(void *stream, const gva_dims *d, const void *q_nope, cons
     dp.n_ctas = 0;
     dp.prefix_ws = reinterpret_cast<int *>(w + plan.pf);
     if (use_mma) {
-        // `early` (stream the cache before the grid dependency resolves) only when the
-        // preceding grid does not write the cache
-        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, !fused);
+        // the cache streams before the grid dependency resolves; after the fused grid,
+        // which also appends, the slab holding each sequence's new row waits for it
+        st = run_mma(stream, dp, cache->rows, sms, o->num_ctas, false, true, false,
+                     fused ? app->pos : nullptr);
     } else if (d->cache_dtype == GVA_F32) {
         st = run_simt<float, false>(stream, dp, sms, o->num_ctas);
     } else {
