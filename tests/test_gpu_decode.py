@@ -468,6 +468,7 @@ STEP_CASES = {
     "350m": ("350m", {}), "paged": ("paged", {}), "tiny": ("tiny", {}),
     "ragged": ("ragged", {}), "long": ("long", {}),
     "350m_f32_query": ("350m", dict(q_dtype="f32")),
+    "350m_dn32": ("350m", dict(d_n=32)),      # tensor-core path, separate append kernel
 }
 
 
