@@ -357,8 +357,9 @@ int gva_rope_keys_decode_attention(void *stream, const gva_dims *dims, const voi
  *     workspace (gva_decode_workspace_size) exceeds it return GVA_ERR_WORKSPACE.
  *   - Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device resolves the array's device address (set-up); make
- *     that first call before any stream capture.  `stream` must belong to the current
- *     device (else GVA_ERR_CUDA).
+ *     that first call before any stream capture, after which the call can be captured
+ *     into a CUDA graph (tested).  `stream` must belong to the current device (else
+ *     GVA_ERR_CUDA); while `stream` is capturing, its device is taken to be that of `out`.
  *   - Every call on a device shares the one array, and its contents persist from the
  *     previous call.  The call takes the automatic path, which writes every scratch
  *     value before it reads it, so nothing in the array has to start at any value.

@@ -68,3 +68,39 @@ def test_static_scratch_rejects_oversize():
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), ctypes.byref(d), p, p, p, p,
         ctypes.byref(cc), p, 1, ctypes.c_float(0.1), p, None)
     assert st == g.GVA_ERR_WORKSPACE
+
+
+def test_static_scratch_in_a_graph():
+    """The reason the entry exists: a warm call, then the static call recorded into a CUDA
+    graph and replayed twice, with new query contents written in place before the second
+    replay; each replay equals the workspace entry on the same contents bit for bit."""
+    c = make_case(workload("350m", T=500, B=4))
+    D = Dev(c)
+    w = c.w
+    out = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+    lse = torch.full((w.B, w.H), float("nan"), device="cuda")
+    _static_call(D, out, lse)                  # the one-time set-up, outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            _static_call(D, out, lse)
+    for it in range(2):
+        if it == 1:
+            D.q_nope.mul_(-0.5)                # new contents, same storage
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gva().gva_get_device_status() == 0
+        ref_out, ref_lse = D.decode()
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref_out), f"replay {it}"
+        assert np.array_equal(lse.cpu().numpy().astype(np.float64), ref_lse), f"replay {it}"
+    q = c.q_nope.clone()
+    c.q_nope.mul_(-0.5)                        # the oracle on the second replay's queries
+    o_ref, l_ref = oracle_decode(c)
+    c.q_nope.copy_(q)
+    assert_close(out.cpu().numpy().astype(np.float64), o_ref, "bf16", "graph replay out vs oracle")
+    assert_close(lse.cpu().numpy().astype(np.float64), l_ref, "bf16", "graph replay lse vs oracle")

@@ -1150,6 +1150,11 @@ int gva_prefill_attention(void *stream, const gva_dims *d, int n, const void *q_
             tp.p = mp;
             tp.p.splits = pp.tc_splits;
             tp.tickets = reinterpret_cast<int *>(w + pp.tk);   // zeroed by the append
+            // the order matters only when the grid takes more than one wave (one CTA per
+            // SM): then the longest sequences' ranges should start in the first
+            tp.by_length = d->B > 1 && d->B <= PT_ORDER_MAX &&
+                                   (long long)pp.tc_splits * d->G * d->B > sms
+                               ? 1 : 0;
             tp.ch = R.layout == GVA_LAYOUT_PAGED ? gcd_int(R.page_size, 64) : 64;
             CUtensorMap tv, tk;
             if (!prefill_tc_maps(&tv, &tk, cache->V, cache->K_rope, R.num_rows, d->G * d->d_h,
@@ -1427,9 +1432,20 @@ int gva_decode_attention_static(void *stream, const gva_dims *d, const void *q_n
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess && stream != nullptr) {
-        // the scratch handed to the kernels must be the stream's device's own copy
+        // the scratch handed to the kernels must be the stream's device's own copy.  A
+        // capturing stream cannot be asked for its device; the output buffer, which the
+        // kernels write on that device, stands for it then.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
         int sdev = -1;
-        e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+        if (e == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+            e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+        } else if (e == cudaSuccess) {
+            cudaPointerAttributes pa;
+            e = cudaPointerGetAttributes(&pa, out);
+            if (e == cudaSuccess && pa.type != cudaMemoryTypeDevice) e = cudaErrorInvalidValue;
+            sdev = pa.device;
+        }
         if (e == cudaSuccess && sdev != dev) e = cudaErrorInvalidDevice;
     }
     if (e != cudaSuccess) {

@@ -47,7 +47,12 @@ struct PrefillTcParams {
     int smem_bytes;
     int *tickets;         // [B][G], zero at launch: the last CTA of each (value group,
                           //   sequence) merges its ranges; null: a merge kernel follows
+    int by_length;        // 1: the kernel instance in which CTA z takes the sequence with
+                          //   the z-th most tiles (B <= PT_ORDER_MAX), so that the longest
+                          //   ranges start first
 };
+
+constexpr int PT_ORDER_MAX = 256;
 
 // Shared-memory matrix descriptor: layout 2 = 128-byte swizzle (rows of 128 B), 4 = 64-byte,
 // 6 = 32-byte; sbo = bytes between groups of 8 rows, lbo = bytes between 64-element blocks
@@ -134,6 +139,35 @@ __device__ __forceinline__ uint32_t pt_chunk(int r, int c, int rows) {
     return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// 128-token tiles of sequence b once the chunk is appended: positions up to L0[b] + n,
+// capped by the capacity; none when L0[b] is out of range (the kernel's own rule).
+__device__ __forceinline__ int pt_tiles(const PrefillMmaParams &p, int b) {
+    const long long l0 = p.L0[b];
+    const long long cap = min(seq_capacity(p.R, b), 0x7fffffffLL);
+    const long long Lt = (l0 >= 0 && l0 <= cap) ? min(l0 + p.n, cap) : 0;
+    return (int)((Lt + PT_TILE - 1) / PT_TILE);
+}
+
+// The sequence CTA z of the grid takes when the grid is ordered by length: sequences
+// ranked by tile count, most first, ties by index (a permutation).  The tile counts are
+// staged in `scratch` (B + 1 ints).  Called by every thread of the CTA.
+__device__ __forceinline__ int pt_seq_by_length(const PrefillMmaParams &p, int *scratch, int tid,
+                                                int nthreads) {
+    for (int bb = tid; bb < p.B; bb += nthreads) scratch[bb] = pt_tiles(p, bb);
+    __syncthreads();
+    for (int bb = tid; bb < p.B; bb += nthreads) {
+        const int t = scratch[bb];
+        int rank = 0;
+        for (int o = 0; o < p.B; ++o) {
+            const int u = scratch[o];
+            rank += (u > t || (u == t && o < bb)) ? 1 : 0;
+        }
+        if (rank == (int)blockIdx.z) scratch[p.B] = bb;   // exactly one thread
+    }
+    __syncthreads();
+    return scratch[p.B];
+}
+
 template <int DH, int DR, int M>
 struct PtSmem {
     static constexpr int KQ = DH / 64 + (DR > 0 ? 1 : 0);   // 64-wide K-blocks of a query row
@@ -157,7 +191,7 @@ struct PtSmem {
 // handles quarter pt = w >> 2 of each tile's 128 columns and of O's d_h columns; the four
 // warps of a quadrant exchange their rows' partial maxima (a 128-thread barrier).  Warp 16
 // is the TMA producer, warp 17 the MMA issuer.
-template <int DH, int DR, int M>
+template <int DH, int DR, int M, bool ORD>
 __global__ void __launch_bounds__(PT_THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_k, const PrefillTcParams tp) {
@@ -189,7 +223,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     volatile int *abort = reinterpret_cast<volatile int *>(tail + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, g = blockIdx.y;
+    // ORD: CTAs start in block order, so CTA z takes the sequence with the z-th most tiles
+    // (its tile counts staged in the first ring stage, which no copy has reached yet; the
+    // start positions and capacities are inputs no kernel of the call writes)
+    const int b = ORD ? pt_seq_by_length(p, reinterpret_cast<int *>(sm + (st_s - base)), tid,
+                                         PT_THREADS)
+                      : (int)blockIdx.z;
     const int nrows = p.n * p.r;
     if (tid == 0) GVA_TRACE_AT(0);
     if (tid == 0) {
@@ -878,8 +918,11 @@ inline cudaError_t prefill_tc_launch_t(void *stream, PrefillTcParams &tp, const 
     if (tp.tickets && (2 * nrows * tp.p.splits + 2 * nrows) * 4 > (long long)SM::PB * 2 * SM::PPART)
         tp.tickets = nullptr;
     const dim3 grid(tp.p.splits, tp.p.G, tp.p.B);
-    cudaError_t e = launch(prefill_tc_kernel<DH, DR, M>, grid, dim3(PT_THREADS), (size_t)tp.smem_bytes,
-                           stream, tv, tk, tp);
+    cudaError_t e = tp.by_length
+                        ? launch(prefill_tc_kernel<DH, DR, M, true>, grid, dim3(PT_THREADS),
+                                 (size_t)tp.smem_bytes, stream, tv, tk, tp)
+                        : launch(prefill_tc_kernel<DH, DR, M, false>, grid, dim3(PT_THREADS),
+                                 (size_t)tp.smem_bytes, stream, tv, tk, tp);
     if (e != cudaSuccess || tp.tickets != nullptr) return e;
     const long long rows = (long long)tp.p.B * tp.p.n * tp.p.H;
     const dim3 cg((unsigned)((rows + PF_COMBINE_WARPS - 1) / PF_COMBINE_WARPS));
@@ -908,9 +951,12 @@ inline cudaError_t prefill_tc_launch(void *stream, int d_h, int d_r, int M, Pref
 
 template <int DH, int M>
 inline cudaError_t prefill_tc_opt_in_dm() {
-    const void *ks[] = {(const void *)prefill_tc_kernel<DH, 0, M>, (const void *)prefill_tc_kernel<DH, 8, M>,
-                        (const void *)prefill_tc_kernel<DH, 16, M>, (const void *)prefill_tc_kernel<DH, 24, M>,
-                        (const void *)prefill_tc_kernel<DH, 32, M>};
+    const void *ks[] = {
+        (const void *)prefill_tc_kernel<DH, 0, M, false>, (const void *)prefill_tc_kernel<DH, 8, M, false>,
+        (const void *)prefill_tc_kernel<DH, 16, M, false>, (const void *)prefill_tc_kernel<DH, 24, M, false>,
+        (const void *)prefill_tc_kernel<DH, 32, M, false>, (const void *)prefill_tc_kernel<DH, 0, M, true>,
+        (const void *)prefill_tc_kernel<DH, 8, M, true>, (const void *)prefill_tc_kernel<DH, 16, M, true>,
+        (const void *)prefill_tc_kernel<DH, 24, M, true>, (const void *)prefill_tc_kernel<DH, 32, M, true>};
     for (const void *k : ks) {
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_LIMIT);
         if (e != cudaSuccess) return e;
