@@ -643,7 +643,8 @@ def _prefill_design(w, n: int, path: str) -> str:
                 "holds the group's chunk rows, streams 128-token tiles of its rows once "
                 "(TMA), S = Q V^T and O += P V accumulate in tensor memory (P's bf16 high and "
                 "low parts stacked as one 128-row product), online softmax in 16 warps; "
-                "ranges merged by log-sum-exp in the last CTA of each (group, sequence)")
+                "ranges merged by log-sum-exp in the last CTA of each (group, sequence); "
+                "a grid of more than one wave starts the longest sequences' ranges first")
     return ("mma.sync prefill kernel: each 16-token slab of a sequence's rows loaded once "
             "per CTA and scored against all the chunk's (query, head) rows, split over the "
             "history and merged by log-sum-exp")
