@@ -173,9 +173,9 @@ void od_absorb(int B, int H, int d_h, int d_n, int d_r,
 /* Query RMSNorm  ([A] 实验: "GVA scale-matched + query RMSNorm"; [S] results   */
 /* table "GVA, scale-matched + query RMSNorm")                                  */
 /* ------------------------------------------------------------------------- */
-/* The pages name the variant without its formula.  Reading (listed in the design
- * notes): each head's content query is divided by its root mean square over its
- * d_n values, then multiplied by a per-dimension gain (ones when gain is NULL):
+/* The pages name the variant without its formula.  The reading taken here, the
+ * ordinary RMSNorm: each head's content query is divided by its root mean square over
+ * its d_n values, then multiplied by a per-dimension gain (ones when gain is NULL):
  *   y[b,h,k] = gain[k] * x[b,h,k] / sqrt( (1/d_n) sum_k' x[b,h,k']^2 + eps )
  * The positional query is not normalised. */
 void od_query_rmsnorm(int B, int H, int d_n, const double *x, const double *gain, double eps,
