@@ -469,6 +469,8 @@ STEP_CASES = {
     "ragged": ("ragged", {}), "long": ("long", {}),
     "350m_f32_query": ("350m", dict(q_dtype="f32")),
     "350m_dn32": ("350m", dict(d_n=32)),      # tensor-core path, separate append kernel
+    # the largest batch: the held slabs' indices take another 16 KB of shared memory
+    "350m_b4096": ("350m", dict(B=4096, T=40, H=4, G=2, d_h=64, d_n=64, d_r=16)),
 }
 
 
@@ -481,7 +483,7 @@ def test_decode_step_matches_per_layer_calls(case):
     the absorption's grid (bf16 and fp32 queries), on the others as its own kernel."""
     g = gva()
     name, extra = STEP_CASES[case]
-    c = make_case(workload(name, **SMALL[name], **extra))
+    c = make_case(workload(name, **{**SMALL[name], **extra}))
     pos = (c.seq_len - 1).to(torch.int32).cuda()
     a = [Dev(c) for _ in range(3)]          # per-layer calls
     s = [Dev(c) for _ in range(3)]          # one step call
