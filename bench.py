@@ -739,38 +739,28 @@ def run_prefill(args, dist: Dist):
     gbs = nbytes / (us_call * 1e-6) / 1e9
     tflops = flops / (us_call * 1e-6) / 1e12
 
-    # end to end: pinned host chunk inputs in, every layer's outputs out, the recorded plan
-    h_in = [t.unsqueeze(0).expand((nl,) + tuple(t.shape)).contiguous().pin_memory()
-            for t in (ch.q_nope, ch.q_rope, ch.v_new, ch.k_new)]
-    h_out = torch.empty(tuple(d_out.shape), dtype=torch.float32).pin_memory()
-    cur = torch.cuda.current_stream()
+    # end to end: pinned host chunk inputs in, every layer's outputs out, the recorded plans
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-
-    plan = gva.create_prefill_plan(
-        dims, n, [dict(q_nope=d_in[0][li], q_rope=d_in[1][li], M=L["M"], v_new=d_in[2][li],
-                       k_rope_new=d_in[3][li], cache=L["cache"], out=d_out[li], lse=d_lse[li])
-                  for li, L in enumerate(layers)], L0d, tab, w.scale, ws, path=path)
-
-    def one_step():
-        for dst, src in zip(d_in, h_in):
-            dst.copy_(src, non_blocking=True)
-        plan.launch(cur)
-        h_out.copy_(d_out, non_blocking=True)
-        cur.synchronize()
-
+    lp = PackedLoop(torch, dev, (ch.q_nope, ch.q_rope, ch.v_new, ch.k_new), nl, d_out,
+                    args.e2e_chunks or 4)
+    lp.record(lambda a, b, view: gva.create_prefill_plan(
+        dims, n, [dict(q_nope=view(li, 0), q_rope=view(li, 1), M=layers[li]["M"],
+                       v_new=view(li, 2), k_rope_new=view(li, 3), cache=layers[li]["cache"],
+                       out=d_out[li], lse=d_lse[li]) for li in range(a, b)],
+        L0d, tab, w.scale, ws, path=path))
     for _ in range(3):
-        one_step()
+        lp.step()
     dist.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        one_step()
+        lp.step()
     te = dist.max(time.perf_counter() - t0, dev)
+    lp.close()
     e2e = {"value": round(w.B * n * nl * e2e_steps * dist.world / te, 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
-           "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": e2e_steps,
-           "how": "one gva_step_plan_launch per step (the chunk's prefill through every "
-                  "layer, recorded once by gva_prefill_plan_create); pinned host chunk inputs "
-                  "and every layer's outputs copied inside the timed region"}
+           "h2d_bytes_per_step": lp.h2d_bytes, "d2h_bytes_per_step": lp.d2h_bytes,
+           "steps": e2e_steps, "chunks": lp.nch,
+           "how": lp.how("each the chunk's prefill through a chunk of layers, recorded once "
+                         "by gva_prefill_plan_create")}
 
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
@@ -881,94 +871,114 @@ def capture_list(torch, stream, items, fn):
     return g
 
 
-def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, bytes_layer,
-            dist):
-    """Same metric through the public API: every step copies its inputs from pinned host
-    memory, launches step plans (gva_step_plan_create recorded each chunk of layers'
-    append and decode once; gva_step_plan_launch replays a chunk with one call), and reads
-    every layer's output back, all inside the timed region.  A layer's four inputs sit in
-    one 256-byte-aligned region of a packed buffer, so a chunk of layers moves in one
-    copy.  With more than one chunk (--e2e-chunks) the copies overlap the compute as in a
-    serving loop: chunk i + 1's inputs arrive on one copy stream while chunk i computes,
-    and chunk i's outputs leave on a second while chunk i + 1 computes."""
-    nl = len(layers)
-    stream = torch.cuda.current_stream()
-    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    srcs = (c.q_nope, c.q_rope, c.v_new, c.k_new)
-    sizes = [t.numel() * t.element_size() for t in srcs]
-    offs, o = [], 0
-    for n in sizes:
-        offs.append(o)
-        o += (n + 255) // 256 * 256
-    per_layer = o
-    h_pack = torch.empty((nl, per_layer), dtype=torch.uint8).pin_memory()
-    for li in range(nl):
-        for t, off, n in zip(srcs, offs, sizes):
-            h_pack[li, off:off + n].copy_(t.contiguous().view(-1).view(torch.uint8))
-    d_pack = torch.empty((nl, per_layer), dtype=torch.uint8, device=dev)
+class PackedLoop:
+    """The end-to-end loop shared by the decode and prefill legs.  Every layer's inputs
+    (the tensors `srcs`, the same for each layer) sit in one 256-byte-aligned region of a
+    pinned host buffer and of a device buffer, so a chunk of layers moves in one copy;
+    `make_plan(a, b, view)` records layers a..b-1 as one plan, `view(li, k)` being layer
+    li's device copy of srcs[k].  A step copies the inputs in, launches the plans and
+    copies `d_out` back, all inside the caller's timed region.  With more than one chunk
+    the copies overlap the compute: chunk i + 1's inputs arrive on one copy stream while
+    chunk i computes, and chunk i's outputs leave on a second while chunk i + 1 computes."""
 
-    def view(li, k):
-        t = srcs[k]
-        return d_pack[li, offs[k]:offs[k] + sizes[k]].view(t.dtype).view(t.shape)
+    def __init__(self, torch, dev, srcs, nl, d_out, nch):
+        self.torch = torch
+        self.stream = torch.cuda.current_stream()
+        self.h2d_s, self.d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        self.srcs = srcs
+        self.sizes = [t.numel() * t.element_size() for t in srcs]
+        self.offs, o = [], 0
+        for n in self.sizes:
+            self.offs.append(o)
+            o += (n + 255) // 256 * 256
+        self.per_layer = o
+        self.h_pack = torch.empty((nl, o), dtype=torch.uint8).pin_memory()
+        for li in range(nl):
+            for t, off, n in zip(srcs, self.offs, self.sizes):
+                self.h_pack[li, off:off + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+        self.d_pack = torch.empty((nl, o), dtype=torch.uint8, device=dev)
+        self.d_out = d_out
+        self.h_out = torch.empty(tuple(d_out.shape), dtype=d_out.dtype).pin_memory()
+        self.nch = max(1, min(nch, nl))
+        bounds = [nl * i // self.nch for i in range(self.nch + 1)]
+        self.chunks = [(bounds[i], bounds[i + 1]) for i in range(self.nch)]
+        self.ev_in = [torch.cuda.Event() for _ in self.chunks]
+        self.ev_done = [torch.cuda.Event() for _ in self.chunks]
+        self.plans = []
+        self.h2d_bytes = nl * o
+        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
 
-    d_out = torch.empty((nl, w.B, w.H, w.d_h), dtype=torch.float32, device=dev)
-    d_lse = torch.empty((nl, w.B, w.H), dtype=torch.float32, device=dev)
-    h_out = torch.empty((nl, w.B, w.H, w.d_h), dtype=torch.float32).pin_memory()
-    step_layers = [dict(q_nope=view(li, 0), q_rope=view(li, 1), v_new=view(li, 2),
-                        k_rope_new=view(li, 3), M=L["M"], cache=L["cache"], out=d_out[li],
-                        lse=d_lse[li])
-                   for li, L in enumerate(layers)]
-    nch = max(1, min(args.e2e_chunks, nl))
-    bounds = [nl * i // nch for i in range(nch + 1)]
-    chunks = [(bounds[i], bounds[i + 1]) for i in range(nch)]
-    plans = [gva.create_step_plan(dims, step_layers[a:b], pos, seq, tab, w.scale, ws, path=path)
-             for a, b in chunks]
-    h2d = nl * per_layer          # the bytes the packed copies move
-    d2h = h_out.numel() * h_out.element_size()
-    steps = max(3, min(args.steps, args.e2e_steps))
-    ev_in = [torch.cuda.Event() for _ in chunks]
-    ev_done = [torch.cuda.Event() for _ in chunks]
+    def view(self, li, k):
+        t = self.srcs[k]
+        return self.d_pack[li, self.offs[k]:self.offs[k] + self.sizes[k]].view(t.dtype).view(t.shape)
 
-    def one_step():
-        if nch == 1:
-            d_pack.copy_(h_pack, non_blocking=True)
-            plans[0].launch(stream)
-            h_out.copy_(d_out, non_blocking=True)
+    def record(self, make_plan):
+        self.plans = [make_plan(a, b, self.view) for a, b in self.chunks]
+
+    def step(self):
+        torch, stream = self.torch, self.stream
+        if self.nch == 1:
+            self.d_pack.copy_(self.h_pack, non_blocking=True)
+            self.plans[0].launch(stream)
+            self.h_out.copy_(self.d_out, non_blocking=True)
             stream.synchronize()
             return
-        with torch.cuda.stream(h2d_s):
-            for i, (a, b) in enumerate(chunks):
-                d_pack[a:b].copy_(h_pack[a:b], non_blocking=True)
-                ev_in[i].record(h2d_s)
-        for i, (a, b) in enumerate(chunks):
-            stream.wait_event(ev_in[i])
-            plans[i].launch(stream)
-            ev_done[i].record(stream)
-            with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(ev_done[i])
-                h_out[a:b].copy_(d_out[a:b], non_blocking=True)
-        d2h_s.synchronize()
+        with torch.cuda.stream(self.h2d_s):
+            for i, (a, b) in enumerate(self.chunks):
+                self.d_pack[a:b].copy_(self.h_pack[a:b], non_blocking=True)
+                self.ev_in[i].record(self.h2d_s)
+        for i, (a, b) in enumerate(self.chunks):
+            stream.wait_event(self.ev_in[i])
+            self.plans[i].launch(stream)
+            self.ev_done[i].record(stream)
+            with torch.cuda.stream(self.d2h_s):
+                self.d2h_s.wait_event(self.ev_done[i])
+                self.h_out[a:b].copy_(self.d_out[a:b], non_blocking=True)
+        self.d2h_s.synchronize()
         stream.synchronize()
 
+    def close(self):
+        for pl in self.plans:
+            pl.close()
+
+    def how(self, what):
+        h = (f"{self.nch} gva_step_plan_launch C-ABI call(s) per step ({what}); pinned "
+             "host->device inputs (one packed copy per chunk of layers) and device->host "
+             "outputs of every layer inside the timed region")
+        return h + (", on two copy streams overlapping the chunks' compute" if self.nch > 1 else "")
+
+
+def run_e2e(args, w, c, dims, gva, torch, dev, layers, seq, pos, tab, ws, path, bytes_layer,
+            dist):
+    """Same metric through the public API (PackedLoop): every step copies its inputs from
+    pinned host memory, launches the step plans (gva_step_plan_create recorded each chunk
+    of layers' append and decode once; gva_step_plan_launch replays a chunk with one call)
+    and reads every layer's output back, all inside the timed region."""
+    nl = len(layers)
+    d_out = torch.empty((nl, w.B, w.H, w.d_h), dtype=torch.float32, device=dev)
+    d_lse = torch.empty((nl, w.B, w.H), dtype=torch.float32, device=dev)
+    lp = PackedLoop(torch, dev, (c.q_nope, c.q_rope, c.v_new, c.k_new), nl, d_out,
+                    args.e2e_chunks or 1)
+    lp.record(lambda a, b, view: gva.create_step_plan(
+        dims, [dict(q_nope=view(li, 0), q_rope=view(li, 1), v_new=view(li, 2),
+                    k_rope_new=view(li, 3), M=layers[li]["M"], cache=layers[li]["cache"],
+                    out=d_out[li], lse=d_lse[li]) for li in range(a, b)],
+        pos, seq, tab, w.scale, ws, path=path))
+    steps = max(3, min(args.steps, args.e2e_steps))
     for _ in range(3):
-        one_step()
+        lp.step()
     dist.barrier()
     t0 = time.perf_counter()
     for _ in range(steps):
-        one_step()
+        lp.step()
     t = dist.max(time.perf_counter() - t0, dev)
+    lp.close()
     val = bytes_layer * nl * steps * dist.world / t / 1e9
-    for pl in plans:
-        pl.close()
-    how = (f"{nch} gva_step_plan_launch C-ABI call(s) per step (each a chunk of layers' "
-           "append + decode, recorded once by gva_step_plan_create as a CUDA graph); pinned "
-           "host->device inputs (one packed copy per chunk) and device->host outputs of "
-           "every layer inside the timed region")
-    if nch > 1:
-        how += ", on two copy streams overlapping the chunks' compute"
-    return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 4),
-            "chunks": nch, "how": how}
+    return {"value": round(val, 2), "unit": "GB/s", "h2d_bytes_per_step": lp.h2d_bytes,
+            "d2h_bytes_per_step": lp.d2h_bytes, "steps": steps,
+            "ms_per_step": round(t / steps * 1e3, 4), "chunks": lp.nch,
+            "how": lp.how("each a chunk of layers' append + decode, recorded once by "
+                          "gva_step_plan_create as a CUDA graph")}
 
 
 def read_probe_gbs(gva, torch, stream, dev, gib: float = 4.0, reps: int = 10):
@@ -1086,8 +1096,10 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing (s)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--e2e-chunks", type=int, default=1,
-                    help="step plans per step in the end-to-end leg (copies overlap compute)")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="plans per step in the end-to-end leg, the copies overlapping the "
+                         "compute; 0: 1 for the decode step (bound by host calls), 4 for the "
+                         "prefill (bound by its 32 MB of copies)")
     ap.add_argument("--no-gqa", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--others", nargs="*", default=["long", "paged", "ragged"],
