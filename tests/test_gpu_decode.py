@@ -447,6 +447,40 @@ def test_gqa_refuses_query_rmsnorm():
     assert st == g.GVA_ERR_UNSUPPORTED
 
 
+def test_two_ctas_per_sm_ragged():
+    """A ragged cache long enough for the two-CTAs-per-SM plan (its row capacity gives every
+    CTA of twice the SM count at least 16 slabs): half the sequences of 1-40 tokens, half
+    of 2600-3200, so that shares cross many short sequences and partial slabs.  GVA and the
+    GQA comparator against the oracle, every sequence and head."""
+    g = gva()
+    gen = np.random.default_rng(11)
+    B = 64
+    lengths = [int(x) for x in gen.integers(1, 41, B // 2)] + \
+              [int(x) for x in gen.integers(2600, 3201, B // 2)]
+    gen.shuffle(lengths)
+    c = make_case(workload("ragged", B=B), lengths=lengths)
+    assert c.num_rows // 16 >= 2 * g.gva_num_sms() * 16      # the plan takes two CTAs per SM
+    D = Dev(c)
+    out, lse = D.decode(path="auto")
+    assert g.gva_get_device_status() == 0
+    ref, ref_lse = oracle_decode(c)
+    assert_close(out, ref, "bf16", "two CTAs per SM out")
+    assert_close(lse, ref_lse, "bf16", "two CTAs per SM lse")
+    w = c.w
+    K = make_gqa_keys(c)
+    q = make_gqa_query(c)
+    kv = g.KVCache(D.rows, K.cuda(), D.V)
+    scale = 1.0 / np.sqrt(w.d_h)
+    gref, gref_lse = oracle.gqa_decode(q, c.seq_len, oracle_rows(c), K, c.V, scale, w.G)
+    gout = torch.full((w.B, w.H, w.d_h), float("nan"), device="cuda")
+    glse = torch.full((w.B, w.H), float("nan"), device="cuda")
+    g.gva_gqa_decode_attention(D.dims, q.cuda(), D.seq_len, kv, scale, gout, glse, D.ws, path="auto")
+    torch.cuda.synchronize()
+    assert g.gva_get_device_status() == 0
+    assert_close(gout.cpu().numpy(), gref, "bf16", "two CTAs per SM gqa out")
+    assert_close(glse.cpu().numpy(), gref_lse, "bf16", "two CTAs per SM gqa lse")
+
+
 def test_largest_batch():
     """B = 4096, the largest batch the in-kernel prefix handles (its lengths and slab
     offsets take 32 KB of shared memory, shrinking the ring): every path, mixed lengths

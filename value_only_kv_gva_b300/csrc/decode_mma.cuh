@@ -624,8 +624,10 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
 // ---------------------------------------------------------------------------- //
 // the kernel
 // ---------------------------------------------------------------------------- //
-template <int DH, int DR, bool GQA, int NT, bool SV = false>
-__global__ void __launch_bounds__(MMA_THREADS, 1)
+// MINB = 2: the instance that runs two CTAs per SM (the registers of two CTAs of the
+// launched size within the SM's 64 K), each with a ring half as large.
+template <int DH, int DR, bool GQA, int NT, bool SV = false, int MINB = 1>
+__global__ void __launch_bounds__(MINB == 1 ? MMA_THREADS : (MMA_CONSUMERS + 1) * 32, MINB)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_k, const MmaParams mp) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1015,6 +1017,16 @@ constexpr int MMA_SMEM_LIMIT = 227 * 1024;
 // precedes the decode: with programmatic dependent launch the decode's CTAs start
 // while that grid's CTAs are still resident, and stream the cache meanwhile.
 constexpr int MMA_SMEM_TARGET = 196 * 1024;
+// Two CTAs per SM: each within half of the SM's 228 KB (less the per-CTA reservation).
+// Taken when the cache's capacity gives each of the 2 x SMs CTAs at least
+// MMA_PAIR_MIN_SLABS slabs and the half-size ring still holds MMA_PAIR_MIN_STAGES: a long
+// share streams while the other CTA of its SM starts or ends, and an SM's time is the
+// sum of two shares, so the spread of CTA ends shrinks.  Measured on the ragged batch
+// (d_h = 64, about 30 slabs per CTA): 26.6 against 29.8 µs per decode op; on the 350M
+// layer (7 slabs per CTA) it is slower, 14.3 against 13.8 µs.
+constexpr int MMA_SMEM_PAIR = 108 * 1024;
+constexpr int MMA_PAIR_MIN_SLABS = 16;
+constexpr int MMA_PAIR_MIN_STAGES = 6;
 
 inline int bar_region_bytes(int ns) { return (int)align_up(16 * ns + 16 + 4 * ns, 16); }
 
@@ -1023,7 +1035,10 @@ inline int merge_bytes_of(int wpg, int G, int DH, int NT) {
     return (wpg - 1) * G * 4 * NT * (DH + 2) * 4;
 }
 
-inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
+// `target`: the shared memory the ring is sized for; with `strict` the plan keeps to it
+// (no fallback to the per-CTA maximum).
+inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT,
+                     int target = MMA_SMEM_TARGET, bool strict = false) {
     const DecodeParams &d = mp.d;
     const int vbytes = mp.vg * DH * SLAB * 2;
     mp.off_k = vbytes;
@@ -1038,8 +1053,8 @@ inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT) {
     const int narr = (mp.hold_pos ? 3 : 2) * d.B + 1;   // Ls, F (and Hs) in shared memory
     const int fixed = 1024 /* alignment slack */ + (int)align_up(sizeof(int) * narr, 16) +
                       merge_bytes + bar_region_bytes(MMA_MAX_STAGES);
-    int ns = (MMA_SMEM_TARGET - fixed) / mp.stage_bytes;
-    if (ns < 4) ns = (MMA_SMEM_LIMIT - fixed) / mp.stage_bytes;
+    int ns = (target - fixed) / mp.stage_bytes;
+    if (ns < 4 && !strict) ns = (MMA_SMEM_LIMIT - fixed) / mp.stage_bytes;
     if (ns > MMA_MAX_STAGES) ns = MMA_MAX_STAGES;
     // Warp w of a group takes the share's slabs w, w + wpg, ... and slab i sits in stage
     // i mod ns, so with ns a multiple of wpg every round of a stage goes to the same
@@ -1063,10 +1078,10 @@ inline size_t mma_smem_bytes(const MmaParams &mp, int DH, int NT) {
     return 1024 + (size_t)mp.off_merge + merge_bytes_of(mp.wpg, mp.d.G, DH, NT);
 }
 
-template <int DH, int DR, bool GQA, int NT, bool SV = false>
+template <int DH, int DR, bool GQA, int NT, bool SV = false, int MINB = 1>
 inline int launch_mma_t(void *stream, MmaParams &mp, const CUtensorMap &tv, const CUtensorMap &tk,
                         int grid) {
-    auto kern = decode_mma_kernel<DH, DR, GQA, NT, SV>;
+    auto kern = decode_mma_kernel<DH, DR, GQA, NT, SV, MINB>;
     const size_t smem = mma_smem_bytes(mp, DH, NT);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -1114,8 +1129,23 @@ inline cudaError_t mma_opt_in_sv() {
     }
     return cudaSuccess;
 }
+inline cudaError_t mma_opt_in_pair() {
+    const void *ks[] = {(const void *)decode_mma_kernel<64, 0, false, 1, false, 2>,
+                        (const void *)decode_mma_kernel<64, 8, false, 1, false, 2>,
+                        (const void *)decode_mma_kernel<64, 16, false, 1, false, 2>,
+                        (const void *)decode_mma_kernel<64, 24, false, 1, false, 2>,
+                        (const void *)decode_mma_kernel<64, 32, false, 1, false, 2>,
+                        (const void *)decode_mma_kernel<64, 0, true, 1, false, 2>};
+    for (const void *k : ks) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_PAIR);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 inline cudaError_t mma_opt_in_all() {
-    cudaError_t e = mma_opt_in_sv<128>();
+    cudaError_t e = mma_opt_in_pair();
+    if (e == cudaSuccess) e = mma_opt_in_sv<128>();
     if (e == cudaSuccess) e = mma_opt_in_sv<256>();
     if (e == cudaSuccess) e = mma_opt_in_dh<64, 1>();
     if (e == cudaSuccess) e = mma_opt_in_dh<64, 2>();
@@ -1124,16 +1154,16 @@ inline cudaError_t mma_opt_in_all() {
     return e;
 }
 
-template <int DH, int NT>
+template <int DH, int NT, int MINB = 1>
 inline int launch_mma_dr(void *stream, MmaParams &mp, const CUtensorMap &tv, const CUtensorMap &tk,
                          int grid, int DR, bool gqa) {
-    if (gqa) return launch_mma_t<DH, 0, true, NT>(stream, mp, tv, tk, grid);
+    if (gqa) return launch_mma_t<DH, 0, true, NT, false, MINB>(stream, mp, tv, tk, grid);
     switch (DR) {
-    case 0: return launch_mma_t<DH, 0, false, NT>(stream, mp, tv, tk, grid);
-    case 8: return launch_mma_t<DH, 8, false, NT>(stream, mp, tv, tk, grid);
-    case 16: return launch_mma_t<DH, 16, false, NT>(stream, mp, tv, tk, grid);
-    case 24: return launch_mma_t<DH, 24, false, NT>(stream, mp, tv, tk, grid);
-    case 32: return launch_mma_t<DH, 32, false, NT>(stream, mp, tv, tk, grid);
+    case 0: return launch_mma_t<DH, 0, false, NT, false, MINB>(stream, mp, tv, tk, grid);
+    case 8: return launch_mma_t<DH, 8, false, NT, false, MINB>(stream, mp, tv, tk, grid);
+    case 16: return launch_mma_t<DH, 16, false, NT, false, MINB>(stream, mp, tv, tk, grid);
+    case 24: return launch_mma_t<DH, 24, false, NT, false, MINB>(stream, mp, tv, tk, grid);
+    case 32: return launch_mma_t<DH, 32, false, NT, false, MINB>(stream, mp, tv, tk, grid);
     default: return GVA_ERR_UNSUPPORTED;
     }
 }
@@ -1165,7 +1195,18 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
     const int NT = dp.r <= 4 ? 1 : 2;   // 8-column tiles holding the group's heads (hi, lo)
     if (shared_v && (gqa || NT != 1 || (DH != 128 && DH != 256))) return GVA_ERR_UNSUPPORTED;
     mp.vg = shared_v ? 1 : dp.G;
-    if (!plan_mma(mp, DH, DR, gqa, NT)) return GVA_ERR_UNSUPPORTED;
+    // two CTAs per SM for long caches (the row capacity bounds the slabs from above)
+    bool pair = false;
+    if (!shared_v && DH == 64 && NT == 1 && req_ctas == 0 &&
+        rows.num_rows / SLAB >= 2LL * sms * MMA_PAIR_MIN_SLABS) {
+        MmaParams m2 = mp;
+        if (plan_mma(m2, DH, DR, gqa, NT, MMA_SMEM_PAIR, true) &&
+            m2.nstages >= MMA_PAIR_MIN_STAGES && mma_smem_bytes(m2, DH, NT) <= MMA_SMEM_PAIR) {
+            mp = m2;
+            pair = true;
+        }
+    }
+    if (!pair && !plan_mma(mp, DH, DR, gqa, NT)) return GVA_ERR_UNSUPPORTED;
     const long long nrows = rows.num_rows > 0 ? rows.num_rows : 1;
     CUtensorMap tv, tk;
     mp.early = early ? 1 : 0;
@@ -1176,10 +1217,11 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
         if (gqa && !make_map(&tk, dp.Kc, nrows, mp.vg * DH, 64, true)) return GVA_ERR_CUDA;
     }
     if (!gqa) tk = tv;
-    int grid = req_ctas > 0 ? req_ctas : sms;
+    int grid = pair ? 2 * sms : req_ctas > 0 ? req_ctas : sms;
     if (grid > sms * 8) grid = sms * 8;
     dp.n_ctas = grid;
     mp.d.n_ctas = grid;
+    if (pair) return launch_mma_dr<64, 1, 2>(stream, mp, tv, tk, grid, DR, gqa);
     if (shared_v)
         return DH == 128 ? launch_mma_sv<128>(stream, mp, tv, grid, DR)
                          : launch_mma_sv<256>(stream, mp, tv, grid, DR);
