@@ -308,20 +308,6 @@ AbsorbLaunch absorb_plan(const gva_dims *d, const void *q_nope, const void *q_ro
     return A;
 }
 
-int absorb_run(void *stream, const gva_dims *d, const AbsorbLaunch &A);
-
-int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
-                  const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
-                  float prescale, float *q_tilde, float *q_hat, int sms,
-                  const gva_rows *rows = nullptr, bool skip_rope = false,
-                  const gva_decode_opts *qn = nullptr, const int *L0 = nullptr,
-                  int chunk_n = 0) {
-    return absorb_run(stream, d,
-                      absorb_plan(d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
-                                  prescale, q_tilde, q_hat, sms, rows, skip_rope, qn, L0,
-                                  chunk_n));
-}
-
 int absorb_run(void *stream, const gva_dims *d, const AbsorbLaunch &A) {
     const AbsorbParams &p = A.p;
     const dim3 grid = A.grid;
@@ -347,6 +333,18 @@ int absorb_run(void *stream, const gva_dims *d, const AbsorbLaunch &A) {
                 : launch(absorb_kernel<__nv_bfloat16, 0>, grid, blk, smem, stream, p);
     }
     return cuda_status(e);
+}
+
+int absorb_launch(void *stream, const gva_dims *d, const void *q_nope, const void *q_rope,
+                  const float *M, const int *seq_len, const float *rope_tab, int rope_max_pos,
+                  float prescale, float *q_tilde, float *q_hat, int sms,
+                  const gva_rows *rows = nullptr, bool skip_rope = false,
+                  const gva_decode_opts *qn = nullptr, const int *L0 = nullptr,
+                  int chunk_n = 0) {
+    return absorb_run(stream, d,
+                      absorb_plan(d, q_nope, q_rope, M, seq_len, rope_tab, rope_max_pos,
+                                  prescale, q_tilde, q_hat, sms, rows, skip_rope, qn, L0,
+                                  chunk_n));
 }
 
 // The append's parameters (arguments validated by the caller).
