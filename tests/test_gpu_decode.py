@@ -447,25 +447,29 @@ def test_gqa_refuses_query_rmsnorm():
     assert st == g.GVA_ERR_UNSUPPORTED
 
 
-def test_two_ctas_per_sm_ragged():
-    """A ragged cache long enough for the two-CTAs-per-SM plan (its row capacity gives every
-    CTA of twice the SM count at least 16 slabs): half the sequences of 1-40 tokens, half
-    of 2600-3200, so that shares cross many short sequences and partial slabs.  GVA and the
-    GQA comparator against the oracle, every sequence and head."""
+@pytest.mark.parametrize("per_sm,long_len", [(2, (2600, 3201)), (3, (4000, 4601))])
+def test_several_ctas_per_sm_ragged(per_sm, long_len):
+    """Ragged caches long enough for the two- and three-CTAs-per-SM plans (the row capacity
+    gives every CTA of that many times the SM count at least 16 slabs; below the next
+    plan's threshold for two): half the sequences of 1-40 tokens, half long, so that shares
+    cross many short sequences and partial slabs.  GVA and the GQA comparator (whose larger
+    stages take the two-CTA plan in both cases) against the oracle, every sequence and
+    head."""
     g = gva()
     gen = np.random.default_rng(11)
     B = 64
     lengths = [int(x) for x in gen.integers(1, 41, B // 2)] + \
-              [int(x) for x in gen.integers(2600, 3201, B // 2)]
+              [int(x) for x in gen.integers(long_len[0], long_len[1], B // 2)]
     gen.shuffle(lengths)
     c = make_case(workload("ragged", B=B), lengths=lengths)
-    assert c.num_rows // 16 >= 2 * g.gva_num_sms() * 16      # the plan takes two CTAs per SM
+    slabs, sms = c.num_rows // 16, g.gva_num_sms()
+    assert slabs >= per_sm * sms * 16 and (per_sm == 3 or slabs < 3 * sms * 16)
     D = Dev(c)
     out, lse = D.decode(path="auto")
     assert g.gva_get_device_status() == 0
     ref, ref_lse = oracle_decode(c)
-    assert_close(out, ref, "bf16", "two CTAs per SM out")
-    assert_close(lse, ref_lse, "bf16", "two CTAs per SM lse")
+    assert_close(out, ref, "bf16", f"{per_sm} CTAs per SM out")
+    assert_close(lse, ref_lse, "bf16", f"{per_sm} CTAs per SM lse")
     w = c.w
     K = make_gqa_keys(c)
     q = make_gqa_query(c)
@@ -477,8 +481,8 @@ def test_two_ctas_per_sm_ragged():
     g.gva_gqa_decode_attention(D.dims, q.cuda(), D.seq_len, kv, scale, gout, glse, D.ws, path="auto")
     torch.cuda.synchronize()
     assert g.gva_get_device_status() == 0
-    assert_close(gout.cpu().numpy(), gref, "bf16", "two CTAs per SM gqa out")
-    assert_close(glse.cpu().numpy(), gref_lse, "bf16", "two CTAs per SM gqa lse")
+    assert_close(gout.cpu().numpy(), gref, "bf16", f"{per_sm} CTAs per SM gqa out")
+    assert_close(glse.cpu().numpy(), gref_lse, "bf16", f"{per_sm} CTAs per SM gqa lse")
 
 
 def test_largest_batch():

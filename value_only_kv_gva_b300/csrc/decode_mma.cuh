@@ -47,6 +47,7 @@ namespace gva {
 #define GVA_MMA_THREADS 512
 #endif
 constexpr int MMA_CONSUMERS = GVA_MMA_CONSUMERS;      // at most GVA_MMA_THREADS / 32 - 1
+constexpr int MMA_TRIPLE_CONSUMERS = 4;               // consumer warps of the three-per-SM plan
 constexpr int MMA_THREADS = GVA_MMA_THREADS;          // launch bound (512 -> <= 128 registers)
 static_assert((MMA_CONSUMERS + 1) * 32 <= MMA_THREADS, "consumer warps exceed the launch bound");
 constexpr float MMA_RESCALE_TH = 8.f;                 // log2 units
@@ -624,10 +625,14 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *tm_v, const CUte
 // ---------------------------------------------------------------------------- //
 // the kernel
 // ---------------------------------------------------------------------------- //
-// MINB = 2: the instance that runs two CTAs per SM (the registers of two CTAs of the
-// launched size within the SM's 64 K), each with a ring half as large.
+// MINB = 2 or 3: the instances that run two or three CTAs per SM (the registers of that
+// many CTAs of the launched size within the SM's 64 K), each with a smaller ring; three
+// per SM with MMA_TRIPLE_CONSUMERS consumer warps.
 template <int DH, int DR, bool GQA, int NT, bool SV = false, int MINB = 1>
-__global__ void __launch_bounds__(MINB == 1 ? MMA_THREADS : (MMA_CONSUMERS + 1) * 32, MINB)
+__global__ void __launch_bounds__(MINB == 1   ? MMA_THREADS
+                                  : MINB == 2 ? (MMA_CONSUMERS + 1) * 32
+                                              : (MMA_TRIPLE_CONSUMERS + 1) * 32,
+                                  MINB)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_k, const MmaParams mp) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1027,6 +1032,10 @@ constexpr int MMA_SMEM_TARGET = 196 * 1024;
 constexpr int MMA_SMEM_PAIR = 108 * 1024;
 constexpr int MMA_PAIR_MIN_SLABS = 16;
 constexpr int MMA_PAIR_MIN_STAGES = 6;
+// Three CTAs per SM, each with one consumer warp per value group (G <= 4) and a third of
+// the SM's shared memory, under the same rules: ragged batch 24.8 against 26.5 µs per
+// decode op with two CTAs per SM.
+constexpr int MMA_SMEM_TRIPLE = 72 * 1024;
 
 inline int bar_region_bytes(int ns) { return (int)align_up(16 * ns + 16 + 4 * ns, 16); }
 
@@ -1038,7 +1047,8 @@ inline int merge_bytes_of(int wpg, int G, int DH, int NT) {
 // `target`: the shared memory the ring is sized for; with `strict` the plan keeps to it
 // (no fallback to the per-CTA maximum).
 inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT,
-                     int target = MMA_SMEM_TARGET, bool strict = false) {
+                     int target = MMA_SMEM_TARGET, bool strict = false,
+                     int consumers = MMA_CONSUMERS) {
     const DecodeParams &d = mp.d;
     const int vbytes = mp.vg * DH * SLAB * 2;
     mp.off_k = vbytes;
@@ -1046,11 +1056,14 @@ inline bool plan_mma(MmaParams &mp, int DH, int DR, bool gqa, int NT,
     const int rbytes = DR * SLAB * 2;
     mp.tx_bytes = mp.off_r + rbytes;
     mp.stage_bytes = (int)align_up((size_t)mp.tx_bytes, 1024);
-    mp.wpg = MMA_CONSUMERS / d.G;
+    mp.wpg = consumers / d.G;
     if (mp.wpg < 1) mp.wpg = 1;
     mp.ncons = d.G * mp.wpg;
     const int merge_bytes = merge_bytes_of(mp.wpg, d.G, DH, NT);
-    const int narr = (mp.hold_pos ? 3 : 2) * d.B + 1;   // Ls, F (and Hs) in shared memory
+    // Ls, F (and Hs) in shared memory.  The several-CTAs-per-SM plans (strict) reserve Hs
+    // whether or not it is used: their choice, which sets the grid and so the order of
+    // the sums, is then the same for a decode call and the decode step's call.
+    const int narr = ((mp.hold_pos || strict) ? 3 : 2) * d.B + 1;
     const int fixed = 1024 /* alignment slack */ + (int)align_up(sizeof(int) * narr, 16) +
                       merge_bytes + bar_region_bytes(MMA_MAX_STAGES);
     int ns = (target - fixed) / mp.stage_bytes;
@@ -1143,8 +1156,23 @@ inline cudaError_t mma_opt_in_pair() {
     }
     return cudaSuccess;
 }
+inline cudaError_t mma_opt_in_triple() {
+    const void *ks[] = {(const void *)decode_mma_kernel<64, 0, false, 1, false, 3>,
+                        (const void *)decode_mma_kernel<64, 8, false, 1, false, 3>,
+                        (const void *)decode_mma_kernel<64, 16, false, 1, false, 3>,
+                        (const void *)decode_mma_kernel<64, 24, false, 1, false, 3>,
+                        (const void *)decode_mma_kernel<64, 32, false, 1, false, 3>,
+                        (const void *)decode_mma_kernel<64, 0, true, 1, false, 3>};
+    for (const void *k : ks) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MMA_SMEM_TRIPLE);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 inline cudaError_t mma_opt_in_all() {
     cudaError_t e = mma_opt_in_pair();
+    if (e == cudaSuccess) e = mma_opt_in_triple();
     if (e == cudaSuccess) e = mma_opt_in_sv<128>();
     if (e == cudaSuccess) e = mma_opt_in_sv<256>();
     if (e == cudaSuccess) e = mma_opt_in_dh<64, 1>();
@@ -1195,18 +1223,27 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
     const int NT = dp.r <= 4 ? 1 : 2;   // 8-column tiles holding the group's heads (hi, lo)
     if (shared_v && (gqa || NT != 1 || (DH != 128 && DH != 256))) return GVA_ERR_UNSUPPORTED;
     mp.vg = shared_v ? 1 : dp.G;
-    // two CTAs per SM for long caches (the row capacity bounds the slabs from above)
-    bool pair = false;
-    if (!shared_v && DH == 64 && NT == 1 && req_ctas == 0 &&
-        rows.num_rows / SLAB >= 2LL * sms * MMA_PAIR_MIN_SLABS) {
-        MmaParams m2 = mp;
-        if (plan_mma(m2, DH, DR, gqa, NT, MMA_SMEM_PAIR, true) &&
-            m2.nstages >= MMA_PAIR_MIN_STAGES && mma_smem_bytes(m2, DH, NT) <= MMA_SMEM_PAIR) {
-            mp = m2;
-            pair = true;
+    // three, else two CTAs per SM for long caches (the row capacity bounds the slabs from
+    // above): the first plan whose ring still holds MMA_PAIR_MIN_STAGES
+    int per_sm = 1;
+    const long long cap_slabs = rows.num_rows / SLAB;
+    if (!shared_v && DH == 64 && NT == 1 && req_ctas == 0) {
+        struct Cand { int n, smem, consumers; };
+        const Cand cands[2] = {{3, MMA_SMEM_TRIPLE, MMA_TRIPLE_CONSUMERS},
+                               {2, MMA_SMEM_PAIR, MMA_CONSUMERS}};
+        for (const Cand &cd : cands) {
+            if (cd.consumers < dp.G || cap_slabs < (long long)cd.n * sms * MMA_PAIR_MIN_SLABS)
+                continue;
+            MmaParams m2 = mp;
+            if (plan_mma(m2, DH, DR, gqa, NT, cd.smem, true, cd.consumers) &&
+                m2.nstages >= MMA_PAIR_MIN_STAGES && mma_smem_bytes(m2, DH, NT) <= (size_t)cd.smem) {
+                mp = m2;
+                per_sm = cd.n;
+                break;
+            }
         }
     }
-    if (!pair && !plan_mma(mp, DH, DR, gqa, NT)) return GVA_ERR_UNSUPPORTED;
+    if (per_sm == 1 && !plan_mma(mp, DH, DR, gqa, NT)) return GVA_ERR_UNSUPPORTED;
     const long long nrows = rows.num_rows > 0 ? rows.num_rows : 1;
     CUtensorMap tv, tk;
     mp.early = early ? 1 : 0;
@@ -1217,11 +1254,12 @@ inline int run_mma(void *stream, DecodeParams &dp, const gva_rows &rows, int sms
         if (gqa && !make_map(&tk, dp.Kc, nrows, mp.vg * DH, 64, true)) return GVA_ERR_CUDA;
     }
     if (!gqa) tk = tv;
-    int grid = pair ? 2 * sms : req_ctas > 0 ? req_ctas : sms;
+    int grid = per_sm > 1 ? per_sm * sms : req_ctas > 0 ? req_ctas : sms;
     if (grid > sms * 8) grid = sms * 8;
     dp.n_ctas = grid;
     mp.d.n_ctas = grid;
-    if (pair) return launch_mma_dr<64, 1, 2>(stream, mp, tv, tk, grid, DR, gqa);
+    if (per_sm == 3) return launch_mma_dr<64, 1, 3>(stream, mp, tv, tk, grid, DR, gqa);
+    if (per_sm == 2) return launch_mma_dr<64, 1, 2>(stream, mp, tv, tk, grid, DR, gqa);
     if (shared_v)
         return DH == 128 ? launch_mma_sv<128>(stream, mp, tv, grid, DR)
                          : launch_mma_sv<256>(stream, mp, tv, grid, DR);
