@@ -447,21 +447,24 @@ def test_gqa_refuses_query_rmsnorm():
     assert st == g.GVA_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("per_sm,long_len", [(2, (2600, 3201)), (3, (4000, 4601))])
-def test_several_ctas_per_sm_ragged(per_sm, long_len):
+@pytest.mark.parametrize("per_sm,long_len,shape", [
+    (2, (2600, 3201), {}), (3, (4000, 4601), {}),
+    (3, (4000, 4601), dict(H=8, G=2)),   # GQA's smaller stages take three CTAs per SM too
+])
+def test_several_ctas_per_sm_ragged(per_sm, long_len, shape):
     """Ragged caches long enough for the two- and three-CTAs-per-SM plans (the row capacity
     gives every CTA of that many times the SM count at least 16 slabs; below the next
     plan's threshold for two): half the sequences of 1-40 tokens, half long, so that shares
     cross many short sequences and partial slabs.  GVA and the GQA comparator (whose larger
     stages take the two-CTA plan in both cases) against the oracle, every sequence and
-    head."""
+    head.  With G = 2 the GQA comparator's stages are small enough for three per SM."""
     g = gva()
     gen = np.random.default_rng(11)
     B = 64
     lengths = [int(x) for x in gen.integers(1, 41, B // 2)] + \
               [int(x) for x in gen.integers(long_len[0], long_len[1], B // 2)]
     gen.shuffle(lengths)
-    c = make_case(workload("ragged", B=B), lengths=lengths)
+    c = make_case(workload("ragged", B=B, **shape), lengths=lengths)
     slabs, sms = c.num_rows // 16, g.gva_num_sms()
     assert slabs >= per_sm * sms * 16 and (per_sm == 3 or slabs < 3 * sms * 16)
     D = Dev(c)
